@@ -1,0 +1,194 @@
+"""CPU oracle for the NVFP4 weight x bf16 activation path.
+
+TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
+``cpu_baseline`` / ``--impl reference`` legs of ``bench.py`` may import this
+package.  The CUDA library never imports, links or calls it, and it shares no
+code with the CUDA library: the only thing both sides consume is the seeded
+synthetic inputs.
+
+The arithmetic lives in ``nvfp4_oracle.c`` (plain C11, single-threaded, fp32
+quantiser steps in the order the recipe writes them, fp64 dot products in k
+order).  This module compiles it with gcc on first use and wraps it with
+ctypes for numpy arrays.
+
+Pins (tests/test_oracle_pins.py) tie every function here to something other
+than itself: brute-force nearest-value searches, PyTorch's float8_e4m3fn
+conversions, a hand-worked block, exact rational arithmetic and closed forms.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "nvfp4_oracle.c")
+_BUILD_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD_DIR, "libnvfp4_oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+# Strict IEEE fp32/fp64: no contraction into FMA, no fast-math.
+CFLAGS = ["-std=c11", "-O2", "-ffp-contract=off", "-fno-fast-math", "-fPIC",
+          "-Wall", "-Wextra"]
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle into ``oracle/_build/libnvfp4_oracle.so``."""
+    os.makedirs(_BUILD_DIR, exist_ok=True)
+    stale = (not os.path.exists(_LIB_PATH)
+             or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC))
+    if force or stale:
+        tmp = _LIB_PATH + f".tmp{os.getpid()}"
+        subprocess.run(["gcc", *CFLAGS, "-shared", _SRC, "-o", tmp, "-lm"],
+                       check=True)
+        os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _bind(lib):
+    i64, f32, f64 = ctypes.c_int64, ctypes.c_float, ctypes.c_double
+    P = ctypes.c_void_p
+    lib.nvfp4_oracle_e2m1_value.restype = f64
+    lib.nvfp4_oracle_e2m1_value.argtypes = [ctypes.c_int]
+    lib.nvfp4_oracle_e4m3_value.restype = f64
+    lib.nvfp4_oracle_e4m3_value.argtypes = [ctypes.c_int]
+    lib.nvfp4_oracle_e4m3_encode.restype = ctypes.c_uint8
+    lib.nvfp4_oracle_e4m3_encode.argtypes = [f32]
+    lib.nvfp4_oracle_e2m1_encode.restype = ctypes.c_uint8
+    lib.nvfp4_oracle_e2m1_encode.argtypes = [f32]
+    lib.nvfp4_oracle_quantize.restype = ctypes.c_int
+    lib.nvfp4_oracle_quantize.argtypes = [P, i64, i64, P, P, P]
+    lib.nvfp4_oracle_gemv.restype = None
+    lib.nvfp4_oracle_gemv.argtypes = [P, i64, i64, P, i64, P, P, f32,
+                                      i64, P, i64, P, P]
+    lib.nvfp4_oracle_swiglu.restype = None
+    lib.nvfp4_oracle_swiglu.argtypes = [P, i64, i64, P, i64,
+                                        P, P, f32, P, P, f32,
+                                        i64, P, i64, P, P, P, P, P]
+    return lib
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            _lib = _bind(ctypes.CDLL(build()))
+        return _lib
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _c(a, dtype):
+    return np.ascontiguousarray(np.asarray(a), dtype=dtype)
+
+
+# --------------------------------------------------------------------------
+# Element formats
+# --------------------------------------------------------------------------
+
+def e2m1_value(code: int, lib=None) -> float:
+    return (lib or _load()).nvfp4_oracle_e2m1_value(int(code))
+
+
+def e4m3_value(byte: int, lib=None) -> float:
+    return (lib or _load()).nvfp4_oracle_e4m3_value(int(byte))
+
+
+def e4m3_encode(q, lib=None) -> int:
+    """fp32 -> E4M3 byte (RNE, saturating at 448)."""
+    return int((lib or _load()).nvfp4_oracle_e4m3_encode(float(np.float32(q))))
+
+
+def e2m1_encode(v, lib=None) -> int:
+    """fp32 -> E2M1 code (nearest, ties to even code, clamp 6, sign kept)."""
+    return int((lib or _load()).nvfp4_oracle_e2m1_encode(float(np.float32(v))))
+
+
+# --------------------------------------------------------------------------
+# Quantiser and products
+# --------------------------------------------------------------------------
+
+def quantize(w, lib=None):
+    """fp32 [M, K] -> (codes uint8 [M, K/2], scales uint8 [M, K/16], ts float32)."""
+    w = _c(w, np.float32)
+    M, K = w.shape
+    codes = np.zeros((M, K // 2), np.uint8)
+    scales = np.zeros((M, K // 16), np.uint8)
+    ts = np.zeros(1, np.float32)
+    rc = (lib or _load()).nvfp4_oracle_quantize(_ptr(w), M, K, _ptr(codes), _ptr(scales), _ptr(ts))
+    if rc != 0:
+        raise ValueError(f"oracle quantize failed ({rc}): K % 16 != 0 or non-finite weight")
+    return codes, scales, np.float32(ts[0])
+
+
+def _index(idx, total):
+    if idx is None:
+        return None, total
+    idx = _c(idx, np.int64)
+    return idx, len(idx)
+
+
+def gemv(x_bf16_bits, codes, scales, ts, rows=None, tokens=None, lib=None):
+    """y_ref, A (fp64) of shape [n_tokens, n_rows]; x given as uint16 bf16 bits [N, K].
+
+    Pass criterion for a device result y: |y - y_ref| <= 1e-5 * A + 1e-7.
+    """
+    x = _c(x_bf16_bits, np.uint16)
+    codes = _c(codes, np.uint8)
+    scales = _c(scales, np.uint8)
+    N, K = x.shape
+    M = codes.shape[0]
+    assert codes.shape == (M, K // 2) and scales.shape == (M, K // 16)
+    r, nr = _index(rows, M)
+    t, nt = _index(tokens, N)
+    y = np.zeros((nt, nr), np.float64)
+    A = np.zeros((nt, nr), np.float64)
+    (lib or _load()).nvfp4_oracle_gemv(_ptr(x), N, K, _ptr(t), nt, _ptr(codes), _ptr(scales),
+                              float(np.float32(ts)), M, _ptr(r), nr, _ptr(y), _ptr(A))
+    return y, A
+
+
+def swiglu(x_bf16_bits, gate, up, rows=None, tokens=None, lib=None):
+    """h_ref, g_ref, u_ref, Ag, Au (fp64) for gate=(codes, scales, ts), up=(...)."""
+    x = _c(x_bf16_bits, np.uint16)
+    gc, gs, gts = _c(gate[0], np.uint8), _c(gate[1], np.uint8), gate[2]
+    uc, us, uts = _c(up[0], np.uint8), _c(up[1], np.uint8), up[2]
+    N, K = x.shape
+    M = gc.shape[0]
+    assert gc.shape == uc.shape == (M, K // 2)
+    r, nr = _index(rows, M)
+    t, nt = _index(tokens, N)
+    outs = [np.zeros((nt, nr), np.float64) for _ in range(5)]
+    (lib or _load()).nvfp4_oracle_swiglu(_ptr(x), N, K, _ptr(t), nt,
+                                _ptr(gc), _ptr(gs), float(np.float32(gts)),
+                                _ptr(uc), _ptr(us), float(np.float32(uts)),
+                                M, _ptr(r), nr, *[_ptr(o) for o in outs])
+    return tuple(outs)
+
+
+def dequantize(codes, scales, ts, lib=None):
+    """Exact fp64 weights [M, K] (for small pins only)."""
+    lib = lib or _load()
+    e2 = np.array([lib.nvfp4_oracle_e2m1_value(c) for c in range(16)])
+    e4 = np.array([lib.nvfp4_oracle_e4m3_value(b) for b in range(256)])
+    codes = np.asarray(codes, np.uint8)
+    M, K2 = codes.shape
+    K = 2 * K2
+    c = np.empty((M, K), np.uint8)
+    c[:, 0::2] = codes & 0xF
+    c[:, 1::2] = codes >> 4
+    s = np.repeat(np.asarray(scales, np.uint8), 16, axis=1)
+    return e2[c] * e4[s] * float(np.float32(ts))
+
+
+def load_variant(path: str):
+    """Bind a separately compiled copy of the oracle (used only by the tests
+    that plant a mistake in a copy of the oracle source and check that the pins
+    catch it)."""
+    return _bind(ctypes.CDLL(path))

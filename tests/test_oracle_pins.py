@@ -1,0 +1,394 @@
+"""Pins for the CPU oracle: tie it to things other than itself.
+
+Each ``check_*`` takes an oracle library handle, so the same pins also run
+against copies of the oracle with a planted mistake (test_oracle_mutants.py)
+to show that a plausible slip anywhere in the oracle fails at least one pin.
+
+Independent sources used here:
+  * the E2M1 magnitude list {0, .5, 1, 1.5, 2, 3, 4, 6} of the FP4 E2M1 format;
+  * PyTorch's float8_e4m3fn decode (all 256 bytes) and fp32 -> e4m3 cast;
+  * brute-force nearest-value searches (Python, exact rational comparisons);
+  * the hand-worked block in tests/golden/hand_block.txt;
+  * exact rational (fractions.Fraction) dot products on tiny inputs;
+  * closed forms (one-hot activations, all-ones activations, zero tensors).
+"""
+from __future__ import annotations
+
+import math
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+E2M1_MAG = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+
+
+# ---------------------------------------------------------------------------
+# Independent references
+# ---------------------------------------------------------------------------
+
+def e2m1_ref(code: int) -> float:
+    mag = E2M1_MAG[code & 7]
+    return -mag if code & 8 else mag
+
+
+def e4m3_torch_table() -> np.ndarray:
+    return torch.arange(256, dtype=torch.uint8).view(torch.float8_e4m3fn).double().numpy()
+
+
+def e4m3_brute(q: float) -> int:
+    """Nearest finite non-negative E4M3 byte to q >= 0, ties to the even byte,
+    values beyond the largest finite saturate (fp32 input, exact comparison)."""
+    table = e4m3_torch_table()
+    qf = Fraction(float(np.float32(q)))
+    best, best_d = None, None
+    for b in range(0x7F):  # 0x00..0x7E, all finite non-negative
+        d = abs(Fraction(float(table[b])) - qf)
+        if best is None or d < best_d or (d == best_d and b % 2 == 0):
+            best, best_d = b, d
+    return best
+
+
+def e2m1_brute(v: float) -> int:
+    """Nearest E2M1 code to fp32 v, ties to the even code, |v| > 6 -> 6, sign kept."""
+    vf = float(np.float32(v))
+    if math.isinf(vf):
+        return 7 | (8 if vf < 0 else 0)
+    a = Fraction(abs(vf))
+    best, best_d = None, None
+    for c in range(8):
+        d = abs(Fraction(E2M1_MAG[c]) - a)
+        if best is None or d < best_d or (d == best_d and c % 2 == 0):
+            best, best_d = c, d
+    return best | (8 if math.copysign(1.0, vf) < 0 else 0)
+
+
+def f32(v) -> np.float32:
+    return np.float32(v)
+
+
+def quantize_ref(w: np.ndarray):
+    """The recipe re-derived with numpy fp32 ops and brute-force rounding."""
+    w = np.asarray(w, np.float32)
+    M, K = w.shape
+    amax = f32(np.max(np.abs(w))) if w.size else f32(0)
+    ts = f32(amax / f32(2688.0))
+    table = e4m3_torch_table()
+    codes = np.zeros((M, K // 2), np.uint8)
+    scales = np.zeros((M, K // 16), np.uint8)
+    for m in range(M):
+        for b in range(K // 16):
+            blk = w[m, 16 * b:16 * b + 16]
+            bamax = f32(np.max(np.abs(blk)))
+            sb = 0
+            if ts > 0:
+                sb = e4m3_brute(f32(f32(bamax / f32(6.0)) / ts))
+            scales[m, b] = sb
+            d = f32(f32(table[sb]) * ts)
+            c = [0 if d == 0 else e2m1_brute(f32(v / d)) for v in blk]
+            for j in range(8):
+                codes[m, 8 * b + j] = c[2 * j] | (c[2 * j + 1] << 4)
+    return codes, scales, ts
+
+
+def dequant_ref(codes, scales, ts) -> list[list[Fraction]]:
+    table = e4m3_torch_table()
+    M, K2 = codes.shape
+    out = []
+    for m in range(M):
+        row = []
+        for k in range(2 * K2):
+            byte = int(codes[m, k // 2])
+            c = (byte >> 4) if k & 1 else (byte & 0xF)
+            row.append(Fraction(e2m1_ref(c)) * Fraction(float(table[scales[m, k // 16]]))
+                       * Fraction(float(ts)))
+        out.append(row)
+    return out
+
+
+def bf16_round(a) -> np.ndarray:
+    return torch.tensor(np.asarray(a, np.float32)).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+
+def bf16_value(bits) -> float:
+    return float(np.array([int(bits) << 16], np.uint32).view(np.float32)[0])
+
+
+def read_golden_block():
+    vals = {}
+    with open(os.path.join(GOLDEN, "hand_block.txt")) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            k, v = (s.strip() for s in line.split("=", 1))
+            vals[k] = v
+    w = np.array([float(t) for t in vals["w"].split()], np.float32)
+    codes = [int(t, 16) for t in vals["codes"].split()]
+    return w, int(vals["scale_byte"], 16), codes
+
+
+# ---------------------------------------------------------------------------
+# Pins (each raises AssertionError on a mismatch)
+# ---------------------------------------------------------------------------
+
+def check_e2m1_table(lib):
+    for c in range(16):
+        got = oracle.e2m1_value(c, lib=lib)
+        exp = e2m1_ref(c)
+        assert got == exp and math.copysign(1, got) == math.copysign(1, exp), (c, got, exp)
+
+
+def check_e4m3_table(lib):
+    table = e4m3_torch_table()
+    for b in range(256):
+        got = oracle.e4m3_value(b, lib=lib)
+        if np.isnan(table[b]):
+            assert math.isnan(got), b
+        else:
+            assert got == table[b], (hex(b), got, table[b])
+    # spot values of the format
+    assert oracle.e4m3_value(0x01, lib=lib) == 2.0 ** -9
+    assert oracle.e4m3_value(0x08, lib=lib) == 2.0 ** -6
+    assert oracle.e4m3_value(0x38, lib=lib) == 1.0
+    assert oracle.e4m3_value(0x7E, lib=lib) == 448.0
+
+
+def e4m3_probe_values():
+    table = e4m3_torch_table()
+    pos = sorted(set(float(table[b]) for b in range(0x7F)))
+    vals = []
+    for a, b in zip(pos, pos[1:]):
+        mid = np.float32((a + b) / 2)  # exact in fp32 for this range
+        vals += [mid, np.nextafter(mid, np.float32(0)), np.nextafter(mid, np.float32(1e9)), np.float32(a)]
+    vals += [np.float32(v) for v in (448.0, 450.0, 463.99, 464.0, 500.0, 1e6, 3e38, 2.0 ** -10, 2.0 ** -11, 1e-30, 0.0)]
+    rng = np.random.default_rng(7)
+    vals += list((rng.standard_normal(400) ** 2 * 30).astype(np.float32))
+    vals += list(np.exp(rng.uniform(-9, 6.2, 400)).astype(np.float32))
+    return vals
+
+
+def check_e4m3_encode(lib):
+    for q in e4m3_probe_values():
+        assert oracle.e4m3_encode(q, lib=lib) == e4m3_brute(q), (repr(q),)
+
+
+def check_e4m3_encode_vs_torch(lib):
+    vals = [v for v in e4m3_probe_values() if v < 464.0]
+    t = torch.tensor(np.array(vals, np.float32)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    got = np.array([oracle.e4m3_encode(v, lib=lib) for v in vals], np.uint8)
+    assert np.array_equal(got, t)
+
+
+def e2m1_probe_values():
+    grid = E2M1_MAG
+    vals = []
+    for a, b in zip(grid, grid[1:]):
+        mid = np.float32((a + b) / 2)
+        vals += [mid, np.nextafter(mid, np.float32(0)), np.nextafter(mid, np.float32(9)), np.float32(a)]
+    vals += [np.float32(v) for v in (6.0, 6.5, 7.0, 100.0, 3e38, np.inf)]
+    vals = vals + [np.float32(-v) for v in vals]
+    rng = np.random.default_rng(11)
+    vals += list(rng.uniform(-8, 8, 800).astype(np.float32))
+    vals += [np.float32(-0.0), np.float32(-0.2), np.float32(-1e-30)]
+    return vals
+
+
+def check_e2m1_encode(lib):
+    for v in e2m1_probe_values():
+        assert oracle.e2m1_encode(v, lib=lib) == e2m1_brute(v), (repr(v),)
+
+
+def check_hand_block(lib):
+    w, sb_exp, codes_exp = read_golden_block()
+    codes, scales, ts = oracle.quantize(w.reshape(1, 16), lib=lib)
+    assert ts == f32(f32(0.6) / f32(2688.0))
+    assert scales[0, 0] == sb_exp
+    got = []
+    for byte in codes[0]:
+        got += [int(byte) & 0xF, int(byte) >> 4]
+    assert got == codes_exp, (got, codes_exp)
+    # all-ones activation: closed form ts * 448 * sum of decoded codes
+    x = bf16_round(np.ones((1, 16), np.float32))
+    y, A = oracle.gemv(x, codes, scales, ts, lib=lib)
+    exact = float(ts) * 448.0 * sum(e2m1_ref(c) for c in codes_exp)
+    assert abs(y[0, 0] - exact) <= 1e-12 * abs(exact)
+    assert abs(A[0, 0] - float(ts) * 448.0 * sum(abs(e2m1_ref(c)) for c in codes_exp)) <= 1e-12
+
+
+def check_quantize_random(lib):
+    rng = np.random.default_rng(3)
+    for (M, K, scale) in [(3, 48, 0.02), (2, 32, 1.0), (4, 16, 1e-3)]:
+        w = (rng.standard_normal((M, K)) * scale).astype(np.float32)
+        # heavy-tailed elements give large and subnormal block scales
+        w[rng.random((M, K)) < 0.05] *= 40.0
+        w[0, :16] *= 1e-4  # a block far below the tensor max
+        c, s, ts = oracle.quantize(w, lib=lib)
+        rc, rs, rts = quantize_ref(w)
+        assert ts == rts
+        assert np.array_equal(s, rs), (s, rs)
+        assert np.array_equal(c, rc)
+
+
+def check_quantize_special(lib):
+    # all-zero tensor: ts 0, scale bytes 0, codes 0
+    c, s, ts = oracle.quantize(np.zeros((2, 32), np.float32), lib=lib)
+    assert ts == 0 and not c.any() and not s.any()
+    # a zero block inside a non-zero tensor, and signed tiny values
+    w = np.zeros((1, 32), np.float32)
+    w[0, 16:] = np.linspace(-1, 1, 16, dtype=np.float32)
+    w[0, 17] = -1e-3  # rounds to magnitude 0 -> keeps its sign (0x8)
+    c, s, ts = oracle.quantize(w, lib=lib)
+    assert s[0, 0] == 0 and not c[0, :8].any()
+    assert (int(c[0, 8]) >> 4) == 0x8
+    rc, rs, rts = quantize_ref(w)
+    assert np.array_equal(c, rc) and np.array_equal(s, rs)
+
+
+def check_gemv_exact_small(lib):
+    rng = np.random.default_rng(5)
+    M, K, N = 5, 48, 3  # non-square, several tokens, 3 blocks per row
+    w = (rng.standard_normal((M, K)) * 0.02).astype(np.float32)
+    codes, scales, ts = oracle.quantize(w, lib=lib)
+    xb = bf16_round(rng.standard_normal((N, K)).astype(np.float32) * np.array([[1.0], [8.0], [0.5]], np.float32))
+    y, A = oracle.gemv(xb, codes, scales, ts, lib=lib)
+    wq = dequant_ref(codes, scales, ts)
+    for n in range(N):
+        for m in range(M):
+            terms = [wq[m][k] * Fraction(bf16_value(xb[n, k])) for k in range(K)]
+            exact = sum(terms, Fraction(0))
+            aexact = sum((abs(t) for t in terms), Fraction(0))
+            assert abs(Fraction(y[n, m]) - exact) <= Fraction(1, 10 ** 12) * aexact + Fraction(1, 10 ** 300)
+            assert abs(Fraction(A[n, m]) - aexact) <= Fraction(1, 10 ** 12) * aexact + Fraction(1, 10 ** 300)
+    # subsets of rows / tokens agree with the full product, in the order asked
+    ys, As = oracle.gemv(xb, codes, scales, ts, rows=[4, 0], tokens=[2], lib=lib)
+    assert ys[0, 0] == y[2, 4] and ys[0, 1] == y[2, 0] and As[0, 0] == A[2, 4]
+
+
+def check_gemv_one_hot(lib):
+    rng = np.random.default_rng(9)
+    M, K = 4, 64
+    w = (rng.standard_normal((M, K)) * 0.02).astype(np.float32)
+    codes, scales, ts = oracle.quantize(w, lib=lib)
+    wq = dequant_ref(codes, scales, ts)
+    for k in (0, 1, 17, 63):
+        x = np.zeros((1, K), np.float32)
+        x[0, k] = 1.0
+        y, _ = oracle.gemv(bf16_round(x), codes, scales, ts, lib=lib)
+        for m in range(M):
+            assert y[0, m] == float(wq[m][k]), (k, m)
+
+
+def check_swiglu(lib):
+    rng = np.random.default_rng(13)
+    M, K, N = 3, 32, 2
+    gw = (rng.standard_normal((M, K)) * 0.3).astype(np.float32)
+    uw = (rng.standard_normal((M, K)) * 0.3).astype(np.float32)
+    g = oracle.quantize(gw, lib=lib)
+    u = oracle.quantize(uw, lib=lib)
+    xb = bf16_round(rng.standard_normal((N, K)).astype(np.float32))
+    h, gr, ur, Ag, Au = oracle.swiglu(xb, g, u, lib=lib)
+    gq, uq = dequant_ref(*g), dequant_ref(*u)
+    for n in range(N):
+        for m in range(M):
+            ge = float(sum((gq[m][k] * Fraction(bf16_value(xb[n, k])) for k in range(K)), Fraction(0)))
+            ue = float(sum((uq[m][k] * Fraction(bf16_value(xb[n, k])) for k in range(K)), Fraction(0)))
+            he = ge / (1.0 + math.exp(-ge)) * ue
+            assert abs(gr[n, m] - ge) <= 1e-12 * Ag[n, m] + 1e-300
+            assert abs(ur[n, m] - ue) <= 1e-12 * Au[n, m] + 1e-300
+            assert abs(h[n, m] - he) <= 1e-12 * abs(he) + 1e-300
+    # limits of SiLU: g = 0 gives 0
+    zero = (np.zeros((M, K // 2), np.uint8), np.zeros((M, K // 16), np.uint8), np.float32(0))
+    h0, *_ = oracle.swiglu(xb, zero, u, lib=lib)
+    assert not h0.any()
+
+
+def rounding_order_matrix():
+    """A matrix whose block scales depend on doing (bamax / 6) / ts in that
+    order (rather than bamax / (6 * ts)) and whose codes depend on dividing by
+    d (rather than multiplying by a rounded 1/d).  Found by a seeded search;
+    the expected values come from quantize_ref, not from the oracle."""
+    rng = np.random.default_rng(21)
+    amax = np.float32(0.0731)
+    ts = f32(amax / f32(2688.0))
+    table = e4m3_torch_table()
+    mids = [(table[b] + table[b + 1]) / 2 for b in (0x02, 0x09, 0x21, 0x33, 0x38, 0x45, 0x5A, 0x6C)]
+    bam = np.concatenate([
+        (np.float32(mq * 6.0 * float(ts)) + np.arange(-400, 401, dtype=np.float32)
+         * np.spacing(np.float32(mq * 6.0 * float(ts)))).astype(np.float32)
+        for mq in mids])
+    q1 = ((bam / f32(6.0)).astype(np.float32) / ts).astype(np.float32)
+    q2 = (bam / f32(f32(6.0) * ts)).astype(np.float32)
+    b1 = torch.tensor(q1).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    b2 = torch.tensor(q2).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    pick = list(bam[b1 != b2][:6])
+    assert len(pick) >= 2, "search found no order-sensitive block amax"
+    rows = [np.full(16, amax / 4, np.float32)]
+    rows[0][5] = amax
+    for b in pick:
+        r = (rng.uniform(-1, 1, 16) * float(b)).astype(np.float32)
+        r[7] = b
+        rows.append(r)
+    # elements whose w/d and w*(1/d) land on opposite sides of an E2M1 midpoint
+    extra = []
+    for sb in (0x30, 0x31, 0x35, 0x3B, 0x46, 0x52, 0x5D, 0x66):
+        d = f32(f32(e4m3_torch_table()[sb]) * ts)
+        inv = f32(f32(1.0) / d)
+        for mid in (0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0):
+            cand = (np.float32(mid) * d + np.arange(-64, 65, dtype=np.float32) * np.spacing(np.float32(mid) * d)).astype(np.float32)
+            dv = (cand / d).astype(np.float32)
+            mv = (cand * inv).astype(np.float32)
+            diff = np.nonzero((dv < mid) != (mv < mid))[0]
+            if len(diff):
+                extra.append((sb, cand[diff[0]]))
+    return np.stack(rows), extra
+
+
+def check_quantize_rounding_order(lib):
+    w, extra = rounding_order_matrix()
+    c, s, ts = oracle.quantize(w, lib=lib)
+    rc, rs, rts = quantize_ref(w)
+    assert ts == rts and np.array_equal(s, rs) and np.array_equal(c, rc)
+    # division by d: build blocks whose scale byte is sb and that hold the element
+    assert extra, "search found no element sensitive to 1/d rounding"
+    ts0 = f32(f32(0.0731) / f32(2688.0))
+    rows = []
+    for sb, v in extra[:12]:
+        target = f32(e4m3_torch_table()[sb])
+        # block amax chosen so that the block scale rounds to sb exactly
+        bam = f32(target * f32(6.0) * ts0)
+        r = np.zeros(16, np.float32)
+        r[0] = bam
+        r[1] = v
+        rows.append(r)
+    amax_row = np.zeros(16, np.float32)
+    amax_row[0] = np.float32(0.0731)
+    w2 = np.stack([amax_row] + rows)
+    c2, s2, t2 = oracle.quantize(w2, lib=lib)
+    rc2, rs2, rt2 = quantize_ref(w2)
+    assert t2 == rt2 and np.array_equal(s2, rs2) and np.array_equal(c2, rc2)
+
+
+ALL_CHECKS = [check_e2m1_table, check_e4m3_table, check_e4m3_encode, check_e4m3_encode_vs_torch,
+              check_e2m1_encode, check_hand_block, check_quantize_random, check_quantize_special,
+              check_gemv_exact_small, check_gemv_one_hot, check_swiglu,
+              check_quantize_rounding_order]
+
+
+@pytest.mark.parametrize("check", ALL_CHECKS, ids=lambda f: f.__name__)
+def test_oracle_pin(check):
+    check(None)
+
+
+def test_oracle_rejects_bad_input():
+    with pytest.raises(ValueError):
+        oracle.quantize(np.zeros((2, 24), np.float32))
+    w = np.zeros((1, 16), np.float32)
+    w[0, 3] = np.nan
+    with pytest.raises(ValueError):
+        oracle.quantize(w)
