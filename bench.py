@@ -1,0 +1,461 @@
+"""Benchmark of the NVFP4 x bf16 decode path on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload dense9b-n1|dense27b-n1|dense27b-n4|dense27b-n9|dense27b-n16]
+
+A step is one pass of the decode hot path over a rotating stream of dense
+decoder layers (weights larger than L2): per layer the fused QKV projection,
+the O projection, the fused gate/up + SwiGLU, and the down projection, all
+NVFP4 weights x bf16 activations, fp32 out.  The default workload is the dense
+9B-class layer stream at N = 1 (36 distinct layers, 3.9 GB of NVFP4 weights).
+The whole stream is captured once as a CUDA graph (one replay per step, as a
+CUDA-graph decode replays one graph per token) and timed with CUDA events.
+
+Printed: one JSON line with the HBM GB/s of the stream (algorithmic bytes:
+codes + scales + x + y), the roofline of the dominant kernel, an end-to-end
+number with host<->device copies, the oracle timed on host cores, and the SM
+clocks sampled during the timed region.
+
+--impl reference times the CPU oracle (the only reference implementation this
+build has) on a bounded sample of the same workload, in the same unit.
+Under torchrun every rank runs its own replica (no collective on the data
+path; the path does not shard), rank 0 prints.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "NVFP4 GEMV achieved HBM GB/s (% of ~8 TB/s) at N=1/4/9; prefill GEMM TFLOPS"
+
+WORKLOADS = {
+    # name: (layer shape, N, layers, heavy-tailed weights, outlier token rows)
+    "dense9b-n1": ("LAYER_9B", 1, 36, False, False),
+    "dense27b-n1": ("LAYER_27B", 1, 64, False, False),
+    "dense27b-n4": ("LAYER_27B", 4, 64, False, False),
+    "dense27b-n9": ("LAYER_27B", 9, 64, True, True),
+    "dense27b-n16": ("LAYER_27B", 16, 64, True, True),
+}
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="dense9b-n1")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing (replicas only)
+# ---------------------------------------------------------------------------
+
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(0)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(v, world):
+    if world == 1:
+        return v
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------
+# clocks sampled during the timed region
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-f", self.path], stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.2)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        if not self.path or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((float(parts[1]), float(parts[2]), parts[4:]))
+            except ValueError:
+                continue
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = [r[0] for r in rows]
+        smax = max(r[1] for r in rows)
+        loaded = [s for s in sm if s > 0.5 * smax] or sm
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i, v in enumerate(r[2][1:5]) if v.strip() == "Active"})
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": smax, "reasons": reasons,
+                "samples": len(rows)}
+
+
+# ---------------------------------------------------------------------------
+# the decode layer stream
+# ---------------------------------------------------------------------------
+
+class LayerStream:
+    """Rotating NVFP4 layers + per-layer activations and outputs on one GPU."""
+
+    def __init__(self, workload: str, device):
+        import gemm_nvfp4_gb300 as g
+        from gemm_nvfp4_gb300 import inputs
+        self.g = g
+        shape_name, self.N, self.n_layers, heavy, outliers = WORKLOADS[workload]
+        self.shape = getattr(inputs, shape_name)
+        self.workload = workload
+        shapes = self.shape.shapes()
+        self.shapes = shapes
+        # base layer: quantise each matrix once on the GPU, then replicate
+        base = {}
+        for name, (M, K) in shapes.items():
+            w = inputs.weights(M, K, seed=inputs.matrix_seed(name), heavy_tail=heavy, device=device)
+            base[name] = g.nvfp4_quantize(w)
+            del w
+        torch.cuda.synchronize()
+        self.layers = []
+        for _ in range(self.n_layers):
+            layer = {}
+            for name, W in base.items():
+                layer[name] = g.NVFP4Weight(W.codes.clone(), W.scales.clone(), W.tensor_scale.clone())
+            self.layers.append(layer)
+        del base
+        # activations per layer and matrix (bf16 N(0,1), the step's inputs) and
+        # outputs, as views into one input and one output buffer so the
+        # end-to-end run moves each with a single copy
+        N = self.N
+        names = ("qkv", "o", "gate", "down")
+        x_sizes = [N * shapes[n][1] for n in names]
+        y_sizes = [N * shapes[n][0] for n in names]
+        self.x_all = torch.empty(self.n_layers * sum(x_sizes), dtype=torch.bfloat16, device=device)
+        self.y_all = torch.empty(self.n_layers * sum(y_sizes), dtype=torch.float32, device=device)
+        self.x, self.y = [], []
+        xo = yo = 0
+        for li in range(self.n_layers):
+            xs, ys = {}, {}
+            for name, xsz, ysz in zip(names, x_sizes, y_sizes):
+                M, K = shapes[name]
+                xs[name] = self.x_all[xo:xo + xsz].view(N, K)
+                xs[name].copy_(inputs.activations(N, K, seed=1000 * li + inputs.matrix_seed(name) + 1,
+                                                  outlier_rows=outliers, device=device))
+                ys[name] = self.y_all[yo:yo + ysz].view(N, M)
+                xo += xsz
+                yo += ysz
+            self.x.append(xs)
+            self.y.append(ys)
+        ws_need = max(g.nvfp4_workspace_bytes(g.NVFP4_OP_GEMV_SKINNY, N, M, K) for M, K in shapes.values())
+        ws_need = max(ws_need, g.nvfp4_workspace_bytes(g.NVFP4_OP_GATEUP_SWIGLU, N, *shapes["gate"]))
+        self.ws = torch.empty(ws_need, dtype=torch.uint8, device=device)
+
+    # algorithmic bytes (codes + scales + x + y) of each call kind
+    def call_bytes(self, name):
+        N = self.N
+        if name == "gateup":
+            M, K = self.shapes["gate"]
+            return 2 * (M * K // 2 + M * K // 16) + N * K * 2 + N * M * 4
+        M, K = self.shapes[name]
+        return M * K // 2 + M * K // 16 + N * K * 2 + N * M * 4
+
+    def step_bytes(self):
+        return self.n_layers * sum(self.call_bytes(n) for n in ("qkv", "o", "gateup", "down"))
+
+    def weight_bytes(self):
+        return self.n_layers * sum(M * K // 2 + M * K // 16 for M, K in self.shapes.values())
+
+    def run_layer(self, li, only=None):
+        g, L, X, Y, ws = self.g, self.layers[self.layer_index(li)], self.x[li], self.y[li], self.ws
+        if only in (None, "qkv"):
+            g.nvfp4_gemv_skinny(X["qkv"], L["qkv"], out=Y["qkv"], workspace=ws)
+        if only in (None, "o"):
+            g.nvfp4_gemv_skinny(X["o"], L["o"], out=Y["o"], workspace=ws)
+        if only in (None, "gateup"):
+            g.nvfp4_gateup_swiglu(X["gate"], L["gate"], L["up"], out=Y["gate"], workspace=ws)
+        if only in (None, "down"):
+            g.nvfp4_gemv_skinny(X["down"], L["down"], out=Y["down"], workspace=ws)
+
+    def layer_index(self, li):
+        return li
+
+    def run_all(self, only=None):
+        for li in range(self.n_layers):
+            self.run_layer(li, only)
+
+    # our kernels per call: main kernel + split-K fixup kernel
+    LAUNCHES_PER_CALL = 2
+
+    def launches_per_step(self, only=None):
+        calls = 4 if only is None else 1
+        return self.n_layers * calls * self.LAUNCHES_PER_CALL
+
+    def capture(self, only=None):
+        graph = torch.cuda.CUDAGraph()
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            self.run_all(only)  # warm (not captured)
+        torch.cuda.current_stream().wait_stream(s)
+        torch.cuda.synchronize()
+        with torch.cuda.graph(graph, stream=s):
+            self.run_all(only)
+        torch.cuda.synchronize()
+        return graph
+
+    def host_io(self):
+        """Pinned host copies of the step's inputs and outputs (for e2e)."""
+        return ([(self.x_all, self.x_all.cpu().pin_memory())],
+                [(self.y_all, torch.empty_like(self.y_all, device="cpu").pin_memory())])
+
+
+def time_graph(graph, steps, warmup, world, stream=None):
+    stream = stream or torch.cuda.current_stream()
+    for _ in range(warmup):
+        graph.replay()
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for _ in range(steps):
+        graph.replay()
+    stop.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    return start.elapsed_time(stop) / steps  # ms per replay
+
+
+def read_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d.get("hbm_gbs"), d.get("bf16_tflops"), "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+def read_traffic(kernel_key):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the current kernel source (the summary records the source hash)."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "traffic.md")
+    if not os.path.exists(path):
+        return None
+    src = os.path.join(ROOT, "gemm_nvfp4_gb300", "csrc", "gemv.cu")
+    h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    for line in open(path):
+        parts = [p.strip() for p in line.strip().strip("|").split("|")]
+        if len(parts) >= 4 and parts[0] == kernel_key and parts[1] == h:
+            try:
+                return float(parts[2])
+            except ValueError:
+                return None
+    return None
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle baseline
+# ---------------------------------------------------------------------------
+
+def oracle_sample(workload, rows_per_matrix=64, device="cpu"):
+    """Quantise a row sample of every matrix of one layer with the oracle and
+    time the oracle's products for it; returns (seconds, algorithmic bytes)."""
+    import oracle
+    from gemm_nvfp4_gb300 import inputs
+    shape_name, N, _, heavy, outliers = WORKLOADS[workload]
+    shape = getattr(inputs, shape_name)
+    jobs = []
+    for name, (M, K) in shape.shapes().items():
+        w = inputs.weights(rows_per_matrix, K, seed=inputs.matrix_seed(name), heavy_tail=heavy)
+        x = inputs.activations(N, K, seed=inputs.matrix_seed(name) + 1, outlier_rows=outliers)
+        jobs.append((oracle.quantize(w.numpy()), inputs.bf16_bits(x), rows_per_matrix, K))
+    t0 = time.perf_counter()
+    nbytes = 0
+    for (codes, scales, ts), xb, M, K in jobs:
+        oracle.gemv(xb, codes, scales, ts)
+        nbytes += M * K // 2 + M * K // 16 + N * K * 2 + N * M * 4
+    return time.perf_counter() - t0, nbytes
+
+
+def cpu_baseline(workload, target_s=10.0):
+    dt, nb = oracle_sample(workload, rows_per_matrix=16)
+    rows = int(max(16, min(4096, 16 * target_s / max(dt, 1e-3))))
+    dt, nb = oracle_sample(workload, rows_per_matrix=rows)
+    return {"value": nb / dt / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"{rows} rows of each of the 5 matrices of one layer of {workload}, "
+                      f"N as in the workload, single-threaded C oracle, {dt:.1f} s"}
+
+
+# ---------------------------------------------------------------------------
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return
+    shape_name, N, layers, _, _ = WORKLOADS[args.workload]
+    times = []
+    nb = 0
+    for i in range(args.warmup + args.steps):
+        dt, nb = oracle_sample(args.workload, rows_per_matrix=24)
+        if i >= args.warmup:
+            times.append(dt)
+    dt = sum(times) / len(times)
+    value = nb / dt / 1e9
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": args.workload, "tokens_N": N, "layers_sampled": 1,
+                       "rows_per_matrix": 24},
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                             "sample": "24 rows of each matrix of one layer per step"},
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    world, rank, local = dist_setup(args)
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+        return
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU (the NVFP4 path has no CPU fallback)")
+    dev = torch.device("cuda", torch.cuda.current_device())
+    st = LayerStream(args.workload, dev)
+    graph = st.capture()
+    dom_graph = st.capture(only="gateup")
+
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        ms = time_graph(graph, args.steps, args.warmup, world)
+        dom_ms = time_graph(dom_graph, args.steps, args.warmup, world)
+    clocks = clk.summary()
+    ms = max_over_ranks(ms, world)
+
+    # end to end: pinned host inputs -> device, graph, device -> pinned host outputs
+    xs, ys = st.host_io()
+    h2d = sum(h.numel() * h.element_size() for _, h in xs)
+    d2h = sum(h.numel() * h.element_size() for _, h in ys)
+    stream = torch.cuda.current_stream()
+
+    def e2e_step():
+        for d, h in xs:
+            d.copy_(h, non_blocking=True)
+        graph.replay()
+        for d, h in ys:
+            h.copy_(d, non_blocking=True)
+
+    for _ in range(args.warmup):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier(world)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, world)
+
+    step_bytes = st.step_bytes()
+    value = world * step_bytes / (ms * 1e-3) / 1e9
+    e2e_value = world * step_bytes / (e2e_ms * 1e-3) / 1e9
+    hbm_peak, _, peak_kind = read_peaks()
+    dom_bytes = st.call_bytes("gateup")
+    dom_per_launch_ms = dom_ms / st.n_layers
+    achieved = dom_bytes / (dom_per_launch_ms * 1e-3) / 1e9
+    traffic = read_traffic("gemv_kernel<2,1>" if st.N <= 8 else "gemv_kernel<2,2>")
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(args.workload)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": args.workload, "layer": st.shape.name, "tokens_N": st.N,
+                       "layers": st.n_layers, "weight_bytes_per_step": st.weight_bytes(),
+                       "algorithmic_bytes_per_step": step_bytes,
+                       "l2": "inputs larger than L2 (rotating layers)", "graph": "one CUDA graph per step",
+                       "tokens_per_s_per_stream": world * st.N / (ms * 1e-3),
+                       "frac_of_8TBs": value / world / 8000.0},
+            "roofline": {"bound": "hbm", "kernel": "nvfp4_gateup_swiglu (fused gate/up + SwiGLU)",
+                         "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                         "frac": achieved / hbm_peak if hbm_peak else None, "traffic": traffic,
+                         "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
+                         else "fallback 6.8 TB/s",
+                         "timing": f"{st.n_layers} back-to-back calls captured alone, CUDA events"},
+            "cpu_baseline": cpu,
+            "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "gpu_launches": st.launches_per_step() * args.steps,
+            "clocks": clocks,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

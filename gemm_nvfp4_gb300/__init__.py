@@ -1,0 +1,21 @@
+"""NVFP4 weights x bf16 activations on GB300 (sm_103a).
+
+The compute path is the C-ABI library libnvfp4.so (include/nvfp4.h), built from
+``gemm_nvfp4_gb300/csrc`` by ``gemm_nvfp4_gb300.build``.  This package only
+marshals PyTorch tensors into that ABI (``binding``) and provides seeded
+synthetic inputs (``inputs``).  There is no CPU fallback: if the library is
+missing, every call raises.
+"""
+from .binding import (NVFP4_OP_GATEUP_SWIGLU, NVFP4_OP_GEMM_PREFILL, NVFP4_OP_GEMV_SKINNY,
+                      NVFP4_OP_QUANTIZE, NVFP4_OUT_BF16, NVFP4_OUT_F32, NVFP4Error, NVFP4Weight,
+                      header_functions, library_path, load_library, nvfp4_gateup_swiglu,
+                      nvfp4_gemm_prefill, nvfp4_gemv_skinny, nvfp4_quantize, nvfp4_status_string,
+                      nvfp4_version, nvfp4_workspace_bytes)
+
+__all__ = [
+    "NVFP4Error", "NVFP4Weight", "header_functions", "library_path", "load_library",
+    "nvfp4_gateup_swiglu", "nvfp4_gemm_prefill", "nvfp4_gemv_skinny", "nvfp4_quantize",
+    "nvfp4_status_string", "nvfp4_version", "nvfp4_workspace_bytes",
+    "NVFP4_OP_QUANTIZE", "NVFP4_OP_GEMV_SKINNY", "NVFP4_OP_GATEUP_SWIGLU", "NVFP4_OP_GEMM_PREFILL",
+    "NVFP4_OUT_F32", "NVFP4_OUT_BF16",
+]

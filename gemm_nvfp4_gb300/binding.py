@@ -1,0 +1,211 @@
+"""ctypes binding of libnvfp4.so (include/nvfp4.h): argument marshalling only.
+
+Every function here has the name of the C entry point it calls and does
+nothing but turn PyTorch tensors into pointers, sizes and the current CUDA
+stream.  All arithmetic runs in the library's CUDA kernels.  If the library is
+missing or fails to load, every call raises: there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+import threading
+from dataclasses import dataclass
+
+import torch
+
+from . import build as _build
+
+NVFP4_OK = 0
+NVFP4_ERR_INVALID_ARG = 1
+NVFP4_ERR_UNSUPPORTED_SHAPE = 2
+NVFP4_ERR_WORKSPACE = 3
+NVFP4_ERR_CUDA = 4
+
+NVFP4_OP_QUANTIZE = 0
+NVFP4_OP_GEMV_SKINNY = 1
+NVFP4_OP_GATEUP_SWIGLU = 2
+NVFP4_OP_GEMM_PREFILL = 3
+
+NVFP4_OUT_F32 = 0
+NVFP4_OUT_BF16 = 1
+
+_lock = threading.Lock()
+_lib = None
+
+
+class NVFP4Error(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {nvfp4_status_string(status)} (status {status})")
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load_library():
+    """Load libnvfp4.so (built by gemm_nvfp4_gb300.build / __graft_entry__.build())."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = library_path()
+        if not os.path.exists(path):
+            raise RuntimeError(
+                f"libnvfp4.so not found at {path}: build it with `python -m gemm_nvfp4_gb300.build` "
+                "(the NVFP4 path has no CPU fallback)")
+        lib = ctypes.CDLL(path)
+        P, i64, sz, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_size_t, ctypes.c_int
+        lib.nvfp4_status_string.restype = ctypes.c_char_p
+        lib.nvfp4_status_string.argtypes = [i32]
+        lib.nvfp4_version.restype = i32
+        lib.nvfp4_version.argtypes = []
+        lib.nvfp4_workspace_bytes.restype = sz
+        lib.nvfp4_workspace_bytes.argtypes = [i32, i64, i64, i64]
+        lib.nvfp4_quantize.restype = i32
+        lib.nvfp4_quantize.argtypes = [P, i64, i64, P, P, P, P, sz, P]
+        lib.nvfp4_gemv_skinny.restype = i32
+        lib.nvfp4_gemv_skinny.argtypes = [P, i64, P, P, P, i64, i64, P, i32, P, sz, P]
+        lib.nvfp4_gateup_swiglu.restype = i32
+        lib.nvfp4_gateup_swiglu.argtypes = [P, i64, P, P, P, P, P, P, i64, i64, P, i32, P, sz, P]
+        lib.nvfp4_gemm_prefill.restype = i32
+        lib.nvfp4_gemm_prefill.argtypes = [P, i64, P, P, P, i64, i64, P, i32, P, sz, P]
+        _lib = lib
+        return lib
+
+
+def header_functions() -> list[str]:
+    """Names of the functions declared in include/nvfp4.h."""
+    text = open(_build.HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(nvfp4_[a-z0-9_]+)\s*\(", text)))
+
+
+# ---------------------------------------------------------------------------
+# Thin wrappers with the C names
+# ---------------------------------------------------------------------------
+
+def nvfp4_status_string(status: int) -> str:
+    return load_library().nvfp4_status_string(int(status)).decode()
+
+
+def nvfp4_version() -> int:
+    return load_library().nvfp4_version()
+
+
+def nvfp4_workspace_bytes(op: int, N: int, M: int, K: int) -> int:
+    return load_library().nvfp4_workspace_bytes(int(op), int(N), int(M), int(K))
+
+
+@dataclass
+class NVFP4Weight:
+    """One NVFP4 tensor W[M][K] in device memory (see include/nvfp4.h)."""
+    codes: torch.Tensor         # uint8 [M, K/2]
+    scales: torch.Tensor        # uint8 [M, K/16]
+    tensor_scale: torch.Tensor  # float32 [1]
+
+    @property
+    def M(self) -> int:
+        return self.codes.shape[0]
+
+    @property
+    def K(self) -> int:
+        return self.codes.shape[1] * 2
+
+    def nbytes(self) -> int:
+        return self.codes.numel() + self.scales.numel()
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _check(status: int, where: str):
+    if status != NVFP4_OK:
+        raise NVFP4Error(status, where)
+
+
+def _workspace(op, N, M, K, device, workspace):
+    need = nvfp4_workspace_bytes(op, N, M, K)
+    if workspace is not None:
+        return workspace, workspace.numel() * workspace.element_size()
+    if need == 0:
+        return None, 0
+    return torch.empty(need, dtype=torch.uint8, device=device), need
+
+
+def _out_code(dtype) -> int:
+    if dtype == torch.float32:
+        return NVFP4_OUT_F32
+    if dtype == torch.bfloat16:
+        return NVFP4_OUT_BF16
+    raise ValueError(f"unsupported output dtype {dtype}")
+
+
+def nvfp4_quantize(w: torch.Tensor, workspace: torch.Tensor | None = None,
+                   out: NVFP4Weight | None = None, stream=None) -> NVFP4Weight:
+    """fp32 [M, K] CUDA tensor -> NVFP4Weight (codes, scales, tensor scale)."""
+    M, K = w.shape
+    if out is None:
+        out = NVFP4Weight(torch.empty(M, K // 2, dtype=torch.uint8, device=w.device),
+                          torch.empty(M, K // 16, dtype=torch.uint8, device=w.device),
+                          torch.empty(1, dtype=torch.float32, device=w.device))
+    ws, ws_bytes = _workspace(NVFP4_OP_QUANTIZE, 0, M, K, w.device, workspace)
+    st = load_library().nvfp4_quantize(_ptr(w), M, K, _ptr(out.codes), _ptr(out.scales),
+                                       _ptr(out.tensor_scale), _ptr(ws), ws_bytes, _stream(stream))
+    _check(st, "nvfp4_quantize")
+    return out
+
+
+def _new_out(N, M, dtype, device, out):
+    return out if out is not None else torch.empty(N, M, dtype=dtype, device=device)
+
+
+def nvfp4_gemv_skinny(x: torch.Tensor, W: NVFP4Weight, out_dtype=torch.float32,
+                      out: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
+                      stream=None) -> torch.Tensor:
+    """y[N, M] = x[N, K] (bf16) . dequant(W)^T for N = 1..16."""
+    N, K = x.shape
+    y = _new_out(N, W.M, out_dtype, x.device, out)
+    ws, ws_bytes = _workspace(NVFP4_OP_GEMV_SKINNY, N, W.M, K, x.device, workspace)
+    st = load_library().nvfp4_gemv_skinny(_ptr(x), N, _ptr(W.codes), _ptr(W.scales), _ptr(W.tensor_scale),
+                                          W.M, K, _ptr(y), _out_code(y.dtype), _ptr(ws), ws_bytes,
+                                          _stream(stream))
+    _check(st, "nvfp4_gemv_skinny")
+    return y
+
+
+def nvfp4_gateup_swiglu(x: torch.Tensor, Wg: NVFP4Weight, Wu: NVFP4Weight, out_dtype=torch.float32,
+                        out: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
+                        stream=None) -> torch.Tensor:
+    """h[N, M] = silu(x . Wg^T) * (x . Wu^T), any N >= 1."""
+    N, K = x.shape
+    h = _new_out(N, Wg.M, out_dtype, x.device, out)
+    ws, ws_bytes = _workspace(NVFP4_OP_GATEUP_SWIGLU, N, Wg.M, K, x.device, workspace)
+    st = load_library().nvfp4_gateup_swiglu(_ptr(x), N, _ptr(Wg.codes), _ptr(Wg.scales),
+                                            _ptr(Wg.tensor_scale), _ptr(Wu.codes), _ptr(Wu.scales),
+                                            _ptr(Wu.tensor_scale), Wg.M, K, _ptr(h), _out_code(h.dtype),
+                                            _ptr(ws), ws_bytes, _stream(stream))
+    _check(st, "nvfp4_gateup_swiglu")
+    return h
+
+
+def nvfp4_gemm_prefill(x: torch.Tensor, W: NVFP4Weight, out_dtype=torch.float32,
+                       out: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
+                       stream=None) -> torch.Tensor:
+    """y[N, M] = x[N, K] (bf16) . dequant(W)^T, any N >= 1 (tensor cores for N > 16)."""
+    N, K = x.shape
+    y = _new_out(N, W.M, out_dtype, x.device, out)
+    ws, ws_bytes = _workspace(NVFP4_OP_GEMM_PREFILL, N, W.M, K, x.device, workspace)
+    st = load_library().nvfp4_gemm_prefill(_ptr(x), N, _ptr(W.codes), _ptr(W.scales), _ptr(W.tensor_scale),
+                                           W.M, K, _ptr(y), _out_code(y.dtype), _ptr(ws), ws_bytes,
+                                           _stream(stream))
+    _check(st, "nvfp4_gemm_prefill")
+    return y

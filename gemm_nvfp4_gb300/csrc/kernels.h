@@ -1,0 +1,38 @@
+// kernels.h -- launch interface between the C ABI (nvfp4_abi.cu) and the
+// kernel translation units.  Internal to libnvfp4.so.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace nvfp4 {
+
+// Partial maxima written by the amax kernel of the quantiser.
+constexpr int kQuantPartials = 1024;
+// Largest grid of the skinny kernel (sizes its split-K workspace).
+constexpr int kGemvMaxCtas = 1024;
+// Split-K partials of one CTA: 2 slots x 16 rows x 16 tokens fp32.
+constexpr int64_t kGemvPartialFloatsPerCta = 2 * 16 * 16;
+
+cudaError_t launch_quantize(const float *w, int64_t M, int64_t K, uint8_t *codes, uint8_t *scales,
+                            float *tensor_scale, void *workspace, int num_sms, cudaStream_t stream);
+
+// n_weights = 1: y = x . W^T; n_weights = 2: h = silu(x . Wg^T) * (x . Wu^T)
+// with codes/scales/ts[0] = gate, [1] = up.
+cudaError_t launch_gemv(const uint16_t *x, int N, int64_t M, int64_t K, const uint8_t *const *codes,
+                        const uint8_t *const *scales, const float *const *ts, int n_weights, void *y,
+                        int out_bf16, void *workspace, int num_sms, cudaStream_t stream);
+
+int64_t gemv_grid(int64_t M, int64_t K, int num_sms);
+
+}  // namespace nvfp4
+
+namespace nvfp4 {
+
+size_t prefill_workspace_bytes(int64_t N, int64_t M, int64_t K, int n_weights);
+
+cudaError_t launch_prefill(const uint16_t *x, int64_t N, int64_t M, int64_t K, const uint8_t *const *codes,
+                           const uint8_t *const *scales, const float *const *ts, int n_weights, void *y,
+                           int out_bf16, void *workspace, int num_sms, cudaStream_t stream);
+
+}  // namespace nvfp4

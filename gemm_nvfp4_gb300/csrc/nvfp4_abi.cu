@@ -1,0 +1,226 @@
+// nvfp4_abi.cu -- the C ABI of libnvfp4.so (declared in include/nvfp4.h):
+// argument checks on the host, workspace sizes, and dispatch by N to the
+// skinny kernel (N <= 16) or the tensor-core prefill kernel (N > 16), the
+// per-shape dispatch of bw24 README, NVFP4 decode path (one entry point per
+// operation, the library picks the kernel from the shape).
+#include <atomic>
+#include <cstdint>
+#include <cstring>
+
+#include "../../include/nvfp4.h"
+#include "kernels.h"
+
+namespace {
+
+using namespace nvfp4;
+
+constexpr int kMaxSkinnyN = 16;
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+// Streaming multiprocessors of the current device (cached per device id).
+int current_num_sms(int *out)
+{
+    static std::atomic<int> cache[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess)
+        return NVFP4_ERR_CUDA;
+    if (dev >= 0 && dev < 64) {
+        int v = cache[dev].load(std::memory_order_relaxed);
+        if (v > 0) {
+            *out = v;
+            return NVFP4_OK;
+        }
+    }
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+        return NVFP4_ERR_CUDA;
+    if (dev >= 0 && dev < 64)
+        cache[dev].store(n, std::memory_order_relaxed);
+    *out = n;
+    return NVFP4_OK;
+}
+
+size_t skinny_ws(int n_weights) { return (size_t)kGemvMaxCtas * kGemvPartialFloatsPerCta * n_weights * 4; }
+
+bool size_ok(int64_t a, int64_t b) { return a >= 0 && b >= 0 && (b == 0 || a <= (INT64_C(1) << 62) / b); }
+
+// Shared checks of the three product calls.
+int check_product(const uint16_t *x, int64_t N, int64_t M, int64_t K, const uint8_t *codes,
+                  const uint8_t *scales, const float *ts, const void *y, int out_dtype)
+{
+    if (N < 0 || M < 0 || K < 0)
+        return NVFP4_ERR_INVALID_ARG;
+    if (out_dtype != NVFP4_OUT_F32 && out_dtype != NVFP4_OUT_BF16)
+        return NVFP4_ERR_INVALID_ARG;
+    if (K % 16 != 0 || !size_ok(N, K) || !size_ok(M, K) || !size_ok(N, M))
+        return NVFP4_ERR_UNSUPPORTED_SHAPE;
+    if (N == 0 || M == 0)
+        return NVFP4_OK;
+    if (!y || !aligned(y, 16))
+        return NVFP4_ERR_INVALID_ARG;
+    if (K == 0)
+        return NVFP4_OK;
+    if (!x || !codes || !scales || !ts)
+        return NVFP4_ERR_INVALID_ARG;
+    if (!aligned(x, 16) || !aligned(codes, 16) || !aligned(scales, 16) || !aligned(ts, 4))
+        return NVFP4_ERR_INVALID_ARG;
+    return NVFP4_OK;
+}
+
+int check_workspace(const void *ws, size_t have, size_t need)
+{
+    if (have < need)
+        return NVFP4_ERR_WORKSPACE;
+    if (need > 0 && (!ws || !aligned(ws, 16)))
+        return NVFP4_ERR_INVALID_ARG;
+    return NVFP4_OK;
+}
+
+int zero_output(void *y, int64_t N, int64_t M, int out_dtype, cudaStream_t s)
+{
+    const size_t bytes = (size_t)N * (size_t)M * (out_dtype == NVFP4_OUT_BF16 ? 2 : 4);
+    return cudaMemsetAsync(y, 0, bytes, s) == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA;
+}
+
+int run_products(const uint16_t *x, int64_t N, int64_t M, int64_t K, const uint8_t *const *codes,
+                 const uint8_t *const *scales, const float *const *ts, int n_weights, void *y, int out_dtype,
+                 void *ws, cudaStream_t stream)
+{
+    int sms = 0;
+    int rc = current_num_sms(&sms);
+    if (rc != NVFP4_OK)
+        return rc;
+    const size_t esize = out_dtype == NVFP4_OUT_BF16 ? 2 : 4;
+    // N <= 16: one skinny launch.  Larger N: tensor-core prefill.
+    if (N <= kMaxSkinnyN) {
+        cudaError_t e = launch_gemv(x, (int)N, M, K, codes, scales, ts, n_weights, y,
+                                    out_dtype == NVFP4_OUT_BF16, ws, sms, stream);
+        return e == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA;
+    }
+    cudaError_t e = launch_prefill(x, N, M, K, codes, scales, ts, n_weights, y, out_dtype == NVFP4_OUT_BF16,
+                                   ws, sms, stream);
+    (void)esize;
+    return e == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *nvfp4_status_string(int status)
+{
+    switch (status) {
+    case NVFP4_OK: return "NVFP4_OK";
+    case NVFP4_ERR_INVALID_ARG: return "NVFP4_ERR_INVALID_ARG: null, negative, misaligned or unknown argument";
+    case NVFP4_ERR_UNSUPPORTED_SHAPE: return "NVFP4_ERR_UNSUPPORTED_SHAPE: K % 16 != 0, N out of range or size overflow";
+    case NVFP4_ERR_WORKSPACE: return "NVFP4_ERR_WORKSPACE: workspace smaller than nvfp4_workspace_bytes()";
+    case NVFP4_ERR_CUDA: return "NVFP4_ERR_CUDA: a CUDA call or kernel launch failed";
+    default: return "NVFP4 unknown status";
+    }
+}
+
+int nvfp4_version(void) { return 100; }
+
+size_t nvfp4_workspace_bytes(int op, int64_t N, int64_t M, int64_t K)
+{
+    if (N < 0 || M < 0 || K < 0 || K % 16 != 0)
+        return 0;
+    switch (op) {
+    case NVFP4_OP_QUANTIZE: return (size_t)kQuantPartials * 4;
+    case NVFP4_OP_GEMV_SKINNY: return (N >= 1 && N <= kMaxSkinnyN) ? skinny_ws(1) : 0;
+    case NVFP4_OP_GATEUP_SWIGLU: return N <= kMaxSkinnyN ? skinny_ws(2) : prefill_workspace_bytes(N, M, K, 2);
+    case NVFP4_OP_GEMM_PREFILL: return N <= kMaxSkinnyN ? skinny_ws(1) : prefill_workspace_bytes(N, M, K, 1);
+    default: return 0;
+    }
+}
+
+int nvfp4_quantize(const float *w, int64_t M, int64_t K, uint8_t *codes, uint8_t *scales, float *tensor_scale,
+                   void *workspace, size_t workspace_bytes, nvfp4_stream_t stream)
+{
+    if (M < 0 || K < 0)
+        return NVFP4_ERR_INVALID_ARG;
+    if (K % 16 != 0 || !size_ok(M, K))
+        return NVFP4_ERR_UNSUPPORTED_SHAPE;
+    if (!tensor_scale || !aligned(tensor_scale, 4))
+        return NVFP4_ERR_INVALID_ARG;
+    if (M * K > 0 && (!w || !codes || !scales || !aligned(w, 16) || !aligned(codes, 16) || !aligned(scales, 16)))
+        return NVFP4_ERR_INVALID_ARG;
+    int rc = check_workspace(workspace, workspace_bytes, nvfp4_workspace_bytes(NVFP4_OP_QUANTIZE, 0, M, K));
+    if (rc != NVFP4_OK)
+        return rc;
+    int sms = 0;
+    rc = current_num_sms(&sms);
+    if (rc != NVFP4_OK)
+        return rc;
+    cudaError_t e = launch_quantize(w, M, K, codes, scales, tensor_scale, workspace, sms, (cudaStream_t)stream);
+    return e == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA;
+}
+
+int nvfp4_gemv_skinny(const uint16_t *x, int64_t N, const uint8_t *codes, const uint8_t *scales,
+                      const float *tensor_scale, int64_t M, int64_t K, void *y, int out_dtype, void *workspace,
+                      size_t workspace_bytes, nvfp4_stream_t stream)
+{
+    int rc = check_product(x, N, M, K, codes, scales, tensor_scale, y, out_dtype);
+    if (rc != NVFP4_OK)
+        return rc;
+    if (N < 1 || N > kMaxSkinnyN)
+        return N == 0 ? NVFP4_OK : NVFP4_ERR_UNSUPPORTED_SHAPE;
+    if (M == 0)
+        return NVFP4_OK;
+    rc = check_workspace(workspace, workspace_bytes, nvfp4_workspace_bytes(NVFP4_OP_GEMV_SKINNY, N, M, K));
+    if (rc != NVFP4_OK)
+        return rc;
+    if (K == 0)
+        return zero_output(y, N, M, out_dtype, (cudaStream_t)stream);
+    const uint8_t *c[1] = {codes};
+    const uint8_t *s[1] = {scales};
+    const float *t[1] = {tensor_scale};
+    return run_products(x, N, M, K, c, s, t, 1, y, out_dtype, workspace, (cudaStream_t)stream);
+}
+
+int nvfp4_gateup_swiglu(const uint16_t *x, int64_t N, const uint8_t *gate_codes, const uint8_t *gate_scales,
+                        const float *gate_tensor_scale, const uint8_t *up_codes, const uint8_t *up_scales,
+                        const float *up_tensor_scale, int64_t M, int64_t K, void *h, int out_dtype,
+                        void *workspace, size_t workspace_bytes, nvfp4_stream_t stream)
+{
+    int rc = check_product(x, N, M, K, gate_codes, gate_scales, gate_tensor_scale, h, out_dtype);
+    if (rc != NVFP4_OK)
+        return rc;
+    rc = check_product(x, N, M, K, up_codes, up_scales, up_tensor_scale, h, out_dtype);
+    if (rc != NVFP4_OK)
+        return rc;
+    if (N == 0 || M == 0)
+        return NVFP4_OK;
+    rc = check_workspace(workspace, workspace_bytes, nvfp4_workspace_bytes(NVFP4_OP_GATEUP_SWIGLU, N, M, K));
+    if (rc != NVFP4_OK)
+        return rc;
+    if (K == 0)  // g = u = 0 -> h = silu(0) * 0 = 0
+        return zero_output(h, N, M, out_dtype, (cudaStream_t)stream);
+    const uint8_t *c[2] = {gate_codes, up_codes};
+    const uint8_t *s[2] = {gate_scales, up_scales};
+    const float *t[2] = {gate_tensor_scale, up_tensor_scale};
+    return run_products(x, N, M, K, c, s, t, 2, h, out_dtype, workspace, (cudaStream_t)stream);
+}
+
+int nvfp4_gemm_prefill(const uint16_t *x, int64_t N, const uint8_t *codes, const uint8_t *scales,
+                       const float *tensor_scale, int64_t M, int64_t K, void *y, int out_dtype, void *workspace,
+                       size_t workspace_bytes, nvfp4_stream_t stream)
+{
+    int rc = check_product(x, N, M, K, codes, scales, tensor_scale, y, out_dtype);
+    if (rc != NVFP4_OK)
+        return rc;
+    if (N == 0 || M == 0)
+        return NVFP4_OK;
+    rc = check_workspace(workspace, workspace_bytes, nvfp4_workspace_bytes(NVFP4_OP_GEMM_PREFILL, N, M, K));
+    if (rc != NVFP4_OK)
+        return rc;
+    if (K == 0)
+        return zero_output(y, N, M, out_dtype, (cudaStream_t)stream);
+    const uint8_t *c[1] = {codes};
+    const uint8_t *s[1] = {scales};
+    const float *t[1] = {tensor_scale};
+    return run_products(x, N, M, K, c, s, t, 1, y, out_dtype, workspace, (cudaStream_t)stream);
+}
+
+}  // extern "C"

@@ -1,0 +1,174 @@
+/*
+ * nvfp4.h -- C ABI of libnvfp4.so: NVFP4 weights x bf16 activations on one GPU.
+ *
+ * The operation (bw24 README, section on the NVFP4 / Q4_0 decode path; bw24
+ * wiki Home, feature list, NVFP4 decode path entry; qwentin README, section
+ * "How it works", wide prefill and batched verify): a weight matrix W[M][K]
+ * stored as NVFP4 is multiplied by N token activations x[N][K] in bf16,
+ *
+ *     y[n][m] = sum_k x[n][k] * ts * e2m1(code[m][k]) * e4m3(scale[m][k/16]),
+ *
+ * with fp32 accumulation and fp32 (or bf16) output.  N = 1 is plain decode,
+ * N = draft+1 a speculative verify that reads every weight once for all draft
+ * tokens (bw24 README, speculative decoding section; qwentin README,
+ * "Highlights", batched verify), and N in the hundreds to thousands a prefill
+ * (qwentin README, "How it works", wide prefill where each weight is read once
+ * for N tokens).
+ *
+ * NVFP4 layout used by every call (one tensor = three device buffers):
+ *   codes        uint8 [M][K/2]  two 4-bit E2M1 codes per byte; element k = 2j
+ *                                in the low nibble of byte j, k = 2j+1 in the
+ *                                high nibble.  E2M1: bit 3 sign, bits 2..1
+ *                                exponent (bias 1), bit 0 mantissa; magnitudes
+ *                                0, .5, 1, 1.5, 2, 3, 4, 6.
+ *   scales       uint8 [M][K/16] one FP8 E4M3 (OCP E4M3FN) scale per 16
+ *                                consecutive k of a row, row-major.
+ *   tensor_scale float [1]       one FP32 scale for the whole tensor, kept in
+ *                                device memory so no call synchronises.
+ * K must be a multiple of 16.  Activations x are bf16 bit patterns, row-major
+ * [N][K]; outputs are row-major [N][M].
+ *
+ * Conventions for every entry point:
+ *   - Ownership: the caller allocates and owns every buffer; the library never
+ *     allocates or frees memory and keeps no pointer after a call returns.
+ *   - Pointers marked "device" must be CUDA device (or managed) memory of the
+ *     current device.  Codes, scales, x and outputs must be 16-byte aligned.
+ *   - Asynchrony: every call enqueues kernels on `stream` (NULL = legacy default
+ *     stream) and returns without synchronising.  Results are ready when the
+ *     stream reaches that point.
+ *   - Workspace: scratch device memory of at least nvfp4_workspace_bytes(...)
+ *     bytes, 256-byte aligned, owned by the caller and not used by anything
+ *     else while the call's kernels run.  Its contents need no initialisation
+ *     and are garbage afterwards.  Calls that share a workspace must be ordered
+ *     on one stream.
+ *   - Errors: arguments are checked on the host before anything is enqueued;
+ *     a bad argument returns a nonzero nvfp4_status and nothing runs.  A
+ *     failed launch returns NVFP4_ERR_CUDA.  The library never aborts or prints.
+ *   - Determinism: the reduction order is fixed by the shapes alone, so repeated
+ *     calls give bit-identical results, and row n of an N-token call equals the
+ *     same token in any other call with the same weights, M and K (floating-
+ *     point summation order is part of the contract: bw24 wiki Home, list of
+ *     checks every kernel change must pass, and bw24 README, where decode and
+ *     verify launch the same kernel symbols and agree bit for bit).
+ *   - Accuracy: every product code * scale * x is exact (bf16 operands, fp32
+ *     accumulation); results satisfy |y - y_ref| <= 1e-5 * sum_k |w*x| + 1e-7
+ *     against an fp64 evaluation of the formula above.
+ */
+#ifndef NVFP4_H
+#define NVFP4_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *nvfp4_stream_t; /* same handle as cudaStream_t */
+
+/* Status codes returned by every entry point. */
+typedef enum {
+    NVFP4_OK = 0,
+    NVFP4_ERR_INVALID_ARG = 1,       /* null pointer, negative size, misalignment, bad enum */
+    NVFP4_ERR_UNSUPPORTED_SHAPE = 2, /* K % 16 != 0, N outside the call's range, size overflow */
+    NVFP4_ERR_WORKSPACE = 3,         /* workspace smaller than nvfp4_workspace_bytes() */
+    NVFP4_ERR_CUDA = 4               /* a CUDA runtime call or kernel launch failed */
+} nvfp4_status;
+
+/* Operation ids for nvfp4_workspace_bytes. */
+typedef enum {
+    NVFP4_OP_QUANTIZE = 0,
+    NVFP4_OP_GEMV_SKINNY = 1,
+    NVFP4_OP_GATEUP_SWIGLU = 2,
+    NVFP4_OP_GEMM_PREFILL = 3
+} nvfp4_op;
+
+/* Output element types. */
+typedef enum { NVFP4_OUT_F32 = 0, NVFP4_OUT_BF16 = 1 } nvfp4_out_dtype;
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char *nvfp4_status_string(int status);
+
+/* Library version as MAJOR*10000 + MINOR*100 + PATCH. */
+int nvfp4_version(void);
+
+/* Bytes of workspace the call `op` needs for these sizes (0 if none).  Host
+ * only, no CUDA call; depends on (op, N, M, K) alone, not on the device.
+ * Returns 0 as well for sizes the call would reject. */
+size_t nvfp4_workspace_bytes(int op, int64_t N, int64_t M, int64_t K);
+
+/* Quantise fp32 weights to NVFP4.
+ * The recipe (fp32 arithmetic in this order, IEEE round-to-nearest-even):
+ *   amax = max |w|;  ts = amax / 2688  (2688 = 6 * 448, the largest E2M1 value
+ *   times the largest E4M3 value);  for every 16-element block of a row:
+ *   scale = E4M3_rne_saturating((block_amax / 6) / ts);  d = e4m3(scale) * ts;
+ *   code[k] = nearest E2M1 to w[k] / d (ties to the even code, |.| > 6 clamps
+ *   to 6, the sign of w kept, so a small negative value gives 0x8).  A block
+ *   with d == 0 (scale 0, or ts == 0) gets all-zero codes.
+ * w            device fp32 [M][K], row-major, finite (non-finite weights give
+ *              unspecified codes).
+ * codes        device uint8 [M][K/2] (output)
+ * scales       device uint8 [M][K/16] (output)
+ * tensor_scale device float [1] (output)
+ * workspace    device scratch of nvfp4_workspace_bytes(NVFP4_OP_QUANTIZE, 0, M, K).
+ * The NVFP4 weights the pages use are produced this way at load time (bw24
+ * README, safetensors loader, re-encoding to NVFP4 at load; qwentin README,
+ * converter section, quantising and packing on the GPU through the C ABI). */
+int nvfp4_quantize(const float *w, int64_t M, int64_t K,
+                   uint8_t *codes, uint8_t *scales, float *tensor_scale,
+                   void *workspace, size_t workspace_bytes, nvfp4_stream_t stream);
+
+/* Skinny product, N = 1..16 tokens: y[N][M] = x[N][K] . dequant(W)^T.
+ * Streams every code and scale byte from HBM once per call for all N tokens
+ * (the decode and batched-verify matvec of bw24 README, NVFP4 decode path, and
+ * qwentin README, batched verify reading each weight once for the tree).
+ * x        device bf16 bits [N][K]
+ * codes, scales, tensor_scale: the NVFP4 weight W[M][K] (device)
+ * y        device [N][M], fp32 (out_dtype NVFP4_OUT_F32) or bf16 bits
+ *          (NVFP4_OUT_BF16, round-to-nearest-even of the fp32 result)
+ * workspace device scratch of nvfp4_workspace_bytes(NVFP4_OP_GEMV_SKINNY, N, M, K)
+ *          (partial sums of rows whose K range is split across thread blocks).
+ * Returns NVFP4_ERR_UNSUPPORTED_SHAPE for N outside 1..16. */
+int nvfp4_gemv_skinny(const uint16_t *x, int64_t N,
+                      const uint8_t *codes, const uint8_t *scales,
+                      const float *tensor_scale, int64_t M, int64_t K,
+                      void *y, int out_dtype,
+                      void *workspace, size_t workspace_bytes, nvfp4_stream_t stream);
+
+/* Fused gate/up projection with SwiGLU, any N >= 1:
+ *   g = x . dequant(Wg)^T,  u = x . dequant(Wu)^T,  h = g / (1 + exp(-g)) * u,
+ * reading both weight matrices once and never writing g or u to memory (the
+ * persistent-MLP GEMV of qwentin README, section on SM120 kernels, fuses the
+ * MLP chain).  N <= 16 runs the skinny kernel; larger N runs the tensor-core
+ * prefill kernel with a SwiGLU epilogue.
+ * Wg and Wu are both [M][K] NVFP4 tensors (device buffers as above), each with
+ * its own tensor scale.  h is device [N][M] fp32 or bf16 bits.
+ * workspace: nvfp4_workspace_bytes(NVFP4_OP_GATEUP_SWIGLU, N, M, K). */
+int nvfp4_gateup_swiglu(const uint16_t *x, int64_t N,
+                        const uint8_t *gate_codes, const uint8_t *gate_scales,
+                        const float *gate_tensor_scale,
+                        const uint8_t *up_codes, const uint8_t *up_scales,
+                        const float *up_tensor_scale,
+                        int64_t M, int64_t K,
+                        void *h, int out_dtype,
+                        void *workspace, size_t workspace_bytes, nvfp4_stream_t stream);
+
+/* Prefill product for any N >= 1: y[N][M] = x[N][K] . dequant(W)^T on the
+ * tensor cores (weights dequantised exactly to bf16 in shared memory, bf16 x
+ * bf16 products accumulated in fp32): the wide GEMM of qwentin README, "How it
+ * works" (the weight read once for N tokens), and the prefill GEMM of bw24
+ * README, NVFP4 decode path.  N <= 16 is forwarded to the skinny kernel, so
+ * there is one entry point per operation for all N.
+ * Arguments as for nvfp4_gemv_skinny; workspace:
+ * nvfp4_workspace_bytes(NVFP4_OP_GEMM_PREFILL, N, M, K). */
+int nvfp4_gemm_prefill(const uint16_t *x, int64_t N,
+                       const uint8_t *codes, const uint8_t *scales,
+                       const float *tensor_scale, int64_t M, int64_t K,
+                       void *y, int out_dtype,
+                       void *workspace, size_t workspace_bytes, nvfp4_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* NVFP4_H */

@@ -1,0 +1,114 @@
+"""C-ABI library checks that need no GPU: it builds, loads, exports every
+symbol include/nvfp4.h declares, and rejects bad arguments on the host before
+any CUDA call (every case below returns before the library touches the device).
+"""
+from __future__ import annotations
+
+import ctypes
+
+import pytest
+
+import gemm_nvfp4_gb300 as g
+from gemm_nvfp4_gb300 import binding, build
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return g.load_library()
+
+
+def test_exports_every_declared_function(lib):
+    names = g.header_functions()
+    assert set(names) >= {"nvfp4_quantize", "nvfp4_gemv_skinny", "nvfp4_gateup_swiglu",
+                          "nvfp4_gemm_prefill", "nvfp4_workspace_bytes", "nvfp4_status_string"}
+    for name in names:
+        assert hasattr(lib, name), f"{name} declared in include/nvfp4.h but not exported"
+
+
+def test_python_binding_has_the_c_names():
+    for name in g.header_functions():
+        assert callable(getattr(g, name)), name
+
+
+def test_version_and_status_strings(lib):
+    assert g.nvfp4_version() >= 100
+    for st in range(5):
+        assert g.nvfp4_status_string(st).startswith("NVFP4_")
+    assert "unknown" in g.nvfp4_status_string(99)
+
+
+def test_workspace_bytes(lib):
+    assert g.nvfp4_workspace_bytes(g.NVFP4_OP_QUANTIZE, 0, 4096, 4096) > 0
+    assert g.nvfp4_workspace_bytes(g.NVFP4_OP_GEMV_SKINNY, 1, 4096, 4096) > 0
+    assert g.nvfp4_workspace_bytes(g.NVFP4_OP_GEMV_SKINNY, 17, 4096, 4096) == 0  # rejected N
+    assert g.nvfp4_workspace_bytes(g.NVFP4_OP_GEMV_SKINNY, 1, 4096, 4100) == 0   # K % 16
+    assert g.nvfp4_workspace_bytes(g.NVFP4_OP_GATEUP_SWIGLU, 16, 17408, 5120) >= \
+        g.nvfp4_workspace_bytes(g.NVFP4_OP_GEMV_SKINNY, 16, 17408, 5120)
+    assert g.nvfp4_workspace_bytes(99, 1, 16, 16) == 0
+    # independent of the device: same answer twice, no CUDA needed
+    a = g.nvfp4_workspace_bytes(g.NVFP4_OP_GEMM_PREFILL, 8192, 17408, 5120)
+    assert a == g.nvfp4_workspace_bytes(g.NVFP4_OP_GEMM_PREFILL, 8192, 17408, 5120)
+
+
+FAKE = 1 << 20  # an aligned address that is never dereferenced (the call fails first)
+
+
+def _P(v):
+    return ctypes.c_void_p(v)
+
+
+def test_gemv_rejects_bad_arguments(lib):
+    ws = g.nvfp4_workspace_bytes(g.NVFP4_OP_GEMV_SKINNY, 4, 64, 64)
+    call = lambda **kw: lib.nvfp4_gemv_skinny(
+        _P(kw.get("x", FAKE)), kw.get("N", 4), _P(kw.get("codes", FAKE)), _P(kw.get("scales", FAKE)),
+        _P(kw.get("ts", FAKE)), kw.get("M", 64), kw.get("K", 64), _P(kw.get("y", FAKE)),
+        kw.get("dt", 0), _P(kw.get("ws", FAKE)), kw.get("wsb", ws), None)
+    assert call(K=72) == binding.NVFP4_ERR_UNSUPPORTED_SHAPE
+    assert call(N=17) == binding.NVFP4_ERR_UNSUPPORTED_SHAPE
+    assert call(N=-1) == binding.NVFP4_ERR_INVALID_ARG
+    assert call(M=-5) == binding.NVFP4_ERR_INVALID_ARG
+    assert call(x=0) == binding.NVFP4_ERR_INVALID_ARG
+    assert call(codes=0) == binding.NVFP4_ERR_INVALID_ARG
+    assert call(scales=0) == binding.NVFP4_ERR_INVALID_ARG
+    assert call(ts=0) == binding.NVFP4_ERR_INVALID_ARG
+    assert call(y=0) == binding.NVFP4_ERR_INVALID_ARG
+    assert call(x=FAKE + 2) == binding.NVFP4_ERR_INVALID_ARG      # x not 16-byte aligned
+    assert call(codes=FAKE + 8) == binding.NVFP4_ERR_INVALID_ARG  # codes not 16-byte aligned
+    assert call(dt=7) == binding.NVFP4_ERR_INVALID_ARG
+    assert call(wsb=ws - 1) == binding.NVFP4_ERR_WORKSPACE
+    assert call(ws=0) == binding.NVFP4_ERR_INVALID_ARG
+    # empty problems are no-ops that touch nothing
+    assert call(N=0, x=0, y=0) == binding.NVFP4_OK
+    assert call(M=0, codes=0, scales=0, ts=0, y=0) == binding.NVFP4_OK
+
+
+def test_gateup_and_prefill_reject_bad_arguments(lib):
+    ws = g.nvfp4_workspace_bytes(g.NVFP4_OP_GATEUP_SWIGLU, 4, 64, 64)
+    st = lib.nvfp4_gateup_swiglu(_P(FAKE), 4, _P(FAKE), _P(FAKE), _P(FAKE), _P(0), _P(FAKE), _P(FAKE),
+                                 64, 64, _P(FAKE), 0, _P(FAKE), ws, None)
+    assert st == binding.NVFP4_ERR_INVALID_ARG  # null up codes
+    st = lib.nvfp4_gateup_swiglu(_P(FAKE), 4, _P(FAKE), _P(FAKE), _P(FAKE), _P(FAKE), _P(FAKE), _P(FAKE),
+                                 64, 64, _P(FAKE), 0, _P(FAKE), ws - 1, None)
+    assert st == binding.NVFP4_ERR_WORKSPACE
+    ws = g.nvfp4_workspace_bytes(g.NVFP4_OP_GEMM_PREFILL, 600, 64, 64)
+    st = lib.nvfp4_gemm_prefill(_P(FAKE), 600, _P(FAKE), _P(FAKE), _P(FAKE), 64, 40, _P(FAKE), 0,
+                                _P(FAKE), ws, None)
+    assert st == binding.NVFP4_ERR_UNSUPPORTED_SHAPE
+    if ws > 0:
+        st = lib.nvfp4_gemm_prefill(_P(FAKE), 600, _P(FAKE), _P(FAKE), _P(FAKE), 64, 64, _P(FAKE), 1,
+                                    _P(FAKE), ws - 1, None)
+        assert st == binding.NVFP4_ERR_WORKSPACE
+
+
+def test_quantize_rejects_bad_arguments(lib):
+    ws = g.nvfp4_workspace_bytes(g.NVFP4_OP_QUANTIZE, 0, 64, 64)
+    q = lambda **kw: lib.nvfp4_quantize(_P(kw.get("w", FAKE)), kw.get("M", 64), kw.get("K", 64),
+                                        _P(kw.get("c", FAKE)), _P(kw.get("s", FAKE)), _P(kw.get("ts", FAKE)),
+                                        _P(kw.get("ws", FAKE)), kw.get("wsb", ws), None)
+    assert q(K=40) == binding.NVFP4_ERR_UNSUPPORTED_SHAPE
+    assert q(M=-1) == binding.NVFP4_ERR_INVALID_ARG
+    assert q(w=0) == binding.NVFP4_ERR_INVALID_ARG
+    assert q(w=FAKE + 4) == binding.NVFP4_ERR_INVALID_ARG
+    assert q(ts=0) == binding.NVFP4_ERR_INVALID_ARG
+    assert q(wsb=ws - 4) == binding.NVFP4_ERR_WORKSPACE

@@ -1,0 +1,128 @@
+"""Skinny product (N = 1..16) through the C ABI vs the oracle."""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import gemm_nvfp4_gb300 as g
+import oracle
+from gemm_nvfp4_gb300 import inputs
+from helpers import DEV, assert_close, bf16_bits, gemv_tol, to_np
+
+pytestmark = pytest.mark.gpu
+
+
+def make_case(M, K, N, seed=0, heavy=False, outliers=False):
+    w = inputs.weights(M, K, seed=seed, heavy_tail=heavy)
+    x = inputs.activations(N, K, seed=seed + 1, outlier_rows=outliers)
+    W = g.nvfp4_quantize(w.to(DEV))
+    ref_w = oracle.quantize(w.numpy())
+    return W, ref_w, x
+
+
+def check(W, ref_w, x, out_dtype=torch.float32, rows=None, what=""):
+    y = g.nvfp4_gemv_skinny(x.to(DEV), W, out_dtype=out_dtype)
+    torch.cuda.synchronize()
+    y_ref, A = oracle.gemv(bf16_bits(x), *ref_w, rows=rows)
+    got = to_np(y) if rows is None else to_np(y[:, torch.as_tensor(rows)])
+    assert_close(got, y_ref, gemv_tol(y_ref, A, out_dtype), what)
+    return y
+
+
+def test_single_matrix_4096_n1():
+    W, ref, x = make_case(4096, 4096, 1)
+    check(W, ref, x, what="4096x4096 N=1")
+
+
+@pytest.mark.parametrize("N", [1, 2, 3, 4, 7, 8, 9, 12, 16])
+@pytest.mark.parametrize("M,K", [(16, 128), (48, 272), (100, 1024), (333, 4112), (1000, 2048)])
+def test_shapes_and_token_counts(M, K, N):
+    W, ref, x = make_case(M, K, N, seed=M * 7 + K)
+    check(W, ref, x, what=f"M={M} K={K} N={N}")
+
+
+@pytest.mark.parametrize("K", [16, 32, 48, 112, 144])
+def test_short_k(K):
+    W, ref, x = make_case(40, K, 5, seed=K)
+    check(W, ref, x, what=f"K={K}")
+
+
+def test_outliers_and_heavy_tail():
+    W, ref, x = make_case(512, 5120, 16, seed=300, heavy=True, outliers=True)
+    check(W, ref, x, what="heavy tail + outlier rows")
+
+
+def test_bf16_output():
+    W, ref, x = make_case(300, 2048, 4, seed=11)
+    check(W, ref, x, out_dtype=torch.bfloat16, what="bf16 out")
+
+
+def test_cross_n_identity_and_determinism():
+    """Token n of an N-token call equals the same token alone, bit for bit, and
+    repeated calls are bit-identical (fixed reduction order)."""
+    W, ref, x = make_case(1000, 5120, 16, seed=21)
+    xd = x.to(DEV)
+    y16 = g.nvfp4_gemv_skinny(xd, W)
+    y16b = g.nvfp4_gemv_skinny(xd, W)
+    singles = [g.nvfp4_gemv_skinny(xd[n:n + 1].contiguous(), W) for n in range(16)]
+    y4 = g.nvfp4_gemv_skinny(xd[4:8].contiguous(), W)
+    torch.cuda.synchronize()
+    assert torch.equal(y16, y16b)
+    for n in range(16):
+        assert torch.equal(y16[n], singles[n][0]), n
+    assert torch.equal(y16[4:8], y4)
+
+
+def test_k_zero_gives_zeros_and_empty_calls():
+    W = g.NVFP4Weight(torch.empty(8, 0, dtype=torch.uint8, device=DEV),
+                      torch.empty(8, 0, dtype=torch.uint8, device=DEV),
+                      torch.ones(1, device=DEV))
+    x = torch.empty(3, 0, dtype=torch.bfloat16, device=DEV)
+    y = torch.full((3, 8), 7.0, device=DEV)
+    g.nvfp4_gemv_skinny(x, W, out=y)
+    torch.cuda.synchronize()
+    assert (y == 0).all()
+
+
+def test_n_out_of_range_raises():
+    W, _, x = make_case(32, 64, 17)
+    with pytest.raises(g.NVFP4Error) as e:
+        g.nvfp4_gemv_skinny(x.to(DEV), W)
+    assert e.value.status == 2
+
+
+@pytest.mark.parametrize("name", ["qkv", "o", "gate", "down"])
+@pytest.mark.parametrize("N", [1, 4])
+def test_27b_layer_shapes_sampled(name, N):
+    """Full 27B-class layer shapes, device-generated weights, sampled rows."""
+    M, K = inputs.LAYER_27B.shapes()[name]
+    seed = inputs.matrix_seed(name)
+    w = inputs.weights(M, K, seed=seed, device=DEV)
+    x = inputs.activations(N, K, seed=seed + 1, device=DEV)
+    W = g.nvfp4_quantize(w)
+    y = g.nvfp4_gemv_skinny(x, W)
+    torch.cuda.synchronize()
+    ref_w = oracle.quantize(w.cpu().numpy())
+    assert np.array_equal(W.codes.cpu().numpy(), ref_w[0])
+    assert np.array_equal(W.scales.cpu().numpy(), ref_w[1])
+    rng = np.random.default_rng(seed)
+    rows = np.unique(np.concatenate([rng.integers(0, M, 48), [0, 15, 16, M - 17, M - 1]]))
+    y_ref, A = oracle.gemv(bf16_bits(x), *ref_w, rows=rows)
+    assert_close(to_np(y)[:, rows], y_ref, gemv_tol(y_ref, A), f"{name} N={N}")
+
+
+@pytest.mark.parametrize("N", [9, 16])
+def test_27b_deep_verify_sampled(N):
+    """The deep-verify workload: heavy-tailed weights and x8 outlier token rows."""
+    M, K = inputs.LAYER_27B.shapes()["down"]
+    w = inputs.weights(M, K, seed=400, heavy_tail=True, device=DEV)
+    x = inputs.activations(N, K, seed=401, outlier_rows=True, device=DEV)
+    W = g.nvfp4_quantize(w)
+    y = g.nvfp4_gemv_skinny(x, W)
+    torch.cuda.synchronize()
+    ref_w = oracle.quantize(w.cpu().numpy())
+    assert np.array_equal(W.codes.cpu().numpy(), ref_w[0])
+    rows = np.unique(np.random.default_rng(N).integers(0, M, 40))
+    y_ref, A = oracle.gemv(bf16_bits(x), *ref_w, rows=rows)
+    assert_close(to_np(y)[:, rows], y_ref, gemv_tol(y_ref, A), f"deep verify N={N}")
