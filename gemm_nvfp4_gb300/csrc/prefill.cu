@@ -1,31 +1,398 @@
-// prefill.cu -- products for N > 16 tokens (prefill).
+// prefill.cu -- NVFP4 x bf16 products for N > 16 tokens on the 5th-generation
+// tensor cores (tcgen05), with an optional SwiGLU epilogue for the gate/up pair.
+//
+// The prefill of both engines on the pages multiplies each weight by many
+// tokens at once: qwentin README, "How it works" (a wide GEMM reading every
+// weight once for N tokens); bw24 README, NVFP4 decode path (a tensor-core GEMM
+// for prefill).  Their kernels target consumer Blackwell (mma.sync, int8 or FP6
+// block-scale); this one is written for sm_103a:
+//
+//   CTA tile: 128 weight rows (MMA M) x 256 tokens (MMA N), K in stages of 64.
+//   warp 0      TMA producer: x tile [256 tokens][64 k] bf16, 128-byte swizzle.
+//   warp 1      allocates TMEM; one thread issues tcgen05.mma (bf16 x bf16 ->
+//               fp32, A and B from shared memory) and commits to mbarriers.
+//   warps 2..9  dequantise: each thread turns 32 k of one weight row (16 code
+//               bytes, 2 scale bytes, read straight from global memory with a
+//               register prefetch ring) into exact bf16 values
+//               e2m1 * scale * 2^-8 and stores them in the 128-byte-swizzled
+//               K-major layout the MMA reads; then, after the K loop, they read
+//               the fp32 accumulator out of TMEM (tcgen05.ld) and store
+//               y = acc * 2^8 * ts, or h = silu(g) * u for the gate/up pair.
+//
+// Exactness: every product e2m1 * scale * x is exact in the fp32 accumulator
+// (bf16 operands with at most 6 and 8 significant bits).  The accumulation
+// order is fixed by the shapes, so results are deterministic.
+//
+// Every mbarrier wait is bounded (2 s of wall time): on a timeout the kernel
+// sets word 0 of the workspace to a nonzero code and every role leaves its
+// loop, so the kernel ends instead of hanging.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include <algorithm>
+#include <mutex>
 
 #include "common.cuh"
 #include "kernels.h"
+#include "tcgen05.cuh"
 
 namespace nvfp4 {
+namespace pf {
+
+constexpr int BM = 128;
+constexpr int BN = 256;
+constexpr int BK = 64;
+constexpr int kDqWarps = 8;
+constexpr int kThreads = 64 + kDqWarps * 32;
+constexpr int kABytes = BM * BK * 2;  // 16 KB per weight matrix per stage
+constexpr int kBBytes = BN * BK * 2;  // 32 KB per stage
+constexpr int kDqThreads = kDqWarps * 32;
+
+template <int NW>
+struct Cfg {
+    static constexpr int kStages = NW == 1 ? 4 : 3;
+    static constexpr int kPf = NW == 1 ? 4 : 3;          // dequant register prefetch depth (stages)
+    static constexpr uint32_t kTmemCols = NW == 1 ? 256 : 512;
+    static constexpr size_t kSmemBytes =
+        (size_t)kStages * (NW * kABytes + kBBytes) + 1024 /* barriers */ + 1024 /* alignment */;
+};
+
+struct Args {
+    const uint8_t *codes[2];
+    const uint8_t *scales[2];
+    const float *ts[2];
+    void *y;
+    int out_bf16;
+    int64_t N, M, K;
+    int num_kb;
+    uint32_t *err;
+};
+
+// Exact bf16 dequantisation of one 32-bit code word (k = 8q .. 8q+7) into
+// four bf16x2 words in natural k order, each value e2m1 * scale * 2^-8.
+NVFP4_DEVINL uint4 dequant_word_natural(uint32_t w, uint32_t mult)
+{
+    constexpr uint32_t kMag = 0x01C001C0u;
+    const uint32_t te = w & 0x08080808u;
+    const uint32_t to = w & 0x80808080u;
+    const uint32_t p0 = bf16x2_mul(((w << 6) & kMag) | ((te << 12) & ~kMag), mult);  // k0, k4
+    const uint32_t p1 = bf16x2_mul(((w << 2) & kMag) | ((to << 8) & ~kMag), mult);   // k1, k5
+    const uint32_t p2 = bf16x2_mul(((w >> 2) & kMag) | ((te << 4) & ~kMag), mult);   // k2, k6
+    const uint32_t p3 = bf16x2_mul(((w >> 6) & kMag) | (to & ~kMag), mult);          // k3, k7
+    return make_uint4(prmt(p0, p1, 0x5410),   // k0, k1
+                      prmt(p2, p3, 0x5410),   // k2, k3
+                      prmt(p0, p1, 0x7632),   // k4, k5
+                      prmt(p2, p3, 0x7632));  // k6, k7
+}
+
+NVFP4_DEVINL uint32_t scale_mult_bf16(uint32_t byte)
+{
+    return f32_to_bf16x2_bcast(__fmul_rn(e4m3_to_f32(byte & 0xFF), 0x1p118f));
+}
+
+struct DqItem {
+    uint4 code;   // 16 code bytes = 32 k of one row
+    uint32_t scl; // 2 scale bytes
+};
+
+template <bool ALIGNED>
+NVFP4_DEVINL DqItem dq_load(const Args &a, int mi, int64_t m, int kb, int half)
+{
+    DqItem it{make_uint4(0, 0, 0, 0), 0};
+    const int64_t k0 = (int64_t)kb * BK + half * 32;
+    const int64_t rem = a.K - k0;
+    if (m >= a.M || rem <= 0)
+        return it;
+    const uint8_t *cp = a.codes[mi] + m * (a.K >> 1) + (k0 >> 1);
+    const uint8_t *sp = a.scales[mi] + m * (a.K >> 4) + (k0 >> 4);
+    if (rem >= 32) {
+        if (ALIGNED) {
+            it.code = ldg_stream_v4(cp);
+            it.scl = __ldg(reinterpret_cast<const uint16_t *>(sp));
+        } else {
+            const uint2 lo = ldg_stream_v2(cp), hi = ldg_stream_v2(cp + 8);
+            it.code = make_uint4(lo.x, lo.y, hi.x, hi.y);
+            it.scl = (uint32_t)__ldg(sp) | ((uint32_t)__ldg(sp + 1) << 8);
+        }
+    } else {  // 16 valid k
+        const uint2 lo = ldg_stream_v2(cp);
+        it.code = make_uint4(lo.x, lo.y, 0, 0);
+        it.scl = __ldg(sp);
+    }
+    return it;
+}
+
+NVFP4_DEVINL void fail(const Args &a, uint32_t code)
+{
+    atomicExch(a.err, code);
+}
+
+template <int NW, bool ALIGNED>
+__global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_constant__ CUtensorMap tmap_x, Args a)
+{
+    using C = Cfg<NW>;
+    constexpr int S = C::kStages;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t *sa = smem;                                  // [S][NW][kABytes]
+    uint8_t *sb = smem + (size_t)S * NW * kABytes;       // [S][kBBytes]
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sb + (size_t)S * kBBytes);
+    uint64_t *full_a = bars, *full_b = bars + S, *empty = bars + 2 * S, *tmem_full = bars + 3 * S;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 3 * S + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t m0 = (int64_t)blockIdx.x * BM;
+    const int n0 = blockIdx.y * BN;
+    const int num_kb = a.num_kb;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            tc::mbar_init(&full_a[s], kDqThreads);
+            tc::mbar_init(&full_b[s], 1);
+            tc::mbar_init(&empty[s], 1);
+        }
+        tc::mbar_init(tmem_full, 1);
+        tc::fence_mbar_init();
+        tc::prefetch_tensormap(&tmap_x);
+        if (blockIdx.x == 0 && blockIdx.y == 0 && *a.err != 0)
+            *a.err = 0;
+    }
+    if (warp == 1)
+        tc::tmem_alloc(tmem_slot, C::kTmemCols);
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem_base = *tmem_slot;
+
+    if (warp == 0) {
+        // ---------------- TMA producer (x tiles) ----------------
+        if (lane == 0) {
+            for (int kb = 0; kb < num_kb; ++kb) {
+                const int s = kb % S;
+                const uint32_t ph = (kb / S) & 1;
+                if (!tc::mbar_wait(&empty[s], ph ^ 1)) {
+                    fail(a, 1);
+                    break;
+                }
+                tc::mbar_arrive_expect_tx(&full_b[s], kBBytes);
+                tc::tma_load_2d(sb + (size_t)s * kBBytes, &tmap_x, &full_b[s], kb * BK, n0);
+            }
+        }
+    } else if (warp == 1) {
+        // ---------------- MMA issuer ----------------
+        if (lane == 0) {
+            constexpr uint32_t idesc = tc::idesc_bf16(BM, BN);
+            bool ok = true;
+            for (int kb = 0; kb < num_kb && ok; ++kb) {
+                const int s = kb % S;
+                const uint32_t ph = (kb / S) & 1;
+                if (!tc::mbar_wait(&full_a[s], ph) || !tc::mbar_wait(&full_b[s], ph)) {
+                    fail(a, 2);
+                    ok = false;
+                    break;
+                }
+                tc::fence_after_sync();
+                const uint64_t bdesc = tc::smem_desc_sw128(sb + (size_t)s * kBBytes);
+#pragma unroll
+                for (int mi = 0; mi < NW; ++mi) {
+                    const uint64_t adesc = tc::smem_desc_sw128(sa + ((size_t)s * NW + mi) * kABytes);
+#pragma unroll
+                    for (int k = 0; k < BK / 16; ++k)
+                        tc::mma_bf16_ss(tmem_base + mi * BN, adesc + 2 * k, bdesc + 2 * k, idesc,
+                                        (kb > 0 || k > 0) ? 1u : 0u);
+                }
+                tc::mma_commit(&empty[s]);
+            }
+            tc::mma_commit(tmem_full);
+        }
+    } else {
+        // ---------------- dequantise producers ----------------
+        const int dq = threadIdx.x - 64;           // 0..255
+        const int row = dq & (BM - 1);             // 0..127
+        const int half = dq >> 7;                  // which 32 k of the 64-k stage
+        const int64_t m = m0 + row;
+        DqItem ring[C::kPf][NW];
+#pragma unroll
+        for (int p = 0; p < C::kPf; ++p)
+#pragma unroll
+            for (int mi = 0; mi < NW; ++mi)
+                ring[p][mi] = p < num_kb ? dq_load<ALIGNED>(a, mi, m, p, half) : DqItem{make_uint4(0, 0, 0, 0), 0};
+        bool ok = true;
+        for (int kb0 = 0; kb0 < num_kb && ok; kb0 += C::kPf) {
+#pragma unroll
+            for (int p = 0; p < C::kPf; ++p) {
+                const int kb = kb0 + p;
+                if (kb >= num_kb || !ok)
+                    break;
+                DqItem cur[NW];
+#pragma unroll
+                for (int mi = 0; mi < NW; ++mi) {
+                    cur[mi] = ring[p][mi];
+                    if (kb + C::kPf < num_kb)
+                        ring[p][mi] = dq_load<ALIGNED>(a, mi, m, kb + C::kPf, half);
+                }
+                const int s = kb % S;
+                const uint32_t ph = (kb / S) & 1;
+                if (!tc::mbar_wait(&empty[s], ph ^ 1)) {
+                    fail(a, 3);
+                    ok = false;
+                    break;
+                }
+#pragma unroll
+                for (int mi = 0; mi < NW; ++mi) {
+                    uint8_t *arow = sa + ((size_t)s * NW + mi) * kABytes + row * 128;
+                    const uint32_t mlo = scale_mult_bf16(cur[mi].scl);
+                    const uint32_t mhi = scale_mult_bf16(cur[mi].scl >> 8);
+                    const uint32_t words[4] = {cur[mi].code.x, cur[mi].code.y, cur[mi].code.z, cur[mi].code.w};
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const uint4 v = dequant_word_natural(words[q], q < 2 ? mlo : mhi);
+                        const int chunk = half * 4 + q;
+                        *reinterpret_cast<uint4 *>(arow + ((chunk ^ (row & 7)) << 4)) = v;
+                    }
+                }
+                tc::fence_proxy_async_smem();
+                tc::mbar_arrive(&full_a[s]);
+            }
+        }
+
+        // ---------------- epilogue: TMEM -> registers -> global ----------------
+        const bool have = tc::mbar_wait(tmem_full, 0);
+        if (!have)
+            fail(a, 4);
+        tc::fence_after_sync();
+        if (have) {
+            const int quarter = warp & 3;          // TMEM lanes this warp may access
+            const int chalf = (warp - 2) >> 2;     // which 128 of the 256 token columns
+            const int64_t mrow = m0 + quarter * 32 + lane;
+            float ts[NW];
+#pragma unroll
+            for (int mi = 0; mi < NW; ++mi)
+                ts[mi] = __ldg(a.ts[mi]) * 256.0f;
+#pragma unroll 1
+            for (int cc = 0; cc < 4; ++cc) {
+                const int col = chalf * 128 + cc * 32;
+                const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + col;
+                uint32_t r[NW][32];
+                tc::tmem_ld_32x32b_x32(taddr, r[0]);
+                if (NW == 2)
+                    tc::tmem_ld_32x32b_x32(taddr + BN, r[NW - 1]);
+                tc::tmem_ld_wait();
+                if (mrow < a.M) {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        const int64_t n = (int64_t)n0 + col + j;
+                        if (n < a.N) {
+                            float v;
+                            if (NW == 1) {
+                                v = __uint_as_float(r[0][j]) * ts[0];
+                            } else {
+                                const float gg = __uint_as_float(r[0][j]) * ts[0];
+                                const float uu = __uint_as_float(r[NW - 1][j]) * ts[NW - 1];
+                                v = __fdiv_rn(gg, 1.0f + expf(-gg)) * uu;
+                            }
+                            const int64_t idx = n * a.M + mrow;
+                            if (a.out_bf16)
+                                reinterpret_cast<uint16_t *>(a.y)[idx] = f32_to_bf16(v);
+                            else
+                                reinterpret_cast<float *>(a.y)[idx] = v;
+                        }
+                    }
+                }
+            }
+        }
+    }
+
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 1) {
+        tc::fence_after_sync();
+        tc::tmem_dealloc(tmem_base, C::kTmemCols);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+template <int NW, bool ALIGNED>
+cudaError_t launch_t(const CUtensorMap &map, const Args &a, cudaStream_t stream)
+{
+    using C = Cfg<NW>;
+    static std::once_flag once;
+    static cudaError_t attr_err = cudaSuccess;
+    std::call_once(once, [] {
+        attr_err = cudaFuncSetAttribute(prefill_kernel<NW, ALIGNED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        (int)C::kSmemBytes);
+    });
+    if (attr_err != cudaSuccess)
+        return attr_err;
+    dim3 grid((unsigned)((a.M + BM - 1) / BM), (unsigned)((a.N + BN - 1) / BN));
+    prefill_kernel<NW, ALIGNED><<<grid, kThreads, C::kSmemBytes, stream>>>(map, a);
+    return cudaGetLastError();
+}
+
+}  // namespace pf
 
 size_t prefill_workspace_bytes(int64_t N, int64_t M, int64_t K, int n_weights)
 {
-    (void)N; (void)M; (void)K;
-    return (size_t)kGemvMaxCtas * kGemvPartialFloatsPerCta * n_weights * 4;
+    (void)N; (void)M; (void)K; (void)n_weights;
+    return 256;  // word 0: pipeline-timeout flag
 }
 
-// Interim: 16-token slices through the skinny kernel.
 cudaError_t launch_prefill(const uint16_t *x, int64_t N, int64_t M, int64_t K, const uint8_t *const *codes,
                            const uint8_t *const *scales, const float *const *ts, int n_weights, void *y,
                            int out_bf16, void *workspace, int num_sms, cudaStream_t stream)
 {
-    const size_t esize = out_bf16 ? 2 : 4;
-    for (int64_t n0 = 0; n0 < N; n0 += 16) {
-        const int n = (int)std::min<int64_t>(16, N - n0);
-        cudaError_t e = launch_gemv(x + n0 * K, n, M, K, codes, scales, ts, n_weights,
-                                    static_cast<char *>(y) + n0 * M * esize, out_bf16, workspace, num_sms, stream);
-        if (e != cudaSuccess)
-            return e;
+    (void)num_sms;
+    auto encode = pf::encode_fn();
+    if (!encode)
+        return cudaErrorNotSupported;
+    if (N > 65535LL * pf::BN || (M + pf::BM - 1) / pf::BM > 0x7FFFFFFF)
+        return cudaErrorInvalidValue;
+    CUtensorMap map;
+    const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)N};
+    const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
+    const cuuint32_t box[2] = {pf::BK, pf::BN};
+    const cuuint32_t estr[2] = {1, 1};
+    CUresult r = encode(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t *>(x), dims, strides, box,
+                        estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
+    pf::Args a{};
+    for (int i = 0; i < 2; ++i) {
+        const int s = i < n_weights ? i : 0;
+        a.codes[i] = codes[s];
+        a.scales[i] = scales[s];
+        a.ts[i] = ts[s];
     }
-    return cudaSuccess;
+    a.y = y;
+    a.out_bf16 = out_bf16;
+    a.N = N;
+    a.M = M;
+    a.K = K;
+    a.num_kb = (int)((K + pf::BK - 1) / pf::BK);
+    a.err = reinterpret_cast<uint32_t *>(workspace);
+    const bool aligned = K % 32 == 0;
+    if (n_weights == 1)
+        return aligned ? pf::launch_t<1, true>(map, a, stream) : pf::launch_t<1, false>(map, a, stream);
+    return aligned ? pf::launch_t<2, true>(map, a, stream) : pf::launch_t<2, false>(map, a, stream);
 }
 
 }  // namespace nvfp4

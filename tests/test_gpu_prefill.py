@@ -1,4 +1,4 @@
-"""Prefill product (N > 16) through the C ABI vs the oracle."""
+"""Prefill product (N > 16, tcgen05 tensor cores) through the C ABI vs the oracle."""
 from __future__ import annotations
 
 import numpy as np
@@ -13,14 +13,28 @@ from helpers import DEV, assert_close, bf16_bits, gemv_tol, swiglu_tol, to_np
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("N,M,K", [(17, 48, 272), (40, 130, 512), (200, 256, 1024), (300, 500, 2064)])
+def workspace(op, N, M, K):
+    n = g.nvfp4_workspace_bytes(op, N, M, K)
+    ws = torch.full((max(n, 16),), 0xAB, dtype=torch.uint8, device=DEV)
+    return ws
+
+
+def timeout_flag(ws):
+    """Word 0 of the prefill workspace: nonzero if a pipeline wait gave up."""
+    return int(ws[:4].view(torch.int32).item())
+
+
+@pytest.mark.parametrize("N,M,K", [(17, 48, 272), (40, 130, 512), (256, 128, 64), (257, 256, 1024),
+                                   (300, 500, 2064), (600, 384, 4096)])
 @pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
 def test_prefill_small(N, M, K, out_dtype):
     w = inputs.weights(M, K, seed=N + M)
     x = inputs.activations(N, K, seed=N + K)
     W = g.nvfp4_quantize(w.to(DEV))
-    y = g.nvfp4_gemm_prefill(x.to(DEV), W, out_dtype=out_dtype)
+    ws = workspace(g.NVFP4_OP_GEMM_PREFILL, N, M, K)
+    y = g.nvfp4_gemm_prefill(x.to(DEV), W, out_dtype=out_dtype, workspace=ws)
     torch.cuda.synchronize()
+    assert timeout_flag(ws) == 0
     ref_w = oracle.quantize(w.numpy())
     y_ref, A = oracle.gemv(bf16_bits(x), *ref_w)
     assert_close(to_np(y), y_ref, gemv_tol(y_ref, A, out_dtype), f"prefill N={N} M={M} K={K}")
@@ -42,8 +56,10 @@ def test_gateup_prefill_small(N):
     wg, wu = inputs.weights(M, K, seed=7), inputs.weights(M, K, seed=8)
     x = inputs.activations(N, K, seed=9)
     Wg, Wu = g.nvfp4_quantize(wg.to(DEV)), g.nvfp4_quantize(wu.to(DEV))
-    h = g.nvfp4_gateup_swiglu(x.to(DEV), Wg, Wu)
+    ws = workspace(g.NVFP4_OP_GATEUP_SWIGLU, N, M, K)
+    h = g.nvfp4_gateup_swiglu(x.to(DEV), Wg, Wu, workspace=ws)
     torch.cuda.synchronize()
+    assert timeout_flag(ws) == 0
     h_ref, g_ref, u_ref, Ag, Au = oracle.swiglu(bf16_bits(x), oracle.quantize(wg.numpy()),
                                                 oracle.quantize(wu.numpy()))
     assert_close(to_np(h), h_ref, swiglu_tol(h_ref, g_ref, u_ref, Ag, Au), f"gate/up prefill N={N}")
@@ -56,3 +72,47 @@ def test_prefill_deterministic():
     a, b = g.nvfp4_gemm_prefill(x, W), g.nvfp4_gemm_prefill(x, W)
     torch.cuda.synchronize()
     assert torch.equal(a, b)
+
+
+def _sample(n, total, seed, edges):
+    rng = np.random.default_rng(seed)
+    return np.unique(np.concatenate([rng.integers(0, total, n), edges]))
+
+
+@pytest.mark.parametrize("N", [512, 2048])
+def test_prefill_gateup_full_size_sampled(N):
+    """Full-size prefill gate/up (5120 -> 17408 each, SwiGLU), sampled outputs."""
+    M, K = inputs.LAYER_27B.shapes()["gate"]
+    wg = inputs.weights(M, K, seed=200, device=DEV)
+    wu = inputs.weights(M, K, seed=300, device=DEV)
+    x = inputs.activations(N, K, seed=201, device=DEV)
+    Wg, Wu = g.nvfp4_quantize(wg), g.nvfp4_quantize(wu)
+    ws = workspace(g.NVFP4_OP_GATEUP_SWIGLU, N, M, K)
+    h = g.nvfp4_gateup_swiglu(x, Wg, Wu, workspace=ws)
+    torch.cuda.synchronize()
+    assert timeout_flag(ws) == 0
+    gref, uref = oracle.quantize(wg.cpu().numpy()), oracle.quantize(wu.cpu().numpy())
+    rows = _sample(24, M, N, [0, 127, 128, M - 1])
+    toks = _sample(6, N, N + 1, [0, 255, 256, N - 1])
+    h_ref, g_ref, u_ref, Ag, Au = oracle.swiglu(bf16_bits(x), gref, uref, rows=rows, tokens=toks)
+    got = to_np(h)[np.ix_(toks, rows)]
+    assert_close(got, h_ref, swiglu_tol(h_ref, g_ref, u_ref, Ag, Au), f"gate/up prefill N={N}")
+
+
+@pytest.mark.parametrize("N", [512, 8192])
+def test_prefill_down_full_size_sampled(N):
+    """Full-size prefill down projection (17408 -> 5120), fresh bf16 inputs."""
+    M, K = inputs.LAYER_27B.shapes()["down"]
+    w = inputs.weights(M, K, seed=400, device=DEV)
+    x = inputs.activations(N, K, seed=401, device=DEV)
+    W = g.nvfp4_quantize(w)
+    ws = workspace(g.NVFP4_OP_GEMM_PREFILL, N, M, K)
+    y = g.nvfp4_gemm_prefill(x, W, workspace=ws, out_dtype=torch.bfloat16)
+    torch.cuda.synchronize()
+    assert timeout_flag(ws) == 0
+    ref_w = oracle.quantize(w.cpu().numpy())
+    rows = _sample(16, M, N, [0, 127, 128, M - 1])
+    toks = _sample(5, N, N + 2, [0, 255, 256, N - 1])
+    y_ref, A = oracle.gemv(bf16_bits(x), *ref_w, rows=rows, tokens=toks)
+    got = to_np(y)[np.ix_(toks, rows)]
+    assert_close(got, y_ref, gemv_tol(y_ref, A, torch.bfloat16), f"down prefill N={N}")
