@@ -72,6 +72,8 @@ def load_library():
         lib.nvfp4_gateup_swiglu.argtypes = [P, i64, P, P, P, P, P, P, i64, i64, P, i32, P, sz, P]
         lib.nvfp4_gemm_prefill.restype = i32
         lib.nvfp4_gemm_prefill.argtypes = [P, i64, P, P, P, i64, i64, P, i32, P, sz, P]
+        lib.nvfp4_gemv_skinny_noalloc.restype = i32
+        lib.nvfp4_gemv_skinny_noalloc.argtypes = [P, i64, P, P, P, i64, i64, P, i32, P]
         _lib = lib
         return lib
 
@@ -208,4 +210,18 @@ def nvfp4_gemm_prefill(x: torch.Tensor, W: NVFP4Weight, out_dtype=torch.float32,
                                            W.M, K, _ptr(y), _out_code(y.dtype), _ptr(ws), ws_bytes,
                                            _stream(stream))
     _check(st, "nvfp4_gemm_prefill")
+    return y
+
+
+def nvfp4_gemv_skinny_noalloc(x: torch.Tensor, W: NVFP4Weight, out_dtype=torch.float32,
+                              out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Skinny product whose scratch is the library's fixed device array (for
+    callers that cannot allocate device memory; see include/nvfp4.h).  The
+    output tensor is the only buffer created here, and only when `out` is None."""
+    N, K = x.shape
+    y = _new_out(N, W.M, out_dtype, x.device, out)
+    st = load_library().nvfp4_gemv_skinny_noalloc(_ptr(x), N, _ptr(W.codes), _ptr(W.scales),
+                                                  _ptr(W.tensor_scale), W.M, K, _ptr(y),
+                                                  _out_code(y.dtype), _stream(stream))
+    _check(st, "nvfp4_gemv_skinny_noalloc")
     return y

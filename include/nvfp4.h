@@ -167,6 +167,33 @@ int nvfp4_gemm_prefill(const uint16_t *x, int64_t N,
                        void *y, int out_dtype,
                        void *workspace, size_t workspace_bytes, nvfp4_stream_t stream);
 
+/* Skinny product without a caller workspace, for callers that cannot allocate
+ * device memory.  The paper has no counterpart for this call: it is an
+ * addition of this library.  A plain C or Fortran host program with no
+ * device allocator of its own, or a latency-critical loop that must not call
+ * cudaMalloc (it synchronises the whole device), can use it.
+ * Same arguments, checks and results as nvfp4_gemv_skinny (N = 1..16), except
+ * that the split-K scratch is a fixed array of NVFP4_NOALLOC_SCRATCH_BYTES in
+ * the library's own device memory, held by every GPU that loads the library
+ * until the process exits.  Nothing is allocated or freed by the call.
+ *   - Set-up: the first call on each device looks up the array's device
+ *     address (cudaGetSymbolAddress) with that device current and caches it;
+ *     make that first call before any stream capture.
+ *   - Size limit: returns NVFP4_ERR_WORKSPACE, with nothing enqueued, when the
+ *     problem needs more scratch than NVFP4_NOALLOC_SCRATCH_BYTES (that is,
+ *     when nvfp4_workspace_bytes(NVFP4_OP_GEMV_SKINNY, N, M, K) exceeds it).
+ *   - Sharing: every call on a device uses the same array, which keeps the last
+ *     call's contents.  The kernels need none of it to start at zero (each call
+ *     writes every partial it reads).  Calls whose kernels overlap on the GPU
+ *     (different streams without ordering) race on the array; order them on
+ *     one stream. */
+#define NVFP4_NOALLOC_SCRATCH_BYTES ((size_t)8 << 20)
+
+int nvfp4_gemv_skinny_noalloc(const uint16_t *x, int64_t N,
+                              const uint8_t *codes, const uint8_t *scales,
+                              const float *tensor_scale, int64_t M, int64_t K,
+                              void *y, int out_dtype, nvfp4_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif
