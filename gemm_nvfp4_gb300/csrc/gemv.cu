@@ -370,6 +370,13 @@ static cudaError_t launch_t(const GemvArgs &a, cudaStream_t stream)
     return cudaGetLastError();
 }
 
+size_t skinny_workspace_bytes(int64_t M, int64_t K, int n_weights)
+{
+    if (skinny_tc_supported(M, K))
+        return skinny_tc_workspace_bytes(M, K, n_weights);
+    return (size_t)kGemvMaxCtas * kGemvPartialFloatsPerCta * n_weights * 4;
+}
+
 int64_t gemv_grid(int64_t M, int64_t K, int num_sms)
 {
     const int64_t tiles = (M + kTileRows - 1) / kTileRows;
@@ -402,6 +409,8 @@ cudaError_t launch_gemv(const uint16_t *x, int N, int64_t M, int64_t K, const ui
     a.P = (int)gemv_grid(M, K, num_sms);
     if (a.total == 0)
         return cudaSuccess;
+    if (skinny_tc_supported(M, K))
+        return launch_skinny_tc(x, N, M, K, codes, scales, ts, n_weights, y, out_bf16, workspace, num_sms, stream);
     const bool aligned = (K % 32) == 0;
     if (n_weights == 1) {
         if (N <= 8)

@@ -36,3 +36,18 @@ cudaError_t launch_prefill(const uint16_t *x, int64_t N, int64_t M, int64_t K, c
                            int out_bf16, void *workspace, int num_sms, cudaStream_t stream);
 
 }  // namespace nvfp4
+
+namespace nvfp4 {
+
+// Skinny tcgen05 path (gemv_tc.cu), used when skinny_tc_supported(M, K).
+constexpr int kSkinnyTcMaxCtas = 256;
+bool skinny_tc_supported(int64_t M, int64_t K);
+size_t skinny_tc_workspace_bytes(int64_t M, int64_t K, int n_weights);
+cudaError_t launch_skinny_tc(const uint16_t *x, int N, int64_t M, int64_t K, const uint8_t *const *codes,
+                             const uint8_t *const *scales, const float *const *ts, int n_weights, void *y,
+                             int out_bf16, void *workspace, int num_sms, cudaStream_t stream);
+
+// Workspace of the skinny product for any K (tcgen05 path or the mma.sync path).
+size_t skinny_workspace_bytes(int64_t M, int64_t K, int n_weights);
+
+}  // namespace nvfp4

@@ -41,7 +41,7 @@ int current_num_sms(int *out)
     return NVFP4_OK;
 }
 
-size_t skinny_ws(int n_weights) { return (size_t)kGemvMaxCtas * kGemvPartialFloatsPerCta * n_weights * 4; }
+size_t skinny_ws(int64_t M, int64_t K, int n_weights) { return skinny_workspace_bytes(M, K, n_weights); }
 
 bool size_ok(int64_t a, int64_t b) { return a >= 0 && b >= 0 && (b == 0 || a <= (INT64_C(1) << 62) / b); }
 
@@ -128,9 +128,9 @@ size_t nvfp4_workspace_bytes(int op, int64_t N, int64_t M, int64_t K)
         return 0;
     switch (op) {
     case NVFP4_OP_QUANTIZE: return (size_t)kQuantPartials * 4;
-    case NVFP4_OP_GEMV_SKINNY: return (N >= 1 && N <= kMaxSkinnyN) ? skinny_ws(1) : 0;
-    case NVFP4_OP_GATEUP_SWIGLU: return N <= kMaxSkinnyN ? skinny_ws(2) : prefill_workspace_bytes(N, M, K, 2);
-    case NVFP4_OP_GEMM_PREFILL: return N <= kMaxSkinnyN ? skinny_ws(1) : prefill_workspace_bytes(N, M, K, 1);
+    case NVFP4_OP_GEMV_SKINNY: return (N >= 1 && N <= kMaxSkinnyN) ? skinny_ws(M, K, 1) : 0;
+    case NVFP4_OP_GATEUP_SWIGLU: return N <= kMaxSkinnyN ? skinny_ws(M, K, 2) : prefill_workspace_bytes(N, M, K, 2);
+    case NVFP4_OP_GEMM_PREFILL: return N <= kMaxSkinnyN ? skinny_ws(M, K, 1) : prefill_workspace_bytes(N, M, K, 1);
     default: return 0;
     }
 }

@@ -303,6 +303,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         }
     }
 
+    // Lane 0 of warps 0 and 1 ran the producer / MMA loops alone: reconverge
+    // each warp first, so the block-wide barrier below really waits for every
+    // thread (a partially arrived warp would otherwise count as arrived).
+    __syncwarp();
     tc::fence_before_sync();
     __syncthreads();
     if (warp == 1) {

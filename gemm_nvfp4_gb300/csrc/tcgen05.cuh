@@ -62,16 +62,24 @@ NVFP4_DEVINL bool mbar_try_wait(uint64_t *bar, uint32_t parity)
 }
 
 // Wait for the phase with the given parity to complete; false on timeout.
+// The wall clock is read only every 1024 polls, so a completed phase is seen
+// within one poll; the bound is still kWaitLimitNs (plus at most 1024 polls).
 NVFP4_DEVINL bool mbar_wait(uint64_t *bar, uint32_t parity)
 {
     if (mbar_try_wait(bar, parity))
         return true;
-    const uint64_t t0 = globaltimer();
-    while (!mbar_try_wait(bar, parity)) {
-        if (globaltimer() - t0 > kWaitLimitNs)
-            return false;
+    uint64_t t0 = 0;
+    for (uint32_t it = 1;; ++it) {
+        if (mbar_try_wait(bar, parity))
+            return true;
+        if ((it & 1023u) == 0) {
+            const uint64_t t = globaltimer();
+            if (t0 == 0)
+                t0 = t;
+            else if (t - t0 > kWaitLimitNs)
+                return false;
+        }
     }
-    return true;
 }
 
 // Generic-proxy shared-memory writes -> visible to the async proxy (TMA, MMA).
@@ -180,6 +188,75 @@ NVFP4_DEVINL void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)[32])
 }
 
 NVFP4_DEVINL void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+}  // namespace tc
+}  // namespace nvfp4
+
+namespace nvfp4 {
+namespace tc {
+
+// ---------------------------------------------------------------------------
+// Additions for the skinny tcgen05 kernel: A operand in tensor memory,
+// programmatic dependent launch, named barriers.
+// ---------------------------------------------------------------------------
+
+// D (TMEM) += A (TMEM) * B (shared memory descriptor), kind::f16.
+NVFP4_DEVINL void mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc, uint32_t accumulate)
+{
+    asm volatile(
+        "{ .reg .pred p; setp.ne.b32 p, %4, 0; "
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p; }"
+        ::"r"(d_tmem), "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Each thread writes 32 consecutive 32-bit columns of its own TMEM lane.
+NVFP4_DEVINL void tmem_st_32x32b_x32(uint32_t taddr, const uint32_t (&r)[32])
+{
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+        "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+        "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};"
+        ::"r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+        "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]),
+        "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]),
+        "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+        : "memory");
+}
+
+NVFP4_DEVINL void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+NVFP4_DEVINL void tmem_ld_32x32b_x16(uint32_t taddr, uint32_t (&r)[16])
+{
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
+          "=r"(r[15])
+        : "r"(taddr)
+        : "memory");
+}
+
+// Instruction descriptor for kind::f16 with A/B format 0 = f16, 1 = bf16.
+__host__ __device__ constexpr uint32_t idesc_f16kind(int M, int N, uint32_t ab_format)
+{
+    return (1u << 4) | (ab_format << 7) | (ab_format << 10) | ((uint32_t)(N >> 3) << 17) |
+           ((uint32_t)(M >> 4) << 24);
+}
+
+// Shared-memory descriptor for a K-major operand with 128-byte rows, 128-byte
+// swizzle and 8-row atoms (same as smem_desc_sw128, kept separate for clarity).
+NVFP4_DEVINL uint64_t smem_desc_kmajor_sw128(const void *base) { return smem_desc_sw128(base); }
+
+// Programmatic dependent launch.
+NVFP4_DEVINL void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+NVFP4_DEVINL void griddep_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+NVFP4_DEVINL void named_bar_sync(uint32_t id, uint32_t nthreads)
+{
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
 
 }  // namespace tc
 }  // namespace nvfp4

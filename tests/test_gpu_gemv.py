@@ -126,3 +126,64 @@ def test_27b_deep_verify_sampled(N):
     rows = np.unique(np.random.default_rng(N).integers(0, M, 40))
     y_ref, A = oracle.gemv(bf16_bits(x), *ref_w, rows=rows)
     assert_close(to_np(y)[:, rows], y_ref, gemv_tol(y_ref, A), f"deep verify N={N}")
+
+
+def test_activations_not_exact_in_f16_fall_back_exactly():
+    """A token whose elements span more than the f16 window after scaling
+    (here 1e4 next to 1e-12) makes the call use bf16 operands; results stay
+    within the bound for every token, including the wide-range one."""
+    M, K, N = 512, 4096, 4
+    w = inputs.weights(M, K, seed=77)
+    x = inputs.activations(N, K, seed=78).float()
+    x[2, 5] = 1.0e4
+    x[2, 6:200] = 1.0e-12
+    xb = x.to(torch.bfloat16)
+    W = g.nvfp4_quantize(w.to(DEV))
+    ref = oracle.quantize(w.numpy())
+    y = g.nvfp4_gemv_skinny(xb.to(DEV), W)
+    torch.cuda.synchronize()
+    y_ref, A = oracle.gemv(bf16_bits(xb), *ref)
+    assert_close(to_np(y), y_ref, gemv_tol(y_ref, A), "wide-range token")
+
+
+def test_zero_and_tiny_token_rows():
+    M, K, N = 256, 2048, 3
+    w = inputs.weights(M, K, seed=79)
+    x = inputs.activations(N, K, seed=80).float()
+    x[0] = 0.0
+    x[1] *= 1e-30
+    xb = x.to(torch.bfloat16)
+    W = g.nvfp4_quantize(w.to(DEV))
+    ref = oracle.quantize(w.numpy())
+    y = g.nvfp4_gemv_skinny(xb.to(DEV), W)
+    torch.cuda.synchronize()
+    y_ref, A = oracle.gemv(bf16_bits(xb), *ref)
+    assert_close(to_np(y), y_ref, gemv_tol(y_ref, A), "zero / tiny rows")
+    assert (to_np(y)[0] == 0).all()
+
+
+@pytest.mark.parametrize("M", [1, 100, 127, 129, 4224])
+def test_ragged_rows_tensor_core_path(M):
+    """M not a multiple of the 128-row tile on the tcgen05 path (K % 256 == 0)."""
+    W, ref, x = make_case(M, 1280, 5, seed=M)
+    check(W, ref, x, what=f"M={M}")
+
+
+def test_workspace_reuse_back_to_back():
+    """Two different shapes sharing one workspace, queued back to back."""
+    W1, r1, x1 = make_case(4096, 4096, 1, seed=1)
+    W2, r2, x2 = make_case(12288, 4096, 4, seed=2)
+    need = max(g.nvfp4_workspace_bytes(g.NVFP4_OP_GEMV_SKINNY, 1, 4096, 4096),
+               g.nvfp4_workspace_bytes(g.NVFP4_OP_GEMV_SKINNY, 4, 12288, 4096))
+    ws = torch.empty(need, dtype=torch.uint8, device=DEV)
+    outs = []
+    for _ in range(3):
+        outs.append(g.nvfp4_gemv_skinny(x1.to(DEV), W1, workspace=ws))
+        outs.append(g.nvfp4_gemv_skinny(x2.to(DEV), W2, workspace=ws))
+    torch.cuda.synchronize()
+    for o in outs[2::2]:
+        assert torch.equal(o, outs[0])
+    for o in outs[3::2]:
+        assert torch.equal(o, outs[1])
+    y_ref, A = oracle.gemv(bf16_bits(x2), *r2, rows=np.arange(0, 12288, 97))
+    assert_close(to_np(outs[1])[:, ::97], y_ref, gemv_tol(y_ref, A), "reuse")
