@@ -53,7 +53,7 @@ namespace sk {
 
 constexpr int BM = 128;          // weight rows per tile (MMA M, TMEM lanes)
 constexpr int BKU = 256;         // k per unit (one code box per matrix)
-constexpr int kScaleUnits = 8;   // units covered by one scale box (2048 k)
+constexpr int kScaleUnits = 4;   // units covered by one scale box (1024 k)
 constexpr int NTOK = 16;         // MMA N (tokens, padded)
 // Warp roles: 0..3 MMA issuers (one per SM sub-partition), 4 and 5 code
 // producers (even / odd units), 6 scale producer, 7 activation producer,
@@ -70,15 +70,17 @@ constexpr int kThreads = (kFirstDqWarp + kDqWarps) * 32;
 constexpr int kDqThreads = kDqWarps * 32;
 constexpr int kEpiThreads = 128;     // the first dequantiser group
 constexpr int kCodeBox = BM * 128;   // 16 KB: 128 rows x 128 code bytes (256 k), 128-byte swizzle
-constexpr int kScaleBox = BM * 128;  // 16 KB: 128 rows x 128 scale bytes (2048 k), 128-byte swizzle
+constexpr int kScaleBox = BM * 64;   // 8 KB: 128 rows x 64 scale bytes (1024 k), 64-byte swizzle
 constexpr int kXUnit = NTOK * BKU * 2;  // 8 KB: activation image of one unit
 constexpr uint32_t kTmemCols = 512;
 
 template <int NW>
 struct Cfg {
-    static constexpr int kCStages = NW == 1 ? 8 : 4;   // code ring (units)
-    static constexpr int kSStages = 2;                  // scale ring (8 units each)
-    static constexpr int kXStages = NW == 1 ? 6 : 3;   // activation ring (units)
+    // The code ring holds most of the shared memory: with ~4 us of loaded
+    // DRAM latency, every SM needs well over 100 KB of weights in flight.
+    static constexpr int kCStages = NW == 1 ? 10 : 5;  // code ring (units)
+    static constexpr int kSStages = 2;                  // scale ring (kScaleUnits units each)
+    static constexpr int kXStages = NW == 1 ? 4 : 3;   // activation ring (units, from L2)
     // One unit = kSubs TMEM A sub-stages of 128 columns.  Group g of the
     // dequantisers fills columns [col0(g), +kGroupCols) of sub-stage sub(g).
     //   NW = 1: 1 sub-stage of 256 k; group g fills k [64g, 64g+64) (32 columns).
@@ -86,7 +88,7 @@ struct Cfg {
     //           sub-stage g%2 (64 columns).
     static constexpr int kSubs = NW;
     static constexpr int kSubK = BKU / kSubs;
-    static constexpr int kAFullCount = kDqThreads / kSubs;
+    static constexpr int kAFullCount = kDqWarps / kSubs;  // one arrival per dequantiser warp
     static constexpr int kAStages = 3;                 // TMEM A ring (128 columns each)
     static constexpr int kACols = 128;
     // Independent accumulation chains per matrix: issuer q accumulates matrix
@@ -211,7 +213,17 @@ NVFP4_DEVINL void dequant_chunk(uint4 c, uint32_t sc2, int mode, uint32_t *out)
     }
 }
 
-NVFP4_DEVINL int cta_of(int64_t q, int64_t total, int P) { return (int)(((q + 1) * P - 1) / total); }
+// Stream-K partition in 32-bit arithmetic (the host keeps total * P < 2^31):
+// CTA b owns units [b * total / P, (b + 1) * total / P).
+NVFP4_DEVINL int cta_of(uint32_t q, uint32_t total, uint32_t P) { return (int)(((q + 1) * P - 1) / total); }
+NVFP4_DEVINL uint32_t cta_lo(uint32_t b, uint32_t total, uint32_t P) { return b * total / P; }
+
+NVFP4_DEVINL uint32_t atom_add_acq_rel(uint32_t *p, uint32_t v)
+{
+    uint32_t old;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
+}
 
 NVFP4_DEVINL void fail(const Args &a, uint32_t code) { atomicExch(a.err, code); }
 
@@ -346,20 +358,15 @@ __global__ void __launch_bounds__(256) skinny_prep_kernel(const uint16_t *__rest
 // Epilogue of one tile segment for thread row r: whole tiles are written
 // directly; split tiles publish this row's partial and the last CTA to arrive
 // for the row (per-row counter) adds all partials of the row in CTA order.
+// fac[mi][n] (shared memory): tensor scale times the activation factor.
 template <int NW>
-__device__ __noinline__ void epilogue(const Args &a, int mode, const float (&v)[NW][16], int64_t tile, int j,
-                                      int64_t u, int64_t lo, int64_t first_tile, int b, int r)
+__device__ __noinline__ void epilogue(const Args &a, const float *fac, const float (&v)[NW][16], int tile, int j,
+                                      int u, int first_tile, int b, int r)
 {
-    float fac[NW][NTOK];
-#pragma unroll
-    for (int mi = 0; mi < NW; ++mi) {
-        const float t = __ldg(a.ts[mi]);
-#pragma unroll
-        for (int n = 0; n < NTOK; ++n)
-            fac[mi][n] = mode ? t * 256.0f : t * a.factor[n];
-    }
-    const int64_t m = tile * BM + r;
-    const bool whole = (j == a.C - 1) && (u - j >= lo);
+    constexpr int kMaxSplit = 8;  // partials loaded together by the last arriver
+    const uint32_t total = (uint32_t)a.total, P = (uint32_t)a.P, C = (uint32_t)a.C;
+    const int64_t m = (int64_t)tile * BM + r;
+    const bool whole = (j == a.C - 1) && (u - j >= (int)cta_lo(b, total, P));
     float acc[NW][NTOK];
 #pragma unroll
     for (int mi = 0; mi < NW; ++mi)
@@ -368,33 +375,50 @@ __device__ __noinline__ void epilogue(const Args &a, int mode, const float (&v)[
             acc[mi][n] = v[mi][n];
     if (!whole) {
         const int slot = (tile == first_tile) ? 0 : 1;
+        float *mine = a.partial + ((size_t)b * 2 + slot) * NW * NTOK * BM + r;
 #pragma unroll
         for (int mi = 0; mi < NW; ++mi)
 #pragma unroll
             for (int n = 0; n < NTOK; ++n)
                 if (n < a.N)
-                    a.partial[((((int64_t)b * 2 + slot) * NW + mi) * NTOK + n) * BM + r] = acc[mi][n];
-        __threadfence();
-        const int b_lo = cta_of(tile * a.C, a.total, a.P);
-        const int b_hi = cta_of((tile + 1) * a.C - 1, a.total, a.P);
-        const uint32_t old = atomicAdd(&a.counters[tile * BM + r], 1u);
+                    mine[(mi * NTOK + n) * BM] = acc[mi][n];
+        const int b_lo = cta_of((uint32_t)tile * C, total, P);
+        const int b_hi = cta_of(((uint32_t)tile + 1) * C - 1, total, P);
+        // acq_rel: publishes this thread's partial (release) and, for the last
+        // arriver, makes the other CTAs' partials of this row visible (acquire).
+        const uint32_t old = atom_add_acq_rel(&a.counters[(size_t)tile * BM + r], 1u);
         if (old != (uint32_t)(b_hi - b_lo))
             return;  // another CTA finishes this row
-        __threadfence();
+        // Sum the partials of CTAs b_lo..b_hi in CTA order, kMaxSplit CTAs per
+        // round, all loads of a round in flight together.
 #pragma unroll
         for (int mi = 0; mi < NW; ++mi)
 #pragma unroll
             for (int n = 0; n < NTOK; ++n)
                 acc[mi][n] = 0.0f;
-        for (int bb = b_lo; bb <= b_hi; ++bb) {
-            const int64_t bfirst = ((int64_t)bb * a.total / a.P) / a.C;
-            const int sl = (bfirst == tile) ? 0 : 1;
+        for (int b0 = b_lo; b0 <= b_hi; b0 += kMaxSplit) {
+            const float *src[kMaxSplit];
+#pragma unroll
+            for (int q = 0; q < kMaxSplit; ++q) {
+                const int bb = b0 + q <= b_hi ? b0 + q : b_hi;
+                const int sl = ((int)(cta_lo((uint32_t)bb, total, P) / C) == tile) ? 0 : 1;
+                src[q] = a.partial + ((size_t)bb * 2 + sl) * NW * NTOK * BM + r;
+            }
 #pragma unroll
             for (int mi = 0; mi < NW; ++mi)
 #pragma unroll
-                for (int n = 0; n < NTOK; ++n)
-                    if (n < a.N)
-                        acc[mi][n] += __ldcg(&a.partial[((((int64_t)bb * 2 + sl) * NW + mi) * NTOK + n) * BM + r]);
+                for (int n = 0; n < NTOK; ++n) {
+                    if (n < a.N) {
+                        float pv[kMaxSplit];
+#pragma unroll
+                        for (int q = 0; q < kMaxSplit; ++q)
+                            pv[q] = __ldcg(src[q] + (mi * NTOK + n) * BM);
+#pragma unroll
+                        for (int q = 0; q < kMaxSplit; ++q)
+                            if (b0 + q <= b_hi)
+                                acc[mi][n] += pv[q];
+                    }
+                }
         }
     }
     if (m >= a.M)
@@ -404,15 +428,102 @@ __device__ __noinline__ void epilogue(const Args &a, int mode, const float (&v)[
         if (n < a.N) {
             float val;
             if (NW == 1)
-                val = acc[0][n] * fac[0][n];
+                val = acc[0][n] * fac[n];
             else
-                val = silu_mul(acc[0][n] * fac[0][n], acc[NW - 1][n] * fac[NW - 1][n]);
+                val = silu_mul(acc[0][n] * fac[n], acc[NW - 1][n] * fac[NTOK + n]);
             const int64_t idx = (int64_t)n * a.M + m;
             if (a.out_bf16)
                 reinterpret_cast<uint16_t *>(a.y)[idx] = f32_to_bf16(val);
             else
                 reinterpret_cast<float *>(a.y)[idx] = val;
         }
+    }
+}
+
+struct IssuerArgs {
+    const uint8_t *x_ring;
+    uint64_t *x_full, *x_empty, *a_full, *a_empty, *d_full, *d_empty;
+    uint32_t tmem_a, tmem_d;
+    int n_units, j_lo;
+};
+
+// One MMA issuer (warp q, lane 0): matrix q / kChains, accumulator chain
+// q % kChains, K steps kk = chain (mod kChains) of every sub-stage - four MMAs
+// per sub-stage in both configurations.  The descriptor and TMEM offsets of
+// those MMAs are computed once, so each MMA costs a few issue slots (the
+// issuing thread shares its sub-partition with ALU-bound dequantisers).  One
+// copy of the loop serves all issuers: per-issuer specialisations multiply the
+// kernel's code size and starve the dequantisers' instruction fetch.
+template <int NW>
+NVFP4_DEVINL void mma_issuer(const Args &a, const IssuerArgs &p, int q)
+{
+    using C = Cfg<NW>;
+    constexpr int kPerSub = C::kSubK / 16 / C::kChains;
+    static_assert(kPerSub == 4, "four MMAs per issuer and sub-stage");
+    const int mi = q / C::kChains;
+    const int chain = q % C::kChains;
+    uint32_t boff[C::kSubs][kPerSub], aoff[kPerSub];
+#pragma unroll
+    for (int t = 0; t < kPerSub; ++t) {
+        const int kk = chain + C::kChains * t;
+        aoff[t] = (uint32_t)(mi * 64 + kk * 8);
+#pragma unroll
+        for (int sub = 0; sub < C::kSubs; ++sub) {
+            const int kl = sub * C::kSubK + kk * 16;  // k within the unit
+            // B: 64-k sub-box kl / 64 of the activation unit (16 rows x 128 B,
+            // 128-byte swizzle), 32-byte step kl % 64 inside it; descriptor
+            // addresses are in 16-byte units.
+            boff[sub][t] = (uint32_t)((kl >> 6) * (NTOK * 128 / 16) + 2 * ((kl >> 4) & 3));
+        }
+    }
+    const uint32_t idesc = tc::idesc_f16kind(BM, NTOK, (uint32_t)load_mode(a));
+    int j = p.j_lo;
+    int seg = -1;
+    int sx = 0, sa = 0;
+    uint32_t phx = 0, pha = 0;
+    for (int i = 0; i < p.n_units; ++i) {
+        const bool first = (i == 0) || j == 0;
+        const bool last = (i == p.n_units - 1) || j == a.C - 1;
+        if (first) {
+            ++seg;
+            if (!tc::mbar_wait(&p.d_empty[seg & 1], (((uint32_t)seg >> 1) & 1) ^ 1)) {
+                fail(a, 13);
+                return;
+            }
+        }
+        if (!tc::mbar_wait(&p.x_full[sx], phx)) {
+            fail(a, 14);
+            return;
+        }
+        const uint64_t bdesc0 = tc::smem_desc_sw128(p.x_ring + (size_t)sx * kXUnit);
+        const uint32_t dcol = p.tmem_d + (uint32_t)(seg & 1) * C::kDCols + (uint32_t)(chain * NW + mi) * 16;
+#pragma unroll
+        for (int sub = 0; sub < C::kSubs; ++sub) {
+            if (!tc::mbar_wait(&p.a_full[sa], pha)) {
+                fail(a, 15);
+                return;
+            }
+            tc::fence_after_sync();
+            const uint32_t acol = p.tmem_a + (uint32_t)(sa * C::kACols);
+#pragma unroll
+            for (int t = 0; t < kPerSub; ++t)
+                tc::mma_f16_ts(dcol, acol + aoff[t], bdesc0 + boff[sub][t], idesc,
+                               (first && sub == 0 && t == 0) ? 0u : 1u);
+            tc::mma_commit(&p.a_empty[sa]);
+            if (++sa == C::kAStages) {
+                sa = 0;
+                pha ^= 1;
+            }
+        }
+        tc::mma_commit(&p.x_empty[sx]);
+        if (++sx == C::kXStages) {
+            sx = 0;
+            phx ^= 1;
+        }
+        if (last)
+            tc::mma_commit(&p.d_full[seg & 1]);
+        if (++j == a.C)
+            j = 0;
     }
 }
 
@@ -439,6 +550,7 @@ skinny_tc_kernel(const __grid_constant__ CUtensorMap m_codes0, const __grid_cons
     uint64_t *d_full = a_empty + C::kAStages;
     uint64_t *d_empty = d_full + 2;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(d_empty + 2);
+    float *fac_s = reinterpret_cast<float *>(tmem_slot + 4);  // [NW][16] epilogue factors
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int b = blockIdx.x;
@@ -449,13 +561,15 @@ skinny_tc_kernel(const __grid_constant__ CUtensorMap m_codes0, const __grid_cons
         // Let the next kernel in the stream be scheduled as soon as SMs free up;
         // it waits for this grid's completion before it reads anything we write.
         tc::griddep_launch_dependents();
+        // Consumers arrive once per warp (lane 0 after __syncwarp): hundreds
+        // of per-thread arrivals on one mbarrier serialise in shared memory.
         for (int s = 0; s < C::kCStages; ++s) {
             tc::mbar_init(&c_full[s], 1);
-            tc::mbar_init(&c_empty[s], kDqThreads);
+            tc::mbar_init(&c_empty[s], kDqWarps);
         }
         for (int s = 0; s < C::kSStages; ++s) {
             tc::mbar_init(&s_full[s], 1);
-            tc::mbar_init(&s_empty[s], kDqThreads);
+            tc::mbar_init(&s_empty[s], kDqWarps);
         }
         for (int s = 0; s < C::kXStages; ++s) {
             tc::mbar_init(&x_full[s], 1);
@@ -467,7 +581,7 @@ skinny_tc_kernel(const __grid_constant__ CUtensorMap m_codes0, const __grid_cons
         }
         for (int s = 0; s < 2; ++s) {
             tc::mbar_init(&d_full[s], kMmaWarps);
-            tc::mbar_init(&d_empty[s], kEpiThreads);
+            tc::mbar_init(&d_empty[s], kEpiThreads / 32);
         }
         tc::fence_mbar_init();
         tc::prefetch_tensormap(&m_codes0);
@@ -502,9 +616,9 @@ skinny_tc_kernel(const __grid_constant__ CUtensorMap m_codes0, const __grid_cons
                 j -= a.C;
                 ++tile;
             }
-            int s = par;
-            uint32_t ph = 0;
             for (int i = par; i < n_units; i += 2) {
+                const int s = i % C::kCStages;
+                const uint32_t ph = (uint32_t)(i / C::kCStages) & 1;
                 if (!tc::mbar_wait(&c_empty[s], ph ^ 1)) {
                     fail(a, 11);
                     break;
@@ -515,11 +629,6 @@ skinny_tc_kernel(const __grid_constant__ CUtensorMap m_codes0, const __grid_cons
                 for (int mi = 0; mi < NW; ++mi)
                     tc::tma_load_2d(st + mi * kCodeBox, mi == 0 ? &m_codes0 : &m_codes1, &c_full[s], j * (BKU / 2),
                                     (int)(tile * BM));
-                s += 2;
-                if (s >= C::kCStages) {
-                    s -= C::kCStages;
-                    ph ^= 1;
-                }
                 j += 2;
                 while (j >= a.C) {
                     j -= a.C;
@@ -545,7 +654,7 @@ skinny_tc_kernel(const __grid_constant__ CUtensorMap m_codes0, const __grid_cons
 #pragma unroll
                     for (int mi = 0; mi < NW; ++mi)
                         tc::tma_load_2d(st + mi * kScaleBox, mi == 0 ? &m_scales0 : &m_scales1, &s_full[s],
-                                        (j / kScaleUnits) * 128, (int)(tile * BM));
+                                        (j / kScaleUnits) * (kScaleUnits * BKU / 16), (int)(tile * BM));
                     if (++s == C::kSStages) {
                         s = 0;
                         ph ^= 1;
@@ -584,70 +693,20 @@ skinny_tc_kernel(const __grid_constant__ CUtensorMap m_codes0, const __grid_cons
         // ---- MMA issuers: issuer q owns matrix q / kChains, chain q % kChains ----
         if (lane == 0) {
             tc::griddep_wait();
-            const int q = warp;
-            const int my_mi = q / C::kChains;
-            const int chain = q % C::kChains;
-            const uint32_t idesc = tc::idesc_f16kind(BM, NTOK, (uint32_t)load_mode(a));
-            int j = j_lo;
-            int seg = -1;
-            int sx = 0, sa = 0;
-            uint32_t phx = 0, pha = 0;
-            bool ok = true;
-            for (int i = 0; i < n_units && ok; ++i) {
-                const bool first = (i == 0) || j == 0;
-                const bool last = (i == n_units - 1) || j == a.C - 1;
-                if (first) {
-                    ++seg;
-                    if (!tc::mbar_wait(&d_empty[seg & 1], (((uint32_t)seg >> 1) & 1) ^ 1)) {
-                        fail(a, 13);
-                        break;
-                    }
-                }
-                if (!tc::mbar_wait(&x_full[sx], phx)) {
-                    fail(a, 14);
-                    break;
-                }
-                const uint8_t *xs = x_ring + (size_t)sx * kXUnit;
-                const uint32_t dcol = tmem_d + (uint32_t)(seg & 1) * C::kDCols + (uint32_t)(chain * NW + my_mi) * 16;
-                for (int sub = 0; sub < C::kSubs; ++sub) {
-                    if (!tc::mbar_wait(&a_full[sa], pha)) {
-                        fail(a, 15);
-                        ok = false;
-                        break;
-                    }
-                    tc::fence_after_sync();
-                    const uint32_t acol = tmem_a + (uint32_t)(sa * C::kACols + my_mi * 64);
-                    for (int kk = chain; kk < C::kSubK / 16; kk += C::kChains) {
-                        const int kl = sub * C::kSubK + kk * 16;  // k within the unit
-                        const uint64_t bdesc =
-                            tc::smem_desc_sw128(xs + (kl >> 6) * (NTOK * 128)) + 2 * ((kl >> 4) & 3);
-                        const bool init = first && sub == 0 && kk == chain;
-                        tc::mma_f16_ts(dcol, acol + kk * 8, bdesc, idesc, init ? 0u : 1u);
-                    }
-                    tc::mma_commit(&a_empty[sa]);
-                    if (++sa == C::kAStages) {
-                        sa = 0;
-                        pha ^= 1;
-                    }
-                }
-                if (!ok)
-                    break;
-                tc::mma_commit(&x_empty[sx]);
-                if (++sx == C::kXStages) {
-                    sx = 0;
-                    phx ^= 1;
-                }
-                if (last)
-                    tc::mma_commit(&d_full[seg & 1]);
-                if (++j == a.C)
-                    j = 0;
-            }
+            IssuerArgs ia{x_ring, x_full, x_empty, a_full, a_empty, d_full, d_empty, tmem_a, tmem_d, n_units, j_lo};
+            mma_issuer<NW>(a, ia, warp);
         }
     } else {
         // ---- dequantisers (warps 8..23) and epilogue (warps 8..11) ----
         tc::griddep_wait();
         const int mode = load_mode(a);
         const int dq = threadIdx.x - kFirstDqWarp * 32;  // 0..511
+        if (dq < NW * NTOK) {
+            const int mi = dq / NTOK, n = dq % NTOK;
+            const float t = __ldg(a.ts[mi]);
+            fac_s[dq] = mode ? t * 256.0f : t * a.factor[n];
+        }
+        tc::named_bar_sync(1, kDqThreads);  // fac_s visible to the epilogue threads
         const int grp = dq >> 7;                          // 0..3
         const int quarter = warp & 3;                     // TMEM lane quarter this warp may access
         const int r = quarter * 32 + lane;                // row within the tile
@@ -697,8 +756,9 @@ skinny_tc_kernel(const __grid_constant__ CUtensorMap m_codes0, const __grid_cons
 #pragma unroll
             for (int c = 0; c < kChunks; ++c)
                 cw[c] = *reinterpret_cast<const uint4 *>(crow + (((chunk0 + c) ^ swz) << 4));
-            const uint8_t *sp = s_ring + ((size_t)ss * NW + my_mi) * kScaleBox + r * 128 +
-                                (((j % kScaleUnits) ^ swz) << 4) + sc_off;
+            // 64-byte rows, 64-byte swizzle: 16-byte chunk c of row r sits at c ^ ((r >> 1) & 3).
+            const uint8_t *sp = s_ring + ((size_t)ss * NW + my_mi) * kScaleBox + r * 64 +
+                                (((j % kScaleUnits) ^ ((r >> 1) & 3)) << 4) + sc_off;
             uint32_t scw[kChunks / 2];
             if (NW == 1) {
                 scw[0] = *reinterpret_cast<const uint32_t *>(sp);
@@ -707,9 +767,12 @@ skinny_tc_kernel(const __grid_constant__ CUtensorMap m_codes0, const __grid_cons
                 scw[0] = v2.x;
                 scw[kChunks / 2 - 1] = v2.y;
             }
-            tc::mbar_arrive(&c_empty[sc]);
-            if (scale_last)
-                tc::mbar_arrive(&s_empty[ss]);
+            __syncwarp();
+            if (lane == 0) {
+                tc::mbar_arrive(&c_empty[sc]);
+                if (scale_last)
+                    tc::mbar_arrive(&s_empty[ss]);
+            }
             if (++sc == C::kCStages) {
                 sc = 0;
                 phc ^= 1;
@@ -732,7 +795,9 @@ skinny_tc_kernel(const __grid_constant__ CUtensorMap m_codes0, const __grid_cons
             }
             tc::tmem_st_wait();
             tc::fence_before_sync();
-            tc::mbar_arrive(&a_full[sa]);
+            __syncwarp();
+            if (lane == 0)
+                tc::mbar_arrive(&a_full[sa]);
             for (int t = 0; t < C::kSubs; ++t)
                 if (++sa == C::kAStages) {
                     sa = 0;
@@ -768,8 +833,10 @@ skinny_tc_kernel(const __grid_constant__ CUtensorMap m_codes0, const __grid_cons
                             sum[mi][n] += __uint_as_float(v[mi][n]);  // chains added in a fixed order
                 }
                 tc::fence_before_sync();
-                tc::mbar_arrive(&d_empty[db]);
-                epilogue<NW>(a, mode, sum, tile, j, lo + i, lo, tile_lo, b, r);
+                __syncwarp();
+                if (lane == 0)
+                    tc::mbar_arrive(&d_empty[db]);
+                epilogue<NW>(a, fac_s, sum, (int)tile, j, (int)(lo + i), (int)tile_lo, b, r);
             }
             if (++j == a.C) {
                 j = 0;
@@ -850,7 +917,15 @@ cudaError_t launch_main(const CUtensorMap (&maps)[4], const Args &a, cudaStream_
 
 }  // namespace sk
 
-bool skinny_tc_supported(int64_t M, int64_t K) { return K >= 256 && K % 256 == 0 && M >= 1; }
+// Units (128 rows x 256 k) times CTAs must stay below 2^31: the kernel's
+// stream-K arithmetic is 32-bit.
+bool skinny_tc_supported(int64_t M, int64_t K)
+{
+    if (K < 256 || K % 256 != 0 || M < 1)
+        return false;
+    const int64_t units = ((M + 127) / 128) * (K / 256);
+    return units * kSkinnyTcMaxCtas < (INT64_C(1) << 31);
+}
 
 size_t skinny_tc_workspace_bytes(int64_t M, int64_t K, int n_weights)
 {
@@ -894,10 +969,11 @@ cudaError_t launch_skinny_tc(const uint16_t *x, int N, int64_t M, int64_t K, con
         // boxes: one unit of codes (BKU/2 bytes per row, 128-byte swizzle) and
         // of scales (BKU/16 bytes per row), 128 rows each
         static_assert(kCodeBox == BM * (BKU / 2) && kScaleBox == BM * (BKU * kScaleUnits / 16), "box sizes");
+        static_assert(BKU * kScaleUnits / 16 == 64, "scale box rows are 64 bytes (64-byte swizzle)");
         if (!make_map(&maps[i], CU_TENSOR_MAP_DATA_TYPE_UINT8, codes[s], (uint64_t)K / 2, (uint64_t)M,
                       (uint64_t)K / 2, BKU / 2, BM, CU_TENSOR_MAP_SWIZZLE_128B) ||
             !make_map(&maps[2 + i], CU_TENSOR_MAP_DATA_TYPE_UINT8, scales[s], (uint64_t)K / 16, (uint64_t)M,
-                      (uint64_t)K / 16, BKU * kScaleUnits / 16, BM, CU_TENSOR_MAP_SWIZZLE_128B))
+                      (uint64_t)K / 16, BKU * kScaleUnits / 16, BM, CU_TENSOR_MAP_SWIZZLE_64B))
             return cudaErrorInvalidValue;
     }
 
