@@ -244,6 +244,7 @@ NVFP4_DEVINL void bulk_load(void *dst, const void *src, uint32_t bytes, uint64_t
                  : "memory");
 }
 
+
 // ---------------------------------------------------------------------------
 // prep kernel: activation images + per-token power of two + exactness flags
 // ---------------------------------------------------------------------------
@@ -667,20 +668,33 @@ skinny_tc_kernel(const __grid_constant__ CUtensorMap m_codes0, const __grid_cons
             }
         }
     } else if (warp == 7) {
-        // ---- activation producer: one bulk copy per unit ----
+        // ---- activation producer: per unit, one bulk copy of the N token rows
+        // of each 64-k sub-box of the activation image (the rows are
+        // contiguous there).  Rows >= N of the MMA's B operand only feed
+        // accumulator columns the epilogue ignores, so they are zeroed once and
+        // never loaded: for small N the activations then take almost no copy
+        // bandwidth from the weight stream.
+        for (int o = lane * 16; o < C::kXStages * kXUnit; o += 32 * 16)
+            *reinterpret_cast<uint4 *>(x_ring + o) = make_uint4(0, 0, 0, 0);
+        tc::fence_proxy_async_smem();
+        __syncwarp();
         if (lane == 0) {
             tc::griddep_wait();
             const uint8_t *img = load_mode(a) ? a.xb_img : a.x_img;
-            int j = j_lo;
-            int s = 0;
+            const uint32_t row_bytes = (uint32_t)a.N * 128;
+            int j = j_lo, s = 0;
             uint32_t ph = 0;
             for (int i = 0; i < n_units; ++i) {
                 if (!tc::mbar_wait(&x_empty[s], ph ^ 1)) {
                     fail(a, 12);
                     break;
                 }
-                tc::mbar_arrive_expect_tx(&x_full[s], kXUnit);
-                bulk_load(x_ring + (size_t)s * kXUnit, img + (size_t)j * kXUnit, kXUnit, &x_full[s]);
+                const uint8_t *src = img + (size_t)j * kXUnit;
+                uint8_t *dst = x_ring + (size_t)s * kXUnit;
+                tc::mbar_arrive_expect_tx(&x_full[s], 4 * row_bytes);
+#pragma unroll
+                for (int sb = 0; sb < 4; ++sb)
+                    bulk_load(dst + sb * (NTOK * 128), src + sb * (NTOK * 128), row_bytes, &x_full[s]);
                 if (++s == C::kXStages) {
                     s = 0;
                     ph ^= 1;

@@ -61,24 +61,33 @@ NVFP4_DEVINL bool mbar_try_wait(uint64_t *bar, uint32_t parity)
     return ok != 0;
 }
 
-// Wait for the phase with the given parity to complete; false on timeout.
-// The wall clock is read only every 1024 polls, so a completed phase is seen
-// within one poll; the bound is still kWaitLimitNs (plus at most 1024 polls).
+// Like mbar_try_wait, but the hardware may park the thread for up to
+// `hint_ns` nanoseconds waiting for the phase instead of returning at once, so
+// a waiting warp does not spin through the issue slots its neighbours need.
+NVFP4_DEVINL bool mbar_try_wait_sleep(uint64_t *bar, uint32_t parity, uint32_t hint_ns)
+{
+    uint32_t ok;
+    asm volatile(
+        "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3; selp.u32 %0, 1, 0, p; }"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+
+// Wait for the phase with the given parity to complete; false on timeout
+// (kWaitLimitNs of wall time).  After one immediate test the thread sleeps in
+// the barrier between tests.
 NVFP4_DEVINL bool mbar_wait(uint64_t *bar, uint32_t parity)
 {
     if (mbar_try_wait(bar, parity))
         return true;
-    uint64_t t0 = 0;
-    for (uint32_t it = 1;; ++it) {
-        if (mbar_try_wait(bar, parity))
+    const uint64_t t0 = globaltimer();
+    for (;;) {
+        if (mbar_try_wait_sleep(bar, parity, 20000u))
             return true;
-        if ((it & 1023u) == 0) {
-            const uint64_t t = globaltimer();
-            if (t0 == 0)
-                t0 = t;
-            else if (t - t0 > kWaitLimitNs)
-                return false;
-        }
+        if (globaltimer() - t0 > kWaitLimitNs)
+            return false;
     }
 }
 
