@@ -58,6 +58,7 @@ def parse():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="dense9b-n1")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-prefill", action="store_true")
     return ap.parse_args()
 
 
@@ -244,7 +245,8 @@ class LayerStream:
         for li in range(self.n_layers):
             self.run_layer(li, only)
 
-    # our kernels per call: main kernel + split-K fixup kernel
+    # our kernels per call: the activation prep kernel and the main kernel
+    # (split-K partials are reduced inside the main kernel)
     LAUNCHES_PER_CALL = 2
 
     def launches_per_step(self, only=None):
@@ -295,15 +297,25 @@ def read_peaks():
     return 6800.0, 1900.0, "fallback"
 
 
+KERNEL_SOURCES = ("gemv_tc.cu", "tcgen05.cuh", "common.cuh")
+
+
+def kernel_source_hash():
+    """Hash of the skinny kernel's sources (the ncu traffic summary records it)."""
+    import hashlib
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES:
+        h.update(open(os.path.join(ROOT, "gemm_nvfp4_gb300", "csrc", name), "rb").read())
+    return h.hexdigest()[:16]
+
+
 def read_traffic(kernel_key):
     """DRAM bytes per launch from the committed ncu summary, if it was taken on
     the current kernel source (the summary records the source hash)."""
-    import hashlib
     path = os.path.join(ROOT, "profiles", "traffic.md")
     if not os.path.exists(path):
         return None
-    src = os.path.join(ROOT, "gemm_nvfp4_gb300", "csrc", "gemv.cu")
-    h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    h = kernel_source_hash()
     for line in open(path):
         parts = [p.strip() for p in line.strip().strip("|").split("|")]
         if len(parts) >= 4 and parts[0] == kernel_key and parts[1] == h:
@@ -312,6 +324,40 @@ def read_traffic(kernel_key):
             except ValueError:
                 return None
     return None
+
+
+def prefill_tflops(dev, reps=5):
+    """Prefill GEMM throughput on the 27B-class gate/up (SwiGLU) and down
+    matrices at N = 512, 2048, 8192 (dense bf16-equivalent FLOPs, 2*N*M*K per
+    matrix), timed with CUDA events after one warm-up call each."""
+    import gemm_nvfp4_gb300 as g
+    from gemm_nvfp4_gb300 import inputs
+    shapes = inputs.LAYER_27B.shapes()
+    out = {"unit": "TFLOP/s", "peak_bf16": read_peaks()[1], "shapes": {}}
+    Mg, Kg = shapes["gate"]
+    Md, Kd = shapes["down"]
+    Wg = g.nvfp4_quantize(inputs.weights(Mg, Kg, seed=inputs.matrix_seed("gate"), device=dev))
+    Wu = g.nvfp4_quantize(inputs.weights(Mg, Kg, seed=inputs.matrix_seed("up"), device=dev))
+    Wd = g.nvfp4_quantize(inputs.weights(Md, Kd, seed=inputs.matrix_seed("down"), device=dev))
+    for N in (512, 2048, 8192):
+        xg = inputs.activations(N, Kg, seed=N, device=dev)
+        xd = inputs.activations(N, Kd, seed=N + 1, device=dev)
+        for name, fn, flops in (
+                ("gateup", lambda: g.nvfp4_gateup_swiglu(xg, Wg, Wu), 2 * 2.0 * N * Mg * Kg),
+                ("down", lambda: g.nvfp4_gemm_prefill(xd, Wd), 2.0 * N * Md * Kd)):
+            fn()
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            for _ in range(reps):
+                fn()
+            e1.record()
+            torch.cuda.synchronize()
+            ms = e0.elapsed_time(e1) / reps
+            out["shapes"][f"{name} N={N}"] = {"ms": ms, "tflops": flops / (ms * 1e-3) / 1e12}
+        del xg, xd
+    torch.cuda.empty_cache()
+    return out
 
 
 # ---------------------------------------------------------------------------
@@ -338,13 +384,18 @@ def oracle_sample(workload, rows_per_matrix=64, device="cpu"):
     return time.perf_counter() - t0, nbytes
 
 
-def cpu_baseline(workload, target_s=10.0):
-    dt, nb = oracle_sample(workload, rows_per_matrix=16)
-    rows = int(max(16, min(4096, 16 * target_s / max(dt, 1e-3))))
-    dt, nb = oracle_sample(workload, rows_per_matrix=rows)
-    return {"value": nb / dt / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+def cpu_baseline(workload, target_s=10.0, rows=1024):
+    """The oracle's products on a row sample of one layer, repeated until about
+    target_s seconds of CPU time have been spent."""
+    total_dt, total_nb, reps = 0.0, 0, 0
+    while total_dt < target_s:
+        dt, nb = oracle_sample(workload, rows_per_matrix=rows)
+        total_dt += dt
+        total_nb += nb
+        reps += 1
+    return {"value": total_nb / total_dt / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
             "sample": f"{rows} rows of each of the 5 matrices of one layer of {workload}, "
-                      f"N as in the workload, single-threaded C oracle, {dt:.1f} s"}
+                      f"N as in the workload, single-threaded C oracle, {reps} passes, {total_dt:.1f} s"}
 
 
 # ---------------------------------------------------------------------------
@@ -423,7 +474,9 @@ def main():
     dom_bytes = st.call_bytes("gateup")
     dom_per_launch_ms = dom_ms / st.n_layers
     achieved = dom_bytes / (dom_per_launch_ms * 1e-3) / 1e9
-    traffic = read_traffic("gemv_kernel<2,1>" if st.N <= 8 else "gemv_kernel<2,2>")
+    traffic = read_traffic(f"skinny_tc_kernel<2> {args.workload}")
+
+    prefill = prefill_tflops(dev) if not args.no_prefill else None
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -450,6 +503,7 @@ def main():
             "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "gpu_launches": st.launches_per_step() * args.steps,
             "clocks": clocks,
+            "prefill": prefill,
         }
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -114,17 +114,16 @@ struct Args {
     const int *flags;      // [16] 1 if token n is not exact in f16
     uint32_t *counters;    // [T][128] per-row arrival counters
     float *partial;        // [P][2][NW][16][128]
-    const uint8_t *x_img;  // [C][16 KB] f16 activation images (shared-memory layout)
-    const uint8_t *xb_img; // [C][16 KB] bf16 activation images
+    const uint8_t *x_img;  // [C][8 KB] f16 activation image (shared-memory layout)
     uint32_t *err;
     void *y;
     int out_bf16;
 };
 
 // Workspace layout (bytes): header 256 (factor[16], flags[16], err), per-row
-// counters, f16 and bf16 activation images, split-K partials.
+// counters, the f16 activation image, split-K partials.
 struct WsLayout {
-    size_t counters, ximg, xbimg, partial, total;
+    size_t counters, ximg, partial, total;
 };
 
 inline size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
@@ -136,8 +135,7 @@ inline WsLayout ws_layout(int64_t M, int64_t K, int nw)
     const int64_t C = (K + BKU - 1) / BKU;
     w.counters = 256;
     w.ximg = w.counters + round_up((size_t)T * BM * 4, 1024);
-    w.xbimg = w.ximg + (size_t)C * kXUnit;
-    w.partial = w.xbimg + (size_t)C * kXUnit;
+    w.partial = w.ximg + (size_t)C * kXUnit;
     w.total = w.partial + (size_t)kSkinnyTcMaxCtas * 2 * nw * NTOK * BM * 4;
     return w;
 }
@@ -261,47 +259,50 @@ NVFP4_DEVINL int64_t ximg_offset(int n, int64_t k)
     return u * kXUnit + sb * (NTOK * 128) + n * 128 + ((c ^ (n & 7)) << 4) + e * 2;
 }
 
-__global__ void __launch_bounds__(256) skinny_prep_kernel(const uint16_t *__restrict__ x, int N, int64_t K,
-                                                          uint8_t *__restrict__ ximg, uint8_t *__restrict__ xbimg,
-                                                          int C, float *factor, int *flags, uint32_t *counters,
-                                                          int64_t T, uint32_t *err)
+constexpr int kPrepThreads = 512;
+constexpr int kPrepCache = 4;  // 16-byte chunks per thread kept in registers between the passes
+
+// One block per token n < N: per-token power of two s (max|x| * 2^s in
+// [2^15, 2^16)), the f16 image of x * 2^s in the shared-memory layout of the
+// main kernel, and the exactness flag (any element not exact in f16 after the
+// scaling -> the call uses bf16 operands and reads x itself).  All blocks also
+// zero the split-K row counters.
+__global__ void __launch_bounds__(kPrepThreads) skinny_prep_kernel(const uint16_t *__restrict__ x, int N, int64_t K,
+                                                                   uint8_t *__restrict__ ximg, float *factor,
+                                                                   int *flags, uint32_t *counters, int64_t T,
+                                                                   uint32_t *err)
 {
     tc::griddep_launch_dependents();
     tc::griddep_wait();  // x may come from the previous kernel; the workspace may be in use by it
     const int n = blockIdx.x;
     const int tid = threadIdx.x;
-    if (n == 0) {
-        for (int64_t i = tid; i < T * BM; i += blockDim.x)
-            counters[i] = 0;
-        if (tid == 0)
-            *err = 0;
-    }
-    const int64_t Kp = (int64_t)C * BKU;  // padded K of the images
-    if (n >= N) {
-        // zero rows of the images for padding tokens
-        for (int64_t k = (int64_t)tid * 8; k < Kp; k += 256 * 8) {
-            *reinterpret_cast<uint4 *>(ximg + ximg_offset(n, k)) = make_uint4(0, 0, 0, 0);
-            *reinterpret_cast<uint4 *>(xbimg + ximg_offset(n, k)) = make_uint4(0, 0, 0, 0);
-        }
-        if (tid == 0) {
-            factor[n] = 1.0f;
-            flags[n] = 0;
-        }
-        return;
-    }
-    __shared__ uint32_t red[8];
+    for (int64_t i = (int64_t)n * kPrepThreads + tid; i < T * BM; i += (int64_t)N * kPrepThreads)
+        counters[i] = 0;
+    if (n == 0 && tid == 0)
+        *err = 0;
+    __shared__ uint32_t red[kPrepThreads / 32];
     __shared__ int bad;
     const uint16_t *xr = x + (int64_t)n * K;
+    uint4 cache[kPrepCache];
     uint32_t m = 0;
-    for (int64_t k = (int64_t)tid * 8; k < K; k += 256 * 8) {
-        const uint4 v = ldg_v4(xr + k);
+    auto vmax = [&](const uint4 &v) {
         const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             m = max(m, w[i] & 0x7FFFu);
             m = max(m, (w[i] >> 16) & 0x7FFFu);
         }
+    };
+#pragma unroll
+    for (int c = 0; c < kPrepCache; ++c) {
+        const int64_t k = ((int64_t)c * kPrepThreads + tid) * 8;
+        cache[c] = k < K ? ldg_v4(xr + k) : make_uint4(0, 0, 0, 0);
     }
+#pragma unroll
+    for (int c = 0; c < kPrepCache; ++c)
+        vmax(cache[c]);
+    for (int64_t k = ((int64_t)kPrepCache * kPrepThreads + tid) * 8; k < K; k += kPrepThreads * 8)
+        vmax(ldg_v4(xr + k));
     for (int o = 16; o > 0; o >>= 1)
         m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
     if ((tid & 31) == 0)
@@ -310,10 +311,9 @@ __global__ void __launch_bounds__(256) skinny_prep_kernel(const uint16_t *__rest
         bad = 0;
     __syncthreads();
     m = 0;
-    for (int i = 0; i < 8; ++i)
+    for (int i = 0; i < kPrepThreads / 32; ++i)
         m = max(m, red[i]);
-    // s: max|x| * 2^s in [2^15, 2^16).  Non-finite, subnormal-only or extreme
-    // rows go to the bf16 mode.
+    // Non-finite, subnormal-only or extreme rows go to the bf16 mode.
     int flag = 0, s = 0;
     if (m >= 0x7F80u || (m != 0 && (m >> 7) == 0)) {
         flag = 1;
@@ -322,25 +322,30 @@ __global__ void __launch_bounds__(256) skinny_prep_kernel(const uint16_t *__rest
         if (s > 120 || s < -120)
             flag = 1;
     }
-    const float scale = flag ? 1.0f : __int_as_float((s + 127) << 23);
     int local_bad = 0;
-    for (int64_t k = (int64_t)tid * 8; k < Kp; k += 256 * 8) {
-        uint4 v = make_uint4(0, 0, 0, 0);
-        if (k < K)
-            v = ldg_v4(xr + k);
-        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-        uint32_t out[4];
+    if (!flag) {
+        const float scale = __int_as_float((s + 127) << 23);
+        auto convert = [&](const uint4 &v, int64_t k) {
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+            uint32_t out[4];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const float lo = __uint_as_float(w[i] << 16) * scale;
-            const float hi = __uint_as_float(w[i] & 0xFFFF0000u) * scale;
-            const __half hl = __float2half_rn(lo), hh = __float2half_rn(hi);
-            local_bad |= (__half2float(hl) != lo) | (__half2float(hh) != hi);
-            out[i] = (uint32_t)__half_as_ushort(hl) | ((uint32_t)__half_as_ushort(hh) << 16);
+            for (int i = 0; i < 4; ++i) {
+                const float lo = __uint_as_float(w[i] << 16) * scale;
+                const float hi = __uint_as_float(w[i] & 0xFFFF0000u) * scale;
+                const __half hl = __float2half_rn(lo), hh = __float2half_rn(hi);
+                local_bad |= (__half2float(hl) != lo) | (__half2float(hh) != hi);
+                out[i] = (uint32_t)__half_as_ushort(hl) | ((uint32_t)__half_as_ushort(hh) << 16);
+            }
+            *reinterpret_cast<uint4 *>(ximg + ximg_offset(n, k)) = make_uint4(out[0], out[1], out[2], out[3]);
+        };
+#pragma unroll
+        for (int c = 0; c < kPrepCache; ++c) {
+            const int64_t k = ((int64_t)c * kPrepThreads + tid) * 8;
+            if (k < K)
+                convert(cache[c], k);
         }
-        const int64_t off = ximg_offset(n, k);
-        *reinterpret_cast<uint4 *>(ximg + off) = make_uint4(out[0], out[1], out[2], out[3]);
-        *reinterpret_cast<uint4 *>(xbimg + off) = v;
+        for (int64_t k = ((int64_t)kPrepCache * kPrepThreads + tid) * 8; k < K; k += kPrepThreads * 8)
+            convert(ldg_v4(xr + k), k);
     }
     if (local_bad)
         atomicOr(&bad, 1);
@@ -531,7 +536,8 @@ NVFP4_DEVINL void mma_issuer(const Args &a, const IssuerArgs &p, int q)
 template <int NW>
 __global__ void __launch_bounds__(kThreads, 1)
 skinny_tc_kernel(const __grid_constant__ CUtensorMap m_codes0, const __grid_constant__ CUtensorMap m_codes1,
-                 const __grid_constant__ CUtensorMap m_scales0, const __grid_constant__ CUtensorMap m_scales1, Args a)
+                 const __grid_constant__ CUtensorMap m_scales0, const __grid_constant__ CUtensorMap m_scales1,
+                 const __grid_constant__ CUtensorMap m_x, Args a)
 {
     using C = Cfg<NW>;
     extern __shared__ uint8_t smem_raw[];
@@ -668,19 +674,21 @@ skinny_tc_kernel(const __grid_constant__ CUtensorMap m_codes0, const __grid_cons
             }
         }
     } else if (warp == 7) {
-        // ---- activation producer: per unit, one bulk copy of the N token rows
-        // of each 64-k sub-box of the activation image (the rows are
-        // contiguous there).  Rows >= N of the MMA's B operand only feed
-        // accumulator columns the epilogue ignores, so they are zeroed once and
-        // never loaded: for small N the activations then take almost no copy
-        // bandwidth from the weight stream.
+        // ---- activation producer: per unit and 64-k sub-box, the N token rows
+        // only - from the f16 image (one bulk copy; the rows are contiguous
+        // there), or in bf16 mode straight from x through its tensor map (the
+        // 128-byte swizzle lands the rows in MMA layout).  Rows >= N of the
+        // MMA's B operand only feed accumulator columns the epilogue ignores,
+        // so they are zeroed once and never loaded: for small N the
+        // activations take almost no copy bandwidth from the weight stream.
         for (int o = lane * 16; o < C::kXStages * kXUnit; o += 32 * 16)
             *reinterpret_cast<uint4 *>(x_ring + o) = make_uint4(0, 0, 0, 0);
         tc::fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
+            tc::prefetch_tensormap(&m_x);
             tc::griddep_wait();
-            const uint8_t *img = load_mode(a) ? a.xb_img : a.x_img;
+            const bool bf16_mode = load_mode(a) != 0;
             const uint32_t row_bytes = (uint32_t)a.N * 128;
             int j = j_lo, s = 0;
             uint32_t ph = 0;
@@ -689,12 +697,18 @@ skinny_tc_kernel(const __grid_constant__ CUtensorMap m_codes0, const __grid_cons
                     fail(a, 12);
                     break;
                 }
-                const uint8_t *src = img + (size_t)j * kXUnit;
                 uint8_t *dst = x_ring + (size_t)s * kXUnit;
                 tc::mbar_arrive_expect_tx(&x_full[s], 4 * row_bytes);
+                if (bf16_mode) {
 #pragma unroll
-                for (int sb = 0; sb < 4; ++sb)
-                    bulk_load(dst + sb * (NTOK * 128), src + sb * (NTOK * 128), row_bytes, &x_full[s]);
+                    for (int sb = 0; sb < 4; ++sb)
+                        tc::tma_load_2d(dst + sb * (NTOK * 128), &m_x, &x_full[s], j * BKU + sb * 64, 0);
+                } else {
+                    const uint8_t *src = a.x_img + (size_t)j * kXUnit;
+#pragma unroll
+                    for (int sb = 0; sb < 4; ++sb)
+                        bulk_load(dst + sb * (NTOK * 128), src + sb * (NTOK * 128), row_bytes, &x_full[s]);
+                }
                 if (++s == C::kXStages) {
                     s = 0;
                     ph ^= 1;
@@ -905,7 +919,7 @@ bool make_map(CUtensorMap *map, CUtensorMapDataType dt, const void *base, uint64
 }
 
 template <int NW>
-cudaError_t launch_main(const CUtensorMap (&maps)[4], const Args &a, cudaStream_t stream)
+cudaError_t launch_main(const CUtensorMap (&maps)[5], const Args &a, cudaStream_t stream)
 {
     using C = Cfg<NW>;
     static std::once_flag once;
@@ -926,7 +940,7 @@ cudaError_t launch_main(const CUtensorMap (&maps)[4], const Args &a, cudaStream_
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, skinny_tc_kernel<NW>, maps[0], maps[1], maps[2], maps[3], a);
+    return cudaLaunchKernelEx(&cfg, skinny_tc_kernel<NW>, maps[0], maps[1], maps[2], maps[3], maps[4], a);
 }
 
 }  // namespace sk
@@ -972,12 +986,11 @@ cudaError_t launch_skinny_tc(const uint16_t *x, int N, int64_t M, int64_t K, con
     a.counters = reinterpret_cast<uint32_t *>(ws + L.counters);
     a.partial = reinterpret_cast<float *>(ws + L.partial);
     a.x_img = ws + L.ximg;
-    a.xb_img = ws + L.xbimg;
     a.err = err;
     a.y = y;
     a.out_bf16 = out_bf16;
 
-    CUtensorMap maps[4];
+    CUtensorMap maps[5];
     for (int i = 0; i < 2; ++i) {
         const int s = i < n_weights ? i : 0;
         // boxes: one unit of codes (BKU/2 bytes per row, 128-byte swizzle) and
@@ -990,20 +1003,25 @@ cudaError_t launch_skinny_tc(const uint16_t *x, int N, int64_t M, int64_t K, con
                       (uint64_t)K / 16, BKU * kScaleUnits / 16, BM, CU_TENSOR_MAP_SWIZZLE_64B))
             return cudaErrorInvalidValue;
     }
+    // x itself ([N][K] bf16), read by the main kernel in bf16 mode: boxes of
+    // 64 k x N rows with the 128-byte swizzle of the MMA operand layout.
+    if (!make_map(&maps[4], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, (uint64_t)K, (uint64_t)N, (uint64_t)K * 2, 64,
+                  (uint32_t)N, CU_TENSOR_MAP_SWIZZLE_128B))
+        return cudaErrorInvalidValue;
 
     // prep (programmatic dependent launch on the previous kernel in the stream)
     {
         cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3(NTOK);
-        cfg.blockDim = dim3(256);
+        cfg.gridDim = dim3(N);
+        cfg.blockDim = dim3(kPrepThreads);
         cfg.stream = stream;
         cudaLaunchAttribute attr[1];
         attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
         attr[0].val.programmaticStreamSerializationAllowed = 1;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
-        cudaError_t e = cudaLaunchKernelEx(&cfg, skinny_prep_kernel, x, N, K, ws + L.ximg, ws + L.xbimg, a.C, factor,
-                                           flags, a.counters, a.T, err);
+        cudaError_t e = cudaLaunchKernelEx(&cfg, skinny_prep_kernel, x, N, K, ws + L.ximg, factor, flags,
+                                           a.counters, a.T, err);
         if (e != cudaSuccess)
             return e;
     }
