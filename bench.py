@@ -59,6 +59,10 @@ def parse():
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="dense9b-n1")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-prefill", action="store_true")
+    # for profiling one call kind on a short stream (ncu captures): not a bench line
+    ap.add_argument("--layers", type=int, default=None, help="override the number of layers in the stream")
+    ap.add_argument("--only", choices=["qkv", "o", "gateup", "down"], default=None,
+                    help="time only this call kind of every layer")
     return ap.parse_args()
 
 
@@ -162,11 +166,13 @@ class ClockSampler:
 class LayerStream:
     """Rotating NVFP4 layers + per-layer activations and outputs on one GPU."""
 
-    def __init__(self, workload: str, device):
+    def __init__(self, workload: str, device, n_layers=None):
         import gemm_nvfp4_gb300 as g
         from gemm_nvfp4_gb300 import inputs
         self.g = g
         shape_name, self.N, self.n_layers, heavy, outliers = WORKLOADS[workload]
+        if n_layers is not None:
+            self.n_layers = n_layers
         self.shape = getattr(inputs, shape_name)
         self.workload = workload
         shapes = self.shape.shapes()
@@ -221,8 +227,9 @@ class LayerStream:
         M, K = self.shapes[name]
         return M * K // 2 + M * K // 16 + N * K * 2 + N * M * 4
 
-    def step_bytes(self):
-        return self.n_layers * sum(self.call_bytes(n) for n in ("qkv", "o", "gateup", "down"))
+    def step_bytes(self, only=None):
+        names = ("qkv", "o", "gateup", "down") if only is None else (only,)
+        return self.n_layers * sum(self.call_bytes(n) for n in names)
 
     def weight_bytes(self):
         return self.n_layers * sum(M * K // 2 + M * K // 16 for M, K in self.shapes.values())
@@ -432,8 +439,8 @@ def main():
     if not torch.cuda.is_available():
         raise SystemExit("bench.py needs a CUDA GPU (the NVFP4 path has no CPU fallback)")
     dev = torch.device("cuda", torch.cuda.current_device())
-    st = LayerStream(args.workload, dev)
-    graph = st.capture()
+    st = LayerStream(args.workload, dev, args.layers)
+    graph = st.capture(only=args.only)
     dom_graph = st.capture(only="gateup")
 
     with ClockSampler(torch.cuda.current_device()) as clk:
@@ -467,7 +474,7 @@ def main():
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, world)
 
-    step_bytes = st.step_bytes()
+    step_bytes = st.step_bytes(args.only)
     value = world * step_bytes / (ms * 1e-3) / 1e9
     e2e_value = world * step_bytes / (e2e_ms * 1e-3) / 1e9
     hbm_peak, _, peak_kind = read_peaks()
@@ -487,7 +494,7 @@ def main():
             "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": args.workload, "layer": st.shape.name, "tokens_N": st.N,
+            "config": {"workload": args.workload, "layer": st.shape.name, "tokens_N": st.N, "only": args.only,
                        "layers": st.n_layers, "weight_bytes_per_step": st.weight_bytes(),
                        "algorithmic_bytes_per_step": step_bytes,
                        "l2": "inputs larger than L2 (rotating layers)", "graph": "one CUDA graph per step",
@@ -501,7 +508,7 @@ def main():
                          "timing": f"{st.n_layers} back-to-back calls captured alone, CUDA events"},
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-            "gpu_launches": st.launches_per_step() * args.steps,
+            "gpu_launches": st.launches_per_step(args.only) * args.steps,
             "clocks": clocks,
             "prefill": prefill,
         }
