@@ -63,6 +63,8 @@ def parse():
     ap.add_argument("--layers", type=int, default=None, help="override the number of layers in the stream")
     ap.add_argument("--only", choices=["qkv", "o", "gateup", "down"], default=None,
                     help="time only this call kind of every layer")
+    ap.add_argument("--prefill-profile", default=None, metavar="gateup:N|down:N",
+                    help="run three prefill calls of one 27B-class shape and exit (for ncu captures)")
     return ap.parse_args()
 
 
@@ -367,6 +369,29 @@ def prefill_tflops(dev, reps=5):
     return out
 
 
+def prefill_profile(dev, spec):
+    """Three prefill calls of one shape (a target for ncu; prints nothing)."""
+    import gemm_nvfp4_gb300 as g
+    from gemm_nvfp4_gb300 import inputs
+    name, n = spec.split(":")
+    N = int(n)
+    shapes = inputs.LAYER_27B.shapes()
+    if name == "gateup":
+        M, K = shapes["gate"]
+        Wg = g.nvfp4_quantize(inputs.weights(M, K, seed=inputs.matrix_seed("gate"), device=dev))
+        Wu = g.nvfp4_quantize(inputs.weights(M, K, seed=inputs.matrix_seed("up"), device=dev))
+        x = inputs.activations(N, K, seed=N, device=dev)
+        for _ in range(3):
+            g.nvfp4_gateup_swiglu(x, Wg, Wu)
+    else:
+        M, K = shapes["down"]
+        W = g.nvfp4_quantize(inputs.weights(M, K, seed=inputs.matrix_seed("down"), device=dev))
+        x = inputs.activations(N, K, seed=N, device=dev)
+        for _ in range(3):
+            g.nvfp4_gemm_prefill(x, W)
+    torch.cuda.synchronize()
+
+
 # ---------------------------------------------------------------------------
 # CPU oracle baseline
 # ---------------------------------------------------------------------------
@@ -439,6 +464,9 @@ def main():
     if not torch.cuda.is_available():
         raise SystemExit("bench.py needs a CUDA GPU (the NVFP4 path has no CPU fallback)")
     dev = torch.device("cuda", torch.cuda.current_device())
+    if args.prefill_profile:
+        prefill_profile(dev, args.prefill_profile)
+        return
     st = LayerStream(args.workload, dev, args.layers)
     graph = st.capture(only=args.only)
     dom_graph = st.capture(only="gateup")

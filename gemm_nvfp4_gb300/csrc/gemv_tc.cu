@@ -773,7 +773,8 @@ skinny_tc_kernel(const __grid_constant__ CUtensorMap m_codes0, const __grid_cons
                 ss = 0;
                 phs ^= 1;
             }
-            if (!tc::mbar_wait(&c_full[sc], phc) || !tc::mbar_wait(&s_full[ss], phs)) {
+            // the scale box of this unit was waited for at its first unit
+            if (!tc::mbar_wait(&c_full[sc], phc) || (scale_first && !tc::mbar_wait(&s_full[ss], phs))) {
                 fail(a, 16);
                 ok = false;
                 break;

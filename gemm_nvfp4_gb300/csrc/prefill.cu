@@ -30,6 +30,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <cmath>
 #include <mutex>
 
 #include "common.cuh"
@@ -51,7 +52,7 @@ constexpr int kDqThreads = kDqWarps * 32;
 template <int NW>
 struct Cfg {
     static constexpr int kStages = NW == 1 ? 4 : 3;
-    static constexpr int kPf = NW == 1 ? 4 : 3;          // dequant register prefetch depth (stages)
+    static constexpr int kPf = NW == 1 ? 4 : 3;          // dequant register prefetch depth (K steps in flight)
     static constexpr uint32_t kTmemCols = NW == 1 ? 256 : 512;
     static constexpr size_t kSmemBytes =
         (size_t)kStages * (NW * kABytes + kBBytes) + 1024 /* barriers */ + 1024 /* alignment */;
@@ -66,6 +67,7 @@ struct Args {
     int64_t N, M, K;
     int num_kb;
     uint32_t *err;
+    int row_tiles, token_tiles, group;  // raster: groups of `group` row tiles
 };
 
 // Exact bf16 dequantisation of one 32-bit code word (k = 8q .. 8q+7) into
@@ -141,8 +143,22 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 3 * S + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int64_t m0 = (int64_t)blockIdx.x * BM;
-    const int n0 = blockIdx.y * BN;
+    // Raster: the grid walks groups of `group` weight row tiles; inside a group
+    // row tiles vary fastest, then token tiles.  The host picks the group so
+    // that the operand re-read across the grid stays resident in L2.
+    int64_t row_tile, token_tile;
+    {
+        const int64_t bid = blockIdx.x;
+        const int64_t per_group = (int64_t)a.group * a.token_tiles;
+        const int64_t gidx = bid / per_group;
+        const int64_t first = gidx * a.group;
+        const int64_t rows = (a.row_tiles - first) < a.group ? (a.row_tiles - first) : a.group;
+        const int64_t in = bid - gidx * per_group;
+        row_tile = first + in % rows;
+        token_tile = in / rows;
+    }
+    const int64_t m0 = row_tile * BM;
+    const int n0 = (int)(token_tile * BN);
     const int num_kb = a.num_kb;
 
     if (threadIdx.x == 0) {
@@ -346,7 +362,7 @@ cudaError_t launch_t(const CUtensorMap &map, const Args &a, cudaStream_t stream)
     });
     if (attr_err != cudaSuccess)
         return attr_err;
-    dim3 grid((unsigned)((a.M + BM - 1) / BM), (unsigned)((a.N + BN - 1) / BN));
+    dim3 grid((unsigned)((int64_t)a.row_tiles * a.token_tiles));
     prefill_kernel<NW, ALIGNED><<<grid, kThreads, C::kSmemBytes, stream>>>(map, a);
     return cudaGetLastError();
 }
@@ -367,7 +383,8 @@ cudaError_t launch_prefill(const uint16_t *x, int64_t N, int64_t M, int64_t K, c
     auto encode = pf::encode_fn();
     if (!encode)
         return cudaErrorNotSupported;
-    if (N > 65535LL * pf::BN || (M + pf::BM - 1) / pf::BM > 0x7FFFFFFF)
+    const int64_t row_tiles = (M + pf::BM - 1) / pf::BM, token_tiles = (N + pf::BN - 1) / pf::BN;
+    if (row_tiles * token_tiles > 0x7FFFFFFF)
         return cudaErrorInvalidValue;
     CUtensorMap map;
     const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)N};
@@ -393,6 +410,26 @@ cudaError_t launch_prefill(const uint16_t *x, int64_t N, int64_t M, int64_t K, c
     a.K = K;
     a.num_kb = (int)((K + pf::BK - 1) / pf::BK);
     a.err = reinterpret_cast<uint32_t *>(workspace);
+    a.row_tiles = (int)row_tiles;
+    a.token_tiles = (int)token_tiles;
+    {
+        // Which operand stays in L2 for the whole grid: if the activations fit,
+        // token tiles vary fastest (group of 1 row tile: x is read from HBM
+        // once, each weight row tile once per wave); else if the weights fit,
+        // row tiles vary fastest (one group of all rows); else groups whose
+        // weights fit.
+        constexpr double kL2Budget = 110e6;  // of the 129 MB L2
+        const double x_bytes = (double)N * (double)K * 2.0;
+        const double w_tile = (double)pf::BM * (double)K * 0.5625 * n_weights;
+        int g;
+        if (x_bytes <= kL2Budget)
+            g = 1;
+        else if (w_tile * (double)row_tiles <= kL2Budget)
+            g = (int)row_tiles;
+        else
+            g = (int)(kL2Budget / w_tile);
+        a.group = g < 1 ? 1 : (g > (int)row_tiles ? (int)row_tiles : g);
+    }
     const bool aligned = K % 32 == 0;
     if (n_weights == 1)
         return aligned ? pf::launch_t<1, true>(map, a, stream) : pf::launch_t<1, false>(map, a, stream);
