@@ -18,22 +18,28 @@
 //                chosen so max|x'_n| is in [2^15, 2^16).  If any element of
 //                any token is not exact in f16, the call falls back to bf16
 //                operands (slower dequant, same exact products).  Also zeroes
-//                the split-K counters.
+//                the split-K tile counters.
 //   main kernel  one CTA per SM, stream-K over units (tile of 128 rows,
-//                128 k) so every SM streams the same bytes:
-//     warp 0     TMA: code tile [128 rows][64 B] (64-byte swizzle) and scale
-//                tile [128 rows][16 B] per unit into an 8-deep ring.  It does
-//                not depend on the prep kernel, so it starts streaming weights
-//                while the previous kernel and the prep kernel still run.
-//     warp 2     TMA: activation tile [16 tokens][128 k] (128-byte swizzle).
-//     warps 3-10 dequantise: thread = weight row = TMEM lane; codes and scales
-//                from shared memory -> f16x2 (or bf16x2) -> tcgen05.st into a
-//                TMEM ring of A operands; group 0 also runs the epilogue.
-//     warp 1     allocates TMEM; one thread issues tcgen05.mma kind::f16
-//                (M=128, N=16, K=16, A in TMEM) into a double-buffered fp32
-//                accumulator in TMEM.
-//   A tile split across CTAs is finished by the last CTA to arrive (counter in
-//   the workspace), which adds the partials in CTA order: deterministic.
+//                256 k) so every SM streams the same bytes:
+//     warps 4,5  TMA: the code box [128 rows][128 B] (128-byte swizzle) and
+//                scale box [128 rows][16 B] of each unit (even / odd units)
+//                into a 10-unit ring.  They do not depend on the prep kernel,
+//                so weights stream while the previous kernel still runs.
+//     warp 6     activation copies: the N token rows of each unit.
+//     warps 12-27 dequantise in four independent groups: item t (half a unit,
+//                or a quarter unit of both gate and up matrices) goes to group
+//                t % 4; thread = weight row = TMEM lane; codes and scales from
+//                shared memory -> f16x2 (or bf16x2) -> tcgen05.st into a
+//                6-item TMEM ring.  Groups work on different items, so one
+//                group's waits overlap another's arithmetic.
+//     warps 0-3  one thread each issues tcgen05.mma kind::f16 (M=128, N=16,
+//                K=16, A in TMEM) into its own fp32 accumulator chain in a
+//                double-buffered TMEM accumulator.
+//     warps 8-11 epilogue: chains added in a fixed order, whole tiles stored.
+//   A tile split across CTAs is finished by the last CTA to arrive (one
+//   counter per tile in the workspace), which adds the partials in CTA order:
+//   deterministic.  The CTA's last segment is added by the epilogue and the
+//   dequantiser threads together.
 //
 // Every product is exact in the fp32 accumulator (f16 operands: at most 6 and
 // 8 significant bits; bf16 fallback likewise).  All waits are bounded.
@@ -53,53 +59,61 @@ namespace sk {
 
 constexpr int BM = 128;          // weight rows per tile (MMA M, TMEM lanes)
 constexpr int BKU = 256;         // k per unit (one code box per matrix)
-constexpr int kScaleUnits = 4;   // units covered by one scale box (1024 k)
 constexpr int NTOK = 16;         // MMA N (tokens, padded)
-// Warp roles: 0..3 MMA issuers (one per SM sub-partition), 4 and 5 code
-// producers (even / odd units), 6 scale producer, 7 activation producer,
-// 8..23 dequantisers (four groups of four warps, one warp per TMEM lane
-// quarter).  Several producer threads are used because one thread issuing TMA
-// copies back to back tops out well below HBM bandwidth on GB300, while two to
-// four issuing threads reach it.  Several MMA issuers are used because a
-// thread issuing tcgen05.mma competes for issue slots with the dequantiser
-// warps of its sub-partition; N = 16 MMAs are short, so issue rate matters.
+// Warp roles: 0..3 MMA issuers (one per SM sub-partition), 4 and 5 weight
+// producers (even / odd units: codes and scales), 6 activation producer,
+// 7 idle, 8..11 epilogue (one warp per TMEM lane quarter), 12..27
+// dequantisers (four groups of four warps, one warp per lane quarter).
+// Several producer threads are used because one thread issuing TMA copies
+// back to back tops out well below HBM bandwidth on GB300, while two to four
+// issuing threads reach it.  Several MMA issuers are used because a thread
+// issuing tcgen05.mma competes for issue slots with the dequantiser warps of
+// its sub-partition; N = 16 MMAs are short, so issue rate matters.
 constexpr int kMmaWarps = 4;
-constexpr int kFirstDqWarp = 8;
+constexpr int kEpiWarp0 = 8;
+constexpr int kFirstDqWarp = 12;
 constexpr int kDqWarps = 16;
+constexpr int kGroups = 4;           // dequantiser groups
 constexpr int kThreads = (kFirstDqWarp + kDqWarps) * 32;
-constexpr int kDqThreads = kDqWarps * 32;
-constexpr int kEpiThreads = 128;     // the first dequantiser group
+constexpr int kEpiThreads = 128;
 constexpr int kCodeBox = BM * 128;   // 16 KB: 128 rows x 128 code bytes (256 k), 128-byte swizzle
-constexpr int kScaleBox = BM * 64;   // 8 KB: 128 rows x 64 scale bytes (1024 k), 64-byte swizzle
+constexpr int kScaleBox = BM * 16;   // 2 KB: 128 rows x 16 scale bytes (256 k), no swizzle
 constexpr int kXUnit = NTOK * BKU * 2;  // 8 KB: activation image of one unit
 constexpr uint32_t kTmemCols = 512;
 
 template <int NW>
 struct Cfg {
-    // The code ring holds most of the shared memory: with ~4 us of loaded
+    // The weight ring holds most of the shared memory: with ~4 us of loaded
     // DRAM latency, every SM needs well over 100 KB of weights in flight.
-    static constexpr int kCStages = NW == 1 ? 10 : 5;  // code ring (units)
-    static constexpr int kSStages = 2;                  // scale ring (kScaleUnits units each)
+    // A stage holds one unit: NW code boxes, then NW scale boxes.
+    static constexpr int kStageBytes = NW * (kCodeBox + kScaleBox);
+    static constexpr int kCStages = NW == 1 ? 10 : 5;  // weight ring (units)
     static constexpr int kXStages = NW == 1 ? 4 : 3;   // activation ring (units, from L2)
-    // One unit = kSubs TMEM A sub-stages of 128 columns.  Group g of the
-    // dequantisers fills columns [col0(g), +kGroupCols) of sub-stage sub(g).
-    //   NW = 1: 1 sub-stage of 256 k; group g fills k [64g, 64g+64) (32 columns).
-    //   NW = 2: 2 sub-stages of 128 k x 2 matrices; group g fills matrix g/2,
-    //           sub-stage g%2 (64 columns).
-    static constexpr int kSubs = NW;
-    static constexpr int kSubK = BKU / kSubs;
-    static constexpr int kAFullCount = kDqWarps / kSubs;  // one arrival per dequantiser warp
-    static constexpr int kAStages = 3;                 // TMEM A ring (128 columns each)
-    static constexpr int kACols = 128;
+    // Work item of one dequantiser group = one TMEM A stage of 64 columns
+    // (128 weights per row):
+    //   NW = 1: half a unit (128 k); group g takes half g % 2 of the units
+    //           i = g / 2 (mod 2) of the CTA's range;
+    //   NW = 2: a quarter unit (64 k) of both matrices (matrix m in columns
+    //           [32m, 32m+32)); group g takes quarter g of every unit.
+    // Item t = i * kItems + h goes to group t % 4, so the groups run on
+    // different items and one group's waits overlap another's arithmetic.
+    static constexpr int kItems = NW == 1 ? 2 : 4;     // items per unit
+    static constexpr int kUnitStep = kGroups / kItems;  // units between two items of a group
+    static constexpr int kItemK = BKU / kItems;          // k per item (per matrix)
+    static constexpr int kReaders = kItems * 4;          // warps that read one weight stage
+    static constexpr int kAStages = 6;                   // TMEM A ring (items)
+    static constexpr int kACols = 64;
     // Independent accumulation chains per matrix: issuer q accumulates matrix
-    // q / kChains over the K steps kk = q % kChains (mod kChains) into its own
-    // chain; the epilogue adds the chains in a fixed order.
+    // q / kChains over the K steps kk = q % kChains (mod kChains) of each item
+    // into its own chain; the epilogue adds the chains in a fixed order.
     static constexpr int kChains = kMmaWarps / NW;
+    static constexpr int kPerItem = kItemK / 16 / kChains;  // MMAs per issuer and item
     static constexpr int kDCols = 16 * NW * kChains;   // one accumulator buffer
-    static constexpr size_t kSmemBytes = (size_t)kCStages * NW * kCodeBox + (size_t)kSStages * NW * kScaleBox +
-                                         (size_t)kXStages * kXUnit + 1024 + 1024;
+    static constexpr size_t kSmemBytes = (size_t)kCStages * kStageBytes + (size_t)kXStages * kXUnit + 1024 + 1024;
+    static_assert(kPerItem == 2, "two MMAs per issuer and item");
     static_assert(kAStages * kACols + 2 * kDCols <= (int)kTmemCols, "TMEM budget");
     static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+    static_assert(kStageBytes % 1024 == 0, "code boxes stay 1024-byte aligned (128-byte swizzle)");
 };
 
 struct Args {
@@ -112,7 +126,7 @@ struct Args {
     const float *ts[2];
     const float *factor;   // [16] 2^-s_n
     const int *flags;      // [16] 1 if token n is not exact in f16
-    uint32_t *counters;    // [T][128] per-row arrival counters
+    uint32_t *counters;    // [T] per-tile arrival counters
     float *partial;        // [P][2][NW][16][128]
     const uint8_t *x_img;  // [C][8 KB] f16 activation image (shared-memory layout)
     uint32_t *err;
@@ -120,7 +134,7 @@ struct Args {
     int out_bf16;
 };
 
-// Workspace layout (bytes): header 256 (factor[16], flags[16], err), per-row
+// Workspace layout (bytes): header 256 (factor[16], flags[16], err), per-tile
 // counters, the f16 activation image, split-K partials.
 struct WsLayout {
     size_t counters, ximg, partial, total;
@@ -134,7 +148,7 @@ inline WsLayout ws_layout(int64_t M, int64_t K, int nw)
     const int64_t T = (M + BM - 1) / BM;
     const int64_t C = (K + BKU - 1) / BKU;
     w.counters = 256;
-    w.ximg = w.counters + round_up((size_t)T * BM * 4, 1024);
+    w.ximg = w.counters + round_up((size_t)T * 4, 1024);
     w.partial = w.ximg + (size_t)C * kXUnit;
     w.total = w.partial + (size_t)kSkinnyTcMaxCtas * 2 * nw * NTOK * BM * 4;
     return w;
@@ -276,7 +290,7 @@ __global__ void __launch_bounds__(kPrepThreads) skinny_prep_kernel(const uint16_
     tc::griddep_wait();  // x may come from the previous kernel; the workspace may be in use by it
     const int n = blockIdx.x;
     const int tid = threadIdx.x;
-    for (int64_t i = (int64_t)n * kPrepThreads + tid; i < T * BM; i += (int64_t)N * kPrepThreads)
+    for (int64_t i = (int64_t)n * kPrepThreads + tid; i < T; i += (int64_t)N * kPrepThreads)
         counters[i] = 0;
     if (n == 0 && tid == 0)
         *err = 0;
@@ -361,88 +375,116 @@ __global__ void __launch_bounds__(kPrepThreads) skinny_prep_kernel(const uint16_
 // main kernel
 // ---------------------------------------------------------------------------
 
-// Epilogue of one tile segment for thread row r: whole tiles are written
-// directly; split tiles publish this row's partial and the last CTA to arrive
-// for the row (per-row counter) adds all partials of the row in CTA order.
-// fac[mi][n] (shared memory): tensor scale times the activation factor.
+// Output value of row m, token n from the fp32 sums of the matrices.
 template <int NW>
-__device__ __noinline__ void epilogue(const Args &a, const float *fac, const float (&v)[NW][16], int tile, int j,
-                                      int u, int first_tile, int b, int r)
+NVFP4_DEVINL void store_out(const Args &a, const float *fac, int n, int64_t m, float s0, float s1)
 {
-    constexpr int kMaxSplit = 8;  // partials loaded together by the last arriver
+    const float val = NW == 1 ? s0 * fac[n] : silu_mul(s0 * fac[n], s1 * fac[NTOK + n]);
+    const int64_t idx = (int64_t)n * a.M + m;
+    if (a.out_bf16)
+        reinterpret_cast<uint16_t *>(a.y)[idx] = f32_to_bf16(val);
+    else
+        reinterpret_cast<float *>(a.y)[idx] = val;
+}
+
+// Split-K bookkeeping of one tile segment, shared by the epilogue threads
+// and (for the CTA's last segment) the dequantiser threads.
+struct SegInfo {
+    int tile, b_lo, b_hi, reduce;
+};
+
+// Epilogue of one tile segment, run by the 128 epilogue threads (thread r
+// holds row r's sums v[mi][n]).  A tile done by this CTA alone is written
+// directly.  Otherwise the CTA publishes its partial ([mi][n][row] floats) and
+// counts its arrival on the tile's counter with one release-acquire atomic
+// after a barrier of the epilogue threads (the barrier orders every thread's
+// partial stores before the release).  Returns in `si` whether this CTA
+// arrived last and must add the tile's partials (reduce_tile).
+template <int NW>
+__device__ __noinline__ void publish_segment(const Args &a, const float *fac, const float (&v)[NW][16], int tile,
+                                             int j, int u, int first_tile, int b, int r, SegInfo *si)
+{
     const uint32_t total = (uint32_t)a.total, P = (uint32_t)a.P, C = (uint32_t)a.C;
     const int64_t m = (int64_t)tile * BM + r;
     const bool whole = (j == a.C - 1) && (u - j >= (int)cta_lo(b, total, P));
-    float acc[NW][NTOK];
+    if (whole) {  // uniform across the epilogue threads
+        if (m < a.M)
+#pragma unroll
+            for (int n = 0; n < NTOK; ++n)
+                if (n < a.N)
+                    store_out<NW>(a, fac, n, m, v[0][n], v[NW - 1][n]);
+        if (r == 0)
+            si->reduce = 0;
+        return;
+    }
+    const int slot = (tile == first_tile) ? 0 : 1;
+    float *mine = a.partial + ((size_t)b * 2 + slot) * NW * NTOK * BM + r;
 #pragma unroll
     for (int mi = 0; mi < NW; ++mi)
 #pragma unroll
         for (int n = 0; n < NTOK; ++n)
-            acc[mi][n] = v[mi][n];
-    if (!whole) {
-        const int slot = (tile == first_tile) ? 0 : 1;
-        float *mine = a.partial + ((size_t)b * 2 + slot) * NW * NTOK * BM + r;
-#pragma unroll
-        for (int mi = 0; mi < NW; ++mi)
-#pragma unroll
-            for (int n = 0; n < NTOK; ++n)
-                if (n < a.N)
-                    mine[(mi * NTOK + n) * BM] = acc[mi][n];
+            if (n < a.N)
+                mine[(mi * NTOK + n) * BM] = v[mi][n];
+    tc::named_bar_sync(1, kEpiThreads);
+    if (r == 0) {
         const int b_lo = cta_of((uint32_t)tile * C, total, P);
         const int b_hi = cta_of(((uint32_t)tile + 1) * C - 1, total, P);
-        // acq_rel: publishes this thread's partial (release) and, for the last
-        // arriver, makes the other CTAs' partials of this row visible (acquire).
-        const uint32_t old = atom_add_acq_rel(&a.counters[(size_t)tile * BM + r], 1u);
-        if (old != (uint32_t)(b_hi - b_lo))
-            return;  // another CTA finishes this row
-        // Sum the partials of CTAs b_lo..b_hi in CTA order, kMaxSplit CTAs per
-        // round, all loads of a round in flight together.
+        // release: this CTA's partial (every thread's stores, ordered before
+        // this atomic by the barrier); acquire: the other CTAs' partials.
+        const uint32_t old = atom_add_acq_rel(&a.counters[tile], 1u);
+        si->tile = tile;
+        si->b_lo = b_lo;
+        si->b_hi = b_hi;
+        si->reduce = old == (uint32_t)(b_hi - b_lo);
+    }
+    tc::named_bar_sync(1, kEpiThreads);
+}
+
+// Last arriver of a split tile: add the partials of CTAs b_lo..b_hi in CTA
+// order (deterministic) and write the outputs.  Threads t = 0..nthr-1 share
+// the work: pair p = (token n, rows 4q..4q+3) for p = t, t + nthr, ...; each
+// pair's partials are read with 16-byte loads, kBatch CTAs in flight.
+template <int NW>
+__device__ __noinline__ void reduce_tile(const Args &a, const float *fac, const SegInfo si, int t, int nthr)
+{
+    constexpr int kBatch = 4;
+    const uint32_t total = (uint32_t)a.total, P = (uint32_t)a.P, C = (uint32_t)a.C;
+    const int np = a.N * (BM / 4);
+    for (int p = t; p < np; p += nthr) {
+        const int n = p / (BM / 4), r4 = (p % (BM / 4)) * 4;
+        float4 acc[NW];
 #pragma unroll
         for (int mi = 0; mi < NW; ++mi)
+            acc[mi] = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int b0 = si.b_lo; b0 <= si.b_hi; b0 += kBatch) {
+            float4 pv[kBatch][NW];
 #pragma unroll
-            for (int n = 0; n < NTOK; ++n)
-                acc[mi][n] = 0.0f;
-        for (int b0 = b_lo; b0 <= b_hi; b0 += kMaxSplit) {
-            const float *src[kMaxSplit];
+            for (int q = 0; q < kBatch; ++q) {
+                const int bb = b0 + q <= si.b_hi ? b0 + q : si.b_hi;
+                const int sl = ((int)(cta_lo((uint32_t)bb, total, P) / C) == si.tile) ? 0 : 1;
+                const float *src = a.partial + ((size_t)bb * 2 + sl) * NW * NTOK * BM + r4;
 #pragma unroll
-            for (int q = 0; q < kMaxSplit; ++q) {
-                const int bb = b0 + q <= b_hi ? b0 + q : b_hi;
-                const int sl = ((int)(cta_lo((uint32_t)bb, total, P) / C) == tile) ? 0 : 1;
-                src[q] = a.partial + ((size_t)bb * 2 + sl) * NW * NTOK * BM + r;
+                for (int mi = 0; mi < NW; ++mi)
+                    pv[q][mi] = __ldcg(reinterpret_cast<const float4 *>(src + (mi * NTOK + n) * BM));
             }
 #pragma unroll
-            for (int mi = 0; mi < NW; ++mi)
+            for (int q = 0; q < kBatch; ++q)
+                if (b0 + q <= si.b_hi)
 #pragma unroll
-                for (int n = 0; n < NTOK; ++n) {
-                    if (n < a.N) {
-                        float pv[kMaxSplit];
-#pragma unroll
-                        for (int q = 0; q < kMaxSplit; ++q)
-                            pv[q] = __ldcg(src[q] + (mi * NTOK + n) * BM);
-#pragma unroll
-                        for (int q = 0; q < kMaxSplit; ++q)
-                            if (b0 + q <= b_hi)
-                                acc[mi][n] += pv[q];
+                    for (int mi = 0; mi < NW; ++mi) {
+                        acc[mi].x += pv[q][mi].x;
+                        acc[mi].y += pv[q][mi].y;
+                        acc[mi].z += pv[q][mi].z;
+                        acc[mi].w += pv[q][mi].w;
                     }
-                }
         }
-    }
-    if (m >= a.M)
-        return;
+        const int64_t m0 = (int64_t)si.tile * BM + r4;
+        const float g[4] = {acc[0].x, acc[0].y, acc[0].z, acc[0].w};
+        const float h[4] = {acc[NW - 1].x, acc[NW - 1].y, acc[NW - 1].z, acc[NW - 1].w};
 #pragma unroll
-    for (int n = 0; n < NTOK; ++n) {
-        if (n < a.N) {
-            float val;
-            if (NW == 1)
-                val = acc[0][n] * fac[n];
-            else
-                val = silu_mul(acc[0][n] * fac[n], acc[NW - 1][n] * fac[NTOK + n]);
-            const int64_t idx = (int64_t)n * a.M + m;
-            if (a.out_bf16)
-                reinterpret_cast<uint16_t *>(a.y)[idx] = f32_to_bf16(val);
-            else
-                reinterpret_cast<float *>(a.y)[idx] = val;
-        }
+        for (int e = 0; e < 4; ++e)
+            if (m0 + e < a.M)
+                store_out<NW>(a, fac, n, m0 + e, g[e], h[e]);
     }
 }
 
@@ -454,32 +496,31 @@ struct IssuerArgs {
 };
 
 // One MMA issuer (warp q, lane 0): matrix q / kChains, accumulator chain
-// q % kChains, K steps kk = chain (mod kChains) of every sub-stage - four MMAs
-// per sub-stage in both configurations.  The descriptor and TMEM offsets of
-// those MMAs are computed once, so each MMA costs a few issue slots (the
-// issuing thread shares its sub-partition with ALU-bound dequantisers).  One
-// copy of the loop serves all issuers: per-issuer specialisations multiply the
-// kernel's code size and starve the dequantisers' instruction fetch.
+// q % kChains, K steps kk = chain (mod kChains) of every item - two MMAs per
+// item in both configurations.  The descriptor and TMEM offsets of those MMAs
+// are computed once, so each MMA costs a few issue slots (the issuing thread
+// shares its sub-partition with ALU-bound dequantisers).  One copy of the loop
+// serves all issuers: per-issuer specialisations multiply the kernel's code
+// size and starve the dequantisers' instruction fetch.
 template <int NW>
 NVFP4_DEVINL void mma_issuer(const Args &a, const IssuerArgs &p, int q)
 {
     using C = Cfg<NW>;
-    constexpr int kPerSub = C::kSubK / 16 / C::kChains;
-    static_assert(kPerSub == 4, "four MMAs per issuer and sub-stage");
+    constexpr int kI = C::kItems, kT = C::kPerItem;
     const int mi = q / C::kChains;
     const int chain = q % C::kChains;
-    uint32_t boff[C::kSubs][kPerSub], aoff[kPerSub];
+    uint32_t boff[kI][kT], aoff[kT];
 #pragma unroll
-    for (int t = 0; t < kPerSub; ++t) {
-        const int kk = chain + C::kChains * t;
-        aoff[t] = (uint32_t)(mi * 64 + kk * 8);
+    for (int t = 0; t < kT; ++t) {
+        const int kk = chain + C::kChains * t;  // K step within the item
+        aoff[t] = (uint32_t)(mi * 32 + kk * 8);
 #pragma unroll
-        for (int sub = 0; sub < C::kSubs; ++sub) {
-            const int kl = sub * C::kSubK + kk * 16;  // k within the unit
+        for (int h = 0; h < kI; ++h) {
+            const int kl = h * C::kItemK + kk * 16;  // k within the unit
             // B: 64-k sub-box kl / 64 of the activation unit (16 rows x 128 B,
             // 128-byte swizzle), 32-byte step kl % 64 inside it; descriptor
             // addresses are in 16-byte units.
-            boff[sub][t] = (uint32_t)((kl >> 6) * (NTOK * 128 / 16) + 2 * ((kl >> 4) & 3));
+            boff[h][t] = (uint32_t)((kl >> 6) * (NTOK * 128 / 16) + 2 * ((kl >> 4) & 3));
         }
     }
     const uint32_t idesc = tc::idesc_f16kind(BM, NTOK, (uint32_t)load_mode(a));
@@ -504,7 +545,7 @@ NVFP4_DEVINL void mma_issuer(const Args &a, const IssuerArgs &p, int q)
         const uint64_t bdesc0 = tc::smem_desc_sw128(p.x_ring + (size_t)sx * kXUnit);
         const uint32_t dcol = p.tmem_d + (uint32_t)(seg & 1) * C::kDCols + (uint32_t)(chain * NW + mi) * 16;
 #pragma unroll
-        for (int sub = 0; sub < C::kSubs; ++sub) {
+        for (int h = 0; h < kI; ++h) {
             if (!tc::mbar_wait(&p.a_full[sa], pha)) {
                 fail(a, 15);
                 return;
@@ -512,9 +553,9 @@ NVFP4_DEVINL void mma_issuer(const Args &a, const IssuerArgs &p, int q)
             tc::fence_after_sync();
             const uint32_t acol = p.tmem_a + (uint32_t)(sa * C::kACols);
 #pragma unroll
-            for (int t = 0; t < kPerSub; ++t)
-                tc::mma_f16_ts(dcol, acol + aoff[t], bdesc0 + boff[sub][t], idesc,
-                               (first && sub == 0 && t == 0) ? 0u : 1u);
+            for (int t = 0; t < kT; ++t)
+                tc::mma_f16_ts(dcol, acol + aoff[t], bdesc0 + boff[h][t], idesc,
+                               (first && h == 0 && t == 0) ? 0u : 1u);
             tc::mma_commit(&p.a_empty[sa]);
             if (++sa == C::kAStages) {
                 sa = 0;
@@ -542,15 +583,12 @@ skinny_tc_kernel(const __grid_constant__ CUtensorMap m_codes0, const __grid_cons
     using C = Cfg<NW>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t *c_ring = smem;                                                   // [kCStages][NW][16 KB]
-    uint8_t *s_ring = c_ring + (size_t)C::kCStages * NW * kCodeBox;           // [kSStages][NW][16 KB]
-    uint8_t *x_ring = s_ring + (size_t)C::kSStages * NW * kScaleBox;          // [kXStages][8 KB]
+    uint8_t *c_ring = smem;                                          // [kCStages][NW codes, NW scales]
+    uint8_t *x_ring = c_ring + (size_t)C::kCStages * C::kStageBytes;  // [kXStages][8 KB]
     uint64_t *bars = reinterpret_cast<uint64_t *>(x_ring + (size_t)C::kXStages * kXUnit);
     uint64_t *c_full = bars;
     uint64_t *c_empty = c_full + C::kCStages;
-    uint64_t *s_full = c_empty + C::kCStages;
-    uint64_t *s_empty = s_full + C::kSStages;
-    uint64_t *x_full = s_empty + C::kSStages;
+    uint64_t *x_full = c_empty + C::kCStages;
     uint64_t *x_empty = x_full + C::kXStages;
     uint64_t *a_full = x_empty + C::kXStages;
     uint64_t *a_empty = a_full + C::kAStages;
@@ -558,6 +596,7 @@ skinny_tc_kernel(const __grid_constant__ CUtensorMap m_codes0, const __grid_cons
     uint64_t *d_empty = d_full + 2;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(d_empty + 2);
     float *fac_s = reinterpret_cast<float *>(tmem_slot + 4);  // [NW][16] epilogue factors
+    SegInfo *seg_s = reinterpret_cast<SegInfo *>(fac_s + 2 * NTOK);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int b = blockIdx.x;
@@ -572,18 +611,14 @@ skinny_tc_kernel(const __grid_constant__ CUtensorMap m_codes0, const __grid_cons
         // of per-thread arrivals on one mbarrier serialise in shared memory.
         for (int s = 0; s < C::kCStages; ++s) {
             tc::mbar_init(&c_full[s], 1);
-            tc::mbar_init(&c_empty[s], kDqWarps);
-        }
-        for (int s = 0; s < C::kSStages; ++s) {
-            tc::mbar_init(&s_full[s], 1);
-            tc::mbar_init(&s_empty[s], kDqWarps);
+            tc::mbar_init(&c_empty[s], C::kReaders);
         }
         for (int s = 0; s < C::kXStages; ++s) {
             tc::mbar_init(&x_full[s], 1);
             tc::mbar_init(&x_empty[s], kMmaWarps);
         }
         for (int s = 0; s < C::kAStages; ++s) {
-            tc::mbar_init(&a_full[s], C::kAFullCount);
+            tc::mbar_init(&a_full[s], 4);  // the four warps of one group
             tc::mbar_init(&a_empty[s], kMmaWarps);
         }
         for (int s = 0; s < 2; ++s) {
@@ -614,7 +649,8 @@ skinny_tc_kernel(const __grid_constant__ CUtensorMap m_codes0, const __grid_cons
     const int j_lo = (int)(lo - tile_lo * a.C);
 
     if (warp == 4 || warp == 5) {
-        // ---- code producers: even units (warp 4) and odd units (warp 5) ----
+        // ---- weight producers: even units (warp 4) and odd units (warp 5);
+        // a unit's code and scale boxes complete one barrier ----
         if (lane == 0) {
             const int par = warp - 4;
             int64_t tile = tile_lo;
@@ -630,12 +666,15 @@ skinny_tc_kernel(const __grid_constant__ CUtensorMap m_codes0, const __grid_cons
                     fail(a, 11);
                     break;
                 }
-                uint8_t *st = c_ring + (size_t)s * NW * kCodeBox;
-                tc::mbar_arrive_expect_tx(&c_full[s], NW * kCodeBox);
+                uint8_t *st = c_ring + (size_t)s * C::kStageBytes;
+                tc::mbar_arrive_expect_tx(&c_full[s], C::kStageBytes);
 #pragma unroll
-                for (int mi = 0; mi < NW; ++mi)
+                for (int mi = 0; mi < NW; ++mi) {
                     tc::tma_load_2d(st + mi * kCodeBox, mi == 0 ? &m_codes0 : &m_codes1, &c_full[s], j * (BKU / 2),
                                     (int)(tile * BM));
+                    tc::tma_load_2d(st + NW * kCodeBox + mi * kScaleBox, mi == 0 ? &m_scales0 : &m_scales1,
+                                    &c_full[s], j * (BKU / 16), (int)(tile * BM));
+                }
                 j += 2;
                 while (j >= a.C) {
                     j -= a.C;
@@ -644,36 +683,6 @@ skinny_tc_kernel(const __grid_constant__ CUtensorMap m_codes0, const __grid_cons
             }
         }
     } else if (warp == 6) {
-        // ---- scale producer: one 2048-k box per matrix per scale stage ----
-        if (lane == 0) {
-            int64_t tile = tile_lo;
-            int j = j_lo;
-            int s = 0;
-            uint32_t ph = 0;
-            for (int i = 0; i < n_units; ++i) {
-                if (i == 0 || j % kScaleUnits == 0) {
-                    if (!tc::mbar_wait(&s_empty[s], ph ^ 1)) {
-                        fail(a, 19);
-                        break;
-                    }
-                    uint8_t *st = s_ring + (size_t)s * NW * kScaleBox;
-                    tc::mbar_arrive_expect_tx(&s_full[s], NW * kScaleBox);
-#pragma unroll
-                    for (int mi = 0; mi < NW; ++mi)
-                        tc::tma_load_2d(st + mi * kScaleBox, mi == 0 ? &m_scales0 : &m_scales1, &s_full[s],
-                                        (j / kScaleUnits) * (kScaleUnits * BKU / 16), (int)(tile * BM));
-                    if (++s == C::kSStages) {
-                        s = 0;
-                        ph ^= 1;
-                    }
-                }
-                if (++j == a.C) {
-                    j = 0;
-                    ++tile;
-                }
-            }
-        }
-    } else if (warp == 7) {
         // ---- activation producer: per unit and 64-k sub-box, the N token rows
         // only - from the f16 image (one bulk copy; the rows are contiguous
         // there), or in bf16 mode straight from x through its tensor map (the
@@ -724,121 +733,37 @@ skinny_tc_kernel(const __grid_constant__ CUtensorMap m_codes0, const __grid_cons
             IssuerArgs ia{x_ring, x_full, x_empty, a_full, a_empty, d_full, d_empty, tmem_a, tmem_d, n_units, j_lo};
             mma_issuer<NW>(a, ia, warp);
         }
-    } else {
-        // ---- dequantisers (warps 8..23) and epilogue (warps 8..11) ----
+    } else if (warp >= kEpiWarp0 && warp < kEpiWarp0 + 4) {
+        // ---- epilogue (warps 8..11, one per TMEM lane quarter) ----
         tc::griddep_wait();
         const int mode = load_mode(a);
-        const int dq = threadIdx.x - kFirstDqWarp * 32;  // 0..511
-        if (dq < NW * NTOK) {
-            const int mi = dq / NTOK, n = dq % NTOK;
+        const int et = threadIdx.x - kEpiWarp0 * 32;  // 0..127
+        if (et < NW * NTOK) {
+            const int mi = et / NTOK, n = et % NTOK;
             const float t = __ldg(a.ts[mi]);
-            fac_s[dq] = mode ? t * 256.0f : t * a.factor[n];
+            fac_s[et] = mode ? t * 256.0f : t * a.factor[n];
         }
-        tc::named_bar_sync(1, kDqThreads);  // fac_s visible to the epilogue threads
-        const int grp = dq >> 7;                          // 0..3
-        const int quarter = warp & 3;                     // TMEM lane quarter this warp may access
-        const int r = quarter * 32 + lane;                // row within the tile
+        if (et == 0)
+            seg_s->reduce = 0;
+        tc::named_bar_sync(1, kEpiThreads);  // fac_s visible to all epilogue threads
+        const int quarter = warp & 3;
+        const int r = quarter * 32 + lane;
         const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-        // This group's share of a unit: 16-byte code chunks chunk0.. (32 k each)
-        // of sub-stage my_sub of matrix my_mi, and the scale bytes of those
-        // chunks (2 per chunk) at byte sc_off of the unit's 16 scale bytes.
-        const int my_sub = (NW == 1) ? 0 : (grp & 1);
-        const int my_mi = (NW == 1) ? 0 : (grp >> 1);
-        const int chunk0 = (NW == 1) ? grp * 2 : (grp & 1) * 4;
-        constexpr int kChunks = NW == 1 ? 2 : 4;
-        const int sc_off = chunk0 * 2;
-        const uint32_t col0 = (NW == 1) ? (uint32_t)grp * 32 : (uint32_t)my_mi * 64;
-        const int swz = r & 7;
         int64_t tile = tile_lo;
         int j = j_lo;
         int seg = -1;
-        int sc = 0, ss = 0, sa = 0;
-        uint32_t phc = 0, phs = 0, pha = 0;
-        // A sub-stage of unit i for this group: the ring advances by kSubs per
-        // unit; this group's slot is my_sub sub-stages further.
-        for (int t = 0; t < my_sub; ++t)
-            if (++sa == C::kAStages) {
-                sa = 0;
-                pha ^= 1;
-            }
-        bool ok = true;
-        for (int i = 0; i < n_units && ok; ++i) {
+        for (int i = 0; i < n_units; ++i) {
             const bool first = (i == 0) || j == 0;
             const bool last = (i == n_units - 1) || j == a.C - 1;
-            const bool scale_first = (i == 0) || (j % kScaleUnits == 0);
-            const bool scale_last = last || ((j + 1) % kScaleUnits == 0);
             if (first)
                 ++seg;
-            if (scale_first && i > 0 && ++ss == C::kSStages) {  // unit 0 uses scale stage 0
-                ss = 0;
-                phs ^= 1;
-            }
-            // the scale box of this unit was waited for at its first unit
-            if (!tc::mbar_wait(&c_full[sc], phc) || (scale_first && !tc::mbar_wait(&s_full[ss], phs))) {
-                fail(a, 16);
-                ok = false;
-                break;
-            }
-            // copy this thread's codes and scales to registers, release the slots
-            const uint8_t *crow = c_ring + ((size_t)sc * NW + my_mi) * kCodeBox + r * 128;
-            uint4 cw[kChunks];
-#pragma unroll
-            for (int c = 0; c < kChunks; ++c)
-                cw[c] = *reinterpret_cast<const uint4 *>(crow + (((chunk0 + c) ^ swz) << 4));
-            // 64-byte rows, 64-byte swizzle: 16-byte chunk c of row r sits at c ^ ((r >> 1) & 3).
-            const uint8_t *sp = s_ring + ((size_t)ss * NW + my_mi) * kScaleBox + r * 64 +
-                                (((j % kScaleUnits) ^ ((r >> 1) & 3)) << 4) + sc_off;
-            uint32_t scw[kChunks / 2];
-            if (NW == 1) {
-                scw[0] = *reinterpret_cast<const uint32_t *>(sp);
-            } else {
-                const uint2 v2 = *reinterpret_cast<const uint2 *>(sp);
-                scw[0] = v2.x;
-                scw[kChunks / 2 - 1] = v2.y;
-            }
-            __syncwarp();
-            if (lane == 0) {
-                tc::mbar_arrive(&c_empty[sc]);
-                if (scale_last)
-                    tc::mbar_arrive(&s_empty[ss]);
-            }
-            if (++sc == C::kCStages) {
-                sc = 0;
-                phc ^= 1;
-            }
-
-            // dequantise and store into this group's columns of A sub-stage (unit i, my_sub)
-            if (!tc::mbar_wait(&a_empty[sa], pha ^ 1)) {
-                fail(a, 17);
-                ok = false;
-                break;
-            }
-            tc::fence_after_sync();
-            const uint32_t acol = tmem_a + sa * C::kACols + col0 + lane_off;
-#pragma unroll
-            for (int h = 0; h < kChunks / 2; ++h) {  // 64 k -> 32 TMEM columns per store
-                uint32_t out[32];
-                dequant_chunk(cw[2 * h], scw[h] & 0xFFFF, mode, out);
-                dequant_chunk(cw[2 * h + 1], scw[h] >> 16, mode, out + 16);
-                tc::tmem_st_32x32b_x32(acol + h * 32, out);
-            }
-            tc::tmem_st_wait();
-            tc::fence_before_sync();
-            __syncwarp();
-            if (lane == 0)
-                tc::mbar_arrive(&a_full[sa]);
-            for (int t = 0; t < C::kSubs; ++t)
-                if (++sa == C::kAStages) {
-                    sa = 0;
-                    pha ^= 1;
-                }
-
-            if (last && grp == 0) {
-                // ---- epilogue for this tile segment (first dequantiser group) ----
+            if (last) {
                 const int db = seg & 1;
-                if (!tc::mbar_wait(&d_full[db], ((uint32_t)seg >> 1) & 1)) {
+                // every epilogue thread takes the same branch (named barriers follow)
+                if (!tc::bar_and(1, kEpiThreads, tc::mbar_wait(&d_full[db], ((uint32_t)seg >> 1) & 1))) {
                     fail(a, 18);
-                    ok = false;
+                    if (et == 0)
+                        seg_s->reduce = 0;
                     break;
                 }
                 tc::fence_after_sync();
@@ -865,13 +790,104 @@ skinny_tc_kernel(const __grid_constant__ CUtensorMap m_codes0, const __grid_cons
                 __syncwarp();
                 if (lane == 0)
                     tc::mbar_arrive(&d_empty[db]);
-                epilogue<NW>(a, fac_s, sum, (int)tile, j, (int)(lo + i), (int)tile_lo, b, r);
+                publish_segment<NW>(a, fac_s, sum, (int)tile, j, (int)(lo + i), (int)tile_lo, b, r, seg_s);
+                if (i == n_units - 1)
+                    break;  // the CTA's last segment is reduced by all threads below
+                if (seg_s->reduce)
+                    reduce_tile<NW>(a, fac_s, *seg_s, r, kEpiThreads);
             }
             if (++j == a.C) {
                 j = 0;
                 ++tile;
             }
         }
+        // The dequantisers have finished: they help with the last segment.
+        tc::named_bar_sync(2, kEpiThreads + kDqWarps * 32);
+        if (seg_s->reduce)
+            reduce_tile<NW>(a, fac_s, *seg_s, r, kEpiThreads + kDqWarps * 32);
+    } else if (warp >= kFirstDqWarp) {
+        // ---- dequantisers (warps 12..27): group g takes items t = g (mod 4) ----
+        tc::griddep_wait();
+        const int mode = load_mode(a);
+        const int g = (warp - kFirstDqWarp) >> 2;
+        const int quarter = warp & 3;  // TMEM lane quarter this warp may access
+        const int r = quarter * 32 + lane;  // row within the tile
+        const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+        const int swz = r & 7;
+        constexpr int kCh = BKU / C::kItems / 32;  // 16-byte code chunks per matrix and item
+        const int h = (NW == 1) ? (g & 1) : g;     // item within the unit
+        int i = (NW == 1) ? (g >> 1) : 0;          // first unit of this group
+        // Ring positions: unit i in the weight ring, item i * kItems + h in the
+        // A ring (both below the ring sizes here, so phase 0).
+        int sc = i, sa = i * C::kItems + h;
+        uint32_t phc = 0, pha = 0;
+        for (; i < n_units; i += C::kUnitStep) {
+            if (!tc::mbar_wait(&c_full[sc], phc)) {
+                fail(a, 16);
+                break;
+            }
+            // copy this thread's codes and scale bytes to registers, release the stage
+            const uint8_t *stage = c_ring + (size_t)sc * C::kStageBytes;
+            uint4 cw[NW][kCh];
+            uint32_t scw[NW][kCh / 2];
+#pragma unroll
+            for (int mi = 0; mi < NW; ++mi) {
+                const uint8_t *crow = stage + mi * kCodeBox + r * 128;
+#pragma unroll
+                for (int c = 0; c < kCh; ++c)
+                    cw[mi][c] = *reinterpret_cast<const uint4 *>(crow + (((h * kCh + c) ^ swz) << 4));
+                // scale bytes of the item: two per chunk, 16 per row and unit
+                const uint8_t *srow = stage + NW * kCodeBox + mi * kScaleBox + r * 16 + h * kCh * 2;
+                if (kCh == 4) {
+                    const uint2 v2 = *reinterpret_cast<const uint2 *>(srow);
+                    scw[mi][0] = v2.x;
+                    scw[mi][kCh / 2 - 1] = v2.y;
+                } else {
+                    scw[mi][0] = *reinterpret_cast<const uint32_t *>(srow);
+                }
+            }
+            __syncwarp();
+            if (lane == 0)
+                tc::mbar_arrive(&c_empty[sc]);
+            sc += C::kUnitStep;
+            if (sc >= C::kCStages) {
+                sc -= C::kCStages;
+                phc ^= 1;
+            }
+
+            // dequantise into A stage sa: 64 columns = two stores of 32
+            if (!tc::mbar_wait(&a_empty[sa], pha ^ 1)) {
+                fail(a, 17);
+                break;
+            }
+            tc::fence_after_sync();
+            const uint32_t acol = tmem_a + sa * C::kACols + lane_off;
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {  // NW = 1: chunks 2q, 2q+1; NW = 2: matrix q
+                const int mi = NW == 1 ? 0 : q;
+                const int c0 = NW == 1 ? 2 * q : 0;
+                const uint32_t sw = scw[mi][NW == 1 ? q : 0];
+                uint32_t out[32];
+                dequant_chunk(cw[mi][c0], sw & 0xFFFF, mode, out);
+                dequant_chunk(cw[mi][c0 + 1], sw >> 16, mode, out + 16);
+                tc::tmem_st_32x32b_x32(acol + q * 32, out);
+            }
+            tc::tmem_st_wait();
+            tc::fence_before_sync();
+            __syncwarp();
+            if (lane == 0)
+                tc::mbar_arrive(&a_full[sa]);
+            sa += kGroups;
+            if (sa >= C::kAStages) {
+                sa -= C::kAStages;
+                pha ^= 1;
+            }
+        }
+        // help the epilogue threads add the partials of the CTA's last segment
+        tc::named_bar_sync(2, kEpiThreads + kDqWarps * 32);
+        if (seg_s->reduce)
+            reduce_tile<NW>(a, fac_s, *seg_s, kEpiThreads + (threadIdx.x - kFirstDqWarp * 32),
+                            kEpiThreads + kDqWarps * 32);
     }
 
     // Lane 0 of the producer and MMA warps ran their loops alone: reconverge
@@ -996,12 +1012,11 @@ cudaError_t launch_skinny_tc(const uint16_t *x, int N, int64_t M, int64_t K, con
         const int s = i < n_weights ? i : 0;
         // boxes: one unit of codes (BKU/2 bytes per row, 128-byte swizzle) and
         // of scales (BKU/16 bytes per row), 128 rows each
-        static_assert(kCodeBox == BM * (BKU / 2) && kScaleBox == BM * (BKU * kScaleUnits / 16), "box sizes");
-        static_assert(BKU * kScaleUnits / 16 == 64, "scale box rows are 64 bytes (64-byte swizzle)");
+        static_assert(kCodeBox == BM * (BKU / 2) && kScaleBox == BM * (BKU / 16), "box sizes");
         if (!make_map(&maps[i], CU_TENSOR_MAP_DATA_TYPE_UINT8, codes[s], (uint64_t)K / 2, (uint64_t)M,
                       (uint64_t)K / 2, BKU / 2, BM, CU_TENSOR_MAP_SWIZZLE_128B) ||
             !make_map(&maps[2 + i], CU_TENSOR_MAP_DATA_TYPE_UINT8, scales[s], (uint64_t)K / 16, (uint64_t)M,
-                      (uint64_t)K / 16, BKU * kScaleUnits / 16, BM, CU_TENSOR_MAP_SWIZZLE_64B))
+                      (uint64_t)K / 16, BKU / 16, BM, CU_TENSOR_MAP_SWIZZLE_NONE))
             return cudaErrorInvalidValue;
     }
     // x itself ([N][K] bf16), read by the main kernel in bf16 mode: boxes of

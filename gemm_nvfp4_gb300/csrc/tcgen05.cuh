@@ -267,5 +267,22 @@ NVFP4_DEVINL void named_bar_sync(uint32_t id, uint32_t nthreads)
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
+// Named barrier that also returns the AND of `v` over the participating
+// threads: every participant gets the same answer, so the branch it guards
+// is uniform (needed before further named barriers).
+NVFP4_DEVINL bool bar_and(uint32_t id, uint32_t nthreads, bool v)
+{
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.and.pred q, %2, %3, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)v), "r"(id), "r"(nthreads)
+        : "memory");
+    return r != 0;
+}
+
 }  // namespace tc
 }  // namespace nvfp4
