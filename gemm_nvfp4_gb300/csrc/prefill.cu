@@ -9,14 +9,19 @@
 //
 //   CTA tile: 128 weight rows (MMA M) x 256 tokens (MMA N), K in stages of 64.
 //   warp 0      TMA producer: x tile [256 tokens][64 k] bf16, 128-byte swizzle.
-//   warp 1      allocates TMEM; one thread issues tcgen05.mma (bf16 x bf16 ->
-//               fp32, A and B from shared memory) and commits to mbarriers.
-//   warps 2..9  dequantise: each thread turns 32 k of one weight row (16 code
+//   warp 1      allocates TMEM.  Warps 1 and 2: one thread each issues
+//               tcgen05.mma (bf16 x bf16 -> fp32, A and B from shared
+//               memory) and commits to mbarriers: for the gate/up pair each
+//               owns one matrix's accumulator, for one matrix each takes half
+//               of every stage's K steps into its own accumulator (a thread
+//               needs longer to issue an M=128, N=256 MMA than the tensor core
+//               needs to run it).
+//   warps 3..10 dequantise: each thread turns 32 k of one weight row (16 code
 //               bytes, 2 scale bytes, read straight from global memory with a
-//               register prefetch ring) into exact bf16 values
+//               4-stage register prefetch ring) into exact bf16 values
 //               e2m1 * scale * 2^-8 and stores them in the 128-byte-swizzled
 //               K-major layout the MMA reads; then, after the K loop, they read
-//               the fp32 accumulator out of TMEM (tcgen05.ld) and store
+//               the fp32 accumulators out of TMEM (tcgen05.ld) and store
 //               y = acc * 2^8 * ts, or h = silu(g) * u for the gate/up pair.
 //
 // Exactness: every product e2m1 * scale * x is exact in the fp32 accumulator
@@ -44,7 +49,9 @@ constexpr int BM = 128;
 constexpr int BN = 256;
 constexpr int BK = 64;
 constexpr int kDqWarps = 8;
-constexpr int kThreads = 64 + kDqWarps * 32;
+constexpr int kIssuers = 2;  // MMA-issuing warps (1 and 2)
+constexpr int kFirstDqWarp = 1 + kIssuers;
+constexpr int kThreads = kFirstDqWarp * 32 + kDqWarps * 32;
 constexpr int kABytes = BM * BK * 2;  // 16 KB per weight matrix per stage
 constexpr int kBBytes = BN * BK * 2;  // 32 KB per stage
 constexpr int kDqThreads = kDqWarps * 32;
@@ -52,8 +59,8 @@ constexpr int kDqThreads = kDqWarps * 32;
 template <int NW>
 struct Cfg {
     static constexpr int kStages = NW == 1 ? 4 : 3;
-    static constexpr int kPf = NW == 1 ? 4 : 3;          // dequant register prefetch depth (K steps in flight)
-    static constexpr uint32_t kTmemCols = NW == 1 ? 256 : 512;
+    static constexpr int kPf = 4;                         // dequant register prefetch depth (K steps in flight)
+    static constexpr uint32_t kTmemCols = 512;  // two accumulators of 256 columns
     static constexpr size_t kSmemBytes =
         (size_t)kStages * (NW * kABytes + kBBytes) + 1024 /* barriers */ + 1024 /* alignment */;
 };
@@ -165,9 +172,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         for (int s = 0; s < S; ++s) {
             tc::mbar_init(&full_a[s], kDqThreads);
             tc::mbar_init(&full_b[s], 1);
-            tc::mbar_init(&empty[s], 1);
+            tc::mbar_init(&empty[s], kIssuers);
         }
-        tc::mbar_init(tmem_full, 1);
+        tc::mbar_init(tmem_full, kIssuers);
         tc::fence_mbar_init();
         tc::prefetch_tensormap(&tmap_x);
         if (blockIdx.x == 0 && blockIdx.y == 0 && *a.err != 0)
@@ -194,9 +201,14 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
                 tc::tma_load_2d(sb + (size_t)s * kBBytes, &tmap_x, &full_b[s], kb * BK, n0);
             }
         }
-    } else if (warp == 1) {
-        // ---------------- MMA issuer ----------------
+    } else if (warp < kFirstDqWarp) {
+        // ---------------- MMA issuers (warps 1, 2) ----------------
+        // A thread spends longer issuing one M=128, N=256 MMA than the tensor
+        // core takes to run it, so two threads issue: for the gate/up pair
+        // issuer q owns matrix q; for one matrix issuer q takes the K steps
+        // 2q, 2q+1 of every stage into accumulator q (added in the epilogue).
         if (lane == 0) {
+            const int q = warp - 1;
             constexpr uint32_t idesc = tc::idesc_bf16(BM, BN);
             bool ok = true;
             for (int kb = 0; kb < num_kb && ok; ++kb) {
@@ -209,13 +221,18 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
                 }
                 tc::fence_after_sync();
                 const uint64_t bdesc = tc::smem_desc_sw128(sb + (size_t)s * kBBytes);
-#pragma unroll
-                for (int mi = 0; mi < NW; ++mi) {
-                    const uint64_t adesc = tc::smem_desc_sw128(sa + ((size_t)s * NW + mi) * kABytes);
+                if (NW == 2) {
+                    const uint64_t adesc = tc::smem_desc_sw128(sa + ((size_t)s * NW + q) * kABytes);
 #pragma unroll
                     for (int k = 0; k < BK / 16; ++k)
-                        tc::mma_bf16_ss(tmem_base + mi * BN, adesc + 2 * k, bdesc + 2 * k, idesc,
+                        tc::mma_bf16_ss(tmem_base + q * BN, adesc + 2 * k, bdesc + 2 * k, idesc,
                                         (kb > 0 || k > 0) ? 1u : 0u);
+                } else {
+                    const uint64_t adesc = tc::smem_desc_sw128(sa + (size_t)s * kABytes);
+#pragma unroll
+                    for (int k = 2 * q; k < 2 * q + 2; ++k)
+                        tc::mma_bf16_ss(tmem_base + q * BN, adesc + 2 * k, bdesc + 2 * k, idesc,
+                                        (kb > 0 || k > 2 * q) ? 1u : 0u);
                 }
                 tc::mma_commit(&empty[s]);
             }
@@ -223,7 +240,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         }
     } else {
         // ---------------- dequantise producers ----------------
-        const int dq = threadIdx.x - 64;           // 0..255
+        const int dq = threadIdx.x - kFirstDqWarp * 32;  // 0..255
         const int row = dq & (BM - 1);             // 0..127
         const int half = dq >> 7;                  // which 32 k of the 64-k stage
         const int64_t m = m0 + row;
@@ -279,7 +296,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         tc::fence_after_sync();
         if (have) {
             const int quarter = warp & 3;          // TMEM lanes this warp may access
-            const int chalf = (warp - 2) >> 2;     // which 128 of the 256 token columns
+            const int chalf = (warp - kFirstDqWarp) >> 2;  // which 128 of the 256 token columns
             const int64_t mrow = m0 + quarter * 32 + lane;
             float ts[NW];
 #pragma unroll
@@ -289,10 +306,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
             for (int cc = 0; cc < 4; ++cc) {
                 const int col = chalf * 128 + cc * 32;
                 const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + col;
-                uint32_t r[NW][32];
+                // two accumulators: gate and up, or (one matrix) K steps 0-1 and 2-3
+                uint32_t r[2][32];
                 tc::tmem_ld_32x32b_x32(taddr, r[0]);
-                if (NW == 2)
-                    tc::tmem_ld_32x32b_x32(taddr + BN, r[NW - 1]);
+                tc::tmem_ld_32x32b_x32(taddr + BN, r[1]);
                 tc::tmem_ld_wait();
                 if (mrow < a.M) {
 #pragma unroll
@@ -301,7 +318,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
                         if (n < a.N) {
                             float v;
                             if (NW == 1) {
-                                v = __uint_as_float(r[0][j]) * ts[0];
+                                v = (__uint_as_float(r[0][j]) + __uint_as_float(r[1][j])) * ts[0];
                             } else {
                                 const float gg = __uint_as_float(r[0][j]) * ts[0];
                                 const float uu = __uint_as_float(r[NW - 1][j]) * ts[NW - 1];
