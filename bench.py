@@ -218,7 +218,7 @@ class LayerStream:
             self.y.append(ys)
         ws_need = max(g.nvfp4_workspace_bytes(g.NVFP4_OP_GEMV_SKINNY, N, M, K) for M, K in shapes.values())
         ws_need = max(ws_need, g.nvfp4_workspace_bytes(g.NVFP4_OP_GATEUP_SWIGLU, N, *shapes["gate"]))
-        self.ws = torch.empty(ws_need, dtype=torch.uint8, device=device)
+        self.ws = torch.zeros(ws_need, dtype=torch.uint8, device=device)  # skinny workspace: zero-filled once
 
     # algorithmic bytes (codes + scales + x + y) of each call kind
     def call_bytes(self, name):

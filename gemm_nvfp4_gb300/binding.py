@@ -140,7 +140,8 @@ def _workspace(op, N, M, K, device, workspace):
         return workspace, workspace.numel() * workspace.element_size()
     if need == 0:
         return None, 0
-    return torch.empty(need, dtype=torch.uint8, device=device), need
+    # zero-filled: the skinny calls keep split-K counters in it
+    return torch.zeros(need, dtype=torch.uint8, device=device), need
 
 
 def _out_code(dtype) -> int:

@@ -341,8 +341,6 @@ __global__ void __launch_bounds__(256) gemv_fixup_kernel(GemvArgs a)
     const int b_hi = cta_of((tile + 1) * a.chunks - 1, a.total, a.P);
     const int tok = threadIdx.x >> 4, row = threadIdx.x & 15;
     const int64_t m = tile * kTileRows + row;
-    if (tok >= a.N || m >= a.M)
-        return;
     float ts[NW];
 #pragma unroll
     for (int mi = 0; mi < NW; ++mi)
@@ -355,10 +353,14 @@ __global__ void __launch_bounds__(256) gemv_fixup_kernel(GemvArgs a)
         const int64_t bfirst = ((int64_t)bb * a.total / a.P) / a.chunks;
         const int slot = (bfirst == tile) ? 0 : 1;
 #pragma unroll
-        for (int mi = 0; mi < NW; ++mi)
-            v[mi] += a.partial[(((int64_t)bb * 2 + slot) * NW + mi) * 256 + row * 16 + tok];
+        for (int mi = 0; mi < NW; ++mi) {
+            float *pp = a.partial + (((int64_t)bb * 2 + slot) * NW + mi) * 256 + row * 16 + tok;
+            v[mi] += *pp;
+            *pp = 0.0f;  // consumed: the workspace is left zero for the next call
+        }
     }
-    store_out(a.y, a.out_bf16, (int64_t)tok * a.M + m, finish<NW>(v, ts));
+    if (tok < a.N && m < a.M)
+        store_out(a.y, a.out_bf16, (int64_t)tok * a.M + m, finish<NW>(v, ts));
 }
 
 template <int NW, int NT, bool ALIGNED>
@@ -374,7 +376,7 @@ size_t skinny_workspace_bytes(int64_t M, int64_t K, int n_weights)
 {
     if (skinny_tc_supported(M, K))
         return skinny_tc_workspace_bytes(M, K, n_weights);
-    return (size_t)kGemvMaxCtas * kGemvPartialFloatsPerCta * n_weights * 4;
+    return 256 + (size_t)kGemvMaxCtas * kGemvPartialFloatsPerCta * n_weights * 4;
 }
 
 int64_t gemv_grid(int64_t M, int64_t K, int num_sms)
@@ -402,7 +404,7 @@ cudaError_t launch_gemv(const uint16_t *x, int N, int64_t M, int64_t K, const ui
     }
     a.y = y;
     a.out_bf16 = out_bf16;
-    a.partial = reinterpret_cast<float *>(workspace);
+    a.partial = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(workspace) + 256);  // after the header
     a.tiles = (M + kTileRows - 1) / kTileRows;
     a.chunks = (K + kChunkK - 1) / kChunkK;
     a.total = a.tiles * a.chunks;

@@ -132,10 +132,18 @@ struct Args {
     uint32_t *err;
     void *y;
     int out_bf16;
+    int bf16_only;  // 1: no prep kernel; bf16 operands read from x itself
 };
 
 // Workspace layout (bytes): header 256 (factor[16], flags[16], err), per-tile
-// counters, the f16 activation image, split-K partials.
+// split-K counters in a fixed region of kCounterRegion bytes, the f16
+// activation image, split-K partials.  The counters must be zero when a call
+// without the prep kernel starts; every call leaves them zero (the last CTA to
+// arrive on a tile resets its counter), and the fixed region keeps any call's
+// image or partials from landing on a later call's counters (the mma.sync
+// path, whose partials do start at byte 256, zeroes every partial it reads).
+constexpr size_t kCounterRegion = size_t(1) << 20;
+
 struct WsLayout {
     size_t counters, ximg, partial, total;
 };
@@ -147,8 +155,9 @@ inline WsLayout ws_layout(int64_t M, int64_t K, int nw)
     WsLayout w;
     const int64_t T = (M + BM - 1) / BM;
     const int64_t C = (K + BKU - 1) / BKU;
+    (void)T;
     w.counters = 256;
-    w.ximg = w.counters + round_up((size_t)T * 4, 1024);
+    w.ximg = w.counters + kCounterRegion;
     w.partial = w.ximg + (size_t)C * kXUnit;
     w.total = w.partial + (size_t)kSkinnyTcMaxCtas * 2 * nw * NTOK * BM * 4;
     return w;
@@ -241,6 +250,8 @@ NVFP4_DEVINL void fail(const Args &a, uint32_t code) { atomicExch(a.err, code); 
 
 NVFP4_DEVINL int load_mode(const Args &a)
 {
+    if (a.bf16_only)
+        return 1;
     int f = 0;
     for (int n = 0; n < a.N; ++n)
         f |= a.flags[n];
@@ -436,6 +447,8 @@ __device__ __noinline__ void publish_segment(const Args &a, const float *fac, co
         si->b_lo = b_lo;
         si->b_hi = b_hi;
         si->reduce = old == (uint32_t)(b_hi - b_lo);
+        if (si->reduce)
+            a.counters[tile] = 0;  // all of the tile's CTAs have arrived: zero for the next call
     }
     tc::named_bar_sync(1, kEpiThreads);
 }
@@ -458,14 +471,15 @@ __device__ __noinline__ void reduce_tile(const Args &a, const float *fac, const 
             acc[mi] = make_float4(0.f, 0.f, 0.f, 0.f);
         for (int b0 = si.b_lo; b0 <= si.b_hi; b0 += kBatch) {
             float4 pv[kBatch][NW];
+            float4 *src[kBatch];
 #pragma unroll
             for (int q = 0; q < kBatch; ++q) {
                 const int bb = b0 + q <= si.b_hi ? b0 + q : si.b_hi;
                 const int sl = ((int)(cta_lo((uint32_t)bb, total, P) / C) == si.tile) ? 0 : 1;
-                const float *src = a.partial + ((size_t)bb * 2 + sl) * NW * NTOK * BM + r4;
+                src[q] = reinterpret_cast<float4 *>(a.partial + ((size_t)bb * 2 + sl) * NW * NTOK * BM + r4 + n * BM);
 #pragma unroll
                 for (int mi = 0; mi < NW; ++mi)
-                    pv[q][mi] = __ldcg(reinterpret_cast<const float4 *>(src + (mi * NTOK + n) * BM));
+                    pv[q][mi] = __ldcg(src[q] + mi * (NTOK * BM / 4));
             }
 #pragma unroll
             for (int q = 0; q < kBatch; ++q)
@@ -968,8 +982,9 @@ bool skinny_tc_supported(int64_t M, int64_t K)
 {
     if (K < 256 || K % 256 != 0 || M < 1)
         return false;
-    const int64_t units = ((M + 127) / 128) * (K / 256);
-    return units * kSkinnyTcMaxCtas < (INT64_C(1) << 31);
+    const int64_t tiles = (M + 127) / 128;
+    const int64_t units = tiles * (K / 256);
+    return units * kSkinnyTcMaxCtas < (INT64_C(1) << 31) && tiles * 4 <= (int64_t)sk::kCounterRegion;
 }
 
 size_t skinny_tc_workspace_bytes(int64_t M, int64_t K, int n_weights)
@@ -1025,8 +1040,15 @@ cudaError_t launch_skinny_tc(const uint16_t *x, int N, int64_t M, int64_t K, con
                   (uint32_t)N, CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
 
-    // prep (programmatic dependent launch on the previous kernel in the stream)
-    {
+    // One matrix with N >= 2: no prep kernel; the main kernel reads x itself as
+    // bf16 operands (products exact either way, and fp32 sums of exactly
+    // scaled products scale exactly, so the results are the same bits).  The
+    // prep's latency outweighs the cheaper f16 dequantisation here, while the
+    // fused gate/up pair (twice the dequantisation per unit) and N = 1 keep
+    // it.  The split-K counters are then zero from the previous call (every
+    // call leaves the workspace zero) instead of being zeroed by the prep.
+    a.bf16_only = (n_weights == 1 && N >= 2) ? 1 : 0;
+    if (!a.bf16_only) {
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(N);
         cfg.blockDim = dim3(kPrepThreads);

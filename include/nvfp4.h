@@ -38,9 +38,15 @@
  *     stream reaches that point.
  *   - Workspace: scratch device memory of at least nvfp4_workspace_bytes(...)
  *     bytes, 256-byte aligned, owned by the caller and not used by anything
- *     else while the call's kernels run.  Its contents need no initialisation
- *     and are garbage afterwards.  Calls that share a workspace must be ordered
- *     on one stream.
+ *     else while the call's kernels run.  Calls that share a workspace must be
+ *     ordered on one stream.  The products with N <= 16 (skinny path) keep
+ *     split-K arrival counters in it: their workspace must be zero-filled
+ *     before its first use (cudaMemsetAsync), and every such call leaves the
+ *     counters at zero again, so one zeroing serves any number of skinny
+ *     calls of any shapes.  Do not write to it between skinny calls (a quantise or
+ *     prefill call on the same buffer counts as writing), and zero it again
+ *     after a call that failed.  The quantise and prefill calls need no
+ *     initialisation and leave their workspace undefined.
  *   - Errors: arguments are checked on the host before anything is enqueued;
  *     a bad argument returns a nonzero nvfp4_status and nothing runs.  A
  *     failed launch returns NVFP4_ERR_CUDA.  The library never aborts or prints.
@@ -126,8 +132,10 @@ int nvfp4_quantize(const float *w, int64_t M, int64_t K,
  * codes, scales, tensor_scale: the NVFP4 weight W[M][K] (device)
  * y        device [N][M], fp32 (out_dtype NVFP4_OUT_F32) or bf16 bits
  *          (NVFP4_OUT_BF16, round-to-nearest-even of the fp32 result)
- * workspace device scratch of nvfp4_workspace_bytes(NVFP4_OP_GEMV_SKINNY, N, M, K)
- *          (partial sums of rows whose K range is split across thread blocks).
+ * workspace device scratch of nvfp4_workspace_bytes(NVFP4_OP_GEMV_SKINNY, N, M, K),
+ *          zero-filled before first use (see Workspace above): partial sums of
+ *          rows whose K range is split across thread blocks, and their
+ *          arrival counters.
  * Returns NVFP4_ERR_UNSUPPORTED_SHAPE for N outside 1..16. */
 int nvfp4_gemv_skinny(const uint16_t *x, int64_t N,
                       const uint8_t *codes, const uint8_t *scales,
@@ -182,9 +190,9 @@ int nvfp4_gemm_prefill(const uint16_t *x, int64_t N,
  *   - Size limit: returns NVFP4_ERR_WORKSPACE, with nothing enqueued, when the
  *     problem needs more scratch than NVFP4_NOALLOC_SCRATCH_BYTES (that is,
  *     when nvfp4_workspace_bytes(NVFP4_OP_GEMV_SKINNY, N, M, K) exceeds it).
- *   - Sharing: every call on a device uses the same array, which keeps the last
- *     call's contents.  The kernels need none of it to start at zero (each call
- *     writes every partial it reads).  Calls whose kernels overlap on the GPU
+ *   - Sharing: every call on a device uses the same array.  It starts
+ *     zero-filled and every call leaves its split-K counters at zero, as the
+ *     skinny workspace contract requires.  Calls whose kernels overlap on the GPU
  *     (different streams without ordering) race on the array; order them on
  *     one stream. */
 #define NVFP4_NOALLOC_SCRATCH_BYTES ((size_t)8 << 20)

@@ -175,7 +175,7 @@ def test_workspace_reuse_back_to_back():
     W2, r2, x2 = make_case(12288, 4096, 4, seed=2)
     need = max(g.nvfp4_workspace_bytes(g.NVFP4_OP_GEMV_SKINNY, 1, 4096, 4096),
                g.nvfp4_workspace_bytes(g.NVFP4_OP_GEMV_SKINNY, 4, 12288, 4096))
-    ws = torch.empty(need, dtype=torch.uint8, device=DEV)
+    ws = torch.zeros(need, dtype=torch.uint8, device=DEV)  # zero-filled once, kept zero by every call
     outs = []
     for _ in range(3):
         outs.append(g.nvfp4_gemv_skinny(x1.to(DEV), W1, workspace=ws))
@@ -187,3 +187,29 @@ def test_workspace_reuse_back_to_back():
         assert torch.equal(o, outs[1])
     y_ref, A = oracle.gemv(bf16_bits(x2), *r2, rows=np.arange(0, 12288, 97))
     assert_close(to_np(outs[1])[:, ::97], y_ref, gemv_tol(y_ref, A), "reuse")
+
+
+def test_workspace_left_zero_across_paths():
+    """The skinny calls keep split-K counters in a fixed region of the
+    workspace (bytes 256 .. 256 + 1 MiB) and leave it zero: one zeroing
+    serves a mixed sequence of shapes and paths (prep kernel or not, gate/up,
+    the mma.sync path for K % 256 != 0), and each result equals the same call
+    on a fresh workspace."""
+    cases = [(4096, 4096, 1, 1), (12288, 4096, 4, 1), (4096, 4096, 2, 2), (300, 4000, 3, 1),
+             (5120, 17408, 16, 1), (640, 2048, 7, 1), (12288, 4096, 1, 2)]
+    need = 0
+    for M, K, N, nw in cases:
+        op = g.NVFP4_OP_GEMV_SKINNY if nw == 1 else g.NVFP4_OP_GATEUP_SWIGLU
+        need = max(need, g.nvfp4_workspace_bytes(op, N, M, K))
+    ws = torch.zeros(need, dtype=torch.uint8, device=DEV)
+    for i, (M, K, N, nw) in enumerate(cases):
+        Ws = [g.nvfp4_quantize(inputs.weights(M, K, seed=50 + 10 * i + j).to(DEV)) for j in range(nw)]
+        x = inputs.activations(N, K, seed=7 + i).to(DEV)
+        call = (lambda w: g.nvfp4_gemv_skinny(x, Ws[0], workspace=w)) if nw == 1 else \
+            (lambda w: g.nvfp4_gateup_swiglu(x, Ws[0], Ws[1], workspace=w))
+        got = call(ws)
+        torch.cuda.synchronize()
+        assert int(torch.count_nonzero(ws[256:256 + (1 << 20)]).item()) == 0, f"counters not left zero after case {i}"
+        ref = call(None)  # fresh zero-filled workspace from the binding
+        torch.cuda.synchronize()
+        assert torch.equal(got, ref), f"case {i}"
