@@ -254,13 +254,16 @@ class LayerStream:
         for li in range(self.n_layers):
             self.run_layer(li, only)
 
-    # our kernels per call: the activation prep kernel and the main kernel
-    # (split-K partials are reduced inside the main kernel)
-    LAUNCHES_PER_CALL = 2
+    def launches_per_call(self, name):
+        """Our kernels per call: the activation prep kernel and the main kernel
+        (split-K partials are reduced inside the main kernel); a single matrix
+        with N >= 2 skips the prep kernel (the main kernel reads x itself)."""
+        single = name != "gateup"
+        return 1 if (single and self.N >= 2) else 2
 
     def launches_per_step(self, only=None):
-        calls = 4 if only is None else 1
-        return self.n_layers * calls * self.LAUNCHES_PER_CALL
+        names = ["qkv", "o", "gateup", "down"] if only is None else [only]
+        return self.n_layers * sum(self.launches_per_call(n) for n in names)
 
     def capture(self, only=None):
         graph = torch.cuda.CUDAGraph()
