@@ -36,10 +36,15 @@
 //                K=16, A in TMEM) into its own fp32 accumulator chain in a
 //                double-buffered TMEM accumulator.
 //     warps 8-11 epilogue: chains added in a fixed order, whole tiles stored.
-//   A tile split across CTAs is finished by the last CTA to arrive (one
-//   counter per tile in the workspace), which adds the partials in CTA order:
-//   deterministic.  The CTA's last segment is added by the epilogue and the
-//   dequantiser threads together.
+//   K is split across CTAs in one of two ways, chosen by the host from the
+//   shapes: stream-K (each CTA a contiguous share of the tile-major unit
+//   list; a tile split across CTAs is finished by the last CTA to arrive, one
+//   counter per tile in the workspace, adding the partials in CTA order; the
+//   CTA's last segment is added by the epilogue and dequantiser threads
+//   together), or cluster-K for one matrix whose tiles fit one per cluster
+//   (a cluster of 4 CTAs splits each tile's K; the leader adds the partials of
+//   ranks 0..3 in order through distributed shared memory).  Both are
+//   deterministic.
 //
 // Every product is exact in the fp32 accumulator (f16 operands: at most 6 and
 // 8 significant bits; bf16 fallback likewise).  All waits are bounded.
@@ -109,7 +114,9 @@ struct Cfg {
     static constexpr int kChains = kMmaWarps / NW;
     static constexpr int kPerItem = kItemK / 16 / kChains;  // MMAs per issuer and item
     static constexpr int kDCols = 16 * NW * kChains;   // one accumulator buffer
-    static constexpr size_t kSmemBytes = (size_t)kCStages * kStageBytes + (size_t)kXStages * kXUnit + 1024 + 1024;
+    static constexpr int kCkBytes = BM * NW * NTOK * 4;  // cluster-K partial staging
+    static constexpr size_t kSmemBytes =
+        (size_t)kCStages * kStageBytes + (size_t)kXStages * kXUnit + kCkBytes + 1024 + 1024;
     static_assert(kPerItem == 2, "two MMAs per issuer and item");
     static_assert(kAStages * kACols + 2 * kDCols <= (int)kTmemCols, "TMEM budget");
     static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
@@ -133,6 +140,8 @@ struct Args {
     void *y;
     int out_bf16;
     int bf16_only;  // 1: no prep kernel; bf16 operands read from x itself
+    int cs;         // > 1: cluster-K (clusters of cs CTAs split every tile's K); 1: stream-K
+    int ncl;        // cluster-K: number of clusters
 };
 
 // Workspace layout (bytes): header 256 (factor[16], flags[16], err), per-tile
@@ -238,6 +247,42 @@ NVFP4_DEVINL void dequant_chunk(uint4 c, uint32_t sc2, int mode, uint32_t *out)
 // CTA b owns units [b * total / P, (b + 1) * total / P).
 NVFP4_DEVINL int cta_of(uint32_t q, uint32_t total, uint32_t P) { return (int)(((q + 1) * P - 1) / total); }
 NVFP4_DEVINL uint32_t cta_lo(uint32_t b, uint32_t total, uint32_t P) { return b * total / P; }
+
+// The units of one CTA: tiles tile0, tile0 + tstep, ...; unit j of a tile
+// runs over [jb, je), except that the first tile starts at j_first.
+struct Range {
+    int64_t tile0, tstep;
+    int j_first, jb, je, n_units;
+};
+
+// Stream-K: CTA b owns units [b * total / P, (b + 1) * total / P) of the
+// tile-major unit list.
+NVFP4_DEVINL Range cta_range(const Args &a, int b)
+{
+    if (a.cs > 1) {
+        // Cluster-K: cluster q takes tiles q, q + ncl, ...; its CTA of rank r
+        // takes units [r * C / cs, (r + 1) * C / cs) of each of them.
+        const int q = b / a.cs, r = b % a.cs;
+        Range g;
+        g.tile0 = q;
+        g.tstep = a.ncl;
+        g.jb = r * a.C / a.cs;
+        g.je = (r + 1) * a.C / a.cs;
+        g.j_first = g.jb;
+        const int64_t k = q < a.T ? (a.T - q + a.ncl - 1) / a.ncl : 0;
+        g.n_units = (int)(k * (g.je - g.jb));
+        return g;
+    }
+    const int64_t lo = (int64_t)b * a.total / a.P, hi = (int64_t)(b + 1) * a.total / a.P;
+    Range g;
+    g.tile0 = lo / a.C;
+    g.tstep = 1;
+    g.j_first = (int)(lo - g.tile0 * a.C);
+    g.jb = 0;
+    g.je = a.C;
+    g.n_units = (int)(hi - lo);
+    return g;
+}
 
 NVFP4_DEVINL uint32_t atom_add_acq_rel(uint32_t *p, uint32_t v)
 {
@@ -413,11 +458,10 @@ struct SegInfo {
 // arrived last and must add the tile's partials (reduce_tile).
 template <int NW>
 __device__ __noinline__ void publish_segment(const Args &a, const float *fac, const float (&v)[NW][16], int tile,
-                                             int j, int u, int first_tile, int b, int r, SegInfo *si)
+                                             bool whole, int first_tile, int b, int r, SegInfo *si)
 {
     const uint32_t total = (uint32_t)a.total, P = (uint32_t)a.P, C = (uint32_t)a.C;
     const int64_t m = (int64_t)tile * BM + r;
-    const bool whole = (j == a.C - 1) && (u - j >= (int)cta_lo(b, total, P));
     if (whole) {  // uniform across the epilogue threads
         if (m < a.M)
 #pragma unroll
@@ -502,11 +546,82 @@ __device__ __noinline__ void reduce_tile(const Args &a, const float *fac, const 
     }
 }
 
+// Cluster-K epilogue of one tile segment (epilogue threads; thread r holds row
+// r's accumulator sums v[mi][n]).  Every CTA of the cluster stages its partial
+// in its own shared memory ([row][matrix * 16 + token] floats) and arrives on
+// the leader's barrier (release at cluster scope); the leader (rank 0) adds
+// the partials of ranks 0, 1, ... in that order through distributed shared
+// memory, writes the outputs and then frees every rank's buffer.  A rank
+// waits for that before reusing the buffer (and before exiting).
+template <int NW>
+__device__ __noinline__ void ck_epilogue(const Args &a, const float *fac, const float (&v)[NW][16], int64_t tile,
+                                         int r, int et, int seg, float *buf, uint64_t *ck_full, uint64_t *ck_free)
+{
+    constexpr int kRow = NW * NTOK;  // floats per row
+    const uint32_t rank = tc::cluster_ctarank();
+    if (seg > 0 && !tc::bar_and(1, kEpiThreads, tc::mbar_wait_cluster(ck_free, (uint32_t)(seg - 1) & 1))) {
+        fail(a, 23);
+        return;
+    }
+    float *row = buf + r * kRow;
+#pragma unroll
+    for (int mi = 0; mi < NW; ++mi)
+#pragma unroll
+        for (int n = 0; n < NTOK; n += 4)
+            *reinterpret_cast<float4 *>(row + mi * NTOK + n) =
+                make_float4(v[mi][n], v[mi][n + 1], v[mi][n + 2], v[mi][n + 3]);
+    tc::fence_acq_rel_cluster();
+    tc::named_bar_sync(1, kEpiThreads);
+    if (et == 0)
+        tc::mbar_arrive_remote(tc::mapa(ck_full, 0));
+    if (rank != 0)
+        return;
+    if (!tc::bar_and(1, kEpiThreads, tc::mbar_wait_cluster(ck_full, (uint32_t)seg & 1))) {
+        fail(a, 24);
+        return;
+    }
+    float acc[NW][NTOK];
+#pragma unroll
+    for (int mi = 0; mi < NW; ++mi)
+#pragma unroll
+        for (int n = 0; n < NTOK; ++n)
+            acc[mi][n] = 0.0f;
+    for (int k = 0; k < a.cs; ++k) {  // ranks in order: deterministic
+        const uint32_t src = tc::mapa(buf + r * kRow, (uint32_t)k);
+#pragma unroll
+        for (int mi = 0; mi < NW; ++mi)
+#pragma unroll
+            for (int n = 0; n < NTOK; n += 4) {
+                const float4 p = tc::ld_shared_cluster_v4(src + (uint32_t)((mi * NTOK + n) * 4));
+                acc[mi][n] += p.x;
+                acc[mi][n + 1] += p.y;
+                acc[mi][n + 2] += p.z;
+                acc[mi][n + 3] += p.w;
+            }
+    }
+    const int64_t m = tile * BM + r;
+    if (m < a.M)
+#pragma unroll
+        for (int n = 0; n < NTOK; ++n)
+            if (n < a.N) {
+                const float val = NW == 1 ? acc[0][n] * fac[n]
+                                          : silu_mul(acc[0][n] * fac[n], acc[NW - 1][n] * fac[NTOK + n]);
+                const int64_t idx = (int64_t)n * a.M + m;
+                if (a.out_bf16)
+                    reinterpret_cast<uint16_t *>(a.y)[idx] = f32_to_bf16(val);
+                else
+                    reinterpret_cast<float *>(a.y)[idx] = val;
+            }
+    tc::named_bar_sync(1, kEpiThreads);  // every read of the ranks' buffers is done
+    if (et < a.cs)
+        tc::mbar_arrive_remote(tc::mapa(ck_free, (uint32_t)et));
+}
+
 struct IssuerArgs {
     const uint8_t *x_ring;
     uint64_t *x_full, *x_empty, *a_full, *a_empty, *d_full, *d_empty;
     uint32_t tmem_a, tmem_d;
-    int n_units, j_lo;
+    int n_units, j_lo, jb, je;
 };
 
 // One MMA issuer (warp q, lane 0): matrix q / kChains, accumulator chain
@@ -543,8 +658,8 @@ NVFP4_DEVINL void mma_issuer(const Args &a, const IssuerArgs &p, int q)
     int sx = 0, sa = 0;
     uint32_t phx = 0, pha = 0;
     for (int i = 0; i < p.n_units; ++i) {
-        const bool first = (i == 0) || j == 0;
-        const bool last = (i == p.n_units - 1) || j == a.C - 1;
+        const bool first = (i == 0) || j == p.jb;
+        const bool last = (i == p.n_units - 1) || j == p.je - 1;
         if (first) {
             ++seg;
             if (!tc::mbar_wait(&p.d_empty[seg & 1], (((uint32_t)seg >> 1) & 1) ^ 1)) {
@@ -583,8 +698,8 @@ NVFP4_DEVINL void mma_issuer(const Args &a, const IssuerArgs &p, int q)
         }
         if (last)
             tc::mma_commit(&p.d_full[seg & 1]);
-        if (++j == a.C)
-            j = 0;
+        if (++j == p.je)
+            j = p.jb;
     }
 }
 
@@ -599,7 +714,8 @@ skinny_tc_kernel(const __grid_constant__ CUtensorMap m_codes0, const __grid_cons
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *c_ring = smem;                                          // [kCStages][NW codes, NW scales]
     uint8_t *x_ring = c_ring + (size_t)C::kCStages * C::kStageBytes;  // [kXStages][8 KB]
-    uint64_t *bars = reinterpret_cast<uint64_t *>(x_ring + (size_t)C::kXStages * kXUnit);
+    float *ck_buf = reinterpret_cast<float *>(x_ring + (size_t)C::kXStages * kXUnit);  // [128][NW * 16]
+    uint64_t *bars = reinterpret_cast<uint64_t *>(reinterpret_cast<uint8_t *>(ck_buf) + C::kCkBytes);
     uint64_t *c_full = bars;
     uint64_t *c_empty = c_full + C::kCStages;
     uint64_t *x_full = c_empty + C::kCStages;
@@ -608,14 +724,14 @@ skinny_tc_kernel(const __grid_constant__ CUtensorMap m_codes0, const __grid_cons
     uint64_t *a_empty = a_full + C::kAStages;
     uint64_t *d_full = a_empty + C::kAStages;
     uint64_t *d_empty = d_full + 2;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(d_empty + 2);
+    uint64_t *ck_full = d_empty + 2;
+    uint64_t *ck_free = ck_full + 1;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(ck_free + 1);
     float *fac_s = reinterpret_cast<float *>(tmem_slot + 4);  // [NW][16] epilogue factors
     SegInfo *seg_s = reinterpret_cast<SegInfo *>(fac_s + 2 * NTOK);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int b = blockIdx.x;
-    const int64_t lo = (int64_t)b * a.total / a.P;
-    const int64_t hi = (int64_t)(b + 1) * a.total / a.P;
 
     if (threadIdx.x == 0) {
         // Let the next kernel in the stream be scheduled as soon as SMs free up;
@@ -639,6 +755,8 @@ skinny_tc_kernel(const __grid_constant__ CUtensorMap m_codes0, const __grid_cons
             tc::mbar_init(&d_full[s], kMmaWarps);
             tc::mbar_init(&d_empty[s], kEpiThreads / 32);
         }
+        tc::mbar_init(ck_full, a.cs > 1 ? a.cs : 1);
+        tc::mbar_init(ck_free, 1);
         tc::fence_mbar_init();
         tc::prefetch_tensormap(&m_codes0);
         tc::prefetch_tensormap(&m_scales0);
@@ -652,15 +770,18 @@ skinny_tc_kernel(const __grid_constant__ CUtensorMap m_codes0, const __grid_cons
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
+    if (a.cs > 1)
+        tc::cluster_sync();  // every CTA's barriers are initialised before remote arrivals
     const uint32_t tmem = *tmem_slot;
     const uint32_t tmem_a = tmem;
     const uint32_t tmem_d = tmem + C::kAStages * C::kACols;
 
     // Every role walks the CTA's units lo..hi-1 with incremental (tile, j)
     // and ring (stage, phase) counters: no 64-bit division in the loops.
-    const int n_units = (int)(hi - lo);
-    const int64_t tile_lo = lo / a.C;
-    const int j_lo = (int)(lo - tile_lo * a.C);
+    const Range rg = cta_range(a, b);
+    const int n_units = rg.n_units;
+    const int64_t tile_lo = rg.tile0;
+    const int j_lo = rg.j_first;
 
     if (warp == 4 || warp == 5) {
         // ---- weight producers: even units (warp 4) and odd units (warp 5);
@@ -669,9 +790,9 @@ skinny_tc_kernel(const __grid_constant__ CUtensorMap m_codes0, const __grid_cons
             const int par = warp - 4;
             int64_t tile = tile_lo;
             int j = j_lo + par;
-            if (j >= a.C) {
-                j -= a.C;
-                ++tile;
+            if (j >= rg.je) {
+                j -= rg.je - rg.jb;
+                tile += rg.tstep;
             }
             for (int i = par; i < n_units; i += 2) {
                 const int s = i % C::kCStages;
@@ -690,9 +811,9 @@ skinny_tc_kernel(const __grid_constant__ CUtensorMap m_codes0, const __grid_cons
                                     &c_full[s], j * (BKU / 16), (int)(tile * BM));
                 }
                 j += 2;
-                while (j >= a.C) {
-                    j -= a.C;
-                    ++tile;
+                while (j >= rg.je) {
+                    j -= rg.je - rg.jb;
+                    tile += rg.tstep;
                 }
             }
         }
@@ -736,15 +857,16 @@ skinny_tc_kernel(const __grid_constant__ CUtensorMap m_codes0, const __grid_cons
                     s = 0;
                     ph ^= 1;
                 }
-                if (++j == a.C)
-                    j = 0;
+                if (++j == rg.je)
+                    j = rg.jb;
             }
         }
     } else if (warp < kMmaWarps) {
         // ---- MMA issuers: issuer q owns matrix q / kChains, chain q % kChains ----
         if (lane == 0) {
             tc::griddep_wait();
-            IssuerArgs ia{x_ring, x_full, x_empty, a_full, a_empty, d_full, d_empty, tmem_a, tmem_d, n_units, j_lo};
+            IssuerArgs ia{x_ring, x_full, x_empty, a_full, a_empty, d_full, d_empty, tmem_a, tmem_d, n_units, j_lo,
+                          rg.jb, rg.je};
             mma_issuer<NW>(a, ia, warp);
         }
     } else if (warp >= kEpiWarp0 && warp < kEpiWarp0 + 4) {
@@ -765,12 +887,14 @@ skinny_tc_kernel(const __grid_constant__ CUtensorMap m_codes0, const __grid_cons
         const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
         int64_t tile = tile_lo;
         int j = j_lo;
-        int seg = -1;
+        int seg = -1, seg_j0 = 0;
         for (int i = 0; i < n_units; ++i) {
-            const bool first = (i == 0) || j == 0;
-            const bool last = (i == n_units - 1) || j == a.C - 1;
-            if (first)
+            const bool first = (i == 0) || j == rg.jb;
+            const bool last = (i == n_units - 1) || j == rg.je - 1;
+            if (first) {
                 ++seg;
+                seg_j0 = j;
+            }
             if (last) {
                 const int db = seg & 1;
                 // every epilogue thread takes the same branch (named barriers follow)
@@ -804,17 +928,30 @@ skinny_tc_kernel(const __grid_constant__ CUtensorMap m_codes0, const __grid_cons
                 __syncwarp();
                 if (lane == 0)
                     tc::mbar_arrive(&d_empty[db]);
-                publish_segment<NW>(a, fac_s, sum, (int)tile, j, (int)(lo + i), (int)tile_lo, b, r, seg_s);
+                if (a.cs > 1) {
+                    ck_epilogue<NW>(a, fac_s, sum, tile, r, et, seg, ck_buf, ck_full, ck_free);
+                    if (++j == rg.je) {
+                        j = rg.jb;
+                        tile += rg.tstep;
+                    }
+                    continue;
+                }
+                // this CTA did the whole tile: units 0 .. C-1
+                const bool whole = seg_j0 == 0 && j == a.C - 1;
+                publish_segment<NW>(a, fac_s, sum, (int)tile, whole, (int)tile_lo, b, r, seg_s);
                 if (i == n_units - 1)
                     break;  // the CTA's last segment is reduced by all threads below
                 if (seg_s->reduce)
                     reduce_tile<NW>(a, fac_s, *seg_s, r, kEpiThreads);
             }
-            if (++j == a.C) {
-                j = 0;
-                ++tile;
+            if (++j == rg.je) {
+                j = rg.jb;
+                tile += rg.tstep;
             }
         }
+        // cluster-K: the leader has read this CTA's last partial before it exits
+        if (a.cs > 1 && seg >= 0 && !tc::mbar_wait_cluster(ck_free, (uint32_t)seg & 1))
+            fail(a, 25);
         // The dequantisers have finished: they help with the last segment.
         tc::named_bar_sync(2, kEpiThreads + kDqWarps * 32);
         if (seg_s->reduce)
@@ -950,28 +1087,113 @@ bool make_map(CUtensorMap *map, CUtensorMapDataType dt, const void *base, uint64
 }
 
 template <int NW>
-cudaError_t launch_main(const CUtensorMap (&maps)[5], const Args &a, cudaStream_t stream)
+cudaError_t set_smem_attr()
 {
-    using C = Cfg<NW>;
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [] {
         attr_err = cudaFuncSetAttribute(skinny_tc_kernel<NW>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        (int)C::kSmemBytes);
+                                        (int)Cfg<NW>::kSmemBytes);
     });
-    if (attr_err != cudaSuccess)
-        return attr_err;
+    return attr_err;
+}
+
+template <int NW>
+cudaLaunchConfig_t main_config(const Args &a, cudaStream_t stream, cudaLaunchAttribute (&attr)[2])
+{
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)a.P);
     cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = C::kSmemBytes;
+    cfg.dynamicSmemBytes = Cfg<NW>::kSmemBytes;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = (unsigned)(a.cs > 1 ? a.cs : 1);
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = a.cs > 1 ? 2 : 1;
+    return cfg;
+}
+
+// Clusters of `cs` CTAs of the main kernel that fit on the current device at
+// once (0 if none), cached per device.
+template <int NW>
+int max_active_clusters(int cs)
+{
+    static std::mutex mu;
+    static int cache[64][3];
+    static bool have[64][3];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64 || set_smem_attr<NW>() != cudaSuccess)
+        return 0;
+    const int ci = cs == 2 ? 0 : (cs == 4 ? 1 : 2);
+    std::lock_guard<std::mutex> lock(mu);
+    if (!have[dev][ci]) {
+        Args probe{};
+        probe.cs = cs;
+        probe.P = cs;
+        cudaLaunchAttribute attr[2];
+        cudaLaunchConfig_t cfg = main_config<NW>(probe, nullptr, attr);
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, skinny_tc_kernel<NW>, &cfg) != cudaSuccess)
+            n = 0;
+        cudaGetLastError();  // a failed query leaves no sticky error
+        cache[dev][ci] = n;
+        have[dev][ci] = true;
+    }
+    return cache[dev][ci];
+}
+
+template <int NW>
+cudaError_t launch_main(const CUtensorMap (&maps)[5], const Args &a, cudaStream_t stream)
+{
+    const cudaError_t attr_err = set_smem_attr<NW>();
+    if (attr_err != cudaSuccess)
+        return attr_err;
+    cudaLaunchAttribute attr[2];
+    cudaLaunchConfig_t cfg = main_config<NW>(a, stream, attr);
     return cudaLaunchKernelEx(&cfg, skinny_tc_kernel<NW>, maps[0], maps[1], maps[2], maps[3], maps[4], a);
+}
+
+// Split of the K dimension of every tile: stream-K over all SMs (any split,
+// partials reduced through global memory by the last CTA to arrive), or
+// cluster-K (clusters of 2 or 4 CTAs each splitting whole tiles, partials
+// reduced through distributed shared memory: a shorter end of call, but the
+// tiles must spread over fewer, fixed-size groups).  The choice depends on
+// the shapes and the device only, never on N, so results do not depend on N.
+// Unit times per SM and the end-of-call saving are measured on GB300.
+template <int NW>
+void choose_split(Args &a, int num_sms)
+{
+    a.cs = 1;
+    a.ncl = 0;
+    a.P = (int)std::max<int64_t>(1, std::min<int64_t>(a.total, std::min<int64_t>(num_sms, kSkinnyTcMaxCtas)));
+    const double t_unit = NW == 1 ? 0.55 : 1.1;  // us per 128 x 256 unit (per matrix pair) per SM
+    const double tail_saving = 3.0;               // us: global split-K reduction vs cluster reduction
+    double best = (double)((a.total + a.P - 1) / a.P) * t_unit + tail_saving;
+    // Measured: cluster-K wins only for one matrix whose tiles fit one per
+    // cluster (e.g. 4096 x 4096: 11.6 -> 10.6 us at N = 1); with several tiles
+    // per cluster, or for the fused gate/up pair, it was slower (whole
+    // clusters must free up before they start).
+    if (NW != 1)
+        return;
+    for (int cs : {4, 2}) {
+        if (a.C < cs)
+            continue;
+        const int64_t ncl = std::min<int64_t>(a.T, max_active_clusters<NW>(cs));
+        if (ncl < 1 || ncl < a.T || ncl * cs > kSkinnyTcMaxCtas)
+            continue;
+        const int64_t tiles = (a.T + ncl - 1) / ncl, units = (a.C + cs - 1) / cs;
+        const double est = (double)(tiles * units) * t_unit;
+        if (est < best) {
+            best = est;
+            a.cs = cs;
+            a.ncl = (int)ncl;
+            a.P = (int)(ncl * cs);
+        }
+    }
 }
 
 }  // namespace sk
@@ -1010,7 +1232,10 @@ cudaError_t launch_skinny_tc(const uint16_t *x, int N, int64_t M, int64_t K, con
     a.C = (int)((K + BKU - 1) / BKU);
     a.T = (M + BM - 1) / BM;
     a.total = a.T * a.C;
-    a.P = (int)std::max<int64_t>(1, std::min<int64_t>(a.total, std::min<int64_t>(num_sms, kSkinnyTcMaxCtas)));
+    if (n_weights == 1)
+        choose_split<1>(a, num_sms);
+    else
+        choose_split<2>(a, num_sms);
     for (int i = 0; i < 2; ++i)
         a.ts[i] = ts[i < n_weights ? i : 0];
     a.factor = factor;

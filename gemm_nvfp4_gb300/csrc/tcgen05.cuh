@@ -267,6 +267,74 @@ NVFP4_DEVINL void named_bar_sync(uint32_t id, uint32_t nthreads)
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
+// ---------------------------------------------------------------------------
+// Thread-block clusters: distributed shared memory and remote mbarriers.
+// ---------------------------------------------------------------------------
+
+NVFP4_DEVINL uint32_t cluster_ctarank()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+// Address of the same shared-memory variable in CTA `rank` of the cluster.
+NVFP4_DEVINL uint32_t mapa(const void *p, uint32_t rank)
+{
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_addr(p)), "r"(rank));
+    return r;
+}
+
+// Every thread of every CTA in the cluster arrives and waits.
+NVFP4_DEVINL void cluster_sync()
+{
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Arrive (release at cluster scope) on an mbarrier given by its cluster address.
+NVFP4_DEVINL void mbar_arrive_remote(uint32_t cluster_addr)
+{
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+
+// Orders this thread's shared-memory writes before later cluster-scope releases.
+NVFP4_DEVINL void fence_acq_rel_cluster() { asm volatile("fence.acq_rel.cluster;" ::: "memory"); }
+
+NVFP4_DEVINL bool mbar_try_wait_cluster(uint64_t *bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{ .reg .pred p; mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait (kWaitLimitNs) with acquire at cluster scope: the waiter sees
+// the shared-memory writes other CTAs released before arriving.
+NVFP4_DEVINL bool mbar_wait_cluster(uint64_t *bar, uint32_t parity)
+{
+    const uint64_t t0 = globaltimer();
+    for (;;) {
+        if (mbar_try_wait_cluster(bar, parity))
+            return true;
+        if (globaltimer() - t0 > kWaitLimitNs)
+            return false;
+    }
+}
+
+NVFP4_DEVINL float4 ld_shared_cluster_v4(uint32_t cluster_addr)
+{
+    float4 v;
+    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(cluster_addr)
+                 : "memory");
+    return v;
+}
+
 // Named barrier that also returns the AND of `v` over the participating
 // threads: every participant gets the same answer, so the branch it guards
 // is uniform (needed before further named barriers).
