@@ -127,6 +127,67 @@ def quantize(w, lib=None):
     return codes, scales, np.float32(ts[0])
 
 
+def quantize_bf16(w_bits, lib=None):
+    """bf16 weights (uint16 bit patterns [M, K]) -> NVFP4 with the same recipe.
+
+    The plain definition: every bf16 value is exactly an fp32 value (its bits
+    followed by 16 zero bits), and the quantiser recipe then runs on those
+    fp32 values unchanged (the ingest step before the path; bw24 README,
+    safetensors loader re-encoding weights to NVFP4 at load time).
+    """
+    w_bits = np.ascontiguousarray(w_bits, dtype=np.uint16)
+    w = (w_bits.astype(np.uint32) << np.uint32(16)).view(np.float32)
+    return quantize(w, lib)
+
+
+# --------------------------------------------------------------------------
+# External scale layout (ingest repack)
+# --------------------------------------------------------------------------
+#
+# The pages re-encode NVFP4 checkpoints into each engine's own layout at load
+# time (bw24 README, safetensors loader; bw24 wiki Home) without printing the
+# source layout.  This build defines one external layout to import: the codes
+# as in the canonical layout ([M][K/2], even k in the low nibble) and the
+# E4M3 block scales in 128 x 4 blocks, the block arrangement block-scaled
+# tensor-core GEMMs read:
+#   blocks in row-major order over (M/128 rounded up) x (K/64 rounded up);
+#   inside a block, scale (row r, scale column c) at byte
+#       (r % 32) * 16 + (r / 32) * 4 + c;
+#   padding entries (rows >= M, columns >= K/16) are zero.
+
+def blocked_scale_bytes(M: int, K: int) -> int:
+    """Bytes of the external blocked scale buffer."""
+    return ((M + 127) // 128) * ((K // 16 + 3) // 4) * 512
+
+
+def interleave_scales(scales):
+    """Canonical scales uint8 [M, K/16] -> external blocked layout (1-D)."""
+    scales = np.asarray(scales, dtype=np.uint8)
+    M, S = scales.shape
+    nb = (S + 3) // 4
+    out = np.zeros(((M + 127) // 128) * nb * 512, np.uint8)
+    for m in range(M):
+        for c in range(S):
+            blk = (m // 128) * nb + c // 4
+            r, cc = m % 128, c % 4
+            out[blk * 512 + (r % 32) * 16 + (r // 32) * 4 + cc] = scales[m, c]
+    return out
+
+
+def deinterleave_scales(blocked, M: int, K: int):
+    """External blocked layout -> canonical scales uint8 [M, K/16]."""
+    blocked = np.asarray(blocked, dtype=np.uint8).reshape(-1)
+    S = K // 16
+    nb = (S + 3) // 4
+    out = np.zeros((M, S), np.uint8)
+    for m in range(M):
+        for c in range(S):
+            blk = (m // 128) * nb + c // 4
+            r, cc = m % 128, c % 4
+            out[m, c] = blocked[blk * 512 + (r % 32) * 16 + (r // 32) * 4 + cc]
+    return out
+
+
 def _index(idx, total):
     if idx is None:
         return None, total

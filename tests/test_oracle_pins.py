@@ -392,3 +392,72 @@ def test_oracle_rejects_bad_input():
     w[0, 3] = np.nan
     with pytest.raises(ValueError):
         oracle.quantize(w)
+
+
+# ---------------------------------------------------------------------------
+# Ingest: bf16 quantiser and the blocked scale layout
+# ---------------------------------------------------------------------------
+
+def test_quantize_bf16_matches_torch_decode_and_recipe():
+    """bf16 bits are decoded by PyTorch (independent of the oracle) and the
+    values re-quantised by the numpy re-derivation of the recipe."""
+    rng = np.random.default_rng(21)
+    for M, K in [(3, 48), (17, 160)]:
+        w = (rng.standard_normal((M, K)) * rng.uniform(0.01, 3.0, (M, 1))).astype(np.float32)
+        bits = torch.from_numpy(w).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+        vals = torch.from_numpy(bits.view(np.int16).copy()).view(torch.bfloat16).float().numpy()
+        c, s, ts = oracle.quantize_bf16(bits)
+        rc, rs, rts = quantize_ref(vals)
+        assert ts == rts and np.array_equal(s, rs) and np.array_equal(c, rc)
+
+
+def test_quantize_bf16_hand_values():
+    """Hand-decoded bf16 patterns: 0x3F00 = 0.5, 0xBE80 = -0.25, 0x3E00 = 0.125,
+    0x0000 = 0.  With amax 0.5: ts = 0.5/2688, block scale 448 (0x7E), d = 448 ts
+    = 0.5/6, so w/d = 6, -3, 1.5, 0 -> codes 7, D, 3, 0."""
+    bits = np.array([[0x3F00, 0xBE80, 0x3E00, 0x0000] * 4], np.uint16)
+    c, s, ts = oracle.quantize_bf16(bits)
+    assert ts == f32(f32(0.5) / f32(2688.0))
+    assert s[0, 0] == 0x7E
+    assert list(c[0]) == [0xD7, 0x03] * 4
+
+
+def test_blocked_scale_positions_hand_worked():
+    """M = 130, K = 128: S = 8 scale columns -> 2 x 2 blocks of 512 bytes.
+    (r, c) -> block (r // 128) * 2 + c // 4, byte (r % 32) * 16 + (r % 128 // 32) * 4 + c % 4:
+      (0, 0) -> 0;  (1, 0) -> 16;  (32, 0) -> 4;  (33, 3) -> 23;  (0, 4) -> 512;
+      (127, 7) -> 512 + 31 * 16 + 3 * 4 + 3 = 1023;  (129, 5) -> 1536 + 16 + 1 = 1553."""
+    assert oracle.blocked_scale_bytes(130, 128) == 2048
+    cases = {(0, 0): 0, (1, 0): 16, (32, 0): 4, (33, 3): 23, (0, 4): 512, (127, 7): 1023, (129, 5): 1553}
+    for (r, c), pos in cases.items():
+        s = np.zeros((130, 8), np.uint8)
+        s[r, c] = 0x5A
+        b = oracle.interleave_scales(s)
+        assert b.shape == (2048,)
+        assert np.flatnonzero(b).tolist() == [pos], ((r, c), np.flatnonzero(b))
+
+
+def test_blocked_scale_layout_is_a_bijection_with_zero_padding():
+    # 64 rows x 4 columns = 256 distinct bytes, one block, rows 64..127 padding
+    s = np.arange(256, dtype=np.uint32).reshape(64, 4).astype(np.uint8)
+    b = oracle.interleave_scales(s)
+    assert b.shape == (512,)
+    live = np.zeros(512, bool)
+    for r in range(64):
+        live[(r % 32) * 16 + (r // 32) * 4: (r % 32) * 16 + (r // 32) * 4 + 4] = True
+    assert sorted(b[live].tolist()) == list(range(256))
+    assert not b[~live].any()
+
+
+@pytest.mark.parametrize("M,K", [(1, 16), (128, 64), (130, 80), (257, 1040), (5, 16 * 9)])
+def test_blocked_scale_round_trip(M, K):
+    rng = np.random.default_rng(M * 1000 + K)
+    s = rng.integers(0, 256, (M, K // 16), dtype=np.uint8)
+    b = oracle.interleave_scales(s)
+    assert b.size == oracle.blocked_scale_bytes(M, K)
+    assert np.array_equal(oracle.deinterleave_scales(b, M, K), s)
+    # padding is ignored on the way back
+    junk = b.copy()
+    pad = oracle.interleave_scales(np.full_like(s, 1)) == 0
+    junk[pad] = 0xEE
+    assert np.array_equal(oracle.deinterleave_scales(junk, M, K), s)
