@@ -59,6 +59,7 @@ def parse():
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="dense9b-n1")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-prefill", action="store_true")
+    ap.add_argument("--no-ingest", action="store_true")
     # for profiling one call kind on a short stream (ncu captures): not a bench line
     ap.add_argument("--layers", type=int, default=None, help="override the number of layers in the stream")
     ap.add_argument("--only", choices=["qkv", "o", "gateup", "down"], default=None,
@@ -372,6 +373,52 @@ def prefill_tflops(dev, reps=5):
     return out
 
 
+def ingest_gbs(dev, reps=5):
+    """Load-time ingest on the 27B-class gate matrix (17408 x 5120): quantise
+    from fp32 and from bf16, and import of blocked scales.  HBM-bound; the
+    algorithmic bytes are two reads of the input (the tensor amax must be known
+    before any block is quantised and the matrix is larger than L2) plus the
+    NVFP4 writes (0.5625 B per weight); the import reads the blocked scales and
+    writes the row-major ones once.  L2 is flushed before every timed call."""
+    import gemm_nvfp4_gb300 as g
+    from gemm_nvfp4_gb300 import inputs
+    M, K = inputs.LAYER_27B.shapes()["gate"]
+    peak = read_peaks()[0]
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    w32 = inputs.weights(M, K, seed=inputs.matrix_seed("gate"), device=dev)
+    w16 = w32.to(torch.bfloat16)
+    W = g.nvfp4_quantize(w32)
+    ws = torch.empty(g.nvfp4_workspace_bytes(g.NVFP4_OP_QUANTIZE, 0, M, K), dtype=torch.uint8, device=dev)
+    blocked = torch.randint(0, 256, (g.nvfp4_blocked_scale_bytes(M, K),), dtype=torch.uint8, device=dev)
+    scales = torch.empty(M, K // 16, dtype=torch.uint8, device=dev)
+    out_bytes = M * K // 2 + M * K // 16 + 4
+    ops = {
+        "quantize fp32": (lambda: g.nvfp4_quantize(w32, workspace=ws, out=W), 2 * 4 * M * K + out_bytes),
+        "quantize bf16": (lambda: g.nvfp4_quantize_bf16(w16, workspace=ws, out=W), 2 * 2 * M * K + out_bytes),
+        "import scales": (lambda: g.nvfp4_import_blocked_scales(blocked, M, K, out=scales),
+                          blocked.numel() + M * K // 16),
+    }
+    out = {"unit": "GB/s", "peak_hbm": peak, "matrix": f"{M}x{K}", "l2": "flushed before each call", "ops": {}}
+    for name, (fn, nbytes) in ops.items():
+        fn()
+        torch.cuda.synchronize()
+        total = 0.0
+        for _ in range(reps):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            fn()
+            e1.record()
+            torch.cuda.synchronize()
+            total += e0.elapsed_time(e1)
+        ms = total / reps
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        out["ops"][name] = {"us": ms * 1e3, "bytes": nbytes, "gbs": gbs, "frac": gbs / peak if peak else None}
+    del flush, w32, w16, W, blocked, scales
+    torch.cuda.empty_cache()
+    return out
+
+
 def prefill_profile(dev, spec):
     """Three prefill calls of one shape (a target for ncu; prints nothing)."""
     import gemm_nvfp4_gb300 as g
@@ -515,6 +562,7 @@ def main():
     traffic = read_traffic(f"skinny_tc_kernel<2> {args.workload}")
 
     prefill = prefill_tflops(dev) if not args.no_prefill else None
+    ingest = ingest_gbs(dev) if not args.no_ingest else None
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -542,6 +590,7 @@ def main():
             "gpu_launches": st.launches_per_step(args.only) * args.steps,
             "clocks": clocks,
             "prefill": prefill,
+            "ingest": ingest,
         }
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -9,13 +9,14 @@ missing, every call raises.
 from .binding import (NVFP4_OP_GATEUP_SWIGLU, NVFP4_OP_GEMM_PREFILL, NVFP4_OP_GEMV_SKINNY,
                       NVFP4_OP_QUANTIZE, NVFP4_OUT_BF16, NVFP4_OUT_F32, NVFP4Error, NVFP4Weight,
                       header_functions, library_path, load_library, nvfp4_gateup_swiglu,
-                      nvfp4_gemm_prefill, nvfp4_gemv_skinny, nvfp4_gemv_skinny_noalloc, nvfp4_quantize, nvfp4_status_string,
-                      nvfp4_version, nvfp4_workspace_bytes)
+                      nvfp4_blocked_scale_bytes, nvfp4_gemm_prefill, nvfp4_gemv_skinny,
+                      nvfp4_gemv_skinny_noalloc, nvfp4_import_blocked_scales, nvfp4_quantize,
+                      nvfp4_quantize_bf16, nvfp4_status_string, nvfp4_version, nvfp4_workspace_bytes)
 
 __all__ = [
     "NVFP4Error", "NVFP4Weight", "header_functions", "library_path", "load_library",
     "nvfp4_gateup_swiglu", "nvfp4_gemm_prefill", "nvfp4_gemv_skinny", "nvfp4_gemv_skinny_noalloc",
-    "nvfp4_quantize",
+    "nvfp4_quantize", "nvfp4_quantize_bf16", "nvfp4_blocked_scale_bytes", "nvfp4_import_blocked_scales",
     "nvfp4_status_string", "nvfp4_version", "nvfp4_workspace_bytes",
     "NVFP4_OP_QUANTIZE", "NVFP4_OP_GEMV_SKINNY", "NVFP4_OP_GATEUP_SWIGLU", "NVFP4_OP_GEMM_PREFILL",
     "NVFP4_OUT_F32", "NVFP4_OUT_BF16",

@@ -66,6 +66,12 @@ def load_library():
         lib.nvfp4_workspace_bytes.argtypes = [i32, i64, i64, i64]
         lib.nvfp4_quantize.restype = i32
         lib.nvfp4_quantize.argtypes = [P, i64, i64, P, P, P, P, sz, P]
+        lib.nvfp4_quantize_bf16.restype = i32
+        lib.nvfp4_quantize_bf16.argtypes = [P, i64, i64, P, P, P, P, sz, P]
+        lib.nvfp4_blocked_scale_bytes.restype = sz
+        lib.nvfp4_blocked_scale_bytes.argtypes = [i64, i64]
+        lib.nvfp4_import_blocked_scales.restype = i32
+        lib.nvfp4_import_blocked_scales.argtypes = [P, i64, i64, P, P]
         lib.nvfp4_gemv_skinny.restype = i32
         lib.nvfp4_gemv_skinny.argtypes = [P, i64, P, P, P, i64, i64, P, i32, P, sz, P]
         lib.nvfp4_gateup_swiglu.restype = i32
@@ -164,6 +170,41 @@ def nvfp4_quantize(w: torch.Tensor, workspace: torch.Tensor | None = None,
     st = load_library().nvfp4_quantize(_ptr(w), M, K, _ptr(out.codes), _ptr(out.scales),
                                        _ptr(out.tensor_scale), _ptr(ws), ws_bytes, _stream(stream))
     _check(st, "nvfp4_quantize")
+    return out
+
+
+def nvfp4_quantize_bf16(w: torch.Tensor, workspace: torch.Tensor | None = None,
+                        out: NVFP4Weight | None = None, stream=None) -> NVFP4Weight:
+    """bf16 [M, K] CUDA tensor -> NVFP4Weight, identical to quantising w.float()."""
+    if w.dtype != torch.bfloat16:
+        raise ValueError(f"nvfp4_quantize_bf16 takes bf16 weights, got {w.dtype}")
+    M, K = w.shape
+    if out is None:
+        out = NVFP4Weight(torch.empty(M, K // 2, dtype=torch.uint8, device=w.device),
+                          torch.empty(M, K // 16, dtype=torch.uint8, device=w.device),
+                          torch.empty(1, dtype=torch.float32, device=w.device))
+    ws, ws_bytes = _workspace(NVFP4_OP_QUANTIZE, 0, M, K, w.device, workspace)
+    st = load_library().nvfp4_quantize_bf16(_ptr(w), M, K, _ptr(out.codes), _ptr(out.scales),
+                                            _ptr(out.tensor_scale), _ptr(ws), ws_bytes, _stream(stream))
+    _check(st, "nvfp4_quantize_bf16")
+    return out
+
+
+def nvfp4_blocked_scale_bytes(M: int, K: int) -> int:
+    return load_library().nvfp4_blocked_scale_bytes(M, K)
+
+
+def nvfp4_import_blocked_scales(blocked: torch.Tensor, M: int, K: int,
+                                out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Blocked (128 x 4) E4M3 scale bytes -> row-major uint8 [M, K/16] scales."""
+    if blocked.dtype != torch.uint8:
+        raise ValueError(f"blocked scales are uint8 bytes, got {blocked.dtype}")
+    if blocked.numel() < nvfp4_blocked_scale_bytes(M, K):
+        raise ValueError("blocked scale buffer smaller than nvfp4_blocked_scale_bytes(M, K)")
+    if out is None:
+        out = torch.empty(M, K // 16, dtype=torch.uint8, device=blocked.device)
+    st = load_library().nvfp4_import_blocked_scales(_ptr(blocked), M, K, _ptr(out), _stream(stream))
+    _check(st, "nvfp4_import_blocked_scales")
     return out
 
 

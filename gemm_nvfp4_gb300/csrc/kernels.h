@@ -16,6 +16,10 @@ constexpr int64_t kGemvPartialFloatsPerCta = 2 * 16 * 16;
 
 cudaError_t launch_quantize(const float *w, int64_t M, int64_t K, uint8_t *codes, uint8_t *scales,
                             float *tensor_scale, void *workspace, int num_sms, cudaStream_t stream);
+cudaError_t launch_quantize_bf16(const uint16_t *w, int64_t M, int64_t K, uint8_t *codes, uint8_t *scales,
+                                 float *tensor_scale, void *workspace, int num_sms, cudaStream_t stream);
+cudaError_t launch_import_blocked_scales(const uint8_t *blocked, int64_t M, int64_t K, uint8_t *scales,
+                                         cudaStream_t stream);
 
 // n_weights = 1: y = x . W^T; n_weights = 2: h = silu(x . Wg^T) * (x . Wu^T)
 // with codes/scales/ts[0] = gate, [1] = up.

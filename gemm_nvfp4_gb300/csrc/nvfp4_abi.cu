@@ -157,6 +157,50 @@ int nvfp4_quantize(const float *w, int64_t M, int64_t K, uint8_t *codes, uint8_t
     return e == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA;
 }
 
+int nvfp4_quantize_bf16(const uint16_t *w, int64_t M, int64_t K, uint8_t *codes, uint8_t *scales,
+                        float *tensor_scale, void *workspace, size_t workspace_bytes, nvfp4_stream_t stream)
+{
+    if (M < 0 || K < 0)
+        return NVFP4_ERR_INVALID_ARG;
+    if (K % 16 != 0 || !size_ok(M, K))
+        return NVFP4_ERR_UNSUPPORTED_SHAPE;
+    if (!tensor_scale || !aligned(tensor_scale, 4))
+        return NVFP4_ERR_INVALID_ARG;
+    if (M * K > 0 && (!w || !codes || !scales || !aligned(w, 16) || !aligned(codes, 16) || !aligned(scales, 16)))
+        return NVFP4_ERR_INVALID_ARG;
+    int rc = check_workspace(workspace, workspace_bytes, nvfp4_workspace_bytes(NVFP4_OP_QUANTIZE, 0, M, K));
+    if (rc != NVFP4_OK)
+        return rc;
+    int sms = 0;
+    rc = current_num_sms(&sms);
+    if (rc != NVFP4_OK)
+        return rc;
+    cudaError_t e = launch_quantize_bf16(w, M, K, codes, scales, tensor_scale, workspace, sms, (cudaStream_t)stream);
+    return e == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA;
+}
+
+size_t nvfp4_blocked_scale_bytes(int64_t M, int64_t K)
+{
+    if (M < 0 || K < 0 || K % 16 != 0 || !size_ok(M, K))
+        return 0;
+    return (size_t)((M + 127) / 128) * (size_t)((K / 16 + 3) / 4) * 512;
+}
+
+int nvfp4_import_blocked_scales(const uint8_t *blocked, int64_t M, int64_t K, uint8_t *scales,
+                                nvfp4_stream_t stream)
+{
+    if (M < 0 || K < 0)
+        return NVFP4_ERR_INVALID_ARG;
+    if (K % 16 != 0 || !size_ok(M, K))
+        return NVFP4_ERR_UNSUPPORTED_SHAPE;
+    if (M == 0 || K == 0)
+        return NVFP4_OK;
+    if (!blocked || !scales || !aligned(blocked, 16) || !aligned(scales, 16))
+        return NVFP4_ERR_INVALID_ARG;
+    cudaError_t e = launch_import_blocked_scales(blocked, M, K, scales, (cudaStream_t)stream);
+    return e == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA;
+}
+
 int nvfp4_gemv_skinny(const uint16_t *x, int64_t N, const uint8_t *codes, const uint8_t *scales,
                       const float *tensor_scale, int64_t M, int64_t K, void *y, int out_dtype, void *workspace,
                       size_t workspace_bytes, nvfp4_stream_t stream)

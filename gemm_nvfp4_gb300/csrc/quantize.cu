@@ -11,7 +11,10 @@
 // and qwentin quantises and packs on the GPU through its C ABI (qwentin README,
 // converter section).
 //
-// Two kernels, both HBM-bound (4 B read per weight; 0.5625 B written):
+// The same recipe runs on bf16 input (values widened exactly to fp32).
+//
+// Two kernels, both HBM-bound (4 B, or 2 B for bf16, read per weight;
+// 0.5625 B written):
 //   1. amax_partial: per-block max of |w| bit patterns (integer max on the
 //      non-negative float bits is exact and order independent) -> workspace.
 //   2. quantize_blocks: every CTA reduces the partial maxima itself (no
@@ -26,18 +29,60 @@ namespace nvfp4 {
 
 constexpr int kQuantThreads = 256;
 
+// Input element types.  A bf16 value is exactly the fp32 value whose bits are
+// its 16 bits followed by 16 zero bits, so both inputs feed the same fp32
+// recipe below and give identical NVFP4 for the same values.
+template <typename T> struct Src;
+
+template <> struct Src<float> {
+    static constexpr int kPer16B = 4;  // elements per 16-byte vector
+    // Largest |value| bit pattern of one 16-byte vector (non-negative float
+    // bits order like the values, so an integer max is exact).
+    static __device__ __forceinline__ uint32_t amax_bits(uint4 v)
+    {
+        return max(max(v.x & 0x7FFFFFFFu, v.y & 0x7FFFFFFFu), max(v.z & 0x7FFFFFFFu, v.w & 0x7FFFFFFFu));
+    }
+    // Eight consecutive values starting at element 8 * hb.
+    static __device__ __forceinline__ void load8(const float *w, int64_t hb, float v[8])
+    {
+        const float4 *p = reinterpret_cast<const float4 *>(w + hb * 8);
+        float4 a = __ldcs(p), b = __ldcs(p + 1);
+        v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+        v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+    }
+};
+
+template <> struct Src<uint16_t> {
+    static constexpr int kPer16B = 8;
+    static __device__ __forceinline__ uint32_t half_bits(uint32_t word)
+    {
+        // the two bf16 values of a word as |fp32| bit patterns
+        return max((word << 16) & 0x7FFF0000u, word & 0x7FFF0000u);
+    }
+    static __device__ __forceinline__ uint32_t amax_bits(uint4 v)
+    {
+        return max(max(half_bits(v.x), half_bits(v.y)), max(half_bits(v.z), half_bits(v.w)));
+    }
+    static __device__ __forceinline__ void load8(const uint16_t *w, int64_t hb, float v[8])
+    {
+        const uint4 a = __ldcs(reinterpret_cast<const uint4 *>(w + hb * 8));
+        const uint32_t words[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            v[2 * j] = __uint_as_float(words[j] << 16);
+            v[2 * j + 1] = __uint_as_float(words[j] & 0xFFFF0000u);
+        }
+    }
+};
+
+template <typename T>
 __global__ void __launch_bounds__(kQuantThreads)
-amax_partial_kernel(const float4 *__restrict__ w, int64_t n_vec4, uint32_t *__restrict__ partial)
+amax_partial_kernel(const uint4 *__restrict__ w, int64_t n_vec, uint32_t *__restrict__ partial)
 {
     uint32_t m = 0;
-    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n_vec4;
-         i += (int64_t)gridDim.x * blockDim.x) {
-        float4 v = __ldcs(w + i);
-        m = max(m, __float_as_uint(v.x) & 0x7FFFFFFFu);
-        m = max(m, __float_as_uint(v.y) & 0x7FFFFFFFu);
-        m = max(m, __float_as_uint(v.z) & 0x7FFFFFFFu);
-        m = max(m, __float_as_uint(v.w) & 0x7FFFFFFFu);
-    }
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n_vec;
+         i += (int64_t)gridDim.x * blockDim.x)
+        m = max(m, Src<T>::amax_bits(__ldcs(w + i)));
     for (int o = 16; o > 0; o >>= 1)
         m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
     __shared__ uint32_t red[kQuantThreads / 32];
@@ -52,8 +97,9 @@ amax_partial_kernel(const float4 *__restrict__ w, int64_t n_vec4, uint32_t *__re
     }
 }
 
+template <typename T>
 __global__ void __launch_bounds__(kQuantThreads)
-quantize_blocks_kernel(const float *__restrict__ w, int64_t n_half_blocks,
+quantize_blocks_kernel(const T *__restrict__ w, int64_t n_half_blocks,
                        const uint32_t *__restrict__ partial, int n_partial,
                        uint8_t *__restrict__ codes, uint8_t *__restrict__ scales,
                        float *__restrict__ tensor_scale)
@@ -87,10 +133,7 @@ quantize_blocks_kernel(const float *__restrict__ w, int64_t n_half_blocks,
         float v[8];
         float amax = 0.0f;
         if (active) {
-            const float4 *p = reinterpret_cast<const float4 *>(w + hb * 8);
-            float4 a = __ldcs(p), b = __ldcs(p + 1);
-            v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
-            v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+            Src<T>::load8(w, hb, v);
 #pragma unroll
             for (int j = 0; j < 8; ++j)
                 amax = fmaxf(amax, fabsf(v[j]));
@@ -121,20 +164,102 @@ quantize_blocks_kernel(const float *__restrict__ w, int64_t n_half_blocks,
     }
 }
 
-cudaError_t launch_quantize(const float *w, int64_t M, int64_t K, uint8_t *codes, uint8_t *scales,
-                            float *tensor_scale, void *workspace, int num_sms, cudaStream_t stream)
+template <typename T>
+static cudaError_t quantize_any(const T *w, int64_t M, int64_t K, uint8_t *codes, uint8_t *scales,
+                                float *tensor_scale, void *workspace, int num_sms, cudaStream_t stream)
 {
     const int64_t n = M * K;
     uint32_t *partial = reinterpret_cast<uint32_t *>(workspace);
-    int64_t want = (n / 4 + kQuantThreads * 8 - 1) / (kQuantThreads * 8);
+    const int64_t n_vec = n / Src<T>::kPer16B;  // K % 16 == 0: whole vectors
+    int64_t want = (n_vec + kQuantThreads * 8 - 1) / (kQuantThreads * 8);
     int grid_a = (int)std::min<int64_t>(std::max<int64_t>(want, 1), kQuantPartials);
-    amax_partial_kernel<<<grid_a, kQuantThreads, 0, stream>>>(reinterpret_cast<const float4 *>(w), n / 4,
-                                                               partial);
+    amax_partial_kernel<T><<<grid_a, kQuantThreads, 0, stream>>>(reinterpret_cast<const uint4 *>(w), n_vec,
+                                                                  partial);
     const int64_t n_half = n / 8;
     int64_t blocks_b = (n_half + kQuantThreads - 1) / kQuantThreads;
     int grid_b = (int)std::min<int64_t>(std::max<int64_t>(blocks_b, 1), (int64_t)num_sms * 8);
-    quantize_blocks_kernel<<<grid_b, kQuantThreads, 0, stream>>>(w, n_half, partial, grid_a, codes, scales,
-                                                                  tensor_scale);
+    quantize_blocks_kernel<T><<<grid_b, kQuantThreads, 0, stream>>>(w, n_half, partial, grid_a, codes, scales,
+                                                                     tensor_scale);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_quantize(const float *w, int64_t M, int64_t K, uint8_t *codes, uint8_t *scales,
+                            float *tensor_scale, void *workspace, int num_sms, cudaStream_t stream)
+{
+    return quantize_any<float>(w, M, K, codes, scales, tensor_scale, workspace, num_sms, stream);
+}
+
+cudaError_t launch_quantize_bf16(const uint16_t *w, int64_t M, int64_t K, uint8_t *codes, uint8_t *scales,
+                                 float *tensor_scale, void *workspace, int num_sms, cudaStream_t stream)
+{
+    return quantize_any<uint16_t>(w, M, K, codes, scales, tensor_scale, workspace, num_sms, stream);
+}
+
+// ---------------------------------------------------------------------------
+// Import of block scales from the blocked (128 x 4) layout.
+//
+// Blocked layout: 128-row x 4-scale-column blocks, row-major over
+// (ceil(M/128), ceil(S/4)) with S = K/16; inside a block, scale (r, c) at byte
+// (r % 32) * 16 + (r / 32) * 4 + c.  Entries past M or S are padding.
+//
+// One CTA per (128-row block, chunk of kImportBlocks scale-column blocks): the
+// chunk is contiguous in the blocked buffer (read with 16-byte loads into
+// shared memory), and its 128 output row segments are written with 4-byte
+// stores where rows start on 4-byte boundaries.  HBM-bound: every byte read
+// and written once.
+constexpr int kImportThreads = 256;
+constexpr int kImportBlocks = 16;  // 4-column blocks per CTA: 64 columns, 8 KB
+
+__global__ void __launch_bounds__(kImportThreads)
+import_blocked_scales_kernel(const uint8_t *__restrict__ blocked, int64_t M, int64_t S, int64_t nb,
+                             int64_t n_chunks, uint8_t *__restrict__ scales)
+{
+    __shared__ __align__(16) uint32_t tile[kImportBlocks * 128];
+    const int64_t mb = blockIdx.x / n_chunks;
+    const int64_t kb0 = (blockIdx.x % n_chunks) * kImportBlocks;
+    const int nblk = (int)(nb - kb0 < kImportBlocks ? nb - kb0 : kImportBlocks);
+    const uint4 *src = reinterpret_cast<const uint4 *>(blocked + (mb * nb + kb0) * 512);
+    for (int i = threadIdx.x; i < nblk * 32; i += kImportThreads)
+        reinterpret_cast<uint4 *>(tile)[i] = __ldcs(src + i);
+    __syncthreads();
+
+    // Thread t writes row t / 2, scale columns [32 * (t % 2), +32) of the chunk.
+    const int r = threadIdx.x >> 1;
+    const int64_t m = mb * 128 + r;
+    if (m >= M)
+        return;
+    const int64_t c0 = kb0 * 4 + (threadIdx.x & 1) * 32;
+    uint8_t *row = scales + m * S;
+    const int widx = (r & 31) * 4 + (r >> 5);  // word of row r inside a block
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const int64_t c = c0 + 4 * j;
+        if (c >= S)
+            break;
+        const int blk = (int)(c / 4 - kb0);
+        const uint32_t word = tile[blk * 128 + widx];
+        if ((S & 3) == 0) {
+            *reinterpret_cast<uint32_t *>(row + c) = word;
+        } else {
+#pragma unroll
+            for (int b = 0; b < 4; ++b)
+                if (c + b < S)
+                    row[c + b] = (uint8_t)(word >> (8 * b));
+        }
+    }
+}
+
+cudaError_t launch_import_blocked_scales(const uint8_t *blocked, int64_t M, int64_t K, uint8_t *scales,
+                                         cudaStream_t stream)
+{
+    const int64_t S = K / 16;
+    const int64_t nb = (S + 3) / 4;
+    const int64_t n_chunks = (nb + kImportBlocks - 1) / kImportBlocks;
+    const int64_t grid = ((M + 127) / 128) * n_chunks;
+    if (grid > 0x7FFFFFFF)
+        return cudaErrorInvalidConfiguration;
+    import_blocked_scales_kernel<<<(unsigned)grid, kImportThreads, 0, stream>>>(blocked, M, S, nb, n_chunks,
+                                                                               scales);
     return cudaGetLastError();
 }
 

@@ -124,6 +124,43 @@ int nvfp4_quantize(const float *w, int64_t M, int64_t K,
                    uint8_t *codes, uint8_t *scales, float *tensor_scale,
                    void *workspace, size_t workspace_bytes, nvfp4_stream_t stream);
 
+/* Quantise bf16 weights to NVFP4: the recipe of nvfp4_quantize applied to the
+ * exact fp32 values of the bf16 inputs, so a bf16 matrix and its fp32 copy give
+ * byte-identical codes, scales and tensor scale.  Checkpoints the pages load
+ * hold bf16 weights that are re-encoded at load time (bw24 README, safetensors
+ * loader; qwentin README, converter section).
+ * w            device bf16 bits [M][K], row-major, finite.
+ * Other arguments, workspace and errors as for nvfp4_quantize (workspace:
+ * nvfp4_workspace_bytes(NVFP4_OP_QUANTIZE, 0, M, K)). */
+int nvfp4_quantize_bf16(const uint16_t *w, int64_t M, int64_t K,
+                        uint8_t *codes, uint8_t *scales, float *tensor_scale,
+                        void *workspace, size_t workspace_bytes, nvfp4_stream_t stream);
+
+/* Import of NVFP4 weights stored with their block scales in the blocked
+ * layout that block-scaled tensor-core GEMMs read.  The pages re-encode
+ * checkpoints into the engine's own layout at load time (bw24 README,
+ * safetensors loader; bw24 wiki Home, NVFP4 decode path) but print no external
+ * layout; this is the one the library accepts:
+ *   codes        uint8 [M][K/2], exactly as in this library (element 2j in the
+ *                low nibble of byte j): no repacking, use the buffer as is.
+ *   scales       E4M3 bytes in 128-row x 4-column blocks, S = K/16 scale
+ *                columns; blocks row-major over (ceil(M/128), ceil(S/4));
+ *                inside a block the scale of row r, column c sits at byte
+ *                (r % 32) * 16 + (r / 32) * 4 + c.  Entries for rows >= M or
+ *                columns >= S are padding and are ignored.
+ *   tensor scale the same fp32 dequantisation factor (weight = code * scale * ts).
+ * nvfp4_blocked_scale_bytes gives the size of the blocked scale buffer (0 for
+ * sizes the call rejects); nvfp4_import_blocked_scales rewrites it into the
+ * row-major [M][K/16] scale buffer this library reads, byte for byte.
+ * blocked  device uint8, nvfp4_blocked_scale_bytes(M, K) bytes, 16-byte aligned.
+ * scales   device uint8 [M][K/16] (output), 16-byte aligned.
+ * Errors: NVFP4_ERR_UNSUPPORTED_SHAPE for K % 16 != 0; NVFP4_ERR_INVALID_ARG
+ * for negative sizes or null / misaligned pointers (M or K = 0 is a no-op). */
+size_t nvfp4_blocked_scale_bytes(int64_t M, int64_t K);
+
+int nvfp4_import_blocked_scales(const uint8_t *blocked, int64_t M, int64_t K,
+                                uint8_t *scales, nvfp4_stream_t stream);
+
 /* Skinny product, N = 1..16 tokens: y[N][M] = x[N][K] . dequant(W)^T.
  * Streams every code and scale byte from HBM once per call for all N tokens
  * (the decode and batched-verify matvec of bw24 README, NVFP4 decode path, and

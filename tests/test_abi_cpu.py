@@ -112,3 +112,35 @@ def test_quantize_rejects_bad_arguments(lib):
     assert q(w=FAKE + 4) == binding.NVFP4_ERR_INVALID_ARG
     assert q(ts=0) == binding.NVFP4_ERR_INVALID_ARG
     assert q(wsb=ws - 4) == binding.NVFP4_ERR_WORKSPACE
+
+
+def test_quantize_bf16_rejects_bad_arguments(lib):
+    ws = g.nvfp4_workspace_bytes(g.NVFP4_OP_QUANTIZE, 0, 64, 64)
+    q = lambda **kw: lib.nvfp4_quantize_bf16(_P(kw.get("w", FAKE)), kw.get("M", 64), kw.get("K", 64),
+                                             _P(kw.get("c", FAKE)), _P(kw.get("s", FAKE)), _P(kw.get("ts", FAKE)),
+                                             _P(kw.get("ws", FAKE)), kw.get("wsb", ws), None)
+    assert q(K=40) == binding.NVFP4_ERR_UNSUPPORTED_SHAPE
+    assert q(M=-1) == binding.NVFP4_ERR_INVALID_ARG
+    assert q(w=0) == binding.NVFP4_ERR_INVALID_ARG
+    assert q(w=FAKE + 2) == binding.NVFP4_ERR_INVALID_ARG
+    assert q(c=FAKE + 8) == binding.NVFP4_ERR_INVALID_ARG
+    assert q(ts=0) == binding.NVFP4_ERR_INVALID_ARG
+    assert q(wsb=ws - 4) == binding.NVFP4_ERR_WORKSPACE
+
+
+def test_blocked_scale_import_arguments(lib):
+    assert g.nvfp4_blocked_scale_bytes(130, 128) == 2048
+    assert g.nvfp4_blocked_scale_bytes(128, 64) == 512
+    assert g.nvfp4_blocked_scale_bytes(1, 16) == 512
+    assert g.nvfp4_blocked_scale_bytes(17408, 5120) == 136 * 80 * 512
+    assert g.nvfp4_blocked_scale_bytes(16, 24) == 0   # K % 16
+    assert g.nvfp4_blocked_scale_bytes(-1, 16) == 0
+    imp = lambda **kw: lib.nvfp4_import_blocked_scales(_P(kw.get("b", FAKE)), kw.get("M", 64), kw.get("K", 64),
+                                                       _P(kw.get("s", FAKE)), None)
+    assert imp(K=40) == binding.NVFP4_ERR_UNSUPPORTED_SHAPE
+    assert imp(M=-1) == binding.NVFP4_ERR_INVALID_ARG
+    assert imp(b=0) == binding.NVFP4_ERR_INVALID_ARG
+    assert imp(s=0) == binding.NVFP4_ERR_INVALID_ARG
+    assert imp(b=FAKE + 4) == binding.NVFP4_ERR_INVALID_ARG
+    assert imp(M=0, b=0, s=0) == binding.NVFP4_OK
+    assert imp(K=0, b=0, s=0) == binding.NVFP4_OK
