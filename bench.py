@@ -60,6 +60,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--no-ingest", action="store_true")
+    ap.add_argument("--ingest-only", action="store_true",
+                    help="print the ingest measurement (quantise fp32 / bf16, scale import) and exit")
     # for profiling one call kind on a short stream (ncu captures): not a bench line
     ap.add_argument("--layers", type=int, default=None, help="override the number of layers in the stream")
     ap.add_argument("--only", choices=["qkv", "o", "gateup", "down"], default=None,
@@ -379,12 +381,13 @@ def ingest_gbs(dev, reps=5):
     algorithmic bytes are two reads of the input (the tensor amax must be known
     before any block is quantised and the matrix is larger than L2) plus the
     NVFP4 writes (0.5625 B per weight); the import reads the blocked scales and
-    writes the row-major ones once.  L2 is flushed before every timed call."""
+    writes the row-major ones once.  L2 is flushed by reading a 256 MB buffer
+    before every timed call."""
     import gemm_nvfp4_gb300 as g
     from gemm_nvfp4_gb300 import inputs
     M, K = inputs.LAYER_27B.shapes()["gate"]
     peak = read_peaks()[0]
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    flush = torch.ones(256 << 20, dtype=torch.uint8, device=dev)
     w32 = inputs.weights(M, K, seed=inputs.matrix_seed("gate"), device=dev)
     w16 = w32.to(torch.bfloat16)
     W = g.nvfp4_quantize(w32)
@@ -404,7 +407,7 @@ def ingest_gbs(dev, reps=5):
         torch.cuda.synchronize()
         total = 0.0
         for _ in range(reps):
-            flush.zero_()
+            torch.amax(flush)  # a read-only flush: leaves no dirty lines to write back
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record()
             fn()
@@ -516,6 +519,9 @@ def main():
     dev = torch.device("cuda", torch.cuda.current_device())
     if args.prefill_profile:
         prefill_profile(dev, args.prefill_profile)
+        return
+    if args.ingest_only:
+        print(json.dumps(ingest_gbs(dev)), flush=True)
         return
     st = LayerStream(args.workload, dev, args.layers)
     graph = st.capture(only=args.only)
