@@ -11,9 +11,12 @@ quantiser steps in the order the recipe writes them, fp64 dot products in k
 order).  This module compiles it with gcc on first use and wraps it with
 ctypes for numpy arrays.
 
+It also covers the ingest helpers (bf16-input quantiser, the blocked 128 x 4
+scale layout) and the FP6 E2M3 block-scaled variant of the weights.
+
 Pins (tests/test_oracle_pins.py) tie every function here to something other
 than itself: brute-force nearest-value searches, PyTorch's float8_e4m3fn
-conversions, a hand-worked block, exact rational arithmetic and closed forms.
+conversions, hand-worked blocks, exact rational arithmetic and closed forms.
 """
 from __future__ import annotations
 
@@ -69,6 +72,14 @@ def _bind(lib):
     lib.nvfp4_oracle_swiglu.argtypes = [P, i64, i64, P, i64,
                                         P, P, f32, P, P, f32,
                                         i64, P, i64, P, P, P, P, P]
+    lib.nvfp4_oracle_e2m3_value.restype = f64
+    lib.nvfp4_oracle_e2m3_value.argtypes = [ctypes.c_int]
+    lib.nvfp4_oracle_e2m3_encode.restype = ctypes.c_uint8
+    lib.nvfp4_oracle_e2m3_encode.argtypes = [f32]
+    lib.nvfp4_oracle_fp6_quantize.restype = ctypes.c_int
+    lib.nvfp4_oracle_fp6_quantize.argtypes = [P, i64, i64, P, P]
+    lib.nvfp4_oracle_fp6_gemv.restype = None
+    lib.nvfp4_oracle_fp6_gemv.argtypes = [P, i64, i64, P, i64, P, P, i64, P, i64, P, P]
     return lib
 
 
@@ -246,6 +257,75 @@ def dequantize(codes, scales, ts, lib=None):
     c[:, 1::2] = codes >> 4
     s = np.repeat(np.asarray(scales, np.uint8), 16, axis=1)
     return e2[c] * e4[s] * float(np.float32(ts))
+
+
+# --------------------------------------------------------------------------
+# FP6 E2M3 block-scaled variant (128-wide UE8M0 block scales, no tensor scale)
+# --------------------------------------------------------------------------
+
+def e2m3_value(code: int, lib=None) -> float:
+    return (lib or _load()).nvfp4_oracle_e2m3_value(int(code))
+
+
+def e2m3_encode(v, lib=None) -> int:
+    """fp32 -> E2M3 code (nearest, ties to even code, saturating at 7.5, sign kept)."""
+    return int((lib or _load()).nvfp4_oracle_e2m3_encode(float(np.float32(v))))
+
+
+def fp6_quantize(w, lib=None):
+    """fp32 [M, K], K % 128 == 0 -> (codes uint8 [M, 3K/4], scales uint8 [M, K/128])."""
+    w = _c(w, np.float32)
+    M, K = w.shape
+    codes = np.zeros((M, K // 8 * 6), np.uint8)
+    scales = np.zeros((M, K // 128), np.uint8)
+    rc = (lib or _load()).nvfp4_oracle_fp6_quantize(_ptr(w), M, K, _ptr(codes), _ptr(scales))
+    if rc != 0:
+        raise ValueError(f"oracle fp6_quantize failed ({rc}): K % 128 != 0 or non-finite weight")
+    return codes, scales
+
+
+def fp6_quantize_bf16(w_bits, lib=None):
+    """bf16 bits [M, K] -> FP6, quantising the exact fp32 values of the inputs."""
+    w_bits = np.ascontiguousarray(w_bits, dtype=np.uint16)
+    return fp6_quantize((w_bits.astype(np.uint32) << np.uint32(16)).view(np.float32), lib)
+
+
+def fp6_gemv(x_bf16_bits, codes, scales, rows=None, tokens=None, lib=None):
+    """y_ref, A (fp64) [n_tokens, n_rows] for FP6 weights; |y - y_ref| <= 1e-5 A + 1e-7."""
+    x = _c(x_bf16_bits, np.uint16)
+    codes = _c(codes, np.uint8)
+    scales = _c(scales, np.uint8)
+    N, K = x.shape
+    M = codes.shape[0]
+    assert codes.shape == (M, K // 8 * 6) and scales.shape == (M, K // 128)
+    r, nr = _index(rows, M)
+    t, nt = _index(tokens, N)
+    y = np.zeros((nt, nr), np.float64)
+    A = np.zeros((nt, nr), np.float64)
+    (lib or _load()).nvfp4_oracle_fp6_gemv(_ptr(x), N, K, _ptr(t), nt, _ptr(codes), _ptr(scales),
+                                           M, _ptr(r), nr, _ptr(y), _ptr(A))
+    return y, A
+
+
+def fp6_swiglu(x_bf16_bits, gate, up, rows=None, tokens=None, lib=None):
+    """h_ref, g_ref, u_ref, Ag, Au for gate = (codes, scales), up = (codes, scales):
+    h = silu(g) * u with silu(g) = g / (1 + exp(-g)), in fp64."""
+    g, Ag = fp6_gemv(x_bf16_bits, gate[0], gate[1], rows, tokens, lib)
+    u, Au = fp6_gemv(x_bf16_bits, up[0], up[1], rows, tokens, lib)
+    return g / (1.0 + np.exp(-g)) * u, g, u, Ag, Au
+
+
+def fp6_dequantize(codes, scales, lib=None):
+    """Exact fp64 FP6 weights [M, K] (for small pins only)."""
+    lib = lib or _load()
+    e = np.array([lib.nvfp4_oracle_e2m3_value(c) for c in range(64)])
+    codes = np.asarray(codes, np.uint8)
+    M, nb = codes.shape
+    K = nb // 6 * 8
+    bits = np.unpackbits(codes, axis=1, bitorder="little").reshape(M, K, 6)
+    c = (bits.astype(np.int64) << np.arange(6)).sum(axis=2)
+    s = np.repeat(np.asarray(scales, np.int64), 128, axis=1)
+    return e[c] * np.exp2(s - 127.0)
 
 
 def load_variant(path: str):

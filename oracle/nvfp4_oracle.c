@@ -19,6 +19,9 @@
  *     (block amax / 6) / tensor scale; code = nearest E2M1 value of
  *     w / (block scale * tensor scale), clamped to +-6.  Every step is done
  *     in fp32, in the order written, with IEEE round-to-nearest-even.
+ *   - The FP6 E2M3 block-scaled variant of the weights (section at the end
+ *     of this file): codes, 128-wide UE8M0 block scales, its quantiser and
+ *     product, with the readings it takes stated there.
  *   - The product y[N,M] = x[N,K] . dequant(W[M,K])^T, computed here in fp64
  *     in k order.  Checking every quantised kernel against a CPU reference is
  *     the first gate of the bw24 wiki Home page (list of checks every kernel
@@ -285,6 +288,150 @@ void nvfp4_oracle_swiglu(const uint16_t *x, int64_t N_total, int64_t K,
             if (u) u[o] = uv;
             if (Ag) Ag[o] = ag;
             if (Au) Au[o] = au;
+        }
+    }
+}
+
+/* ------------------------------------------------------------------------- */
+/* FP6 E2M3 block-scaled weights                                              */
+/* ------------------------------------------------------------------------- */
+/*
+ * The FP6 variant of the weight format (qwentin README, "Highlights" and
+ * "How it works": E2M3 weights, block-scaled, 128-wide block scales, fed to the
+ * block-scaled tensor-core MMA of kind mxf8f6f4).  The pages give no more than
+ * that; the readings below take the OCP microscaling (MX) conversion rule the
+ * named MMA kind is built for, with blocks of 128 instead of 32:
+ *   - element: E2M3, bit 5 sign, bits 4..3 exponent (bias 1), bits 2..0
+ *     mantissa; exponent 0 is subnormal (m/8); largest magnitude 7.5;
+ *   - block scale: one UE8M0 byte s per 128 consecutive k of a row, value
+ *     2^(s-127); no tensor scale;
+ *   - quantise a block: shared exponent = floor(log2(block amax)) - 2 (2 is
+ *     the exponent of E2M3's largest normal, 7.5 = 1.875 * 2^2), raised to -127
+ *     when lower (and -127 for an all-zero block); each element is the nearest
+ *     E2M3 value to w / 2^shared (an fp32 division), ties to the even code,
+ *     magnitudes above 7.5 saturating to 7.5, the sign kept;
+ *   - layout: codes[m][3K/4], each row a little-endian bit stream of 6-bit
+ *     codes (element k at bits 6k..6k+5, so four codes fill three bytes);
+ *     scales[m][K/128].  K must be a multiple of 128.
+ */
+
+double nvfp4_oracle_e2m3_value(int code)
+{
+    int e = (code >> 3) & 3, m = code & 7;
+    double mag = (e == 0) ? m / 8.0 : ldexp(1.0 + m / 8.0, e - 1);
+    return (code & 0x20) ? -mag : mag;
+}
+
+/* fp32 -> E2M3: nearest of the 32 magnitudes (a search over all of them),
+ * ties to the even code, saturating at 7.5, sign bit of the input kept. */
+uint8_t nvfp4_oracle_e2m3_encode(float vf)
+{
+    double a = fabs((double)vf);
+    int best = 0;
+    double best_d = INFINITY;
+    for (int c = 0; c < 32; ++c) {
+        double d = fabs(nvfp4_oracle_e2m3_value(c) - a);
+        if (d < best_d || (d == best_d && (c & 1) == 0)) {
+            best = c;
+            best_d = d;
+        }
+    }
+    return (uint8_t)(best | (signbit(vf) ? 0x20 : 0));
+}
+
+static void put_code6(uint8_t *row, int64_t k, unsigned code)
+{
+    int64_t bit = 6 * k;
+    unsigned v = (code & 63u) << (bit % 8);  /* at most 14 bits */
+    row[bit / 8] |= (uint8_t)(v & 0xFF);
+    if (v >> 8)
+        row[bit / 8 + 1] |= (uint8_t)(v >> 8);
+}
+
+static int get_code6(const uint8_t *row, int64_t k)
+{
+    int64_t bit = 6 * k;
+    unsigned v = row[bit / 8];
+    if (bit % 8 > 2)
+        v |= (unsigned)row[bit / 8 + 1] << 8;
+    return (int)((v >> (bit % 8)) & 63u);
+}
+
+/* Quantise fp32 w[M][K] (K % 128 == 0) to FP6 E2M3 codes and UE8M0 scales.
+ * Returns 0, -1 for a bad shape, -2 for a non-finite weight. */
+int nvfp4_oracle_fp6_quantize(const float *w, int64_t M, int64_t K,
+                              uint8_t *codes, uint8_t *scales)
+{
+    if (M < 0 || K < 0 || K % 128 != 0)
+        return -1;
+    for (int64_t i = 0; i < M * K; ++i)
+        if (!isfinite(w[i]))
+            return -2;
+    const int64_t row_bytes = K / 8 * 6;
+    memset(codes, 0, (size_t)(M * row_bytes));
+    for (int64_t m = 0; m < M; ++m) {
+        for (int64_t b = 0; b < K / 128; ++b) {
+            const float *blk = w + m * K + 128 * b;
+            /* Step 1: block amax. */
+            float amax = 0.0f;
+            for (int i = 0; i < 128; ++i)
+                if (fabsf(blk[i]) > amax)
+                    amax = fabsf(blk[i]);
+            /* Step 2: shared exponent and the UE8M0 scale byte. */
+            int shared = -127;
+            if (amax > 0.0f) {
+                int e;
+                frexpf(amax, &e);           /* amax = f * 2^e, f in [0.5, 1) */
+                shared = (e - 1) - 2;       /* floor(log2(amax)) - 2 */
+                if (shared < -127)
+                    shared = -127;
+            }
+            scales[m * (K / 128) + b] = (uint8_t)(shared + 127);
+            const float X = ldexpf(1.0f, shared);  /* exact; 2^-127 is subnormal */
+            /* Step 3: elements. */
+            for (int i = 0; i < 128; ++i)
+                put_code6(codes + m * row_bytes, 128 * b + i,
+                          nvfp4_oracle_e2m3_encode(blk[i] / X));
+        }
+    }
+    return 0;
+}
+
+/* One FP6 weight, exactly. */
+static double fp6_weight(const uint8_t *codes, const uint8_t *scales,
+                         int64_t K, int64_t m, int64_t k)
+{
+    int code = get_code6(codes + m * (K / 8 * 6), k);
+    return nvfp4_oracle_e2m3_value(code) *
+           ldexp(1.0, (int)scales[m * (K / 128) + k / 128] - 127);
+}
+
+/* y[i][j] = sum_k w(rows[j], k) * x[tokens[i]][k]  (fp64, k order), and
+ * A[i][j] = sum_k |w * x| (may be NULL); rows / tokens as for nvfp4_oracle_gemv. */
+void nvfp4_oracle_fp6_gemv(const uint16_t *x, int64_t N_total, int64_t K,
+                           const int64_t *tokens, int64_t n_tokens,
+                           const uint8_t *codes, const uint8_t *scales,
+                           int64_t M, const int64_t *rows, int64_t n_rows,
+                           double *y, double *A)
+{
+    if (tokens == NULL)
+        n_tokens = N_total;
+    if (rows == NULL)
+        n_rows = M;
+    for (int64_t i = 0; i < n_tokens; ++i) {
+        int64_t n = tokens ? tokens[i] : i;
+        const uint16_t *xrow = x + n * K;
+        for (int64_t j = 0; j < n_rows; ++j) {
+            int64_t m = rows ? rows[j] : j;
+            double sum = 0.0, asum = 0.0;
+            for (int64_t k = 0; k < K; ++k) {
+                double t = fp6_weight(codes, scales, K, m, k) * bf16_value(xrow[k]);
+                sum += t;
+                asum += fabs(t);
+            }
+            y[i * n_rows + j] = sum;
+            if (A)
+                A[i * n_rows + j] = asum;
         }
     }
 }

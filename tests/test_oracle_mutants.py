@@ -44,6 +44,17 @@ MUTANTS = {
                                        "int code = (k & 1) ? (byte & 0xF) : (byte >> 4);"),
     "silu_sign_flipped": ("h[o] = gv / (1.0 + exp(-gv)) * uv;", "h[o] = gv / (1.0 + exp(gv)) * uv;"),
     "clamp_at_4": ("if (a >= 6.0) {\n        code = 7;", "if (a >= 4.0) {\n        code = 6;"),
+    "fp6_emax_3": ("shared = (e - 1) - 2;", "shared = (e - 1) - 3;"),
+    "fp6_no_clamp": ("if (shared < -127)\n                    shared = -127;", ""),
+    "fp6_subnormal_as_quarter": ("double mag = (e == 0) ? m / 8.0 :", "double mag = (e == 0) ? m / 4.0 :"),
+    "fp6_ties_to_odd": ("if (d < best_d || (d == best_d && (c & 1) == 0)) {",
+                        "if (d < best_d || (d == best_d && (c & 1) == 1)) {"),
+    "fp6_sign_of_zero_dropped": ("(signbit(vf) ? 0x20 : 0)", "(vf < 0.0f ? 0x20 : 0)"),
+    "fp6_multiply_by_scale": ("nvfp4_oracle_e2m3_encode(blk[i] / X)", "nvfp4_oracle_e2m3_encode(blk[i] * X)"),
+    "fp6_unpack_misses_byte": ("if (bit % 8 > 2)", "if (bit % 8 > 4)"),
+    "fp6_x_row_stride_wrong": ("const uint16_t *xrow = x + n * K;", "const uint16_t *xrow = x + n;"),
+    "fp6_scale_bias_126": ("ldexp(1.0, (int)scales[m * (K / 128) + k / 128] - 127)",
+                           "ldexp(1.0, (int)scales[m * (K / 128) + k / 128] - 126)"),
 }
 
 

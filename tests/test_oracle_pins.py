@@ -461,3 +461,171 @@ def test_blocked_scale_round_trip(M, K):
     pad = oracle.interleave_scales(np.full_like(s, 1)) == 0
     junk[pad] = 0xEE
     assert np.array_equal(oracle.deinterleave_scales(junk, M, K), s)
+
+
+# ---------------------------------------------------------------------------
+# FP6 E2M3 block-scaled variant
+# ---------------------------------------------------------------------------
+
+# The 32 E2M3 magnitudes listed by their spacing: [0, 2) in steps of 1/8,
+# [2, 4) in steps of 1/4, [4, 7.5] in steps of 1/2.
+E2M3_MAG = [m / 8 for m in range(16)] + [2 + m / 4 for m in range(8)] + [4 + m / 2 for m in range(8)]
+
+
+def e2m3_ref(code: int) -> float:
+    mag = E2M3_MAG[code & 31]
+    return -mag if code & 32 else mag
+
+
+def e2m3_brute(v: float) -> int:
+    """Nearest E2M3 code to fp32 v, ties to the even code, saturating at 7.5, sign kept."""
+    vf = float(np.float32(v))
+    a = Fraction(abs(vf))
+    best, best_d = None, None
+    for c in range(32):
+        d = abs(Fraction(E2M3_MAG[c]) - a)
+        if best is None or d < best_d or (d == best_d and c % 2 == 0):
+            best, best_d = c, d
+    return best | (32 if math.copysign(1.0, vf) < 0 else 0)
+
+
+def floor_log2_f32(a: np.float32) -> int:
+    """floor(log2(a)) of a positive fp32 from its bit pattern."""
+    bits = int(np.array([a], np.float32).view(np.uint32)[0])
+    e = bits >> 23
+    if e:
+        return e - 127
+    return bits.bit_length() - 1 - 149  # subnormal: value = bits * 2^-149
+
+
+def pack6_ref(codes_row) -> np.ndarray:
+    """Little-endian 6-bit stream built as a bit string."""
+    s = "".join(format(int(c), "06b")[::-1] for c in codes_row)  # LSB first
+    return np.array([int(s[i:i + 8][::-1], 2) for i in range(0, len(s), 8)], np.uint8)
+
+
+def fp6_quantize_ref(w: np.ndarray):
+    w = np.asarray(w, np.float32)
+    M, K = w.shape
+    codes = np.zeros((M, K // 8 * 6), np.uint8)
+    scales = np.zeros((M, K // 128), np.uint8)
+    for m in range(M):
+        row = []
+        for b in range(K // 128):
+            blk = w[m, 128 * b:128 * b + 128]
+            amax = np.float32(np.max(np.abs(blk)))
+            shared = max(floor_log2_f32(amax) - 2, -127) if amax > 0 else -127
+            scales[m, b] = shared + 127
+            X = np.float32(2.0 ** shared)
+            row += [e2m3_brute(np.float32(v / X)) for v in blk]
+        codes[m] = pack6_ref(row)
+    return codes, scales
+
+
+def unpack6_ref(codes_row, K):
+    s = "".join(format(int(b), "08b")[::-1] for b in codes_row)
+    return [int(s[6 * k:6 * k + 6][::-1], 2) for k in range(K)]
+
+
+def read_fp6_golden():
+    vals = {}
+    with open(os.path.join(GOLDEN, "fp6_hand_block.txt")) as f:
+        for line in f:
+            line = line.strip()
+            if line and not line.startswith("#"):
+                k, v = (t.strip() for t in line.split("=", 1))
+                vals[k] = v
+    w = np.zeros(128, np.float32)
+    given = [float(t) for t in vals["w"].split()]
+    w[:len(given)] = given
+    return (w, int(vals["scale_byte"], 16), [int(t, 16) for t in vals["codes"].split()],
+            [int(t, 16) for t in vals["first_bytes"].split()])
+
+
+def check_fp6_e2m3_table(lib):
+    for c in range(64):
+        got = oracle.e2m3_value(c, lib=lib)
+        exp = e2m3_ref(c)
+        assert got == exp and math.copysign(1, got) == math.copysign(1, exp), (c, got, exp)
+    assert oracle.e2m3_value(0x1F, lib=lib) == 7.5 and oracle.e2m3_value(0x01, lib=lib) == 0.125
+
+
+def check_fp6_e2m3_encode(lib):
+    vals = []
+    for a, b in zip(E2M3_MAG, E2M3_MAG[1:]):
+        mid = np.float32((a + b) / 2)
+        vals += [mid, np.nextafter(mid, np.float32(0)), np.nextafter(mid, np.float32(9)), np.float32(a)]
+    vals += [np.float32(v) for v in (7.5, 7.7, 7.75, 7.8, 7.99, 100.0, 1e-40)]
+    vals = vals + [np.float32(-v) for v in vals]
+    rng = np.random.default_rng(17)
+    vals += list(rng.uniform(-8, 8, 600).astype(np.float32)) + [np.float32(-0.0), np.float32(-0.03)]
+    for v in vals:
+        assert oracle.e2m3_encode(v, lib=lib) == e2m3_brute(v), (repr(v),)
+
+
+def check_fp6_hand_block(lib):
+    w, sb, codes_exp, first = read_fp6_golden()
+    codes, scales = oracle.fp6_quantize(w.reshape(1, 128), lib=lib)
+    assert scales[0, 0] == sb
+    got = unpack6_ref(codes[0], 128)
+    assert got[:len(codes_exp)] == codes_exp, (got[:12], codes_exp)
+    assert not any(got[len(codes_exp):])
+    assert list(codes[0, :3]) == first
+    # one-hot activation at k = 4 reads back 7.5 * 2^-1
+    x = np.zeros((1, 128), np.uint16)
+    x[0, 4] = 0x3F80  # bf16 1.0
+    y, A = oracle.fp6_gemv(x, codes, scales, lib=lib)
+    assert y[0, 0] == 3.75 and A[0, 0] == 3.75
+
+
+def check_fp6_quantize_random(lib):
+    rng = np.random.default_rng(23)
+    w = (rng.standard_normal((5, 256)) * np.array([[0.02], [1.0], [300.0], [1e-20], [1e-39]])).astype(np.float32)
+    w[0, 7] = np.float32(-0.0)
+    w = np.concatenate([w, np.zeros((1, 256), np.float32)])
+    w[5, 130] = np.float32(2.0 ** -120)   # block 1 of row 5: amax a power of two
+    w[5, 131] = np.float32(-(2.0 ** -120) * 0.75)
+    c, s = oracle.fp6_quantize(w, lib=lib)
+    rc, rs = fp6_quantize_ref(w)
+    assert np.array_equal(s, rs), (s, rs)
+    assert np.array_equal(c, rc)
+    assert s[5, 0] == 0 and s[5, 1] == 127 - 122 and s[4, 0] == 0  # zero block; 2^-120; clamped
+
+
+def check_fp6_gemv_exact_small(lib):
+    rng = np.random.default_rng(29)
+    w = (rng.standard_normal((3, 256)) * 0.05).astype(np.float32)
+    c, s = fp6_quantize_ref(w)  # expected bytes from the independent re-derivation
+    x = bf16_round(rng.standard_normal((2, 256)))
+    y, A = oracle.fp6_gemv(x, c, s, lib=lib)
+    for m in range(3):
+        codes = unpack6_ref(c[m], 256)
+        wq = [Fraction(e2m3_ref(codes[k])) * Fraction(2) ** (int(s[m, k // 128]) - 127) for k in range(256)]
+        for n in range(2):
+            xs = [Fraction(bf16_value(b)) for b in x[n]]
+            exact = sum(a * b for a, b in zip(wq, xs))
+            aexact = sum(abs(a * b) for a, b in zip(wq, xs))
+            assert abs(Fraction(y[n, m]) - exact) <= Fraction(1, 10 ** 12) * aexact
+            assert abs(Fraction(A[n, m]) - aexact) <= Fraction(1, 10 ** 12) * aexact
+
+
+ALL_CHECKS += [check_fp6_e2m3_table, check_fp6_e2m3_encode, check_fp6_hand_block,
+               check_fp6_quantize_random, check_fp6_gemv_exact_small]
+
+
+# (test_oracle_pin above runs every entry of ALL_CHECKS, these included)
+
+
+def test_fp6_pack_and_dequantize_helpers():
+    codes = [1, 2, 3, 4, 63, 0, 32, 31]
+    packed = pack6_ref(codes)
+    assert list(packed[:3]) == [0x81, 0x30, 0x10]  # 1 | 2<<6 | 3<<12 | 4<<18 = 0x103081
+    assert unpack6_ref(packed, 8) == codes
+    w = np.random.default_rng(31).standard_normal((2, 128)).astype(np.float32)
+    c, s = oracle.fp6_quantize(w)
+    d = oracle.fp6_dequantize(c, s)
+    for m in range(2):
+        cc = unpack6_ref(c[m], 128)
+        assert all(d[m, k] == e2m3_ref(cc[k]) * 2.0 ** (int(s[m, 0]) - 127) for k in range(128))
+    with pytest.raises(ValueError):
+        oracle.fp6_quantize(np.zeros((1, 64), np.float32))
