@@ -60,6 +60,9 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--no-ingest", action="store_true")
+    ap.add_argument("--no-fp6", action="store_true")
+    ap.add_argument("--fp6-only", action="store_true",
+                    help="print the FP6 measurement (27B-class MLP stream and prefill) and exit")
     ap.add_argument("--ingest-only", action="store_true",
                     help="print the ingest measurement (quantise fp32 / bf16, scale import) and exit")
     # for profiling one call kind on a short stream (ncu captures): not a bench line
@@ -422,6 +425,72 @@ def ingest_gbs(dev, reps=5):
     return out
 
 
+def fp6_measure(dev, layers=4, reps=10):
+    """FP6 E2M3 weights on the 27B-class MLP matrices: the skinny product
+    streaming `layers` rotating copies of gate/up (SwiGLU) and down (larger
+    than L2 together) at N = 1, 4, 16, as one CUDA graph per N (algorithmic
+    bytes: codes + scales + x + outputs), and the prefill GEMMs at N = 2048
+    (dense bf16-equivalent FLOPs)."""
+    import gemm_nvfp4_gb300 as g
+    from gemm_nvfp4_gb300 import inputs
+    shapes = inputs.LAYER_27B.shapes()
+    Mg, Kg = shapes["gate"]
+    Md, Kd = shapes["down"]
+    peak_hbm, peak_tf, _ = read_peaks()
+    Ws = []
+    for li in range(layers):
+        ws = [g.nvfp4_fp6_quantize(inputs.weights(M, K, seed=inputs.matrix_seed(n) + 7 * li, device=dev))
+              for n, (M, K) in (("gate", (Mg, Kg)), ("up", (Mg, Kg)), ("down", (Md, Kd)))]
+        Ws.append(ws)
+    torch.cuda.synchronize()
+    out = {"unit_stream": "GB/s", "unit_prefill": "TFLOP/s", "peak_hbm": peak_hbm, "peak_bf16": peak_tf,
+           "layers": layers, "weight_bytes": sum(W.nbytes() for ws in Ws for W in ws), "stream": {}, "prefill": {}}
+    for N in (1, 4, 16):
+        xg = inputs.activations(N, Kg, seed=N, device=dev)
+        xd = inputs.activations(N, Kd, seed=N + 1, device=dev)
+        h = torch.empty(N, Mg, dtype=torch.float32, device=dev)
+        y = torch.empty(N, Md, dtype=torch.float32, device=dev)
+        wsg = torch.zeros(g.nvfp4_workspace_bytes(g.NVFP4_OP_FP6_GATEUP_SWIGLU, N, Mg, Kg), dtype=torch.uint8,
+                          device=dev)
+        wsd = torch.zeros(g.nvfp4_workspace_bytes(g.NVFP4_OP_FP6_GEMM, N, Md, Kd), dtype=torch.uint8, device=dev)
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            def run():
+                for ws in Ws:
+                    g.nvfp4_fp6_gateup_swiglu(xg, ws[0], ws[1], out=h, workspace=wsg, stream=s)
+                    g.nvfp4_fp6_gemm(xd, ws[2], out=y, workspace=wsd, stream=s)
+            run()
+            s.synchronize()
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph, stream=s):
+                run()
+        ms = time_graph(graph, reps, 3, 1)  # replays run on the current stream
+        nbytes = out["weight_bytes"] + layers * (N * Kg * 2 + N * Mg * 4 + N * Kd * 2 + N * Md * 4)
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        out["stream"][f"N={N}"] = {"ms": ms, "gbs": gbs, "frac": gbs / peak_hbm if peak_hbm else None}
+    N = 2048
+    xg = inputs.activations(N, Kg, seed=5, device=dev)
+    xd = inputs.activations(N, Kd, seed=6, device=dev)
+    for name, fn, flops in (("gateup", lambda: g.nvfp4_fp6_gateup_swiglu(xg, Ws[0][0], Ws[0][1]),
+                             2 * 2.0 * N * Mg * Kg),
+                            ("down", lambda: g.nvfp4_fp6_gemm(xd, Ws[0][2]), 2.0 * N * Md * Kd)):
+        fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(5):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / 5
+        tf = flops / (ms * 1e-3) / 1e12
+        out["prefill"][f"{name} N={N}"] = {"ms": ms, "tflops": tf, "frac": tf / peak_tf if peak_tf else None}
+    del Ws
+    torch.cuda.empty_cache()
+    return out
+
+
 def prefill_profile(dev, spec):
     """Three prefill calls of one shape (a target for ncu; prints nothing)."""
     import gemm_nvfp4_gb300 as g
@@ -523,6 +592,9 @@ def main():
     if args.ingest_only:
         print(json.dumps(ingest_gbs(dev)), flush=True)
         return
+    if args.fp6_only:
+        print(json.dumps(fp6_measure(dev)), flush=True)
+        return
     st = LayerStream(args.workload, dev, args.layers)
     graph = st.capture(only=args.only)
     dom_graph = st.capture(only="gateup")
@@ -569,6 +641,7 @@ def main():
 
     prefill = prefill_tflops(dev) if not args.no_prefill else None
     ingest = ingest_gbs(dev) if not args.no_ingest else None
+    fp6 = fp6_measure(dev) if not args.no_fp6 else None
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -597,6 +670,7 @@ def main():
             "clocks": clocks,
             "prefill": prefill,
             "ingest": ingest,
+            "fp6": fp6,
         }
         print(json.dumps(line), flush=True)
     if world > 1:

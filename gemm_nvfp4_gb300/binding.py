@@ -27,6 +27,8 @@ NVFP4_OP_QUANTIZE = 0
 NVFP4_OP_GEMV_SKINNY = 1
 NVFP4_OP_GATEUP_SWIGLU = 2
 NVFP4_OP_GEMM_PREFILL = 3
+NVFP4_OP_FP6_GEMM = 4
+NVFP4_OP_FP6_GATEUP_SWIGLU = 5
 
 NVFP4_OUT_F32 = 0
 NVFP4_OUT_BF16 = 1
@@ -72,6 +74,14 @@ def load_library():
         lib.nvfp4_blocked_scale_bytes.argtypes = [i64, i64]
         lib.nvfp4_import_blocked_scales.restype = i32
         lib.nvfp4_import_blocked_scales.argtypes = [P, i64, i64, P, P]
+        lib.nvfp4_fp6_quantize.restype = i32
+        lib.nvfp4_fp6_quantize.argtypes = [P, i64, i64, P, P, P]
+        lib.nvfp4_fp6_quantize_bf16.restype = i32
+        lib.nvfp4_fp6_quantize_bf16.argtypes = [P, i64, i64, P, P, P]
+        lib.nvfp4_fp6_gemm.restype = i32
+        lib.nvfp4_fp6_gemm.argtypes = [P, i64, P, P, i64, i64, P, i32, P, sz, P]
+        lib.nvfp4_fp6_gateup_swiglu.restype = i32
+        lib.nvfp4_fp6_gateup_swiglu.argtypes = [P, i64, P, P, P, P, i64, i64, P, i32, P, sz, P]
         lib.nvfp4_gemv_skinny.restype = i32
         lib.nvfp4_gemv_skinny.argtypes = [P, i64, P, P, P, i64, i64, P, i32, P, sz, P]
         lib.nvfp4_gateup_swiglu.restype = i32
@@ -253,6 +263,80 @@ def nvfp4_gemm_prefill(x: torch.Tensor, W: NVFP4Weight, out_dtype=torch.float32,
                                            _stream(stream))
     _check(st, "nvfp4_gemm_prefill")
     return y
+
+
+@dataclass
+class FP6Weight:
+    """One FP6 E2M3 block-scaled tensor W[M][K] in device memory (include/nvfp4.h)."""
+    codes: torch.Tensor   # uint8 [M, 3K/4]
+    scales: torch.Tensor  # uint8 [M, K/128] (UE8M0)
+
+    @property
+    def M(self) -> int:
+        return self.codes.shape[0]
+
+    @property
+    def K(self) -> int:
+        return self.codes.shape[1] // 6 * 8
+
+    def nbytes(self) -> int:
+        return self.codes.numel() + self.scales.numel()
+
+
+def _fp6_out(M, K, device, out):
+    if out is not None:
+        return out
+    return FP6Weight(torch.empty(M, K // 8 * 6, dtype=torch.uint8, device=device),
+                     torch.empty(M, K // 128, dtype=torch.uint8, device=device))
+
+
+def nvfp4_fp6_quantize(w: torch.Tensor, out: FP6Weight | None = None, stream=None) -> FP6Weight:
+    """fp32 [M, K] CUDA tensor (K % 128 == 0) -> FP6Weight."""
+    if w.dtype != torch.float32:
+        raise ValueError(f"nvfp4_fp6_quantize takes fp32 weights, got {w.dtype}")
+    M, K = w.shape
+    out = _fp6_out(M, K, w.device, out)
+    st = load_library().nvfp4_fp6_quantize(_ptr(w), M, K, _ptr(out.codes), _ptr(out.scales), _stream(stream))
+    _check(st, "nvfp4_fp6_quantize")
+    return out
+
+
+def nvfp4_fp6_quantize_bf16(w: torch.Tensor, out: FP6Weight | None = None, stream=None) -> FP6Weight:
+    """bf16 [M, K] CUDA tensor -> FP6Weight, identical to quantising w.float()."""
+    if w.dtype != torch.bfloat16:
+        raise ValueError(f"nvfp4_fp6_quantize_bf16 takes bf16 weights, got {w.dtype}")
+    M, K = w.shape
+    out = _fp6_out(M, K, w.device, out)
+    st = load_library().nvfp4_fp6_quantize_bf16(_ptr(w), M, K, _ptr(out.codes), _ptr(out.scales),
+                                                _stream(stream))
+    _check(st, "nvfp4_fp6_quantize_bf16")
+    return out
+
+
+def nvfp4_fp6_gemm(x: torch.Tensor, W: FP6Weight, out_dtype=torch.float32, out: torch.Tensor | None = None,
+                   workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """y[N, M] = x[N, K] (bf16) . dequant(W)^T for FP6 weights, any N >= 1."""
+    N, K = x.shape
+    y = _new_out(N, W.M, out_dtype, x.device, out)
+    ws, ws_bytes = _workspace(NVFP4_OP_FP6_GEMM, N, W.M, K, x.device, workspace)
+    st = load_library().nvfp4_fp6_gemm(_ptr(x), N, _ptr(W.codes), _ptr(W.scales), W.M, K, _ptr(y),
+                                       _out_code(y.dtype), _ptr(ws), ws_bytes, _stream(stream))
+    _check(st, "nvfp4_fp6_gemm")
+    return y
+
+
+def nvfp4_fp6_gateup_swiglu(x: torch.Tensor, Wg: FP6Weight, Wu: FP6Weight, out_dtype=torch.float32,
+                            out: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
+                            stream=None) -> torch.Tensor:
+    """h[N, M] = silu(x . Wg^T) * (x . Wu^T) for FP6 weights, any N >= 1."""
+    N, K = x.shape
+    h = _new_out(N, Wg.M, out_dtype, x.device, out)
+    ws, ws_bytes = _workspace(NVFP4_OP_FP6_GATEUP_SWIGLU, N, Wg.M, K, x.device, workspace)
+    st = load_library().nvfp4_fp6_gateup_swiglu(_ptr(x), N, _ptr(Wg.codes), _ptr(Wg.scales), _ptr(Wu.codes),
+                                                _ptr(Wu.scales), Wg.M, K, _ptr(h), _out_code(h.dtype),
+                                                _ptr(ws), ws_bytes, _stream(stream))
+    _check(st, "nvfp4_fp6_gateup_swiglu")
+    return h
 
 
 def nvfp4_gemv_skinny_noalloc(x: torch.Tensor, W: NVFP4Weight, out_dtype=torch.float32,

@@ -124,4 +124,76 @@ NVFP4_DEVINL uint16_t f32_to_bf16(float v)
     return r;
 }
 
+// ---------------------------------------------------------------------------
+// FP6 E2M3 weights (block-scaled variant: UE8M0 scale per 128 k)
+// ---------------------------------------------------------------------------
+
+// Two E2M3 codes (bits 0..5 and 6..11 of u) -> bf16x2 holding e2m3 * 2^-126
+// each.  The five magnitude bits (2 exponent, 3 mantissa) land on bf16 bits
+// 8..4, so the bf16 exponent field is the E2M3 exponent field and the mantissa
+// is m/8: a normal code reads 2^(e-127) * (1 + m/8) = e2m3 * 2^-126 and a
+// subnormal code (e = 0) the bf16 subnormal 2^-126 * m/8 = e2m3 * 2^-126.
+// The sign goes to bit 15.
+NVFP4_DEVINL uint32_t e2m3x2_to_bf16x2(uint32_t u)
+{
+    return ((u << 4) & 0x000001F0u) | ((u << 10) & 0x00008000u) | ((u << 14) & 0x01F00000u) |
+           ((u << 20) & 0x80000000u);
+}
+
+// Eight codes of a 48-bit little-endian group (lo = bits 0..31, hi = 32..47)
+// -> four bf16x2 words in natural k order (k0k1, k2k3, k4k5, k6k7).
+NVFP4_DEVINL uint4 e2m3x8_to_bf16(uint32_t lo, uint32_t hi)
+{
+    return make_uint4(e2m3x2_to_bf16x2(lo), e2m3x2_to_bf16x2(lo >> 12),
+                      e2m3x2_to_bf16x2((lo >> 24) | (hi << 8)), e2m3x2_to_bf16x2(hi >> 4));
+}
+
+// Multipliers that turn e2m3 * 2^-126 into e2m3 * 2^(s-127) (s = UE8M0 byte)
+// with exact bf16 multiplies: 2^(s-1) when s <= 128, else 2^127 then 2^(s-128)
+// (every factor and product stays a bf16 value with at most 4 significant bits).
+struct Fp6Mult {
+    uint32_t m1, m2;
+    bool two;
+};
+
+NVFP4_DEVINL Fp6Mult fp6_mult(uint32_t s)
+{
+    Fp6Mult r;
+    r.two = s > 128u;
+    const uint32_t b1 = ((r.two ? 127u : s - 1u) + 127u) << 7;  // s = 0 wraps to 2^-1
+    const uint32_t b2 = ((s - 128u) + 127u) << 7;
+    r.m1 = b1 | (b1 << 16);
+    r.m2 = b2 | (b2 << 16);
+    return r;
+}
+
+NVFP4_DEVINL uint32_t fp6_apply(uint32_t p, const Fp6Mult &m)
+{
+    p = bf16x2_mul(p, m.m1);
+    return m.two ? bf16x2_mul(p, m.m2) : p;
+}
+
+// 8-k group q (0..3) of 32 consecutive codes held as 24 bytes (three uint2,
+// little-endian 6-bit stream): bf16 pairs in natural k order, each value
+// e2m3 * 2^(s-127).  Group q occupies bytes 6q .. 6q+5.
+NVFP4_DEVINL uint4 fp6_group(const uint2 (&c)[3], int q, const Fp6Mult &mult)
+{
+    uint32_t lo, hi;
+    if (q == 0) {
+        lo = c[0].x;
+        hi = c[0].y & 0xFFFFu;
+    } else if (q == 1) {
+        lo = (c[0].y >> 16) | (c[1].x << 16);
+        hi = c[1].x >> 16;
+    } else if (q == 2) {
+        lo = c[1].y;
+        hi = c[2].x & 0xFFFFu;
+    } else {
+        lo = (c[2].x >> 16) | (c[2].y << 16);
+        hi = c[2].y >> 16;
+    }
+    const uint4 p = e2m3x8_to_bf16(lo, hi);
+    return make_uint4(fp6_apply(p.x, mult), fp6_apply(p.y, mult), fp6_apply(p.z, mult), fp6_apply(p.w, mult));
+}
+
 }  // namespace nvfp4

@@ -30,6 +30,7 @@
 //   * Epilogue: y = acc * 2^8 * ts (fp32 or bf16), or for the gate/up pair
 //     h = g / (1 + exp(-g)) * u with g and u from their own tensor scales.
 #include <algorithm>
+#include <type_traits>
 
 #include "common.cuh"
 #include "kernels.h"
@@ -195,6 +196,83 @@ NVFP4_DEVINL void compute_chunk(const Chunk<NW> &ch, const GemvArgs &a, int64_t 
     }
 }
 
+// ---- FP6 E2M3 weights (one UE8M0 scale per 128 k = per chunk and row) ----
+//
+// A lane holds the same 32 k of rows g and g+8 as above (24 code bytes each).
+// The codes unpack to bf16 pairs in natural k order (k, k+1), and the
+// activations are used in natural order too: the MMA's logical k slot 2t,2t+1
+// holds the lane's pair (k0, k1) of an 8-k group in both operands, slot
+// 2t+8,2t+9 the pair (k2, k3); the second MMA of the group takes (k4,k5) and
+// (k6,k7).  Each dequantised weight is e2m3 * 2^(s-127), exact in bf16.
+template <int NW>
+struct Chunk6 {
+    uint2 code[NW][2][3];  // rows g, g+8: 24 code bytes (32 k) each
+    uint32_t scl[NW][2];   // rows g, g+8: the chunk's scale byte
+};
+
+template <int NW>
+NVFP4_DEVINL void load_chunk6(Chunk6<NW> &ch, const GemvArgs &a, int64_t tile, int64_t c, int g, int t)
+{
+    const int64_t row_bytes = a.K / 8 * 6, nblk = a.K / 128;
+#pragma unroll
+    for (int mi = 0; mi < NW; ++mi) {
+#pragma unroll
+        for (int ri = 0; ri < 2; ++ri) {
+            const int64_t r = tile * kTileRows + g + 8 * ri;
+            if (r < a.M) {
+                const uint8_t *cp = a.codes[mi] + r * row_bytes + c * 96 + 24 * t;
+#pragma unroll
+                for (int i = 0; i < 3; ++i)
+                    ch.code[mi][ri][i] = ldg_stream_v2(cp + 8 * i);
+                ch.scl[mi][ri] = __ldg(a.scales[mi] + r * nblk + c);
+            } else {
+#pragma unroll
+                for (int i = 0; i < 3; ++i)
+                    ch.code[mi][ri][i] = make_uint2(0, 0);
+                ch.scl[mi][ri] = 127;
+            }
+        }
+    }
+}
+
+template <int NW, int NT>
+NVFP4_DEVINL void compute_chunk6(const Chunk6<NW> &ch, const GemvArgs &a, int64_t c, int g, int t,
+                                 float (&acc)[NW][NT][4])
+{
+    const int64_t k0 = c * kChunkK + 32 * t;  // K % 128 == 0: all 32 k are valid
+    uint4 xv[NT][4];
+#pragma unroll
+    for (int j = 0; j < NT; ++j) {
+        const int n = g + 8 * j;
+        if (n < a.N) {
+            const uint16_t *xp = a.x + (int64_t)n * a.K + k0;
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                xv[j][q] = ldg_v4(xp + 8 * q);
+        } else {
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                xv[j][q] = make_uint4(0, 0, 0, 0);
+        }
+    }
+#pragma unroll
+    for (int mi = 0; mi < NW; ++mi) {
+        const Fp6Mult m0 = fp6_mult(ch.scl[mi][0]), m1 = fp6_mult(ch.scl[mi][1]);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const uint4 pa = fp6_group(ch.code[mi][0], q, m0);
+            const uint4 pb = fp6_group(ch.code[mi][1], q, m1);
+            const uint32_t a0[4] = {pa.x, pb.x, pa.y, pb.y};
+            const uint32_t a1[4] = {pa.z, pb.z, pa.w, pb.w};
+#pragma unroll
+            for (int j = 0; j < NT; ++j) {
+                mma_bf16_16816(acc[mi][j], a0, xv[j][q].x, xv[j][q].y);
+                mma_bf16_16816(acc[mi][j], a1, xv[j][q].z, xv[j][q].w);
+            }
+        }
+    }
+}
+
 NVFP4_DEVINL float silu_mul(float g, float u)
 {
     return __fdiv_rn(g, 1.0f + expf(-g)) * u;
@@ -208,9 +286,13 @@ NVFP4_DEVINL void store_out(void *y, int out_bf16, int64_t idx, float v)
         reinterpret_cast<float *>(y)[idx] = v;
 }
 
-template <int NW>
+// FMT 0: NVFP4 (accumulators hold sum * 2^-8, times the tensor scale);
+// FMT 1: FP6 (accumulators hold the sum itself).
+template <int NW, int FMT>
 NVFP4_DEVINL float finish(const float (&v)[NW], const float (&ts)[NW])
 {
+    if (FMT == 1)
+        return NW == 1 ? v[0] : silu_mul(v[0], v[NW - 1]);
     if (NW == 1)
         return v[0] * 256.0f * ts[0];
     const float g = v[0] * 256.0f * ts[0];
@@ -218,9 +300,10 @@ NVFP4_DEVINL float finish(const float (&v)[NW], const float (&ts)[NW])
     return silu_mul(g, u);
 }
 
-template <int NW, int NT, bool ALIGNED>
+template <int NW, int NT, bool ALIGNED, int FMT>
 __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(GemvArgs a)
 {
+    using Ch = typename std::conditional<FMT == 0, Chunk<NW>, Chunk6<NW>>::type;
     // Chunks of codes in flight per warp (registers): ~48 KB per SM at 2 CTAs.
     constexpr int kPrefetch = NW == 1 ? 3 : 2;
     __shared__ float red[kWarps][NW][kTileRows][16];
@@ -234,7 +317,7 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(GemvArgs a)
     float ts[NW];
 #pragma unroll
     for (int mi = 0; mi < NW; ++mi)
-        ts[mi] = __ldg(a.ts[mi]);
+        ts[mi] = FMT == 0 ? __ldg(a.ts[mi]) : 1.0f;
     const int64_t first_tile = lo / a.chunks;
 
     for (int64_t tile = first_tile; tile * a.chunks < hi; ++tile) {
@@ -251,22 +334,31 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(GemvArgs a)
                 for (int e = 0; e < 4; ++e)
                     acc[mi][j][e] = 0.0f;
 
-        Chunk<NW> buf[kPrefetch];
+        Ch buf[kPrefetch];
+        auto load = [&](Ch &dst, int64_t c) {
+            if constexpr (FMT == 0)
+                load_chunk<NW, ALIGNED>(dst, a, tile, c, g, t);
+            else
+                load_chunk6<NW>(dst, a, tile, c, g, t);
+        };
 #pragma unroll
         for (int s = 0; s < kPrefetch; ++s) {
             const int64_t c = c0 + warp + s * kWarps;
             if (c < c1)
-                load_chunk<NW, ALIGNED>(buf[s], a, tile, c, g, t);
+                load(buf[s], c);
         }
         for (int64_t cb = c0 + warp; cb < c1; cb += kPrefetch * kWarps) {
 #pragma unroll
             for (int s = 0; s < kPrefetch; ++s) {
                 const int64_t c = cb + s * kWarps;
                 if (c < c1) {
-                    compute_chunk<NW, NT>(buf[s], a, c, g, t, acc);
+                    if constexpr (FMT == 0)
+                        compute_chunk<NW, NT>(buf[s], a, c, g, t, acc);
+                    else
+                        compute_chunk6<NW, NT>(buf[s], a, c, g, t, acc);
                     const int64_t cn = c + kPrefetch * kWarps;
                     if (cn < c1)
-                        load_chunk<NW, ALIGNED>(buf[s], a, tile, cn, g, t);
+                        load(buf[s], cn);
                 }
             }
         }
@@ -305,7 +397,7 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(GemvArgs a)
             }
             if (c0 == 0 && c1 == a.chunks) {
                 if (tok < a.N && m < a.M)
-                    store_out(a.y, a.out_bf16, (int64_t)tok * a.M + m, finish<NW>(v, ts));
+                    store_out(a.y, a.out_bf16, (int64_t)tok * a.M + m, finish<NW, FMT>(v, ts));
             } else {
                 const int slot = (tile == first_tile) ? 0 : 1;
 #pragma unroll
@@ -326,7 +418,7 @@ NVFP4_DEVINL int cta_of(int64_t q, int64_t total, int P)
 // One block per CTA boundary: the tile holding boundary lo_b (if it lies
 // strictly inside a tile and is that tile's first inner boundary) is summed
 // over the CTAs that touch it, in CTA order.
-template <int NW>
+template <int NW, int FMT>
 __global__ void __launch_bounds__(256) gemv_fixup_kernel(GemvArgs a)
 {
     const int b = blockIdx.x + 1;
@@ -344,7 +436,7 @@ __global__ void __launch_bounds__(256) gemv_fixup_kernel(GemvArgs a)
     float ts[NW];
 #pragma unroll
     for (int mi = 0; mi < NW; ++mi)
-        ts[mi] = __ldg(a.ts[mi]);
+        ts[mi] = FMT == 0 ? __ldg(a.ts[mi]) : 1.0f;
     float v[NW];
 #pragma unroll
     for (int mi = 0; mi < NW; ++mi)
@@ -360,15 +452,15 @@ __global__ void __launch_bounds__(256) gemv_fixup_kernel(GemvArgs a)
         }
     }
     if (tok < a.N && m < a.M)
-        store_out(a.y, a.out_bf16, (int64_t)tok * a.M + m, finish<NW>(v, ts));
+        store_out(a.y, a.out_bf16, (int64_t)tok * a.M + m, finish<NW, FMT>(v, ts));
 }
 
-template <int NW, int NT, bool ALIGNED>
+template <int NW, int NT, bool ALIGNED, int FMT = 0>
 static cudaError_t launch_t(const GemvArgs &a, cudaStream_t stream)
 {
-    gemv_kernel<NW, NT, ALIGNED><<<a.P, kThreads, 0, stream>>>(a);
+    gemv_kernel<NW, NT, ALIGNED, FMT><<<a.P, kThreads, 0, stream>>>(a);
     if (a.P > 1)
-        gemv_fixup_kernel<NW><<<a.P - 1, 256, 0, stream>>>(a);
+        gemv_fixup_kernel<NW, FMT><<<a.P - 1, 256, 0, stream>>>(a);
     return cudaGetLastError();
 }
 
@@ -376,7 +468,7 @@ size_t skinny_workspace_bytes(int64_t M, int64_t K, int n_weights)
 {
     if (skinny_tc_supported(M, K))
         return skinny_tc_workspace_bytes(M, K, n_weights);
-    return 256 + (size_t)kGemvMaxCtas * kGemvPartialFloatsPerCta * n_weights * 4;
+    return gemv_mma_workspace_bytes(n_weights);
 }
 
 int64_t gemv_grid(int64_t M, int64_t K, int num_sms)
@@ -422,6 +514,40 @@ cudaError_t launch_gemv(const uint16_t *x, int N, int64_t M, int64_t K, const ui
     if (N <= 8)
         return aligned ? launch_t<2, 1, true>(a, stream) : launch_t<2, 1, false>(a, stream);
     return aligned ? launch_t<2, 2, true>(a, stream) : launch_t<2, 2, false>(a, stream);
+}
+
+size_t gemv_mma_workspace_bytes(int n_weights)
+{
+    return 256 + (size_t)kGemvMaxCtas * kGemvPartialFloatsPerCta * n_weights * 4;
+}
+
+cudaError_t launch_gemv_fp6(const uint16_t *x, int N, int64_t M, int64_t K, const uint8_t *const *codes,
+                            const uint8_t *const *scales, int n_weights, void *y, int out_bf16, void *workspace,
+                            int num_sms, cudaStream_t stream)
+{
+    GemvArgs a{};
+    a.x = x;
+    a.N = N;
+    a.M = M;
+    a.K = K;
+    for (int i = 0; i < 2; ++i) {
+        const int s = i < n_weights ? i : 0;
+        a.codes[i] = codes[s];
+        a.scales[i] = scales[s];
+        a.ts[i] = nullptr;
+    }
+    a.y = y;
+    a.out_bf16 = out_bf16;
+    a.partial = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(workspace) + 256);
+    a.tiles = (M + kTileRows - 1) / kTileRows;
+    a.chunks = K / kChunkK;  // K % 128 == 0
+    a.total = a.tiles * a.chunks;
+    a.P = (int)gemv_grid(M, K, num_sms);
+    if (a.total == 0)
+        return cudaSuccess;
+    if (n_weights == 1)
+        return N <= 8 ? launch_t<1, 1, true, 1>(a, stream) : launch_t<1, 2, true, 1>(a, stream);
+    return N <= 8 ? launch_t<2, 1, true, 1>(a, stream) : launch_t<2, 2, true, 1>(a, stream);
 }
 
 }  // namespace nvfp4

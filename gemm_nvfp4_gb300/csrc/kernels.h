@@ -18,6 +18,10 @@ cudaError_t launch_quantize(const float *w, int64_t M, int64_t K, uint8_t *codes
                             float *tensor_scale, void *workspace, int num_sms, cudaStream_t stream);
 cudaError_t launch_quantize_bf16(const uint16_t *w, int64_t M, int64_t K, uint8_t *codes, uint8_t *scales,
                                  float *tensor_scale, void *workspace, int num_sms, cudaStream_t stream);
+cudaError_t launch_fp6_quantize(const float *w, int64_t M, int64_t K, uint8_t *codes, uint8_t *scales,
+                                int num_sms, cudaStream_t stream);
+cudaError_t launch_fp6_quantize_bf16(const uint16_t *w, int64_t M, int64_t K, uint8_t *codes, uint8_t *scales,
+                                     int num_sms, cudaStream_t stream);
 cudaError_t launch_import_blocked_scales(const uint8_t *blocked, int64_t M, int64_t K, uint8_t *scales,
                                          cudaStream_t stream);
 
@@ -28,6 +32,18 @@ cudaError_t launch_gemv(const uint16_t *x, int N, int64_t M, int64_t K, const ui
                         int out_bf16, void *workspace, int num_sms, cudaStream_t stream);
 
 int64_t gemv_grid(int64_t M, int64_t K, int num_sms);
+
+// FP6 E2M3 weights (codes [M][3K/4], UE8M0 scales [M][K/128], K % 128 == 0):
+// the skinny product for N = 1..16 on the warp-level MMA kernel of gemv.cu
+// (split-K partials in the workspace, gemv_mma_workspace_bytes), and the
+// tensor-core prefill for larger N.
+size_t gemv_mma_workspace_bytes(int n_weights);
+cudaError_t launch_gemv_fp6(const uint16_t *x, int N, int64_t M, int64_t K, const uint8_t *const *codes,
+                            const uint8_t *const *scales, int n_weights, void *y, int out_bf16, void *workspace,
+                            int num_sms, cudaStream_t stream);
+cudaError_t launch_prefill_fp6(const uint16_t *x, int64_t N, int64_t M, int64_t K, const uint8_t *const *codes,
+                               const uint8_t *const *scales, int n_weights, void *y, int out_bf16,
+                               void *workspace, int num_sms, cudaStream_t stream);
 
 }  // namespace nvfp4
 

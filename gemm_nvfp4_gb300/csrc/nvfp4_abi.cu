@@ -131,6 +131,13 @@ size_t nvfp4_workspace_bytes(int op, int64_t N, int64_t M, int64_t K)
     case NVFP4_OP_GEMV_SKINNY: return (N >= 1 && N <= kMaxSkinnyN) ? skinny_ws(M, K, 1) : 0;
     case NVFP4_OP_GATEUP_SWIGLU: return N <= kMaxSkinnyN ? skinny_ws(M, K, 2) : prefill_workspace_bytes(N, M, K, 2);
     case NVFP4_OP_GEMM_PREFILL: return N <= kMaxSkinnyN ? skinny_ws(M, K, 1) : prefill_workspace_bytes(N, M, K, 1);
+    case NVFP4_OP_FP6_GEMM:
+    case NVFP4_OP_FP6_GATEUP_SWIGLU: {
+        if (K % 128 != 0)
+            return 0;
+        const int nw = op == NVFP4_OP_FP6_GEMM ? 1 : 2;
+        return N <= kMaxSkinnyN ? gemv_mma_workspace_bytes(nw) : prefill_workspace_bytes(N, M, K, nw);
+    }
     default: return 0;
     }
 }
@@ -199,6 +206,101 @@ int nvfp4_import_blocked_scales(const uint8_t *blocked, int64_t M, int64_t K, ui
         return NVFP4_ERR_INVALID_ARG;
     cudaError_t e = launch_import_blocked_scales(blocked, M, K, scales, (cudaStream_t)stream);
     return e == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA;
+}
+
+// ---------------------------------------------------------------------------
+// FP6 E2M3 block-scaled weights
+// ---------------------------------------------------------------------------
+
+static int fp6_check_quantize(const void *w, int64_t M, int64_t K, const uint8_t *codes, const uint8_t *scales)
+{
+    if (M < 0 || K < 0)
+        return NVFP4_ERR_INVALID_ARG;
+    if (K % 128 != 0 || !size_ok(M, K))
+        return NVFP4_ERR_UNSUPPORTED_SHAPE;
+    if (M * K > 0 && (!w || !codes || !scales || !aligned(w, 16) || !aligned(codes, 16) || !aligned(scales, 16)))
+        return NVFP4_ERR_INVALID_ARG;
+    return NVFP4_OK;
+}
+
+int nvfp4_fp6_quantize(const float *w, int64_t M, int64_t K, uint8_t *codes, uint8_t *scales,
+                       nvfp4_stream_t stream)
+{
+    int rc = fp6_check_quantize(w, M, K, codes, scales);
+    if (rc != NVFP4_OK || M * K == 0)
+        return rc;
+    int sms = 0;
+    if ((rc = current_num_sms(&sms)) != NVFP4_OK)
+        return rc;
+    cudaError_t e = launch_fp6_quantize(w, M, K, codes, scales, sms, (cudaStream_t)stream);
+    return e == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA;
+}
+
+int nvfp4_fp6_quantize_bf16(const uint16_t *w, int64_t M, int64_t K, uint8_t *codes, uint8_t *scales,
+                            nvfp4_stream_t stream)
+{
+    int rc = fp6_check_quantize(w, M, K, codes, scales);
+    if (rc != NVFP4_OK || M * K == 0)
+        return rc;
+    int sms = 0;
+    if ((rc = current_num_sms(&sms)) != NVFP4_OK)
+        return rc;
+    cudaError_t e = launch_fp6_quantize_bf16(w, M, K, codes, scales, sms, (cudaStream_t)stream);
+    return e == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA;
+}
+
+static int fp6_products(const uint16_t *x, int64_t N, int64_t M, int64_t K, const uint8_t *const *codes,
+                        const uint8_t *const *scales, int n_weights, void *y, int out_dtype, void *ws,
+                        size_t ws_bytes, cudaStream_t stream)
+{
+    if (N < 0 || M < 0 || K < 0)
+        return NVFP4_ERR_INVALID_ARG;
+    if (out_dtype != NVFP4_OUT_F32 && out_dtype != NVFP4_OUT_BF16)
+        return NVFP4_ERR_INVALID_ARG;
+    if (K % 128 != 0 || !size_ok(N, K) || !size_ok(M, K) || !size_ok(N, M))
+        return NVFP4_ERR_UNSUPPORTED_SHAPE;
+    if (N == 0 || M == 0)
+        return NVFP4_OK;
+    if (!y || !aligned(y, 16))
+        return NVFP4_ERR_INVALID_ARG;
+    if (K > 0) {
+        if (!x || !aligned(x, 16))
+            return NVFP4_ERR_INVALID_ARG;
+        for (int i = 0; i < n_weights; ++i)
+            if (!codes[i] || !scales[i] || !aligned(codes[i], 16) || !aligned(scales[i], 16))
+                return NVFP4_ERR_INVALID_ARG;
+    }
+    const int op = n_weights == 1 ? NVFP4_OP_FP6_GEMM : NVFP4_OP_FP6_GATEUP_SWIGLU;
+    int rc = check_workspace(ws, ws_bytes, nvfp4_workspace_bytes(op, N, M, K));
+    if (rc != NVFP4_OK)
+        return rc;
+    if (K == 0)
+        return zero_output(y, N, M, out_dtype, stream);
+    int sms = 0;
+    if ((rc = current_num_sms(&sms)) != NVFP4_OK)
+        return rc;
+    const int bf16 = out_dtype == NVFP4_OUT_BF16;
+    cudaError_t e = N <= kMaxSkinnyN
+                        ? launch_gemv_fp6(x, (int)N, M, K, codes, scales, n_weights, y, bf16, ws, sms, stream)
+                        : launch_prefill_fp6(x, N, M, K, codes, scales, n_weights, y, bf16, ws, sms, stream);
+    return e == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA;
+}
+
+int nvfp4_fp6_gemm(const uint16_t *x, int64_t N, const uint8_t *codes, const uint8_t *scales, int64_t M, int64_t K,
+                   void *y, int out_dtype, void *workspace, size_t workspace_bytes, nvfp4_stream_t stream)
+{
+    const uint8_t *c[1] = {codes};
+    const uint8_t *s[1] = {scales};
+    return fp6_products(x, N, M, K, c, s, 1, y, out_dtype, workspace, workspace_bytes, (cudaStream_t)stream);
+}
+
+int nvfp4_fp6_gateup_swiglu(const uint16_t *x, int64_t N, const uint8_t *gate_codes, const uint8_t *gate_scales,
+                            const uint8_t *up_codes, const uint8_t *up_scales, int64_t M, int64_t K, void *h,
+                            int out_dtype, void *workspace, size_t workspace_bytes, nvfp4_stream_t stream)
+{
+    const uint8_t *c[2] = {gate_codes, up_codes};
+    const uint8_t *s[2] = {gate_scales, up_scales};
+    return fp6_products(x, N, M, K, c, s, 2, h, out_dtype, workspace, workspace_bytes, (cudaStream_t)stream);
 }
 
 int nvfp4_gemv_skinny(const uint16_t *x, int64_t N, const uint8_t *codes, const uint8_t *scales,

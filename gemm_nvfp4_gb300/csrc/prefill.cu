@@ -37,6 +37,7 @@
 #include <algorithm>
 #include <cmath>
 #include <mutex>
+#include <type_traits>
 
 #include "common.cuh"
 #include "kernels.h"
@@ -131,15 +132,39 @@ NVFP4_DEVINL DqItem dq_load(const Args &a, int mi, int64_t m, int kb, int half)
     return it;
 }
 
+// FP6 E2M3 weights: 32 k of one row = 24 code bytes and the scale byte of the
+// row's 128-k block (K % 128 == 0, so every stage is complete).
+struct DqItem6 {
+    uint2 code[3];
+    uint32_t scl;
+};
+
+NVFP4_DEVINL DqItem6 dq_load6(const Args &a, int mi, int64_t m, int kb, int half)
+{
+    DqItem6 it{{make_uint2(0, 0), make_uint2(0, 0), make_uint2(0, 0)}, 127u};
+    const int64_t k0 = (int64_t)kb * BK + half * 32;
+    if (m >= a.M || k0 >= a.K)
+        return it;
+    const uint8_t *cp = a.codes[mi] + m * (a.K / 8 * 6) + k0 / 4 * 3;
+#pragma unroll
+    for (int i = 0; i < 3; ++i)
+        it.code[i] = ldg_stream_v2(cp + 8 * i);
+    it.scl = __ldg(a.scales[mi] + m * (a.K / 128) + k0 / 128);
+    return it;
+}
+
 NVFP4_DEVINL void fail(const Args &a, uint32_t code)
 {
     atomicExch(a.err, code);
 }
 
-template <int NW, bool ALIGNED>
+// FMT 0: NVFP4 weights; FMT 1: FP6 E2M3 weights (dequantised exactly to
+// e2m3 * 2^(s-127), no tensor scale).
+template <int NW, bool ALIGNED, int FMT = 0>
 __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_constant__ CUtensorMap tmap_x, Args a)
 {
     using C = Cfg<NW>;
+    using Item = typename std::conditional<FMT == 0, DqItem, DqItem6>::type;
     constexpr int S = C::kStages;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -244,12 +269,18 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         const int row = dq & (BM - 1);             // 0..127
         const int half = dq >> 7;                  // which 32 k of the 64-k stage
         const int64_t m = m0 + row;
-        DqItem ring[C::kPf][NW];
+        auto load = [&](int mi, int kb) -> Item {
+            if constexpr (FMT == 0)
+                return dq_load<ALIGNED>(a, mi, m, kb, half);
+            else
+                return dq_load6(a, mi, m, kb, half);
+        };
+        Item ring[C::kPf][NW];
 #pragma unroll
         for (int p = 0; p < C::kPf; ++p)
 #pragma unroll
             for (int mi = 0; mi < NW; ++mi)
-                ring[p][mi] = p < num_kb ? dq_load<ALIGNED>(a, mi, m, p, half) : DqItem{make_uint4(0, 0, 0, 0), 0};
+                ring[p][mi] = load(mi, p < num_kb ? p : num_kb);
         bool ok = true;
         for (int kb0 = 0; kb0 < num_kb && ok; kb0 += C::kPf) {
 #pragma unroll
@@ -257,12 +288,12 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
                 const int kb = kb0 + p;
                 if (kb >= num_kb || !ok)
                     break;
-                DqItem cur[NW];
+                Item cur[NW];
 #pragma unroll
                 for (int mi = 0; mi < NW; ++mi) {
                     cur[mi] = ring[p][mi];
                     if (kb + C::kPf < num_kb)
-                        ring[p][mi] = dq_load<ALIGNED>(a, mi, m, kb + C::kPf, half);
+                        ring[p][mi] = load(mi, kb + C::kPf);
                 }
                 const int s = kb % S;
                 const uint32_t ph = (kb / S) & 1;
@@ -274,14 +305,25 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
 #pragma unroll
                 for (int mi = 0; mi < NW; ++mi) {
                     uint8_t *arow = sa + ((size_t)s * NW + mi) * kABytes + row * 128;
-                    const uint32_t mlo = scale_mult_bf16(cur[mi].scl);
-                    const uint32_t mhi = scale_mult_bf16(cur[mi].scl >> 8);
-                    const uint32_t words[4] = {cur[mi].code.x, cur[mi].code.y, cur[mi].code.z, cur[mi].code.w};
+                    if constexpr (FMT == 0) {
+                        const uint32_t mlo = scale_mult_bf16(cur[mi].scl);
+                        const uint32_t mhi = scale_mult_bf16(cur[mi].scl >> 8);
+                        const uint32_t words[4] = {cur[mi].code.x, cur[mi].code.y, cur[mi].code.z,
+                                                   cur[mi].code.w};
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        const uint4 v = dequant_word_natural(words[q], q < 2 ? mlo : mhi);
-                        const int chunk = half * 4 + q;
-                        *reinterpret_cast<uint4 *>(arow + ((chunk ^ (row & 7)) << 4)) = v;
+                        for (int q = 0; q < 4; ++q) {
+                            const uint4 v = dequant_word_natural(words[q], q < 2 ? mlo : mhi);
+                            const int chunk = half * 4 + q;
+                            *reinterpret_cast<uint4 *>(arow + ((chunk ^ (row & 7)) << 4)) = v;
+                        }
+                    } else {
+                        const Fp6Mult mult = fp6_mult(cur[mi].scl);
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            const uint4 v = fp6_group(cur[mi].code, q, mult);
+                            const int chunk = half * 4 + q;
+                            *reinterpret_cast<uint4 *>(arow + ((chunk ^ (row & 7)) << 4)) = v;
+                        }
                     }
                 }
                 tc::fence_proxy_async_smem();
@@ -301,7 +343,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
             float ts[NW];
 #pragma unroll
             for (int mi = 0; mi < NW; ++mi)
-                ts[mi] = __ldg(a.ts[mi]) * 256.0f;
+                ts[mi] = FMT == 0 ? __ldg(a.ts[mi]) * 256.0f : 1.0f;
 #pragma unroll 1
             for (int cc = 0; cc < 4; ++cc) {
                 const int col = chalf * 128 + cc * 32;
@@ -367,20 +409,20 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
     return fn;
 }
 
-template <int NW, bool ALIGNED>
+template <int NW, bool ALIGNED, int FMT = 0>
 cudaError_t launch_t(const CUtensorMap &map, const Args &a, cudaStream_t stream)
 {
     using C = Cfg<NW>;
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [] {
-        attr_err = cudaFuncSetAttribute(prefill_kernel<NW, ALIGNED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        (int)C::kSmemBytes);
+        attr_err = cudaFuncSetAttribute(prefill_kernel<NW, ALIGNED, FMT>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmemBytes);
     });
     if (attr_err != cudaSuccess)
         return attr_err;
     dim3 grid((unsigned)((int64_t)a.row_tiles * a.token_tiles));
-    prefill_kernel<NW, ALIGNED><<<grid, kThreads, C::kSmemBytes, stream>>>(map, a);
+    prefill_kernel<NW, ALIGNED, FMT><<<grid, kThreads, C::kSmemBytes, stream>>>(map, a);
     return cudaGetLastError();
 }
 
@@ -392,11 +434,10 @@ size_t prefill_workspace_bytes(int64_t N, int64_t M, int64_t K, int n_weights)
     return 256;  // word 0: pipeline-timeout flag
 }
 
-cudaError_t launch_prefill(const uint16_t *x, int64_t N, int64_t M, int64_t K, const uint8_t *const *codes,
-                           const uint8_t *const *scales, const float *const *ts, int n_weights, void *y,
-                           int out_bf16, void *workspace, int num_sms, cudaStream_t stream)
+static cudaError_t prefill_impl(const uint16_t *x, int64_t N, int64_t M, int64_t K, const uint8_t *const *codes,
+                                const uint8_t *const *scales, const float *const *ts, int n_weights, void *y,
+                                int out_bf16, void *workspace, int fmt, cudaStream_t stream)
 {
-    (void)num_sms;
     auto encode = pf::encode_fn();
     if (!encode)
         return cudaErrorNotSupported;
@@ -418,7 +459,7 @@ cudaError_t launch_prefill(const uint16_t *x, int64_t N, int64_t M, int64_t K, c
         const int s = i < n_weights ? i : 0;
         a.codes[i] = codes[s];
         a.scales[i] = scales[s];
-        a.ts[i] = ts[s];
+        a.ts[i] = ts ? ts[s] : nullptr;
     }
     a.y = y;
     a.out_bf16 = out_bf16;
@@ -437,7 +478,7 @@ cudaError_t launch_prefill(const uint16_t *x, int64_t N, int64_t M, int64_t K, c
         // weights fit.
         constexpr double kL2Budget = 110e6;  // of the 129 MB L2
         const double x_bytes = (double)N * (double)K * 2.0;
-        const double w_tile = (double)pf::BM * (double)K * 0.5625 * n_weights;
+        const double w_tile = (double)pf::BM * (double)K * (fmt == 1 ? 0.7578125 : 0.5625) * n_weights;
         int g;
         if (x_bytes <= kL2Budget)
             g = 1;
@@ -447,10 +488,28 @@ cudaError_t launch_prefill(const uint16_t *x, int64_t N, int64_t M, int64_t K, c
             g = (int)(kL2Budget / w_tile);
         a.group = g < 1 ? 1 : (g > (int)row_tiles ? (int)row_tiles : g);
     }
+    if (fmt == 1)
+        return n_weights == 1 ? pf::launch_t<1, true, 1>(map, a, stream) : pf::launch_t<2, true, 1>(map, a, stream);
     const bool aligned = K % 32 == 0;
     if (n_weights == 1)
         return aligned ? pf::launch_t<1, true>(map, a, stream) : pf::launch_t<1, false>(map, a, stream);
     return aligned ? pf::launch_t<2, true>(map, a, stream) : pf::launch_t<2, false>(map, a, stream);
+}
+
+cudaError_t launch_prefill(const uint16_t *x, int64_t N, int64_t M, int64_t K, const uint8_t *const *codes,
+                           const uint8_t *const *scales, const float *const *ts, int n_weights, void *y,
+                           int out_bf16, void *workspace, int num_sms, cudaStream_t stream)
+{
+    (void)num_sms;
+    return prefill_impl(x, N, M, K, codes, scales, ts, n_weights, y, out_bf16, workspace, 0, stream);
+}
+
+cudaError_t launch_prefill_fp6(const uint16_t *x, int64_t N, int64_t M, int64_t K, const uint8_t *const *codes,
+                               const uint8_t *const *scales, int n_weights, void *y, int out_bf16,
+                               void *workspace, int num_sms, cudaStream_t stream)
+{
+    (void)num_sms;
+    return prefill_impl(x, N, M, K, codes, scales, nullptr, n_weights, y, out_bf16, workspace, 1, stream);
 }
 
 }  // namespace nvfp4

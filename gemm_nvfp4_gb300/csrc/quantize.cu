@@ -196,6 +196,124 @@ cudaError_t launch_quantize_bf16(const uint16_t *w, int64_t M, int64_t K, uint8_
 }
 
 // ---------------------------------------------------------------------------
+// FP6 E2M3 quantiser (block-scaled variant, one UE8M0 scale per 128 k).
+//
+//   shared = max(floor(log2(block amax)) - 2, -127)   (-127 for a zero block)
+//   scale byte = shared + 127
+//   code = nearest E2M3 value to w / 2^shared, ties to the even code,
+//          saturating at 7.5, sign kept
+// One warp per 128-element block, four consecutive elements per lane; the
+// codes form a little-endian 6-bit stream per row (4 codes = 3 bytes), which
+// the warp assembles with shuffles into 24 aligned 32-bit stores.  One pass:
+// no tensor-wide amax.  HBM-bound: 4 B (fp32) or 2 B (bf16) read and 0.7578 B
+// written per weight.
+
+// E2M3 code of an fp32 value.  On [0, 2) the grid step is 1/8 and the code
+// magnitude is the step count, on [2, 4) the step is 1/4 (code 8 + 4a), on
+// [4, 7.5] 1/2 (code 16 + 2a); the scalings by 8, 4, 2 are exact, rintf rounds
+// half to even, which on each range is the even code.  7.5 and above -> 31.
+NVFP4_DEVINL uint32_t f32_to_e2m3(float q)
+{
+    const float a = fabsf(q);
+    uint32_t mag;
+    if (a >= 7.5f)
+        mag = 31u;
+    else if (a < 2.0f)
+        mag = (uint32_t)rintf(a * 8.0f);
+    else if (a < 4.0f)
+        mag = (uint32_t)rintf(a * 4.0f) + 8u;
+    else
+        mag = (uint32_t)rintf(a * 2.0f) + 16u;
+    return mag | ((__float_as_uint(q) >> 26) & 0x20u);
+}
+
+template <typename T> struct Src4;  // four consecutive elements of one lane
+template <> struct Src4<float> {
+    static __device__ __forceinline__ void load(const float *w, int64_t i, float v[4])
+    {
+        const float4 a = __ldcs(reinterpret_cast<const float4 *>(w + i));
+        v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+    }
+};
+template <> struct Src4<uint16_t> {
+    static __device__ __forceinline__ void load(const uint16_t *w, int64_t i, float v[4])
+    {
+        const uint2 a = __ldcs(reinterpret_cast<const uint2 *>(w + i));
+        v[0] = __uint_as_float(a.x << 16); v[1] = __uint_as_float(a.x & 0xFFFF0000u);
+        v[2] = __uint_as_float(a.y << 16); v[3] = __uint_as_float(a.y & 0xFFFF0000u);
+    }
+};
+
+template <typename T>
+__global__ void __launch_bounds__(kQuantThreads)
+fp6_quantize_kernel(const T *__restrict__ w, int64_t n_blocks, uint8_t *__restrict__ codes,
+                    uint8_t *__restrict__ scales)
+{
+    const int lane = threadIdx.x & 31;
+    const int64_t warps = (int64_t)gridDim.x * (kQuantThreads / 32);
+    for (int64_t blk = (int64_t)blockIdx.x * (kQuantThreads / 32) + (threadIdx.x >> 5); blk < n_blocks;
+         blk += warps) {
+        float v[4];
+        Src4<T>::load(w, blk * 128 + 4 * lane, v);
+        uint32_t m = 0;
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            m = max(m, __float_as_uint(v[j]) & 0x7FFFFFFFu);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1)
+            m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+        // floor(log2(amax)) from the bit pattern (normal or subnormal amax)
+        int shared = -127;
+        if (m != 0) {
+            const int e = (int)(m >> 23);
+            const int fl = e != 0 ? e - 127 : (31 - __clz((int)m)) - 149;
+            shared = max(fl - 2, -127);
+        }
+        // 2^-shared is a normal fp32 (-shared <= 127), and w * 2^-shared is the
+        // same correctly rounded real number as w / 2^shared.
+        const float inv = __uint_as_float((uint32_t)(127 - shared) << 23);
+        uint32_t packed = 0;
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            packed |= f32_to_e2m3(__fmul_rn(v[j], inv)) << (6 * j);
+        // 24 bits per lane -> word l of the block's 96 bytes holds bytes
+        // 4l .. 4l+3, which start at byte (4l) % 3 of lane (4l) / 3.
+        const int src = min((4 * lane) / 3, 30);
+        const int off = (4 * lane) % 3;
+        const uint32_t va = __shfl_sync(0xFFFFFFFFu, packed, src);
+        const uint32_t vb = __shfl_sync(0xFFFFFFFFu, packed, src + 1);
+        const uint32_t word = (va >> (8 * off)) | (vb << (24 - 8 * off));
+        if (lane < 24)
+            reinterpret_cast<uint32_t *>(codes + blk * 96)[lane] = word;
+        if (lane == 0)
+            scales[blk] = (uint8_t)(shared + 127);
+    }
+}
+
+template <typename T>
+static cudaError_t fp6_quantize_any(const T *w, int64_t M, int64_t K, uint8_t *codes, uint8_t *scales,
+                                    int num_sms, cudaStream_t stream)
+{
+    const int64_t n_blocks = M * (K / 128);
+    const int64_t want = (n_blocks + kQuantThreads / 32 - 1) / (kQuantThreads / 32);
+    const int grid = (int)std::min<int64_t>(std::max<int64_t>(want, 1), (int64_t)num_sms * 16);
+    fp6_quantize_kernel<T><<<grid, kQuantThreads, 0, stream>>>(w, n_blocks, codes, scales);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_fp6_quantize(const float *w, int64_t M, int64_t K, uint8_t *codes, uint8_t *scales,
+                                int num_sms, cudaStream_t stream)
+{
+    return fp6_quantize_any<float>(w, M, K, codes, scales, num_sms, stream);
+}
+
+cudaError_t launch_fp6_quantize_bf16(const uint16_t *w, int64_t M, int64_t K, uint8_t *codes, uint8_t *scales,
+                                     int num_sms, cudaStream_t stream)
+{
+    return fp6_quantize_any<uint16_t>(w, M, K, codes, scales, num_sms, stream);
+}
+
+// ---------------------------------------------------------------------------
 // Import of block scales from the blocked (128 x 4) layout.
 //
 // Blocked layout: 128-row x 4-scale-column blocks, row-major over

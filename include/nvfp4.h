@@ -86,7 +86,9 @@ typedef enum {
     NVFP4_OP_QUANTIZE = 0,
     NVFP4_OP_GEMV_SKINNY = 1,
     NVFP4_OP_GATEUP_SWIGLU = 2,
-    NVFP4_OP_GEMM_PREFILL = 3
+    NVFP4_OP_GEMM_PREFILL = 3,
+    NVFP4_OP_FP6_GEMM = 4,
+    NVFP4_OP_FP6_GATEUP_SWIGLU = 5
 } nvfp4_op;
 
 /* Output element types. */
@@ -211,6 +213,58 @@ int nvfp4_gemm_prefill(const uint16_t *x, int64_t N,
                        const float *tensor_scale, int64_t M, int64_t K,
                        void *y, int out_dtype,
                        void *workspace, size_t workspace_bytes, nvfp4_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * FP6 E2M3 block-scaled weights: the 6-bit weight tier the pages use for
+ * quality (qwentin README, "Highlights" and "How it works": E2M3 weights with
+ * 128-wide block scales on the block-scaled tensor-core MMA).  Same products,
+ * same activations and outputs; only the weight format differs:
+ *   codes   uint8 [M][3K/4]  each row a little-endian stream of 6-bit E2M3
+ *                            codes (element k at bits 6k..6k+5 of the row, so
+ *                            four codes fill three bytes).  E2M3: bit 5 sign,
+ *                            bits 4..3 exponent (bias 1), bits 2..0 mantissa;
+ *                            exponent 0 is subnormal (m/8); largest 7.5.
+ *   scales  uint8 [M][K/128] one UE8M0 scale per 128 consecutive k of a row,
+ *                            value 2^(s - 127).  No tensor scale.
+ * K must be a multiple of 128.  weight = e2m3(code) * 2^(s - 127), exact in
+ * bf16 for every scale byte up to 252 (all the quantiser produces); the
+ * accuracy bound and determinism are those of the NVFP4 calls.
+ * ------------------------------------------------------------------------- */
+
+/* Quantise fp32 (or, _bf16, bf16-bit) weights to FP6 E2M3, block by block
+ * (128 k of a row), in fp32:
+ *   shared = floor(log2(block amax)) - 2, raised to -127 if lower (and -127
+ *            for an all-zero block);  scale byte = shared + 127;
+ *   code   = nearest E2M3 value to w / 2^shared, ties to the even code,
+ *            magnitudes above 7.5 saturating to 7.5, the sign of w kept.
+ * (the microscaling conversion rule of the mxf8f6f4 MMA kind, with 128-wide
+ * blocks).  One pass, no workspace.  w device [M][K] row-major, finite;
+ * codes / scales device outputs as above; all 16-byte aligned.
+ * Returns NVFP4_ERR_UNSUPPORTED_SHAPE for K % 128 != 0. */
+int nvfp4_fp6_quantize(const float *w, int64_t M, int64_t K,
+                       uint8_t *codes, uint8_t *scales, nvfp4_stream_t stream);
+int nvfp4_fp6_quantize_bf16(const uint16_t *w, int64_t M, int64_t K,
+                            uint8_t *codes, uint8_t *scales, nvfp4_stream_t stream);
+
+/* y[N][M] = x[N][K] . dequant(W)^T for FP6 weights, any N >= 1: N <= 16 runs
+ * a skinny kernel that streams every weight byte once for all N tokens, larger
+ * N the tensor-core prefill kernel (the same kernels as the NVFP4 calls, with
+ * the FP6 dequantiser).  x, y, out_dtype as for nvfp4_gemv_skinny; workspace:
+ * nvfp4_workspace_bytes(NVFP4_OP_FP6_GEMM, N, M, K), needing no
+ * initialisation. */
+int nvfp4_fp6_gemm(const uint16_t *x, int64_t N,
+                   const uint8_t *codes, const uint8_t *scales, int64_t M, int64_t K,
+                   void *y, int out_dtype,
+                   void *workspace, size_t workspace_bytes, nvfp4_stream_t stream);
+
+/* Fused gate/up + SwiGLU for FP6 weights, any N >= 1:
+ * h = silu(x . Wg^T) * (x . Wu^T), g and u never written to memory.
+ * workspace: nvfp4_workspace_bytes(NVFP4_OP_FP6_GATEUP_SWIGLU, N, M, K). */
+int nvfp4_fp6_gateup_swiglu(const uint16_t *x, int64_t N,
+                            const uint8_t *gate_codes, const uint8_t *gate_scales,
+                            const uint8_t *up_codes, const uint8_t *up_scales,
+                            int64_t M, int64_t K, void *h, int out_dtype,
+                            void *workspace, size_t workspace_bytes, nvfp4_stream_t stream);
 
 /* Skinny product without a caller workspace, for callers that cannot allocate
  * device memory.  The paper has no counterpart for this call: it is an

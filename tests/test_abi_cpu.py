@@ -144,3 +144,33 @@ def test_blocked_scale_import_arguments(lib):
     assert imp(b=FAKE + 4) == binding.NVFP4_ERR_INVALID_ARG
     assert imp(M=0, b=0, s=0) == binding.NVFP4_OK
     assert imp(K=0, b=0, s=0) == binding.NVFP4_OK
+
+
+def test_fp6_calls_reject_bad_arguments(lib):
+    assert g.nvfp4_workspace_bytes(g.NVFP4_OP_FP6_GEMM, 4, 1024, 1024) > 0
+    assert g.nvfp4_workspace_bytes(g.NVFP4_OP_FP6_GEMM, 4, 1024, 1040) == 0   # K % 128
+    assert g.nvfp4_workspace_bytes(g.NVFP4_OP_FP6_GATEUP_SWIGLU, 600, 1024, 1024) > 0
+    q = lambda **kw: lib.nvfp4_fp6_quantize(_P(kw.get("w", FAKE)), kw.get("M", 64), kw.get("K", 128),
+                                            _P(kw.get("c", FAKE)), _P(kw.get("s", FAKE)), None)
+    assert q(K=144) == binding.NVFP4_ERR_UNSUPPORTED_SHAPE
+    assert q(M=-1) == binding.NVFP4_ERR_INVALID_ARG
+    assert q(w=0) == binding.NVFP4_ERR_INVALID_ARG
+    assert q(c=FAKE + 4) == binding.NVFP4_ERR_INVALID_ARG
+    assert q(M=0, w=0, c=0, s=0) == binding.NVFP4_OK
+    assert lib.nvfp4_fp6_quantize_bf16(_P(FAKE), 64, 96, _P(FAKE), _P(FAKE), None) == \
+        binding.NVFP4_ERR_UNSUPPORTED_SHAPE
+    ws = g.nvfp4_workspace_bytes(g.NVFP4_OP_FP6_GEMM, 4, 64, 128)
+    mm = lambda **kw: lib.nvfp4_fp6_gemm(_P(kw.get("x", FAKE)), kw.get("N", 4), _P(kw.get("c", FAKE)),
+                                         _P(kw.get("s", FAKE)), kw.get("M", 64), kw.get("K", 128),
+                                         _P(kw.get("y", FAKE)), kw.get("dt", 0), _P(kw.get("ws", FAKE)),
+                                         kw.get("wsb", ws), None)
+    assert mm(K=144) == binding.NVFP4_ERR_UNSUPPORTED_SHAPE
+    assert mm(x=0) == binding.NVFP4_ERR_INVALID_ARG
+    assert mm(s=FAKE + 1) == binding.NVFP4_ERR_INVALID_ARG
+    assert mm(dt=5) == binding.NVFP4_ERR_INVALID_ARG
+    assert mm(wsb=ws - 1) == binding.NVFP4_ERR_WORKSPACE
+    assert mm(N=0, x=0, y=0) == binding.NVFP4_OK
+    st = lib.nvfp4_fp6_gateup_swiglu(_P(FAKE), 4, _P(FAKE), _P(FAKE), _P(0), _P(FAKE), 64, 128, _P(FAKE), 0,
+                                     _P(FAKE), g.nvfp4_workspace_bytes(g.NVFP4_OP_FP6_GATEUP_SWIGLU, 4, 64, 128),
+                                     None)
+    assert st == binding.NVFP4_ERR_INVALID_ARG  # null up codes
