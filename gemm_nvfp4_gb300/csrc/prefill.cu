@@ -17,12 +17,19 @@
 //               needs longer to issue an M=128, N=256 MMA than the tensor core
 //               needs to run it).
 //   warps 3..10 dequantise: each thread turns 32 k of one weight row (16 code
-//               bytes, 2 scale bytes, read straight from global memory with a
-//               4-stage register prefetch ring) into exact bf16 values
-//               e2m1 * scale * 2^-8 and stores them in the 128-byte-swizzled
-//               K-major layout the MMA reads; then, after the K loop, they read
-//               the fp32 accumulators out of TMEM (tcgen05.ld) and store
+//               bytes, 2 scale bytes) into exact bf16 values e2m1 * scale * 2^-8
+//               and stores them in the 128-byte-swizzled K-major layout the
+//               MMA reads; then, after the K loop, they read the fp32
+//               accumulators out of TMEM (tcgen05.ld) and store
 //               y = acc * 2^8 * ts, or h = silu(g) * u for the gate/up pair.
+//   warp 11     (K % 256 == 0) streams the weight codes ([128 rows][32 B] per
+//               stage) and scales ([128 rows][16 B] per four stages) into
+//               shared-memory rings by TMA, so the dequantisers read shared
+//               memory.  Per-thread global loads of 16 bytes from 128
+//               different rows kept the load/store unit busy with one
+//               wavefront per row; that, not the tensor pipe, bounded the
+//               kernel.  Other K (and the FP6 format) load codes and scales per
+//               thread from global memory through a 4-stage register ring.
 //
 // Exactness: every product e2m1 * scale * x is exact in the fp32 accumulator
 // (bf16 operands with at most 6 and 8 significant bits).  The accumulation
@@ -36,6 +43,7 @@
 
 #include <algorithm>
 #include <cmath>
+#include <cstring>
 #include <mutex>
 #include <type_traits>
 
@@ -53,17 +61,27 @@ constexpr int kDqWarps = 8;
 constexpr int kIssuers = 2;  // MMA-issuing warps (1 and 2)
 constexpr int kFirstDqWarp = 1 + kIssuers;
 constexpr int kThreads = kFirstDqWarp * 32 + kDqWarps * 32;
+constexpr int kCodeWarp = kFirstDqWarp + kDqWarps;  // code / scale TMA producer (TMA-code mode)
+constexpr int kThreadsTma = kThreads + 32;
+constexpr int kCBytes = BM * BK / 2;     // NVFP4 codes of one stage: 128 rows x 32 bytes
+constexpr int kSBytes = BM * 16;         // scales of four stages: 128 rows x 16 bytes
 constexpr int kABytes = BM * BK * 2;  // 16 KB per weight matrix per stage
 constexpr int kBBytes = BN * BK * 2;  // 32 KB per stage
 constexpr int kDqThreads = kDqWarps * 32;
 
-template <int NW>
+// TMAC: the weight codes and scales reach shared memory by TMA (a code ring
+// of kSc stages and a scale ring of two 4-stage groups) instead of per-thread
+// global loads; needs K % 256 == 0 (16-byte row pitch of the scale rows).
+template <int NW, bool TMAC = false>
 struct Cfg {
     static constexpr int kStages = NW == 1 ? 4 : 3;
     static constexpr int kPf = 4;                         // dequant register prefetch depth (K steps in flight)
+    static constexpr int kSc = NW == 1 ? 6 : 3;           // code ring stages (TMAC)
     static constexpr uint32_t kTmemCols = 512;  // two accumulators of 256 columns
+    static constexpr size_t kRingBytes = TMAC ? (size_t)kSc * NW * kCBytes + 2 * NW * kSBytes : 0;
     static constexpr size_t kSmemBytes =
-        (size_t)kStages * (NW * kABytes + kBBytes) + 1024 /* barriers */ + 1024 /* alignment */;
+        (size_t)kStages * (NW * kABytes + kBBytes) + kRingBytes + 1024 /* barriers */ + 1024 /* alignment */;
+    static_assert(kSmemBytes <= 232448, "shared memory per block");
 };
 
 struct Args {
@@ -160,19 +178,31 @@ NVFP4_DEVINL void fail(const Args &a, uint32_t code)
 
 // FMT 0: NVFP4 weights; FMT 1: FP6 E2M3 weights (dequantised exactly to
 // e2m3 * 2^(s-127), no tensor scale).
-template <int NW, bool ALIGNED, int FMT = 0>
-__global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_constant__ CUtensorMap tmap_x, Args a)
+// Weight tiles by TMA (TMAC) need the code and scale tensor maps; without it
+// they are unused.
+struct WeightMaps {
+    CUtensorMap codes[2];
+    CUtensorMap scales[2];
+};
+
+template <int NW, bool ALIGNED, int FMT = 0, bool TMAC = false>
+__global__ void __launch_bounds__(TMAC ? kThreadsTma : kThreads, 1)
+    prefill_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ WeightMaps wmaps, Args a)
 {
-    using C = Cfg<NW>;
+    using C = Cfg<NW, TMAC>;
     using Item = typename std::conditional<FMT == 0, DqItem, DqItem6>::type;
     constexpr int S = C::kStages;
+    constexpr int SC = C::kSc;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *sa = smem;                                  // [S][NW][kABytes]
     uint8_t *sb = smem + (size_t)S * NW * kABytes;       // [S][kBBytes]
-    uint64_t *bars = reinterpret_cast<uint64_t *>(sb + (size_t)S * kBBytes);
+    uint8_t *sc_ring = sb + (size_t)S * kBBytes;         // [SC][NW][kCBytes]      (TMAC)
+    uint8_t *ss_ring = sc_ring + (size_t)SC * NW * kCBytes;  // [2][NW][kSBytes] (TMAC)
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sb + (size_t)S * kBBytes + C::kRingBytes);
     uint64_t *full_a = bars, *full_b = bars + S, *empty = bars + 2 * S, *tmem_full = bars + 3 * S;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 3 * S + 1);
+    uint64_t *cfull = bars + 3 * S + 1, *cempty = cfull + SC, *sfull = cempty + SC, *sempty = sfull + 2;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sempty + 2);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     // Raster: the grid walks groups of `group` weight row tiles; inside a group
@@ -200,6 +230,16 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
             tc::mbar_init(&empty[s], kIssuers);
         }
         tc::mbar_init(tmem_full, kIssuers);
+        if (TMAC) {
+            for (int c = 0; c < SC; ++c) {
+                tc::mbar_init(&cfull[c], 1);
+                tc::mbar_init(&cempty[c], kDqWarps);
+            }
+            for (int c = 0; c < 2; ++c) {
+                tc::mbar_init(&sfull[c], 1);
+                tc::mbar_init(&sempty[c], kDqWarps);
+            }
+        }
         tc::fence_mbar_init();
         tc::prefetch_tensormap(&tmap_x);
         if (blockIdx.x == 0 && blockIdx.y == 0 && *a.err != 0)
@@ -263,12 +303,97 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
             }
             tc::mma_commit(tmem_full);
         }
+    } else if (TMAC && warp == kCodeWarp) {
+        // ---------------- weight code / scale TMA producer ----------------
+        // Codes: one [128 rows][32 B] box per matrix and stage into a ring of
+        // SC stages.  Scales: one [128 rows][16 B] box per matrix and group of
+        // four stages into a ring of two groups.  Rows past M read as zeros.
+        if (lane == 0) {
+            for (int mi = 0; mi < NW; ++mi) {
+                tc::prefetch_tensormap(&wmaps.codes[mi]);
+                tc::prefetch_tensormap(&wmaps.scales[mi]);
+            }
+            for (int kb = 0; kb < num_kb; ++kb) {
+                if ((kb & 3) == 0) {
+                    const int sg = kb >> 2, ss = sg & 1;
+                    if (!tc::mbar_wait(&sempty[ss], ((uint32_t)(sg >> 1) & 1) ^ 1)) {
+                        fail(a, 6);
+                        break;
+                    }
+                    tc::mbar_arrive_expect_tx(&sfull[ss], NW * kSBytes);
+#pragma unroll
+                    for (int mi = 0; mi < NW; ++mi)
+                        tc::tma_load_2d(ss_ring + ((size_t)ss * NW + mi) * kSBytes, &wmaps.scales[mi], &sfull[ss],
+                                        sg * 16, (int)m0);
+                }
+                const int c = kb % SC;
+                if (!tc::mbar_wait(&cempty[c], ((uint32_t)(kb / SC) & 1) ^ 1)) {
+                    fail(a, 7);
+                    break;
+                }
+                tc::mbar_arrive_expect_tx(&cfull[c], NW * kCBytes);
+#pragma unroll
+                for (int mi = 0; mi < NW; ++mi)
+                    tc::tma_load_2d(sc_ring + ((size_t)c * NW + mi) * kCBytes, &wmaps.codes[mi], &cfull[c],
+                                    kb * (BK / 2), (int)m0);
+            }
+        }
     } else {
         // ---------------- dequantise producers ----------------
         const int dq = threadIdx.x - kFirstDqWarp * 32;  // 0..255
         const int row = dq & (BM - 1);             // 0..127
         const int half = dq >> 7;                  // which 32 k of the 64-k stage
         const int64_t m = m0 + row;
+        bool ok = true;
+        if constexpr (TMAC) {
+            // Codes and scales from the TMA rings; a warp releases a ring slot
+            // once its lanes have turned the slot's bytes into bf16 tiles.
+            for (int kb = 0; kb < num_kb; ++kb) {
+                const int c = kb % SC;
+                const int ss = (kb >> 2) & 1;
+                if (!tc::mbar_wait(&cfull[c], (uint32_t)(kb / SC) & 1) ||
+                    ((kb & 3) == 0 && !tc::mbar_wait(&sfull[ss], (uint32_t)(kb >> 3) & 1))) {
+                    fail(a, 5);
+                    ok = false;
+                    break;
+                }
+                DqItem cur[NW];
+#pragma unroll
+                for (int mi = 0; mi < NW; ++mi) {
+                    cur[mi].code = *reinterpret_cast<const uint4 *>(sc_ring + ((size_t)c * NW + mi) * kCBytes +
+                                                                    row * (BK / 2) + half * 16);
+                    cur[mi].scl = *reinterpret_cast<const uint16_t *>(ss_ring + ((size_t)ss * NW + mi) * kSBytes +
+                                                                      row * 16 + (kb & 3) * 4 + half * 2);
+                }
+                const int s = kb % S;
+                if (!tc::mbar_wait(&empty[s], ((uint32_t)(kb / S) & 1) ^ 1)) {
+                    fail(a, 3);
+                    ok = false;
+                    break;
+                }
+#pragma unroll
+                for (int mi = 0; mi < NW; ++mi) {
+                    uint8_t *arow = sa + ((size_t)s * NW + mi) * kABytes + row * 128;
+                    const uint32_t mlo = scale_mult_bf16(cur[mi].scl);
+                    const uint32_t mhi = scale_mult_bf16(cur[mi].scl >> 8);
+                    const uint32_t words[4] = {cur[mi].code.x, cur[mi].code.y, cur[mi].code.z, cur[mi].code.w};
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const uint4 v = dequant_word_natural(words[q], q < 2 ? mlo : mhi);
+                        const int chunk = half * 4 + q;
+                        *reinterpret_cast<uint4 *>(arow + ((chunk ^ (row & 7)) << 4)) = v;
+                    }
+                }
+                tc::fence_proxy_async_smem();
+                tc::mbar_arrive(&full_a[s]);
+                __syncwarp();
+                if (lane == 0) {
+                    tc::mbar_arrive(&cempty[c]);
+                    if ((kb & 3) == 3)
+                        tc::mbar_arrive(&sempty[ss]);
+                }
+            }
+        }
         auto load = [&](int mi, int kb) -> Item {
             if constexpr (FMT == 0)
                 return dq_load<ALIGNED>(a, mi, m, kb, half);
@@ -276,13 +401,14 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
                 return dq_load6(a, mi, m, kb, half);
         };
         Item ring[C::kPf][NW];
+        if (!TMAC) {
 #pragma unroll
-        for (int p = 0; p < C::kPf; ++p)
+            for (int p = 0; p < C::kPf; ++p)
 #pragma unroll
-            for (int mi = 0; mi < NW; ++mi)
-                ring[p][mi] = load(mi, p < num_kb ? p : num_kb);
-        bool ok = true;
-        for (int kb0 = 0; kb0 < num_kb && ok; kb0 += C::kPf) {
+                for (int mi = 0; mi < NW; ++mi)
+                    ring[p][mi] = load(mi, p < num_kb ? p : num_kb);
+        }
+        for (int kb0 = 0; !TMAC && kb0 < num_kb && ok; kb0 += C::kPf) {
 #pragma unroll
             for (int p = 0; p < C::kPf; ++p) {
                 const int kb = kb0 + p;
@@ -409,21 +535,34 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
     return fn;
 }
 
-template <int NW, bool ALIGNED, int FMT = 0>
-cudaError_t launch_t(const CUtensorMap &map, const Args &a, cudaStream_t stream)
+template <int NW, bool ALIGNED, int FMT = 0, bool TMAC = false>
+cudaError_t launch_t(const CUtensorMap &map, const WeightMaps &wm, const Args &a, cudaStream_t stream)
 {
-    using C = Cfg<NW>;
+    using C = Cfg<NW, TMAC>;
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [] {
-        attr_err = cudaFuncSetAttribute(prefill_kernel<NW, ALIGNED, FMT>,
+        attr_err = cudaFuncSetAttribute(prefill_kernel<NW, ALIGNED, FMT, TMAC>,
                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmemBytes);
     });
     if (attr_err != cudaSuccess)
         return attr_err;
     dim3 grid((unsigned)((int64_t)a.row_tiles * a.token_tiles));
-    prefill_kernel<NW, ALIGNED, FMT><<<grid, kThreads, C::kSmemBytes, stream>>>(map, a);
+    prefill_kernel<NW, ALIGNED, FMT, TMAC><<<grid, TMAC ? kThreadsTma : kThreads, C::kSmemBytes, stream>>>(map, wm, a);
     return cudaGetLastError();
+}
+
+// 2-D uint8 tensor map over rows of `pitch` bytes (box: 128 rows x box_bytes).
+static bool encode_rows(PFN_cuTensorMapEncodeTiled_v12000 encode, CUtensorMap *m, const uint8_t *base,
+                        int64_t pitch, int64_t rows, uint32_t box_bytes)
+{
+    const cuuint64_t dims[2] = {(cuuint64_t)pitch, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)pitch};
+    const cuuint32_t box[2] = {box_bytes, (cuuint32_t)BM};
+    const cuuint32_t estr[2] = {1, 1};
+    return encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t *>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 }  // namespace pf
@@ -488,12 +627,24 @@ static cudaError_t prefill_impl(const uint16_t *x, int64_t N, int64_t M, int64_t
             g = (int)(kL2Budget / w_tile);
         a.group = g < 1 ? 1 : (g > (int)row_tiles ? (int)row_tiles : g);
     }
+    pf::WeightMaps wm;
+    memset(&wm, 0, sizeof(wm));
     if (fmt == 1)
-        return n_weights == 1 ? pf::launch_t<1, true, 1>(map, a, stream) : pf::launch_t<2, true, 1>(map, a, stream);
+        return n_weights == 1 ? pf::launch_t<1, true, 1>(map, wm, a, stream)
+                              : pf::launch_t<2, true, 1>(map, wm, a, stream);
+    if (K % 256 == 0) {
+        // Codes and scales by TMA: row pitches K/2 and K/16 are multiples of 16 bytes.
+        for (int i = 0; i < n_weights; ++i)
+            if (!pf::encode_rows(encode, &wm.codes[i], codes[i], K / 2, M, pf::BK / 2) ||
+                !pf::encode_rows(encode, &wm.scales[i], scales[i], K / 16, M, 16))
+                return cudaErrorInvalidValue;
+        return n_weights == 1 ? pf::launch_t<1, true, 0, true>(map, wm, a, stream)
+                              : pf::launch_t<2, true, 0, true>(map, wm, a, stream);
+    }
     const bool aligned = K % 32 == 0;
     if (n_weights == 1)
-        return aligned ? pf::launch_t<1, true>(map, a, stream) : pf::launch_t<1, false>(map, a, stream);
-    return aligned ? pf::launch_t<2, true>(map, a, stream) : pf::launch_t<2, false>(map, a, stream);
+        return aligned ? pf::launch_t<1, true>(map, wm, a, stream) : pf::launch_t<1, false>(map, wm, a, stream);
+    return aligned ? pf::launch_t<2, true>(map, wm, a, stream) : pf::launch_t<2, false>(map, wm, a, stream);
 }
 
 cudaError_t launch_prefill(const uint16_t *x, int64_t N, int64_t M, int64_t K, const uint8_t *const *codes,
