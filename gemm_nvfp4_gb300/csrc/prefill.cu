@@ -30,6 +30,9 @@
 //               wavefront per row; that, not the tensor pipe, bounded the
 //               kernel.  Other K (and the FP6 format) load codes and scales per
 //               thread from global memory through a 4-stage register ring.
+//               FP6 weights (K % 128 == 0) take their codes ([128 rows][48 B]
+//               per stage) by TMA as well and their scale bytes (one per 128 k)
+//               through a small register ring.
 //
 // Exactness: every product e2m1 * scale * x is exact in the fp32 accumulator
 // (bf16 operands with at most 6 and 8 significant bits).  The accumulation
@@ -63,8 +66,9 @@ constexpr int kFirstDqWarp = 1 + kIssuers;
 constexpr int kThreads = kFirstDqWarp * 32 + kDqWarps * 32;
 constexpr int kCodeWarp = kFirstDqWarp + kDqWarps;  // code / scale TMA producer (TMA-code mode)
 constexpr int kThreadsTma = kThreads + 32;
-constexpr int kCBytes = BM * BK / 2;     // NVFP4 codes of one stage: 128 rows x 32 bytes
-constexpr int kSBytes = BM * 16;         // scales of four stages: 128 rows x 16 bytes
+constexpr int kSBytes = BM * 16;         // NVFP4 scales of four stages: 128 rows x 16 bytes
+// codes of one stage: 128 rows x 32 bytes (NVFP4) or 48 bytes (FP6)
+template <int FMT> constexpr int code_row_bytes() { return FMT == 0 ? BK / 2 : BK / 4 * 3; }
 constexpr int kABytes = BM * BK * 2;  // 16 KB per weight matrix per stage
 constexpr int kBBytes = BN * BK * 2;  // 32 KB per stage
 constexpr int kDqThreads = kDqWarps * 32;
@@ -72,13 +76,15 @@ constexpr int kDqThreads = kDqWarps * 32;
 // TMAC: the weight codes and scales reach shared memory by TMA (a code ring
 // of kSc stages and a scale ring of two 4-stage groups) instead of per-thread
 // global loads; needs K % 256 == 0 (16-byte row pitch of the scale rows).
-template <int NW, bool TMAC = false>
+template <int NW, bool TMAC = false, int FMT = 0>
 struct Cfg {
     static constexpr int kStages = NW == 1 ? 4 : 3;
     static constexpr int kPf = 4;                         // dequant register prefetch depth (K steps in flight)
-    static constexpr int kSc = NW == 1 ? 6 : 3;           // code ring stages (TMAC)
+    static constexpr int kCBytes = BM * code_row_bytes<FMT>();
+    static constexpr int kSc = FMT == 0 ? (NW == 1 ? 6 : 3) : (NW == 1 ? 5 : 2);  // code ring stages (TMAC)
     static constexpr uint32_t kTmemCols = 512;  // two accumulators of 256 columns
-    static constexpr size_t kRingBytes = TMAC ? (size_t)kSc * NW * kCBytes + 2 * NW * kSBytes : 0;
+    static constexpr size_t kRingBytes =
+        TMAC ? (size_t)kSc * NW * kCBytes + (FMT == 0 ? 2 * NW * kSBytes : 0) : 0;
     static constexpr size_t kSmemBytes =
         (size_t)kStages * (NW * kABytes + kBBytes) + kRingBytes + 1024 /* barriers */ + 1024 /* alignment */;
     static_assert(kSmemBytes <= 232448, "shared memory per block");
@@ -189,10 +195,12 @@ template <int NW, bool ALIGNED, int FMT = 0, bool TMAC = false>
 __global__ void __launch_bounds__(TMAC ? kThreadsTma : kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ WeightMaps wmaps, Args a)
 {
-    using C = Cfg<NW, TMAC>;
+    using C = Cfg<NW, TMAC, FMT>;
     using Item = typename std::conditional<FMT == 0, DqItem, DqItem6>::type;
     constexpr int S = C::kStages;
     constexpr int SC = C::kSc;
+    constexpr int kCBytes = C::kCBytes;
+    constexpr int kCRow = code_row_bytes<FMT>();
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *sa = smem;                                  // [S][NW][kABytes]
@@ -311,10 +319,11 @@ __global__ void __launch_bounds__(TMAC ? kThreadsTma : kThreads, 1)
         if (lane == 0) {
             for (int mi = 0; mi < NW; ++mi) {
                 tc::prefetch_tensormap(&wmaps.codes[mi]);
-                tc::prefetch_tensormap(&wmaps.scales[mi]);
+                if (FMT == 0)
+                    tc::prefetch_tensormap(&wmaps.scales[mi]);
             }
             for (int kb = 0; kb < num_kb; ++kb) {
-                if ((kb & 3) == 0) {
+                if (FMT == 0 && (kb & 3) == 0) {
                     const int sg = kb >> 2, ss = sg & 1;
                     if (!tc::mbar_wait(&sempty[ss], ((uint32_t)(sg >> 1) & 1) ^ 1)) {
                         fail(a, 6);
@@ -335,7 +344,7 @@ __global__ void __launch_bounds__(TMAC ? kThreadsTma : kThreads, 1)
 #pragma unroll
                 for (int mi = 0; mi < NW; ++mi)
                     tc::tma_load_2d(sc_ring + ((size_t)c * NW + mi) * kCBytes, &wmaps.codes[mi], &cfull[c],
-                                    kb * (BK / 2), (int)m0);
+                                    kb * kCRow, (int)m0);
             }
         }
     } else {
@@ -345,7 +354,71 @@ __global__ void __launch_bounds__(TMAC ? kThreadsTma : kThreads, 1)
         const int half = dq >> 7;                  // which 32 k of the 64-k stage
         const int64_t m = m0 + row;
         bool ok = true;
-        if constexpr (TMAC) {
+        if constexpr (TMAC && FMT == 1) {
+            // FP6 codes from the TMA ring; the scale byte of a row (one per
+            // 128 k = two stages) through a small register prefetch ring.
+            const int64_t nblk = a.K / 128;
+            auto scale_at = [&](int mi, int64_t blk) -> uint32_t {
+                return (m < a.M && blk < nblk) ? (uint32_t)__ldg(a.scales[mi] + m * nblk + blk) : 127u;
+            };
+            uint32_t sring[4][NW];
+#pragma unroll
+            for (int p = 0; p < 4; ++p)
+#pragma unroll
+                for (int mi = 0; mi < NW; ++mi)
+                    sring[p][mi] = scale_at(mi, p);
+            uint32_t scl[NW];
+            for (int kb = 0; kb < num_kb; ++kb) {
+                if ((kb & 1) == 0) {
+                    const int blk = kb >> 1;
+#pragma unroll
+                    for (int p = 0; p < 4; ++p)
+                        if ((blk & 3) == p) {
+#pragma unroll
+                            for (int mi = 0; mi < NW; ++mi) {
+                                scl[mi] = sring[p][mi];
+                                sring[p][mi] = scale_at(mi, blk + 4);
+                            }
+                        }
+                }
+                const int c = kb % SC;
+                if (!tc::mbar_wait(&cfull[c], (uint32_t)(kb / SC) & 1)) {
+                    fail(a, 5);
+                    ok = false;
+                    break;
+                }
+                uint2 cw[NW][3];
+#pragma unroll
+                for (int mi = 0; mi < NW; ++mi)
+#pragma unroll
+                    for (int i = 0; i < 3; ++i)
+                        cw[mi][i] = *reinterpret_cast<const uint2 *>(sc_ring + ((size_t)c * NW + mi) * kCBytes +
+                                                                     row * kCRow + half * 24 + 8 * i);
+                const int s = kb % S;
+                if (!tc::mbar_wait(&empty[s], ((uint32_t)(kb / S) & 1) ^ 1)) {
+                    fail(a, 3);
+                    ok = false;
+                    break;
+                }
+#pragma unroll
+                for (int mi = 0; mi < NW; ++mi) {
+                    uint8_t *arow = sa + ((size_t)s * NW + mi) * kABytes + row * 128;
+                    const Fp6Mult mult = fp6_mult(scl[mi]);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const uint4 v = fp6_group(cw[mi], q, mult);
+                        const int chunk = half * 4 + q;
+                        *reinterpret_cast<uint4 *>(arow + ((chunk ^ (row & 7)) << 4)) = v;
+                    }
+                }
+                tc::fence_proxy_async_smem();
+                tc::mbar_arrive(&full_a[s]);
+                __syncwarp();
+                if (lane == 0)
+                    tc::mbar_arrive(&cempty[c]);
+            }
+        }
+        if constexpr (TMAC && FMT == 0) {
             // Codes and scales from the TMA rings; a warp releases a ring slot
             // once its lanes have turned the slot's bytes into bf16 tiles.
             for (int kb = 0; kb < num_kb; ++kb) {
@@ -361,7 +434,7 @@ __global__ void __launch_bounds__(TMAC ? kThreadsTma : kThreads, 1)
 #pragma unroll
                 for (int mi = 0; mi < NW; ++mi) {
                     cur[mi].code = *reinterpret_cast<const uint4 *>(sc_ring + ((size_t)c * NW + mi) * kCBytes +
-                                                                    row * (BK / 2) + half * 16);
+                                                                    row * kCRow + half * 16);
                     cur[mi].scl = *reinterpret_cast<const uint16_t *>(ss_ring + ((size_t)ss * NW + mi) * kSBytes +
                                                                       row * 16 + (kb & 3) * 4 + half * 2);
                 }
@@ -538,7 +611,7 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
 template <int NW, bool ALIGNED, int FMT = 0, bool TMAC = false>
 cudaError_t launch_t(const CUtensorMap &map, const WeightMaps &wm, const Args &a, cudaStream_t stream)
 {
-    using C = Cfg<NW, TMAC>;
+    using C = Cfg<NW, TMAC, FMT>;
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [] {
@@ -629,9 +702,14 @@ static cudaError_t prefill_impl(const uint16_t *x, int64_t N, int64_t M, int64_t
     }
     pf::WeightMaps wm;
     memset(&wm, 0, sizeof(wm));
-    if (fmt == 1)
-        return n_weights == 1 ? pf::launch_t<1, true, 1>(map, wm, a, stream)
-                              : pf::launch_t<2, true, 1>(map, wm, a, stream);
+    if (fmt == 1) {
+        // FP6 codes by TMA: row pitch 3K/4 is a multiple of 16 bytes (K % 128 == 0)
+        for (int i = 0; i < n_weights; ++i)
+            if (!pf::encode_rows(encode, &wm.codes[i], codes[i], K / 4 * 3, M, pf::code_row_bytes<1>()))
+                return cudaErrorInvalidValue;
+        return n_weights == 1 ? pf::launch_t<1, true, 1, true>(map, wm, a, stream)
+                              : pf::launch_t<2, true, 1, true>(map, wm, a, stream);
+    }
     if (K % 256 == 0) {
         // Codes and scales by TMA: row pitches K/2 and K/16 are multiples of 16 bytes.
         for (int i = 0; i < n_weights; ++i)
