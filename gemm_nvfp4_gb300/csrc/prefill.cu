@@ -70,14 +70,14 @@ constexpr int kSBytes = BM * 16;         // NVFP4 scales of four stages: 128 row
 // codes of one stage: 128 rows x 32 bytes (NVFP4) or 48 bytes (FP6)
 template <int FMT> constexpr int code_row_bytes() { return FMT == 0 ? BK / 2 : BK / 4 * 3; }
 constexpr int kABytes = BM * BK * 2;  // 16 KB per weight matrix per stage
-constexpr int kBBytes = BN * BK * 2;  // 32 KB per stage
 constexpr int kDqThreads = kDqWarps * 32;
 
 // TMAC: the weight codes and scales reach shared memory by TMA (a code ring
 // of kSc stages and a scale ring of two 4-stage groups) instead of per-thread
 // global loads; needs K % 256 == 0 (16-byte row pitch of the scale rows).
-template <int NW, bool TMAC = false, int FMT = 0>
+template <int NW, bool TMAC = false, int FMT = 0, int TN = BN>
 struct Cfg {
+    static constexpr int kBBytes = TN * BK * 2;           // activation tile of one stage
     static constexpr int kStages = NW == 1 ? 4 : 3;
     static constexpr int kPf = 4;                         // dequant register prefetch depth (K steps in flight)
     static constexpr int kCBytes = BM * code_row_bytes<FMT>();
@@ -191,11 +191,14 @@ struct WeightMaps {
     CUtensorMap scales[2];
 };
 
-template <int NW, bool ALIGNED, int FMT = 0, bool TMAC = false>
+// TN: tokens per tile (MMA N), 256 or 192; the host picks it per call so that
+// the grid fills the SMs' waves (the accumulation order does not depend on it).
+template <int NW, bool ALIGNED, int FMT = 0, bool TMAC = false, int TN = BN>
 __global__ void __launch_bounds__(TMAC ? kThreadsTma : kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ WeightMaps wmaps, Args a)
 {
-    using C = Cfg<NW, TMAC, FMT>;
+    using C = Cfg<NW, TMAC, FMT, TN>;
+    constexpr int kBBytes = C::kBBytes;
     using Item = typename std::conditional<FMT == 0, DqItem, DqItem6>::type;
     constexpr int S = C::kStages;
     constexpr int SC = C::kSc;
@@ -228,7 +231,7 @@ __global__ void __launch_bounds__(TMAC ? kThreadsTma : kThreads, 1)
         token_tile = in / rows;
     }
     const int64_t m0 = row_tile * BM;
-    const int n0 = (int)(token_tile * BN);
+    const int n0 = (int)(token_tile * TN);
     const int num_kb = a.num_kb;
 
     if (threadIdx.x == 0) {
@@ -282,7 +285,7 @@ __global__ void __launch_bounds__(TMAC ? kThreadsTma : kThreads, 1)
         // 2q, 2q+1 of every stage into accumulator q (added in the epilogue).
         if (lane == 0) {
             const int q = warp - 1;
-            constexpr uint32_t idesc = tc::idesc_bf16(BM, BN);
+            constexpr uint32_t idesc = tc::idesc_bf16(BM, TN);
             bool ok = true;
             for (int kb = 0; kb < num_kb && ok; ++kb) {
                 const int s = kb % S;
@@ -298,13 +301,13 @@ __global__ void __launch_bounds__(TMAC ? kThreadsTma : kThreads, 1)
                     const uint64_t adesc = tc::smem_desc_sw128(sa + ((size_t)s * NW + q) * kABytes);
 #pragma unroll
                     for (int k = 0; k < BK / 16; ++k)
-                        tc::mma_bf16_ss(tmem_base + q * BN, adesc + 2 * k, bdesc + 2 * k, idesc,
+                        tc::mma_bf16_ss(tmem_base + q * TN, adesc + 2 * k, bdesc + 2 * k, idesc,
                                         (kb > 0 || k > 0) ? 1u : 0u);
                 } else {
                     const uint64_t adesc = tc::smem_desc_sw128(sa + (size_t)s * kABytes);
 #pragma unroll
                     for (int k = 2 * q; k < 2 * q + 2; ++k)
-                        tc::mma_bf16_ss(tmem_base + q * BN, adesc + 2 * k, bdesc + 2 * k, idesc,
+                        tc::mma_bf16_ss(tmem_base + q * TN, adesc + 2 * k, bdesc + 2 * k, idesc,
                                         (kb > 0 || k > 2 * q) ? 1u : 0u);
                 }
                 tc::mma_commit(&empty[s]);
@@ -537,20 +540,20 @@ __global__ void __launch_bounds__(TMAC ? kThreadsTma : kThreads, 1)
         tc::fence_after_sync();
         if (have) {
             const int quarter = warp & 3;          // TMEM lanes this warp may access
-            const int chalf = (warp - kFirstDqWarp) >> 2;  // which 128 of the 256 token columns
+            const int chalf = (warp - kFirstDqWarp) >> 2;  // which half of the TN token columns
             const int64_t mrow = m0 + quarter * 32 + lane;
             float ts[NW];
 #pragma unroll
             for (int mi = 0; mi < NW; ++mi)
                 ts[mi] = FMT == 0 ? __ldg(a.ts[mi]) * 256.0f : 1.0f;
 #pragma unroll 1
-            for (int cc = 0; cc < 4; ++cc) {
-                const int col = chalf * 128 + cc * 32;
+            for (int cc = 0; cc < TN / 64; ++cc) {
+                const int col = chalf * (TN / 2) + cc * 32;
                 const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + col;
                 // two accumulators: gate and up, or (one matrix) K steps 0-1 and 2-3
                 uint32_t r[2][32];
                 tc::tmem_ld_32x32b_x32(taddr, r[0]);
-                tc::tmem_ld_32x32b_x32(taddr + BN, r[1]);
+                tc::tmem_ld_32x32b_x32(taddr + TN, r[1]);
                 tc::tmem_ld_wait();
                 if (mrow < a.M) {
 #pragma unroll
@@ -608,21 +611,36 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
     return fn;
 }
 
-template <int NW, bool ALIGNED, int FMT = 0, bool TMAC = false>
+template <int NW, bool ALIGNED, int FMT = 0, bool TMAC = false, int TN = BN>
 cudaError_t launch_t(const CUtensorMap &map, const WeightMaps &wm, const Args &a, cudaStream_t stream)
 {
-    using C = Cfg<NW, TMAC, FMT>;
+    using C = Cfg<NW, TMAC, FMT, TN>;
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [] {
-        attr_err = cudaFuncSetAttribute(prefill_kernel<NW, ALIGNED, FMT, TMAC>,
+        attr_err = cudaFuncSetAttribute(prefill_kernel<NW, ALIGNED, FMT, TMAC, TN>,
                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmemBytes);
     });
     if (attr_err != cudaSuccess)
         return attr_err;
     dim3 grid((unsigned)((int64_t)a.row_tiles * a.token_tiles));
-    prefill_kernel<NW, ALIGNED, FMT, TMAC><<<grid, TMAC ? kThreadsTma : kThreads, C::kSmemBytes, stream>>>(map, wm, a);
+    prefill_kernel<NW, ALIGNED, FMT, TMAC, TN>
+        <<<grid, TMAC ? kThreadsTma : kThreads, C::kSmemBytes, stream>>>(map, wm, a);
     return cudaGetLastError();
+}
+
+// Token tile for a TMA-fed launch: 192 instead of 256 when that fills the
+// SMs' waves better.  A CTA's time is modelled as a part that does not scale
+// with the tile (dequantisation, prologue, epilogue: ~1/4) plus the MMA part
+// proportional to TN.
+inline int pick_token_tile(int64_t N, int64_t row_tiles, int num_sms)
+{
+    auto cost = [&](int tn) {
+        const int64_t ctas = row_tiles * ((N + tn - 1) / tn);
+        const int64_t waves = (ctas + num_sms - 1) / num_sms;
+        return (double)waves * (0.25 + tn / 256.0);
+    };
+    return cost(192) < cost(256) ? 192 : 256;
 }
 
 // 2-D uint8 tensor map over rows of `pitch` bytes (box: 128 rows x box_bytes).
@@ -648,18 +666,21 @@ size_t prefill_workspace_bytes(int64_t N, int64_t M, int64_t K, int n_weights)
 
 static cudaError_t prefill_impl(const uint16_t *x, int64_t N, int64_t M, int64_t K, const uint8_t *const *codes,
                                 const uint8_t *const *scales, const float *const *ts, int n_weights, void *y,
-                                int out_bf16, void *workspace, int fmt, cudaStream_t stream)
+                                int out_bf16, void *workspace, int fmt, int num_sms, cudaStream_t stream)
 {
     auto encode = pf::encode_fn();
     if (!encode)
         return cudaErrorNotSupported;
-    const int64_t row_tiles = (M + pf::BM - 1) / pf::BM, token_tiles = (N + pf::BN - 1) / pf::BN;
+    const bool tma_weights = fmt == 1 || K % 256 == 0;
+    const int64_t row_tiles = (M + pf::BM - 1) / pf::BM;
+    const int tn = tma_weights ? pf::pick_token_tile(N, row_tiles, num_sms) : pf::BN;
+    const int64_t token_tiles = (N + tn - 1) / tn;
     if (row_tiles * token_tiles > 0x7FFFFFFF)
         return cudaErrorInvalidValue;
     CUtensorMap map;
     const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)N};
     const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
-    const cuuint32_t box[2] = {pf::BK, pf::BN};
+    const cuuint32_t box[2] = {pf::BK, (cuuint32_t)tn};
     const cuuint32_t estr[2] = {1, 1};
     CUresult r = encode(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t *>(x), dims, strides, box,
                         estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -707,6 +728,9 @@ static cudaError_t prefill_impl(const uint16_t *x, int64_t N, int64_t M, int64_t
         for (int i = 0; i < n_weights; ++i)
             if (!pf::encode_rows(encode, &wm.codes[i], codes[i], K / 4 * 3, M, pf::code_row_bytes<1>()))
                 return cudaErrorInvalidValue;
+        if (tn == 192)
+            return n_weights == 1 ? pf::launch_t<1, true, 1, true, 192>(map, wm, a, stream)
+                                  : pf::launch_t<2, true, 1, true, 192>(map, wm, a, stream);
         return n_weights == 1 ? pf::launch_t<1, true, 1, true>(map, wm, a, stream)
                               : pf::launch_t<2, true, 1, true>(map, wm, a, stream);
     }
@@ -716,6 +740,9 @@ static cudaError_t prefill_impl(const uint16_t *x, int64_t N, int64_t M, int64_t
             if (!pf::encode_rows(encode, &wm.codes[i], codes[i], K / 2, M, pf::BK / 2) ||
                 !pf::encode_rows(encode, &wm.scales[i], scales[i], K / 16, M, 16))
                 return cudaErrorInvalidValue;
+        if (tn == 192)
+            return n_weights == 1 ? pf::launch_t<1, true, 0, true, 192>(map, wm, a, stream)
+                                  : pf::launch_t<2, true, 0, true, 192>(map, wm, a, stream);
         return n_weights == 1 ? pf::launch_t<1, true, 0, true>(map, wm, a, stream)
                               : pf::launch_t<2, true, 0, true>(map, wm, a, stream);
     }
@@ -729,16 +756,14 @@ cudaError_t launch_prefill(const uint16_t *x, int64_t N, int64_t M, int64_t K, c
                            const uint8_t *const *scales, const float *const *ts, int n_weights, void *y,
                            int out_bf16, void *workspace, int num_sms, cudaStream_t stream)
 {
-    (void)num_sms;
-    return prefill_impl(x, N, M, K, codes, scales, ts, n_weights, y, out_bf16, workspace, 0, stream);
+    return prefill_impl(x, N, M, K, codes, scales, ts, n_weights, y, out_bf16, workspace, 0, num_sms, stream);
 }
 
 cudaError_t launch_prefill_fp6(const uint16_t *x, int64_t N, int64_t M, int64_t K, const uint8_t *const *codes,
                                const uint8_t *const *scales, int n_weights, void *y, int out_bf16,
                                void *workspace, int num_sms, cudaStream_t stream)
 {
-    (void)num_sms;
-    return prefill_impl(x, N, M, K, codes, scales, nullptr, n_weights, y, out_bf16, workspace, 1, stream);
+    return prefill_impl(x, N, M, K, codes, scales, nullptr, n_weights, y, out_bf16, workspace, 1, num_sms, stream);
 }
 
 }  // namespace nvfp4

@@ -116,3 +116,25 @@ def test_prefill_down_full_size_sampled(N):
     y_ref, A = oracle.gemv(bf16_bits(x), *ref_w, rows=rows, tokens=toks)
     got = to_np(y)[np.ix_(toks, rows)]
     assert_close(got, y_ref, gemv_tol(y_ref, A, torch.bfloat16), f"down prefill N={N}")
+
+
+@pytest.mark.parametrize("fmt", ["nvfp4", "fp6"])
+def test_token_rows_independent_of_tile_choice(fmt):
+    """The launch picks 192- or 256-token tiles from N and the SM count
+    (N = 600 and N = 4096 over 32 row tiles take different tiles on a 152-SM
+    GPU); a token's row is the same bits either way."""
+    M, K = 4096, 1024
+    w = inputs.weights(M, K, seed=81, device=DEV)
+    x = inputs.activations(4096, K, seed=82, device=DEV)
+    if fmt == "nvfp4":
+        W = g.nvfp4_quantize(w)
+        run = lambda xx: g.nvfp4_gemm_prefill(xx, W)
+    else:
+        W = g.nvfp4_fp6_quantize(w)
+        run = lambda xx: g.nvfp4_fp6_gemm(xx, W)
+    y_all = run(x)
+    y_600 = run(x[:600].contiguous())
+    y_40 = run(x[100:140].contiguous())
+    torch.cuda.synchronize()
+    assert torch.equal(y_600, y_all[:600])
+    assert torch.equal(y_40, y_all[100:140])
