@@ -33,6 +33,12 @@
 //               FP6 weights (K % 128 == 0) take their codes ([128 rows][48 B]
 //               per stage) by TMA as well and their scale bytes (one per 128 k)
 //               through a small register ring.
+//   One matrix with TMA-fed weights: the dequantisers write the A operand to
+//   tensor memory (tcgen05.st, a 4-stage ring beside the accumulator) and
+//   warp 1 alone issues every MMA (kind::f16, A from tensor memory) into one
+//   accumulator; the shared-memory A path's proxy fence per stage cost that
+//   kernel ~12 %.  The gate/up pair keeps A in shared memory: its two
+//   256-column accumulators fill the tensor memory.
 //
 // Exactness: every product e2m1 * scale * x is exact in the fp32 accumulator
 // (bf16 operands with at most 6 and 8 significant bits).  The accumulation
@@ -75,18 +81,27 @@ constexpr int kDqThreads = kDqWarps * 32;
 // TMAC: the weight codes and scales reach shared memory by TMA (a code ring
 // of kSc stages and a scale ring of two 4-stage groups) instead of per-thread
 // global loads; needs K % 256 == 0 (16-byte row pitch of the scale rows).
+// TA (TMA-fed, one matrix): the dequantised A operand goes to tensor memory
+// (tcgen05.st) instead of shared memory, and one thread issues every MMA into
+// a single accumulator: no generic-to-async proxy fence per stage, no A tile
+// in shared memory.  Tensor memory: accumulator in columns [0, TN), A ring of
+// kStages x 32 columns from column kAcol0.
 template <int NW, bool TMAC = false, int FMT = 0, int TN = BN>
 struct Cfg {
+    static constexpr bool kTA = TMAC && NW == 1;
     static constexpr int kBBytes = TN * BK * 2;           // activation tile of one stage
     static constexpr int kStages = NW == 1 ? 4 : 3;
     static constexpr int kPf = 4;                         // dequant register prefetch depth (K steps in flight)
     static constexpr int kCBytes = BM * code_row_bytes<FMT>();
-    static constexpr int kSc = FMT == 0 ? (NW == 1 ? 6 : 3) : (NW == 1 ? 5 : 2);  // code ring stages (TMAC)
-    static constexpr uint32_t kTmemCols = 512;  // two accumulators of 256 columns
+    static constexpr int kSc =
+        kTA ? (FMT == 0 ? 12 : 8) : (FMT == 0 ? (NW == 1 ? 6 : 3) : (NW == 1 ? 5 : 2));  // code ring (TMAC)
+    static constexpr int kAcol0 = 256;
+    static constexpr uint32_t kTmemCols = 512;  // two accumulators of 256 columns, or one + the A ring
+    static constexpr int kIssue = kTA ? 1 : kIssuers;     // threads issuing MMAs
     static constexpr size_t kRingBytes =
         TMAC ? (size_t)kSc * NW * kCBytes + (FMT == 0 ? 2 * NW * kSBytes : 0) : 0;
-    static constexpr size_t kSmemBytes =
-        (size_t)kStages * (NW * kABytes + kBBytes) + kRingBytes + 1024 /* barriers */ + 1024 /* alignment */;
+    static constexpr size_t kSmemBytes = (size_t)kStages * ((kTA ? 0 : NW * kABytes) + kBBytes) + kRingBytes +
+                                         1024 /* barriers */ + 1024 /* alignment */;
     static_assert(kSmemBytes <= 232448, "shared memory per block");
 };
 
@@ -206,8 +221,9 @@ __global__ void __launch_bounds__(TMAC ? kThreadsTma : kThreads, 1)
     constexpr int kCRow = code_row_bytes<FMT>();
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t *sa = smem;                                  // [S][NW][kABytes]
-    uint8_t *sb = smem + (size_t)S * NW * kABytes;       // [S][kBBytes]
+    constexpr bool TA = C::kTA;
+    uint8_t *sa = smem;                                  // [S][NW][kABytes] (not TA)
+    uint8_t *sb = smem + (TA ? 0 : (size_t)S * NW * kABytes);  // [S][kBBytes]
     uint8_t *sc_ring = sb + (size_t)S * kBBytes;         // [SC][NW][kCBytes]      (TMAC)
     uint8_t *ss_ring = sc_ring + (size_t)SC * NW * kCBytes;  // [2][NW][kSBytes] (TMAC)
     uint64_t *bars = reinterpret_cast<uint64_t *>(sb + (size_t)S * kBBytes + C::kRingBytes);
@@ -236,11 +252,11 @@ __global__ void __launch_bounds__(TMAC ? kThreadsTma : kThreads, 1)
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
-            tc::mbar_init(&full_a[s], kDqThreads);
+            tc::mbar_init(&full_a[s], TA ? kDqWarps : kDqThreads);
             tc::mbar_init(&full_b[s], 1);
-            tc::mbar_init(&empty[s], kIssuers);
+            tc::mbar_init(&empty[s], C::kIssue);
         }
-        tc::mbar_init(tmem_full, kIssuers);
+        tc::mbar_init(tmem_full, C::kIssue);
         if (TMAC) {
             for (int c = 0; c < SC; ++c) {
                 tc::mbar_init(&cfull[c], 1);
@@ -283,7 +299,26 @@ __global__ void __launch_bounds__(TMAC ? kThreadsTma : kThreads, 1)
         // core takes to run it, so two threads issue: for the gate/up pair
         // issuer q owns matrix q; for one matrix issuer q takes the K steps
         // 2q, 2q+1 of every stage into accumulator q (added in the epilogue).
-        if (lane == 0) {
+        if (TA && lane == 0 && warp == 1) {
+            // one issuer, one accumulator, A from tensor memory
+            constexpr uint32_t idesc = tc::idesc_bf16(BM, TN);
+            for (int kb = 0; kb < num_kb; ++kb) {
+                const int s = kb % S;
+                const uint32_t ph = (kb / S) & 1;
+                if (!tc::mbar_wait(&full_a[s], ph) || !tc::mbar_wait(&full_b[s], ph)) {
+                    fail(a, 2);
+                    break;
+                }
+                tc::fence_after_sync();
+                const uint64_t bdesc = tc::smem_desc_sw128(sb + (size_t)s * kBBytes);
+                const uint32_t acol = tmem_base + C::kAcol0 + s * (BK / 2);
+#pragma unroll
+                for (int k = 0; k < BK / 16; ++k)
+                    tc::mma_f16_ts(tmem_base, acol + 8 * k, bdesc + 2 * k, idesc, (kb > 0 || k > 0) ? 1u : 0u);
+                tc::mma_commit(&empty[s]);
+            }
+            tc::mma_commit(tmem_full);
+        } else if (!TA && lane == 0) {
             const int q = warp - 1;
             constexpr uint32_t idesc = tc::idesc_bf16(BM, TN);
             bool ok = true;
@@ -353,10 +388,34 @@ __global__ void __launch_bounds__(TMAC ? kThreadsTma : kThreads, 1)
     } else {
         // ---------------- dequantise producers ----------------
         const int dq = threadIdx.x - kFirstDqWarp * 32;  // 0..255
-        const int row = dq & (BM - 1);             // 0..127
+        // TA: a warp may write only its own quarter of the tensor-memory lanes
+        const int row = TA ? 32 * (warp & 3) + lane : (dq & (BM - 1));  // 0..127
         const int half = dq >> 7;                  // which 32 k of the 64-k stage
         const int64_t m = m0 + row;
         bool ok = true;
+        // TA: the dequantised 32 k of this row (four 8-k chunks, 16 columns)
+        // for stage s go to tensor memory.
+        auto put_a_tmem = [&](int s, const uint4 (&v)[4]) {
+            const uint32_t w[16] = {v[0].x, v[0].y, v[0].z, v[0].w, v[1].x, v[1].y, v[1].z, v[1].w,
+                                    v[2].x, v[2].y, v[2].z, v[2].w, v[3].x, v[3].y, v[3].z, v[3].w};
+            tc::tmem_st_32x32b_x16(tmem_base + ((uint32_t)(32 * (warp & 3)) << 16) + C::kAcol0 + s * (BK / 2) +
+                                       half * 16,
+                                   w);
+        };
+        // Hand stage s to the MMA: proxy fence for shared memory, or the
+        // tensor-memory store wait.
+        auto publish_a = [&](int s) {
+            if constexpr (TA) {
+                tc::tmem_st_wait();
+                tc::fence_before_sync();
+                __syncwarp();
+                if (lane == 0)
+                    tc::mbar_arrive(&full_a[s]);
+            } else {
+                tc::fence_proxy_async_smem();
+                tc::mbar_arrive(&full_a[s]);
+            }
+        };
         if constexpr (TMAC && FMT == 1) {
             // FP6 codes from the TMA ring; the scale byte of a row (one per
             // 128 k = two stages) through a small register prefetch ring.
@@ -403,19 +462,28 @@ __global__ void __launch_bounds__(TMAC ? kThreadsTma : kThreads, 1)
                     ok = false;
                     break;
                 }
+                if (TA)
+                    tc::fence_after_sync();  // the MMAs that read this A stage are complete
 #pragma unroll
                 for (int mi = 0; mi < NW; ++mi) {
-                    uint8_t *arow = sa + ((size_t)s * NW + mi) * kABytes + row * 128;
                     const Fp6Mult mult = fp6_mult(scl[mi]);
+                    if constexpr (TA) {
+                        uint4 v[4];
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        const uint4 v = fp6_group(cw[mi], q, mult);
-                        const int chunk = half * 4 + q;
-                        *reinterpret_cast<uint4 *>(arow + ((chunk ^ (row & 7)) << 4)) = v;
+                        for (int q = 0; q < 4; ++q)
+                            v[q] = fp6_group(cw[mi], q, mult);
+                        put_a_tmem(s, v);
+                    } else {
+                        uint8_t *arow = sa + ((size_t)s * NW + mi) * kABytes + row * 128;
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            const uint4 v = fp6_group(cw[mi], q, mult);
+                            const int chunk = half * 4 + q;
+                            *reinterpret_cast<uint4 *>(arow + ((chunk ^ (row & 7)) << 4)) = v;
+                        }
                     }
                 }
-                tc::fence_proxy_async_smem();
-                tc::mbar_arrive(&full_a[s]);
+                publish_a(s);
                 __syncwarp();
                 if (lane == 0)
                     tc::mbar_arrive(&cempty[c]);
@@ -447,21 +515,30 @@ __global__ void __launch_bounds__(TMAC ? kThreadsTma : kThreads, 1)
                     ok = false;
                     break;
                 }
+                if (TA)
+                    tc::fence_after_sync();  // the MMAs that read this A stage are complete
 #pragma unroll
                 for (int mi = 0; mi < NW; ++mi) {
-                    uint8_t *arow = sa + ((size_t)s * NW + mi) * kABytes + row * 128;
                     const uint32_t mlo = scale_mult_bf16(cur[mi].scl);
                     const uint32_t mhi = scale_mult_bf16(cur[mi].scl >> 8);
                     const uint32_t words[4] = {cur[mi].code.x, cur[mi].code.y, cur[mi].code.z, cur[mi].code.w};
+                    if constexpr (TA) {
+                        uint4 v[4];
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        const uint4 v = dequant_word_natural(words[q], q < 2 ? mlo : mhi);
-                        const int chunk = half * 4 + q;
-                        *reinterpret_cast<uint4 *>(arow + ((chunk ^ (row & 7)) << 4)) = v;
+                        for (int q = 0; q < 4; ++q)
+                            v[q] = dequant_word_natural(words[q], q < 2 ? mlo : mhi);
+                        put_a_tmem(s, v);
+                    } else {
+                        uint8_t *arow = sa + ((size_t)s * NW + mi) * kABytes + row * 128;
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            const uint4 v = dequant_word_natural(words[q], q < 2 ? mlo : mhi);
+                            const int chunk = half * 4 + q;
+                            *reinterpret_cast<uint4 *>(arow + ((chunk ^ (row & 7)) << 4)) = v;
+                        }
                     }
                 }
-                tc::fence_proxy_async_smem();
-                tc::mbar_arrive(&full_a[s]);
+                publish_a(s);
                 __syncwarp();
                 if (lane == 0) {
                     tc::mbar_arrive(&cempty[c]);
@@ -546,14 +623,17 @@ __global__ void __launch_bounds__(TMAC ? kThreadsTma : kThreads, 1)
 #pragma unroll
             for (int mi = 0; mi < NW; ++mi)
                 ts[mi] = FMT == 0 ? __ldg(a.ts[mi]) * 256.0f : 1.0f;
+            // TA: only column chunks holding at least one real token
+            // (warp-uniform; a runtime bound also keeps this loop rolled)
 #pragma unroll 1
-            for (int cc = 0; cc < TN / 64; ++cc) {
+            for (int cc = 0; cc < TN / 64 && (!TA || n0 + chalf * (TN / 2) + cc * 32 < a.N); ++cc) {
                 const int col = chalf * (TN / 2) + cc * 32;
                 const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + col;
                 // two accumulators: gate and up, or (one matrix) K steps 0-1 and 2-3
                 uint32_t r[2][32];
                 tc::tmem_ld_32x32b_x32(taddr, r[0]);
-                tc::tmem_ld_32x32b_x32(taddr + TN, r[1]);
+                if (!TA)
+                    tc::tmem_ld_32x32b_x32(taddr + TN, r[1]);
                 tc::tmem_ld_wait();
                 if (mrow < a.M) {
 #pragma unroll
@@ -561,7 +641,9 @@ __global__ void __launch_bounds__(TMAC ? kThreadsTma : kThreads, 1)
                         const int64_t n = (int64_t)n0 + col + j;
                         if (n < a.N) {
                             float v;
-                            if (NW == 1) {
+                            if (TA) {
+                                v = __uint_as_float(r[0][j]) * ts[0];
+                            } else if (NW == 1) {
                                 v = (__uint_as_float(r[0][j]) + __uint_as_float(r[1][j])) * ts[0];
                             } else {
                                 const float gg = __uint_as_float(r[0][j]) * ts[0];
