@@ -52,10 +52,14 @@
  *     failed launch returns NVFP4_ERR_CUDA.  The library never aborts or prints.
  *   - Determinism: the reduction order is fixed by the shapes alone, so repeated
  *     calls give bit-identical results, and row n of an N-token call equals the
- *     same token in any other call with the same weights, M and K (floating-
- *     point summation order is part of the contract: bw24 wiki Home, list of
- *     checks every kernel change must pass, and bw24 README, where decode and
- *     verify launch the same kernel symbols and agree bit for bit).
+ *     same token in any other call with the same weights, M and K on the same
+ *     side of N = 16 (floating-point summation order is part of the contract:
+ *     bw24 wiki Home, list of checks every kernel change must pass, and bw24
+ *     README, where decode and verify launch the same kernel symbols and agree
+ *     bit for bit).  Across N = 16 (skinny vs tensor-core prefill kernel) the
+ *     rows agree within the accuracy bound below.  A skinny call in which
+ *     some token's activations do not fit an f16 window of 2^30 switches the
+ *     whole call to bf16 operands; its rows also agree within the bound.
  *   - Accuracy: every product code * scale * x is exact (bf16 operands, fp32
  *     accumulation); results satisfy |y - y_ref| <= 1e-5 * sum_k |w*x| + 1e-7
  *     against an fp64 evaluation of the formula above.
