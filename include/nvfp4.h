@@ -58,8 +58,9 @@
  *     README, where decode and verify launch the same kernel symbols and agree
  *     bit for bit).  Across N = 16 (skinny vs tensor-core prefill kernel) the
  *     rows agree within the accuracy bound below.  A skinny call in which
- *     some token's activations do not fit an f16 window of 2^30 switches the
- *     whole call to bf16 operands; its rows also agree within the bound.
+ *     some token's activations are not all exact in f16 after scaling by a
+ *     power of two (a dynamic range wider than f16's) switches the whole call
+ *     to bf16 operands; its rows also agree within the bound.
  *   - Accuracy: every product code * scale * x is exact (bf16 operands, fp32
  *     accumulation); results satisfy |y - y_ref| <= 1e-5 * sum_k |w*x| + 1e-7
  *     against an fp64 evaluation of the formula above.
