@@ -76,7 +76,6 @@ constexpr int kSBytes = BM * 16;         // NVFP4 scales of four stages: 128 row
 // codes of one stage: 128 rows x 32 bytes (NVFP4) or 48 bytes (FP6)
 template <int FMT> constexpr int code_row_bytes() { return FMT == 0 ? BK / 2 : BK / 4 * 3; }
 constexpr int kABytes = BM * BK * 2;  // 16 KB per weight matrix per stage
-constexpr int kDqThreads = kDqWarps * 32;
 
 // TMAC: the weight codes and scales reach shared memory by TMA (a code ring
 // of kSc stages and a scale ring of two 4-stage groups) instead of per-thread
@@ -252,7 +251,7 @@ __global__ void __launch_bounds__(TMAC ? kThreadsTma : kThreads, 1)
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
-            tc::mbar_init(&full_a[s], TA ? kDqWarps : kDqThreads);
+            tc::mbar_init(&full_a[s], kDqWarps);
             tc::mbar_init(&full_b[s], 1);
             tc::mbar_init(&empty[s], C::kIssue);
         }
@@ -412,8 +411,12 @@ __global__ void __launch_bounds__(TMAC ? kThreadsTma : kThreads, 1)
                 if (lane == 0)
                     tc::mbar_arrive(&full_a[s]);
             } else {
+                // every thread orders its own shared-memory writes before the
+                // async proxy; the warp then arrives once
                 tc::fence_proxy_async_smem();
-                tc::mbar_arrive(&full_a[s]);
+                __syncwarp();
+                if (lane == 0)
+                    tc::mbar_arrive(&full_a[s]);
             }
         };
         if constexpr (TMAC && FMT == 1) {
@@ -605,8 +608,7 @@ __global__ void __launch_bounds__(TMAC ? kThreadsTma : kThreads, 1)
                         }
                     }
                 }
-                tc::fence_proxy_async_smem();
-                tc::mbar_arrive(&full_a[s]);
+                publish_a(s);
             }
         }
 
