@@ -213,3 +213,26 @@ def test_workspace_left_zero_across_paths():
         ref = call(None)  # fresh zero-filled workspace from the binding
         torch.cuda.synchronize()
         assert torch.equal(got, ref), f"case {i}"
+
+
+def test_workspace_shared_with_fp6_and_prefill_calls():
+    """FP6 skinny calls (split-K partials in the same region, zeroed after
+    use) and prefill calls (word 0 only) on a workspace shared with NVFP4
+    skinny calls leave the counter region zero, and the NVFP4 results stay
+    those of a fresh workspace."""
+    M, K = 5120, 4096
+    need = max(g.nvfp4_workspace_bytes(g.NVFP4_OP_GEMV_SKINNY, 16, M, K),
+               g.nvfp4_workspace_bytes(g.NVFP4_OP_FP6_GATEUP_SWIGLU, 16, M, K),
+               g.nvfp4_workspace_bytes(g.NVFP4_OP_GEMM_PREFILL, 300, M, K))
+    ws = torch.zeros(need, dtype=torch.uint8, device=DEV)
+    w = inputs.weights(M, K, seed=91).to(DEV)
+    W, W6 = g.nvfp4_quantize(w), g.nvfp4_fp6_quantize(w)
+    x = inputs.activations(300, K, seed=92).to(DEV)
+    for step in range(3):
+        g.nvfp4_fp6_gemm(x[:9].contiguous(), W6, workspace=ws)
+        g.nvfp4_fp6_gateup_swiglu(x[:3].contiguous(), W6, W6, workspace=ws)
+        g.nvfp4_gemm_prefill(x, W, workspace=ws)
+        y = g.nvfp4_gemv_skinny(x[:5].contiguous(), W, workspace=ws)
+        torch.cuda.synchronize()
+        assert int(torch.count_nonzero(ws[256:256 + (1 << 20)]).item()) == 0, step
+        assert torch.equal(y, g.nvfp4_gemv_skinny(x[:5].contiguous(), W))
