@@ -86,13 +86,19 @@ constexpr int kScaleBox = BM * 16;   // 2 KB: 128 rows x 16 scale bytes (256 k),
 constexpr int kXUnit = NTOK * BKU * 2;  // 8 KB: activation image of one unit
 constexpr uint32_t kTmemCols = 512;
 
-template <int NW>
+// FP6 E2M3 weights (FMT 1): a unit's 192 code bytes per row arrive as three
+// [128 rows][64 B] boxes with the 64-byte swizzle; the scale bytes (one per
+// 128 k) are read by the dequantisers from global memory ahead of use.
+constexpr int kCodeBox6 = BM * 64;    // 8 KB
+
+template <int NW, int FMT = 0>
 struct Cfg {
     // The weight ring holds most of the shared memory: with ~4 us of loaded
     // DRAM latency, every SM needs well over 100 KB of weights in flight.
-    // A stage holds one unit: NW code boxes, then NW scale boxes.
-    static constexpr int kStageBytes = NW * (kCodeBox + kScaleBox);
-    static constexpr int kCStages = NW == 1 ? 10 : 5;  // weight ring (units)
+    // A stage holds one unit: NW code boxes, then NW scale boxes (NVFP4), or
+    // NW x 3 FP6 code boxes.
+    static constexpr int kStageBytes = FMT == 0 ? NW * (kCodeBox + kScaleBox) : NW * 3 * kCodeBox6;
+    static constexpr int kCStages = FMT == 0 ? (NW == 1 ? 10 : 5) : (NW == 1 ? 7 : 3);  // weight ring (units)
     static constexpr int kXStages = NW == 1 ? 4 : 3;   // activation ring (units, from L2)
     // Work item of one dequantiser group = one TMEM A stage of 64 columns
     // (128 weights per row):
@@ -142,6 +148,7 @@ struct Args {
     int bf16_only;  // 1: no prep kernel; bf16 operands read from x itself
     int cs;         // > 1: cluster-K (clusters of cs CTAs split every tile's K); 1: stream-K
     int ncl;        // cluster-K: number of clusters
+    const uint8_t *scales6[2];  // FP6: UE8M0 scales [M][K/128] (read by the dequantisers)
 };
 
 // Workspace layout (bytes): header 256 (factor[16], flags[16], err), per-tile
@@ -703,13 +710,13 @@ NVFP4_DEVINL void mma_issuer(const Args &a, const IssuerArgs &p, int q)
     }
 }
 
-template <int NW>
+template <int NW, int FMT = 0>
 __global__ void __launch_bounds__(kThreads, 1)
 skinny_tc_kernel(const __grid_constant__ CUtensorMap m_codes0, const __grid_constant__ CUtensorMap m_codes1,
                  const __grid_constant__ CUtensorMap m_scales0, const __grid_constant__ CUtensorMap m_scales1,
                  const __grid_constant__ CUtensorMap m_x, Args a)
 {
-    using C = Cfg<NW>;
+    using C = Cfg<NW, FMT>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *c_ring = smem;                                          // [kCStages][NW codes, NW scales]
@@ -759,10 +766,12 @@ skinny_tc_kernel(const __grid_constant__ CUtensorMap m_codes0, const __grid_cons
         tc::mbar_init(ck_free, 1);
         tc::fence_mbar_init();
         tc::prefetch_tensormap(&m_codes0);
-        tc::prefetch_tensormap(&m_scales0);
+        if (FMT == 0)
+            tc::prefetch_tensormap(&m_scales0);
         if (NW == 2) {
             tc::prefetch_tensormap(&m_codes1);
-            tc::prefetch_tensormap(&m_scales1);
+            if (FMT == 0)
+                tc::prefetch_tensormap(&m_scales1);
         }
     }
     if (warp == 0)
@@ -805,10 +814,17 @@ skinny_tc_kernel(const __grid_constant__ CUtensorMap m_codes0, const __grid_cons
                 tc::mbar_arrive_expect_tx(&c_full[s], C::kStageBytes);
 #pragma unroll
                 for (int mi = 0; mi < NW; ++mi) {
-                    tc::tma_load_2d(st + mi * kCodeBox, mi == 0 ? &m_codes0 : &m_codes1, &c_full[s], j * (BKU / 2),
-                                    (int)(tile * BM));
-                    tc::tma_load_2d(st + NW * kCodeBox + mi * kScaleBox, mi == 0 ? &m_scales0 : &m_scales1,
-                                    &c_full[s], j * (BKU / 16), (int)(tile * BM));
+                    if (FMT == 0) {
+                        tc::tma_load_2d(st + mi * kCodeBox, mi == 0 ? &m_codes0 : &m_codes1, &c_full[s],
+                                        j * (BKU / 2), (int)(tile * BM));
+                        tc::tma_load_2d(st + NW * kCodeBox + mi * kScaleBox, mi == 0 ? &m_scales0 : &m_scales1,
+                                        &c_full[s], j * (BKU / 16), (int)(tile * BM));
+                    } else {
+#pragma unroll
+                        for (int bx = 0; bx < 3; ++bx)
+                            tc::tma_load_2d(st + (mi * 3 + bx) * kCodeBox6, mi == 0 ? &m_codes0 : &m_codes1,
+                                            &c_full[s], j * (BKU / 4 * 3) + bx * 64, (int)(tile * BM));
+                    }
                 }
                 j += 2;
                 while (j >= rg.je) {
@@ -876,8 +892,12 @@ skinny_tc_kernel(const __grid_constant__ CUtensorMap m_codes0, const __grid_cons
         const int et = threadIdx.x - kEpiWarp0 * 32;  // 0..127
         if (et < NW * NTOK) {
             const int mi = et / NTOK, n = et % NTOK;
-            const float t = __ldg(a.ts[mi]);
-            fac_s[et] = mode ? t * 256.0f : t * a.factor[n];
+            if (FMT == 1) {
+                fac_s[et] = 1.0f;  // FP6: the dequantised weights carry their scale exactly
+            } else {
+                const float t = __ldg(a.ts[mi]);
+                fac_s[et] = mode ? t * 256.0f : t * a.factor[n];
+            }
         }
         if (et == 0)
             seg_s->reduce = 0;
@@ -972,17 +992,56 @@ skinny_tc_kernel(const __grid_constant__ CUtensorMap m_codes0, const __grid_cons
         // A ring (both below the ring sizes here, so phase 0).
         int sc = i, sa = i * C::kItems + h;
         uint32_t phc = 0, pha = 0;
-        for (; i < n_units; i += C::kUnitStep) {
+        // FP6: this thread's scale byte of each item (one per 128 k of its row)
+        // comes from global memory, loaded kSPf items of the group ahead.
+        constexpr int kSPf = 3;
+        constexpr int kCh6 = BKU / C::kItems * 3 / 4 / 16;  // 16-byte FP6 code chunks per matrix and item
+        auto scale6 = [&](int iu, int mi) -> uint32_t {
+            if (FMT != 1 || iu >= n_units)
+                return 127u;
+            const uint32_t span = (uint32_t)(rg.je - rg.jb);
+            const uint32_t L = (uint32_t)(rg.j_first - rg.jb) + (uint32_t)iu;
+            const int64_t m = (rg.tile0 + (int64_t)(L / span) * rg.tstep) * BM + r;
+            const int blk = 2 * (rg.jb + (int)(L % span)) + (NW == 1 ? h : (h >> 1));
+            return m < a.M ? (uint32_t)__ldg(a.scales6[mi] + m * (a.K / 128) + blk) : 127u;
+        };
+        uint32_t s6ring[kSPf][NW], scl6[NW];
+        if (FMT == 1) {
+#pragma unroll
+            for (int p = 0; p < kSPf; ++p)
+#pragma unroll
+                for (int mi = 0; mi < NW; ++mi)
+                    s6ring[p][mi] = scale6(i + p * C::kUnitStep, mi);
+        }
+        for (int it = 0; i < n_units; i += C::kUnitStep, ++it) {
             if (!tc::mbar_wait(&c_full[sc], phc)) {
                 fail(a, 16);
                 break;
             }
             // copy this thread's codes and scale bytes to registers, release the stage
             const uint8_t *stage = c_ring + (size_t)sc * C::kStageBytes;
-            uint4 cw[NW][kCh];
+            uint4 cw[NW][FMT == 0 ? kCh : kCh6];
             uint32_t scw[NW][kCh / 2];
+            if (FMT == 1) {
 #pragma unroll
-            for (int mi = 0; mi < NW; ++mi) {
+                for (int mi = 0; mi < NW; ++mi) {
+#pragma unroll
+                    for (int c = 0; c < kCh6; ++c) {
+                        // byte b of the unit row: box b / 64, 16-byte chunk (b / 16) % 4, 64-byte swizzle
+                        const int b6 = h * kCh6 * 16 + 16 * c;
+                        cw[mi][c] = *reinterpret_cast<const uint4 *>(
+                            stage + (mi * 3 + (b6 >> 6)) * kCodeBox6 + r * 64 + ((((b6 >> 4) & 3) ^ ((r >> 1) & 3)) << 4));
+                    }
+#pragma unroll
+                    for (int p = 0; p < kSPf; ++p)
+                        if (it % kSPf == p) {
+                            scl6[mi] = s6ring[p][mi];
+                            s6ring[p][mi] = scale6(i + kSPf * C::kUnitStep, mi);
+                        }
+                }
+            }
+#pragma unroll
+            for (int mi = 0; mi < NW && FMT == 0; ++mi) {
                 const uint8_t *crow = stage + mi * kCodeBox + r * 128;
 #pragma unroll
                 for (int c = 0; c < kCh; ++c)
@@ -1016,12 +1075,39 @@ skinny_tc_kernel(const __grid_constant__ CUtensorMap m_codes0, const __grid_cons
 #pragma unroll
             for (int q = 0; q < 2; ++q) {  // NW = 1: chunks 2q, 2q+1; NW = 2: matrix q
                 const int mi = NW == 1 ? 0 : q;
-                const int c0 = NW == 1 ? 2 * q : 0;
-                const uint32_t sw = scw[mi][NW == 1 ? q : 0];
-                uint32_t out[32];
-                dequant_chunk(cw[mi][c0], sw & 0xFFFF, mode, out);
-                dequant_chunk(cw[mi][c0 + 1], sw >> 16, mode, out + 16);
-                tc::tmem_st_32x32b_x32(acol + q * 32, out);
+                if constexpr (FMT == 1) {
+                    // 64 k = eight 8-code groups of 6 bytes, from this item's code words
+                    const Fp6Mult mult = fp6_mult(scl6[mi]);
+                    auto w = [&](int k) -> uint32_t {  // code word k of the item (constant after unrolling)
+                        const uint4 &v = cw[mi][k >> 2];
+                        return (k & 3) == 0 ? v.x : (k & 3) == 1 ? v.y : (k & 3) == 2 ? v.z : v.w;
+                    };
+#pragma unroll
+                    for (int hh = 0; hh < 2; ++hh) {
+                        uint32_t out[16];
+#pragma unroll
+                        for (int gg = 0; gg < 4; ++gg) {
+                            const int gi = (NW == 1 ? 8 * q : 0) + 4 * hh + gg;  // group within the item
+                            const int wi = (6 * gi) >> 2;
+                            const bool odd = ((6 * gi) & 3) != 0;             // group starts mid-word
+                            const uint32_t lo = odd ? (w(wi) >> 16) | (w(wi + 1) << 16) : w(wi);
+                            const uint32_t hi = odd ? (w(wi + 1) >> 16) : (w(wi + 1) & 0xFFFFu);
+                            const uint4 pv = e2m3x8_to_bf16(lo, hi);
+                            out[4 * gg + 0] = fp6_apply(pv.x, mult);
+                            out[4 * gg + 1] = fp6_apply(pv.y, mult);
+                            out[4 * gg + 2] = fp6_apply(pv.z, mult);
+                            out[4 * gg + 3] = fp6_apply(pv.w, mult);
+                        }
+                        tc::tmem_st_32x32b_x16(acol + q * 32 + hh * 16, out);
+                    }
+                } else {
+                    const int c0 = NW == 1 ? 2 * q : 0;
+                    const uint32_t sw = scw[mi][NW == 1 ? q : 0];
+                    uint32_t out[32];
+                    dequant_chunk(cw[mi][c0], sw & 0xFFFF, mode, out);
+                    dequant_chunk(cw[mi][c0 + 1], sw >> 16, mode, out + 16);
+                    tc::tmem_st_32x32b_x32(acol + q * 32, out);
+                }
             }
             tc::tmem_st_wait();
             tc::fence_before_sync();
@@ -1086,25 +1172,25 @@ bool make_map(CUtensorMap *map, CUtensorMapDataType dt, const void *base, uint64
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int NW>
+template <int NW, int FMT = 0>
 cudaError_t set_smem_attr()
 {
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [] {
-        attr_err = cudaFuncSetAttribute(skinny_tc_kernel<NW>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        (int)Cfg<NW>::kSmemBytes);
+        attr_err = cudaFuncSetAttribute(skinny_tc_kernel<NW, FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        (int)Cfg<NW, FMT>::kSmemBytes);
     });
     return attr_err;
 }
 
-template <int NW>
+template <int NW, int FMT = 0>
 cudaLaunchConfig_t main_config(const Args &a, cudaStream_t stream, cudaLaunchAttribute (&attr)[2])
 {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)a.P);
     cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = Cfg<NW>::kSmemBytes;
+    cfg.dynamicSmemBytes = Cfg<NW, FMT>::kSmemBytes;
     cfg.stream = stream;
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
@@ -1119,14 +1205,14 @@ cudaLaunchConfig_t main_config(const Args &a, cudaStream_t stream, cudaLaunchAtt
 
 // Clusters of `cs` CTAs of the main kernel that fit on the current device at
 // once (0 if none), cached per device.
-template <int NW>
+template <int NW, int FMT = 0>
 int max_active_clusters(int cs)
 {
     static std::mutex mu;
     static int cache[64][3];
     static bool have[64][3];
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64 || set_smem_attr<NW>() != cudaSuccess)
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64 || set_smem_attr<NW, FMT>() != cudaSuccess)
         return 0;
     const int ci = cs == 2 ? 0 : (cs == 4 ? 1 : 2);
     std::lock_guard<std::mutex> lock(mu);
@@ -1135,9 +1221,9 @@ int max_active_clusters(int cs)
         probe.cs = cs;
         probe.P = cs;
         cudaLaunchAttribute attr[2];
-        cudaLaunchConfig_t cfg = main_config<NW>(probe, nullptr, attr);
+        cudaLaunchConfig_t cfg = main_config<NW, FMT>(probe, nullptr, attr);
         int n = 0;
-        if (cudaOccupancyMaxActiveClusters(&n, skinny_tc_kernel<NW>, &cfg) != cudaSuccess)
+        if (cudaOccupancyMaxActiveClusters(&n, skinny_tc_kernel<NW, FMT>, &cfg) != cudaSuccess)
             n = 0;
         cudaGetLastError();  // a failed query leaves no sticky error
         cache[dev][ci] = n;
@@ -1146,15 +1232,15 @@ int max_active_clusters(int cs)
     return cache[dev][ci];
 }
 
-template <int NW>
+template <int NW, int FMT = 0>
 cudaError_t launch_main(const CUtensorMap (&maps)[5], const Args &a, cudaStream_t stream)
 {
-    const cudaError_t attr_err = set_smem_attr<NW>();
+    const cudaError_t attr_err = set_smem_attr<NW, FMT>();
     if (attr_err != cudaSuccess)
         return attr_err;
     cudaLaunchAttribute attr[2];
-    cudaLaunchConfig_t cfg = main_config<NW>(a, stream, attr);
-    return cudaLaunchKernelEx(&cfg, skinny_tc_kernel<NW>, maps[0], maps[1], maps[2], maps[3], maps[4], a);
+    cudaLaunchConfig_t cfg = main_config<NW, FMT>(a, stream, attr);
+    return cudaLaunchKernelEx(&cfg, skinny_tc_kernel<NW, FMT>, maps[0], maps[1], maps[2], maps[3], maps[4], a);
 }
 
 // Split of the K dimension of every tile: stream-K over all SMs (any split,
@@ -1164,34 +1250,35 @@ cudaError_t launch_main(const CUtensorMap (&maps)[5], const Args &a, cudaStream_
 // tiles must spread over fewer, fixed-size groups).  The choice depends on
 // the shapes and the device only, never on N, so results do not depend on N.
 // Unit times per SM and the end-of-call saving are measured on GB300.
-template <int NW>
+template <int NW, int FMT = 0>
 void choose_split(Args &a, int num_sms)
 {
     a.cs = 1;
     a.ncl = 0;
     a.P = (int)std::max<int64_t>(1, std::min<int64_t>(a.total, std::min<int64_t>(num_sms, kSkinnyTcMaxCtas)));
-    const double t_unit = NW == 1 ? 0.55 : 1.1;  // us per 128 x 256 unit (per matrix pair) per SM
+    // us per 128 x 256 unit (per matrix pair) per SM; FP6 units carry 1.35x the bytes
+    const double t_unit = (NW == 1 ? 0.55 : 1.1) * (FMT == 1 ? 1.35 : 1.0);
     const double tail_saving = 3.0;               // us: global split-K reduction vs cluster reduction
     double best = (double)((a.total + a.P - 1) / a.P) * t_unit + tail_saving;
     // Measured: cluster-K wins only for one matrix whose tiles fit one per
     // cluster (e.g. 4096 x 4096: 11.6 -> 10.6 us at N = 1); with several tiles
     // per cluster, or for the fused gate/up pair, it was slower (whole
     // clusters must free up before they start).
-    if (NW != 1)
-        return;
-    for (int cs : {4, 2}) {
-        if (a.C < cs)
-            continue;
-        const int64_t ncl = std::min<int64_t>(a.T, max_active_clusters<NW>(cs));
-        if (ncl < 1 || ncl < a.T || ncl * cs > kSkinnyTcMaxCtas)
-            continue;
-        const int64_t tiles = (a.T + ncl - 1) / ncl, units = (a.C + cs - 1) / cs;
-        const double est = (double)(tiles * units) * t_unit;
-        if (est < best) {
-            best = est;
-            a.cs = cs;
-            a.ncl = (int)ncl;
-            a.P = (int)(ncl * cs);
+    if constexpr (NW == 1) {
+        for (int cs : {4, 2}) {
+            if (a.C < cs)
+                continue;
+            const int64_t ncl = std::min<int64_t>(a.T, max_active_clusters<NW, FMT>(cs));
+            if (ncl < 1 || ncl < a.T || ncl * cs > kSkinnyTcMaxCtas)
+                continue;
+            const int64_t tiles = (a.T + ncl - 1) / ncl, units = (a.C + cs - 1) / cs;
+            const double est = (double)(tiles * units) * t_unit;
+            if (est < best) {
+                best = est;
+                a.cs = cs;
+                a.ncl = (int)ncl;
+                a.P = (int)(ncl * cs);
+            }
         }
     }
 }
@@ -1289,6 +1376,53 @@ cudaError_t launch_skinny_tc(const uint16_t *x, int N, int64_t M, int64_t K, con
             return e;
     }
     return n_weights == 1 ? launch_main<1>(maps, a, stream) : launch_main<2>(maps, a, stream);
+}
+
+cudaError_t launch_skinny_tc_fp6(const uint16_t *x, int N, int64_t M, int64_t K, const uint8_t *const *codes,
+                                 const uint8_t *const *scales, int n_weights, void *y, int out_bf16,
+                                 void *workspace, int num_sms, cudaStream_t stream)
+{
+    using namespace sk;
+    const WsLayout L = ws_layout(M, K, n_weights);
+    uint8_t *ws = reinterpret_cast<uint8_t *>(workspace);
+    Args a{};
+    a.N = N;
+    a.M = M;
+    a.K = K;
+    a.C = (int)(K / BKU);
+    a.T = (M + BM - 1) / BM;
+    a.total = a.T * a.C;
+    if (n_weights == 1)
+        choose_split<1, 1>(a, num_sms);
+    else
+        choose_split<2, 1>(a, num_sms);
+    for (int i = 0; i < 2; ++i) {
+        a.ts[i] = nullptr;
+        a.scales6[i] = scales[i < n_weights ? i : 0];
+    }
+    a.factor = reinterpret_cast<float *>(ws);
+    a.flags = reinterpret_cast<int *>(ws + 64);
+    a.counters = reinterpret_cast<uint32_t *>(ws + L.counters);
+    a.partial = reinterpret_cast<float *>(ws + L.partial);
+    a.x_img = ws + L.ximg;
+    a.err = reinterpret_cast<uint32_t *>(ws + 128);
+    a.y = y;
+    a.out_bf16 = out_bf16;
+    a.bf16_only = 1;  // FP6 weights take bf16 operands: no prep kernel
+
+    CUtensorMap maps[5];
+    for (int i = 0; i < 2; ++i) {
+        const int s = i < n_weights ? i : 0;
+        // a unit's 192 code bytes per row as three [128 rows][64 B] boxes, 64-byte swizzle
+        if (!make_map(&maps[i], CU_TENSOR_MAP_DATA_TYPE_UINT8, codes[s], (uint64_t)K / 4 * 3, (uint64_t)M,
+                      (uint64_t)K / 4 * 3, 64, BM, CU_TENSOR_MAP_SWIZZLE_64B))
+            return cudaErrorInvalidValue;
+        maps[2 + i] = maps[i];  // no scale maps
+    }
+    if (!make_map(&maps[4], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, (uint64_t)K, (uint64_t)N, (uint64_t)K * 2, 64,
+                  (uint32_t)N, CU_TENSOR_MAP_SWIZZLE_128B))
+        return cudaErrorInvalidValue;
+    return n_weights == 1 ? launch_main<1, 1>(maps, a, stream) : launch_main<2, 1>(maps, a, stream);
 }
 
 }  // namespace nvfp4

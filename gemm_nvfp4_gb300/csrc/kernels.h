@@ -41,6 +41,9 @@ size_t gemv_mma_workspace_bytes(int n_weights);
 cudaError_t launch_gemv_fp6(const uint16_t *x, int N, int64_t M, int64_t K, const uint8_t *const *codes,
                             const uint8_t *const *scales, int n_weights, void *y, int out_bf16, void *workspace,
                             int num_sms, cudaStream_t stream);
+cudaError_t launch_skinny_tc_fp6(const uint16_t *x, int N, int64_t M, int64_t K, const uint8_t *const *codes,
+                                 const uint8_t *const *scales, int n_weights, void *y, int out_bf16,
+                                 void *workspace, int num_sms, cudaStream_t stream);
 cudaError_t launch_prefill_fp6(const uint16_t *x, int64_t N, int64_t M, int64_t K, const uint8_t *const *codes,
                                const uint8_t *const *scales, int n_weights, void *y, int out_bf16,
                                void *workspace, int num_sms, cudaStream_t stream);

@@ -136,7 +136,9 @@ size_t nvfp4_workspace_bytes(int op, int64_t N, int64_t M, int64_t K)
         if (K % 128 != 0)
             return 0;
         const int nw = op == NVFP4_OP_FP6_GEMM ? 1 : 2;
-        return N <= kMaxSkinnyN ? gemv_mma_workspace_bytes(nw) : prefill_workspace_bytes(N, M, K, nw);
+        if (N > kMaxSkinnyN)
+            return prefill_workspace_bytes(N, M, K, nw);
+        return skinny_tc_supported(M, K) ? skinny_tc_workspace_bytes(M, K, nw) : gemv_mma_workspace_bytes(nw);
     }
     default: return 0;
     }
@@ -280,9 +282,13 @@ static int fp6_products(const uint16_t *x, int64_t N, int64_t M, int64_t K, cons
     if ((rc = current_num_sms(&sms)) != NVFP4_OK)
         return rc;
     const int bf16 = out_dtype == NVFP4_OUT_BF16;
-    cudaError_t e = N <= kMaxSkinnyN
-                        ? launch_gemv_fp6(x, (int)N, M, K, codes, scales, n_weights, y, bf16, ws, sms, stream)
-                        : launch_prefill_fp6(x, N, M, K, codes, scales, n_weights, y, bf16, ws, sms, stream);
+    cudaError_t e;
+    if (N > kMaxSkinnyN)
+        e = launch_prefill_fp6(x, N, M, K, codes, scales, n_weights, y, bf16, ws, sms, stream);
+    else if (skinny_tc_supported(M, K))
+        e = launch_skinny_tc_fp6(x, (int)N, M, K, codes, scales, n_weights, y, bf16, ws, sms, stream);
+    else
+        e = launch_gemv_fp6(x, (int)N, M, K, codes, scales, n_weights, y, bf16, ws, sms, stream);
     return e == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA;
 }
 

@@ -255,8 +255,9 @@ int nvfp4_fp6_quantize_bf16(const uint16_t *w, int64_t M, int64_t K,
  * a skinny kernel that streams every weight byte once for all N tokens, larger
  * N the tensor-core prefill kernel (the same kernels as the NVFP4 calls, with
  * the FP6 dequantiser).  x, y, out_dtype as for nvfp4_gemv_skinny; workspace:
- * nvfp4_workspace_bytes(NVFP4_OP_FP6_GEMM, N, M, K), needing no
- * initialisation. */
+ * nvfp4_workspace_bytes(NVFP4_OP_FP6_GEMM, N, M, K), under the same contract
+ * as the NVFP4 skinny calls (zero-filled before its first use; every call
+ * leaves its split-K counters zero; it may be shared with them). */
 int nvfp4_fp6_gemm(const uint16_t *x, int64_t N,
                    const uint8_t *codes, const uint8_t *scales, int64_t M, int64_t K,
                    void *y, int out_dtype,
