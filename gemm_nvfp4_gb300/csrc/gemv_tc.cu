@@ -1259,6 +1259,15 @@ void choose_split(Args &a, int num_sms)
     // us per 128 x 256 unit (per matrix pair) per SM; FP6 units carry 1.35x the bytes
     const double t_unit = (NW == 1 ? 0.55 : 1.1) * (FMT == 1 ? 1.35 : 1.0);
     const double tail_saving = 3.0;               // us: global split-K reduction vs cluster reduction
+    // Enough tiles to fill most SMs one each: whole tiles, no split-K.  The
+    // split's partial stores and last-arriver reduction cost more than the
+    // idle SMs (measured, 9B gate/up with 96 tiles: 23.6 / 25.2 / 38.5 us split
+    // over 152 SMs against 24.4 / 24.7 / 27.8 us whole at N = 1 / 4 / 16; 27B
+    // gate/up with 136 tiles: 32.9 / 34.4 / 42.1 against 30.9 / 31.4 / 34.4).
+    if (a.T <= num_sms && a.T <= kSkinnyTcMaxCtas && a.T * 10 >= (int64_t)num_sms * 6) {
+        a.P = (int)a.T;
+        return;
+    }
     double best = (double)((a.total + a.P - 1) / a.P) * t_unit + tail_saving;
     // Measured: cluster-K wins only for one matrix whose tiles fit one per
     // cluster (e.g. 4096 x 4096: 11.6 -> 10.6 us at N = 1); with several tiles
