@@ -1259,12 +1259,13 @@ void choose_split(Args &a, int num_sms)
     // us per 128 x 256 unit (per matrix pair) per SM; FP6 units carry 1.35x the bytes
     const double t_unit = (NW == 1 ? 0.55 : 1.1) * (FMT == 1 ? 1.35 : 1.0);
     const double tail_saving = 3.0;               // us: global split-K reduction vs cluster reduction
-    // Enough tiles to fill most SMs one each: whole tiles, no split-K.  The
-    // split's partial stores and last-arriver reduction cost more than the
-    // idle SMs (measured, 9B gate/up with 96 tiles: 23.6 / 25.2 / 38.5 us split
-    // over 152 SMs against 24.4 / 24.7 / 27.8 us whole at N = 1 / 4 / 16; 27B
-    // gate/up with 136 tiles: 32.9 / 34.4 / 42.1 against 30.9 / 31.4 / 34.4).
-    if (a.T <= num_sms && a.T <= kSkinnyTcMaxCtas && a.T * 10 >= (int64_t)num_sms * 6) {
+    // Enough tiles to fill nearly every SM one each: whole tiles, no split-K.
+    // The split's partial stores and last-arriver reduction then cost more
+    // than the few idle SMs (27B gate/up, 136 tiles on 152 SMs: decode streams
+    // at N = 4 / 9 / 16 +3 / +11 / +22 %, N = 1 -2 %).  With 60 % of the SMs
+    // (9B gate/up, 96 tiles) the N = 1 decode stream lost 8 %, so the bar is
+    // 85 %.
+    if (a.T <= num_sms && a.T <= kSkinnyTcMaxCtas && a.T * 100 >= (int64_t)num_sms * 85) {
         a.P = (int)a.T;
         return;
     }
