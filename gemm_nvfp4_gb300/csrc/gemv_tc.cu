@@ -1264,8 +1264,10 @@ void choose_split(Args &a, int num_sms)
     // than the few idle SMs (27B gate/up, 136 tiles on 152 SMs: decode streams
     // at N = 4 / 9 / 16 +3 / +11 / +22 %, N = 1 -2 %).  With 60 % of the SMs
     // (9B gate/up, 96 tiles) the N = 1 decode stream lost 8 %, so the bar is
-    // 85 %.
-    if (a.T <= num_sms && a.T <= kSkinnyTcMaxCtas && a.T * 100 >= (int64_t)num_sms * 85) {
+    // 85 %.  FP6 units carry 1.35x the bytes, so the split's overhead weighs
+    // less: its 27B gate/up stream went 2.11 -> 2.00 TB/s at N = 1 without the
+    // split (1.87 -> 1.95 at N = 16), and FP6 keeps stream-K.
+    if (FMT == 0 && a.T <= num_sms && a.T <= kSkinnyTcMaxCtas && a.T * 100 >= (int64_t)num_sms * 85) {
         a.P = (int)a.T;
         return;
     }
