@@ -6,14 +6,16 @@ marshals PyTorch tensors into that ABI (``binding``) and provides seeded
 synthetic inputs (``inputs``).  There is no CPU fallback: if the library is
 missing, every call raises.
 """
-from .binding import (NVFP4_OP_FP6_GATEUP_SWIGLU, NVFP4_OP_FP6_GEMM, NVFP4_OP_GATEUP_SWIGLU,
+from .binding import (NVFP4_ERR_DEVICE_TIMEOUT, NVFP4_OK, NVFP4_STATUS_WORD_OFFSET,
+                      NVFP4_OP_FP6_GATEUP_SWIGLU, NVFP4_OP_FP6_GEMM, NVFP4_OP_GATEUP_SWIGLU,
                       NVFP4_OP_GEMM_PREFILL, NVFP4_OP_GEMV_SKINNY, NVFP4_OP_QUANTIZE, NVFP4_OUT_BF16,
                       NVFP4_OUT_F32, FP6Weight, NVFP4Error, NVFP4Weight, nvfp4_fp6_gateup_swiglu,
-                      nvfp4_fp6_gemm, nvfp4_fp6_quantize, nvfp4_fp6_quantize_bf16,
+                      nvfp4_device_status, nvfp4_fp6_gemm, nvfp4_fp6_quantize, nvfp4_fp6_quantize_bf16,
                       header_functions, library_path, load_library, nvfp4_gateup_swiglu,
                       nvfp4_blocked_scale_bytes, nvfp4_gemm_prefill, nvfp4_gemv_skinny,
                       nvfp4_gemv_skinny_noalloc, nvfp4_import_blocked_scales, nvfp4_quantize,
-                      nvfp4_quantize_bf16, nvfp4_status_string, nvfp4_version, nvfp4_workspace_bytes)
+                      nvfp4_quantize_bf16, nvfp4_selftest_wait_timeout, nvfp4_status_string, nvfp4_version,
+                      nvfp4_workspace_bytes)
 
 __all__ = [
     "NVFP4Error", "NVFP4Weight", "FP6Weight",
@@ -24,4 +26,6 @@ __all__ = [
     "nvfp4_status_string", "nvfp4_version", "nvfp4_workspace_bytes",
     "NVFP4_OP_QUANTIZE", "NVFP4_OP_GEMV_SKINNY", "NVFP4_OP_GATEUP_SWIGLU", "NVFP4_OP_GEMM_PREFILL",
     "NVFP4_OUT_F32", "NVFP4_OUT_BF16",
+    "nvfp4_device_status", "nvfp4_selftest_wait_timeout", "NVFP4_OK", "NVFP4_ERR_DEVICE_TIMEOUT",
+    "NVFP4_STATUS_WORD_OFFSET",
 ]

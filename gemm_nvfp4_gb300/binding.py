@@ -22,6 +22,9 @@ NVFP4_ERR_INVALID_ARG = 1
 NVFP4_ERR_UNSUPPORTED_SHAPE = 2
 NVFP4_ERR_WORKSPACE = 3
 NVFP4_ERR_CUDA = 4
+NVFP4_ERR_DEVICE_TIMEOUT = 5
+
+NVFP4_STATUS_WORD_OFFSET = 128
 
 NVFP4_OP_QUANTIZE = 0
 NVFP4_OP_GEMV_SKINNY = 1
@@ -90,6 +93,10 @@ def load_library():
         lib.nvfp4_gemm_prefill.argtypes = [P, i64, P, P, P, i64, i64, P, i32, P, sz, P]
         lib.nvfp4_gemv_skinny_noalloc.restype = i32
         lib.nvfp4_gemv_skinny_noalloc.argtypes = [P, i64, P, P, P, i64, i64, P, i32, P]
+        lib.nvfp4_device_status.restype = i32
+        lib.nvfp4_device_status.argtypes = [P, sz, i32, ctypes.POINTER(ctypes.c_uint32), P]
+        lib.nvfp4_selftest_wait_timeout.restype = i32
+        lib.nvfp4_selftest_wait_timeout.argtypes = [P, sz, P]
         _lib = lib
         return lib
 
@@ -263,6 +270,27 @@ def nvfp4_gemm_prefill(x: torch.Tensor, W: NVFP4Weight, out_dtype=torch.float32,
                                            _stream(stream))
     _check(st, "nvfp4_gemm_prefill")
     return y
+
+
+def nvfp4_device_status(workspace: torch.Tensor, clear: bool = True, stream=None) -> tuple[int, int]:
+    """(status, code) of the device status word in a product call's workspace:
+    (NVFP4_OK, 0), or (NVFP4_ERR_DEVICE_TIMEOUT, code) when a kernel's bounded
+    wait gave up since the word was last cleared.  Synchronises the stream;
+    with clear=True a nonzero word is reset."""
+    code = ctypes.c_uint32(0)
+    st = load_library().nvfp4_device_status(_ptr(workspace), workspace.numel() * workspace.element_size(),
+                                            int(bool(clear)), ctypes.byref(code), _stream(stream))
+    if st not in (NVFP4_OK, NVFP4_ERR_DEVICE_TIMEOUT):
+        raise NVFP4Error(st, "nvfp4_device_status")
+    return st, code.value
+
+
+def nvfp4_selftest_wait_timeout(workspace: torch.Tensor, stream=None) -> None:
+    """Enqueue the failure-path self-test: a bounded wait that runs out after
+    2 s and records code 127 in the workspace's status word."""
+    st = load_library().nvfp4_selftest_wait_timeout(_ptr(workspace), workspace.numel() * workspace.element_size(),
+                                                    _stream(stream))
+    _check(st, "nvfp4_selftest_wait_timeout")
 
 
 @dataclass

@@ -346,8 +346,7 @@ constexpr int kPrepCache = 4;  // 16-byte chunks per thread kept in registers be
 // zero the split-K row counters.
 __global__ void __launch_bounds__(kPrepThreads) skinny_prep_kernel(const uint16_t *__restrict__ x, int N, int64_t K,
                                                                    uint8_t *__restrict__ ximg, float *factor,
-                                                                   int *flags, uint32_t *counters, int64_t T,
-                                                                   uint32_t *err)
+                                                                   int *flags, uint32_t *counters, int64_t T)
 {
     tc::griddep_launch_dependents();
     tc::griddep_wait();  // x may come from the previous kernel; the workspace may be in use by it
@@ -355,8 +354,6 @@ __global__ void __launch_bounds__(kPrepThreads) skinny_prep_kernel(const uint16_
     const int tid = threadIdx.x;
     for (int64_t i = (int64_t)n * kPrepThreads + tid; i < T; i += (int64_t)N * kPrepThreads)
         counters[i] = 0;
-    if (n == 0 && tid == 0)
-        *err = 0;
     __shared__ uint32_t red[kPrepThreads / 32];
     __shared__ int bad;
     const uint16_t *xr = x + (int64_t)n * K;
@@ -1322,7 +1319,7 @@ cudaError_t launch_skinny_tc(const uint16_t *x, int N, int64_t M, int64_t K, con
     uint8_t *ws = reinterpret_cast<uint8_t *>(workspace);
     float *factor = reinterpret_cast<float *>(ws);
     int *flags = reinterpret_cast<int *>(ws + 64);
-    uint32_t *err = reinterpret_cast<uint32_t *>(ws + 128);
+    uint32_t *err = reinterpret_cast<uint32_t *>(ws + kStatusWordOffset);
 
     Args a{};
     a.N = N;
@@ -1383,7 +1380,7 @@ cudaError_t launch_skinny_tc(const uint16_t *x, int N, int64_t M, int64_t K, con
         cfg.attrs = attr;
         cfg.numAttrs = 1;
         cudaError_t e = cudaLaunchKernelEx(&cfg, skinny_prep_kernel, x, N, K, ws + L.ximg, factor, flags,
-                                           a.counters, a.T, err);
+                                           a.counters, a.T);
         if (e != cudaSuccess)
             return e;
     }
@@ -1417,7 +1414,7 @@ cudaError_t launch_skinny_tc_fp6(const uint16_t *x, int N, int64_t M, int64_t K,
     a.counters = reinterpret_cast<uint32_t *>(ws + L.counters);
     a.partial = reinterpret_cast<float *>(ws + L.partial);
     a.x_img = ws + L.ximg;
-    a.err = reinterpret_cast<uint32_t *>(ws + 128);
+    a.err = reinterpret_cast<uint32_t *>(ws + kStatusWordOffset);
     a.y = y;
     a.out_bf16 = out_bf16;
     a.bf16_only = 1;  // FP6 weights take bf16 operands: no prep kernel

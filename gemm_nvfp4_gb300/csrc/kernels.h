@@ -7,6 +7,19 @@
 
 namespace nvfp4 {
 
+// Byte offset of the device status word inside the workspace of every product
+// call (skinny, gate/up, prefill; NVFP4 and FP6).  A tensor-core kernel whose
+// bounded pipeline wait runs out stores a nonzero code there (atomicExch) and
+// returns; no kernel ever clears it, so it stays set until the caller clears
+// it (nvfp4_device_status).  Codes: 1..7 prefill, 11..25 skinny, and
+// kStatusSelftest for the wait-timeout self-test.
+constexpr size_t kStatusWordOffset = 128;
+constexpr uint32_t kStatusSelftest = 127;
+
+// One thread waits on a shared-memory barrier that nothing completes; after
+// the bounded wait gives up it records kStatusSelftest in the status word.
+cudaError_t launch_wait_timeout_selftest(void *workspace, cudaStream_t stream);
+
 // Partial maxima written by the amax kernel of the quantiser.
 constexpr int kQuantPartials = 1024;
 // Largest grid of the skinny kernel (sizes its split-K workspace).

@@ -15,6 +15,7 @@ namespace {
 using namespace nvfp4;
 
 constexpr int kMaxSkinnyN = 16;
+static_assert(kStatusWordOffset == NVFP4_STATUS_WORD_OFFSET, "status word offset differs from the header");
 
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
@@ -91,7 +92,6 @@ int run_products(const uint16_t *x, int64_t N, int64_t M, int64_t K, const uint8
     int rc = current_num_sms(&sms);
     if (rc != NVFP4_OK)
         return rc;
-    const size_t esize = out_dtype == NVFP4_OUT_BF16 ? 2 : 4;
     // N <= 16: one skinny launch.  Larger N: tensor-core prefill.
     if (N <= kMaxSkinnyN) {
         cudaError_t e = launch_gemv(x, (int)N, M, K, codes, scales, ts, n_weights, y,
@@ -100,7 +100,6 @@ int run_products(const uint16_t *x, int64_t N, int64_t M, int64_t K, const uint8
     }
     cudaError_t e = launch_prefill(x, N, M, K, codes, scales, ts, n_weights, y, out_dtype == NVFP4_OUT_BF16,
                                    ws, sms, stream);
-    (void)esize;
     return e == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA;
 }
 
@@ -116,6 +115,9 @@ const char *nvfp4_status_string(int status)
     case NVFP4_ERR_UNSUPPORTED_SHAPE: return "NVFP4_ERR_UNSUPPORTED_SHAPE: K % 16 != 0, N out of range or size overflow";
     case NVFP4_ERR_WORKSPACE: return "NVFP4_ERR_WORKSPACE: workspace smaller than nvfp4_workspace_bytes()";
     case NVFP4_ERR_CUDA: return "NVFP4_ERR_CUDA: a CUDA call or kernel launch failed";
+    case NVFP4_ERR_DEVICE_TIMEOUT:
+        return "NVFP4_ERR_DEVICE_TIMEOUT: a kernel's bounded pipeline wait gave up; outputs since the status "
+               "word was last cleared are undefined";
     default: return "NVFP4 unknown status";
     }
 }
@@ -373,6 +375,42 @@ int nvfp4_gemm_prefill(const uint16_t *x, int64_t N, const uint8_t *codes, const
     const uint8_t *s[1] = {scales};
     const float *t[1] = {tensor_scale};
     return run_products(x, N, M, K, c, s, t, 1, y, out_dtype, workspace, (cudaStream_t)stream);
+}
+
+// Status word checks shared by the two calls below: a workspace that holds it.
+static int check_status_workspace(const void *workspace, size_t workspace_bytes)
+{
+    if (!workspace || !aligned(workspace, 16) || workspace_bytes < kStatusWordOffset + sizeof(uint32_t))
+        return NVFP4_ERR_INVALID_ARG;
+    return NVFP4_OK;
+}
+
+int nvfp4_device_status(const void *workspace, size_t workspace_bytes, int clear, uint32_t *code,
+                        nvfp4_stream_t stream)
+{
+    int rc = check_status_workspace(workspace, workspace_bytes);
+    if (rc != NVFP4_OK)
+        return rc;
+    uint8_t *word = const_cast<uint8_t *>(reinterpret_cast<const uint8_t *>(workspace)) + kStatusWordOffset;
+    uint32_t v = 0;
+    cudaStream_t s = (cudaStream_t)stream;
+    if (cudaMemcpyAsync(&v, word, sizeof(v), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess)
+        return NVFP4_ERR_CUDA;
+    if (clear && v != 0 && cudaMemsetAsync(word, 0, sizeof(v), s) != cudaSuccess)
+        return NVFP4_ERR_CUDA;
+    if (code)
+        *code = v;
+    return v == 0 ? NVFP4_OK : NVFP4_ERR_DEVICE_TIMEOUT;
+}
+
+int nvfp4_selftest_wait_timeout(void *workspace, size_t workspace_bytes, nvfp4_stream_t stream)
+{
+    int rc = check_status_workspace(workspace, workspace_bytes);
+    if (rc != NVFP4_OK)
+        return rc;
+    return launch_wait_timeout_selftest(workspace, (cudaStream_t)stream) == cudaSuccess ? NVFP4_OK
+                                                                                        : NVFP4_ERR_CUDA;
 }
 
 }  // extern "C"

@@ -268,8 +268,6 @@ __global__ void __launch_bounds__(TMAC ? kThreadsTma : kThreads, 1)
         }
         tc::fence_mbar_init();
         tc::prefetch_tensormap(&tmap_x);
-        if (blockIdx.x == 0 && blockIdx.y == 0 && *a.err != 0)
-            *a.err = 0;
     }
     if (warp == 1)
         tc::tmem_alloc(tmem_slot, C::kTmemCols);
@@ -745,7 +743,7 @@ static bool encode_rows(PFN_cuTensorMapEncodeTiled_v12000 encode, CUtensorMap *m
 size_t prefill_workspace_bytes(int64_t N, int64_t M, int64_t K, int n_weights)
 {
     (void)N; (void)M; (void)K; (void)n_weights;
-    return 256;  // word 0: pipeline-timeout flag
+    return 256;  // the device status word at kStatusWordOffset, nothing else
 }
 
 static cudaError_t prefill_impl(const uint16_t *x, int64_t N, int64_t M, int64_t K, const uint8_t *const *codes,
@@ -784,7 +782,7 @@ static cudaError_t prefill_impl(const uint16_t *x, int64_t N, int64_t M, int64_t
     a.M = M;
     a.K = K;
     a.num_kb = (int)((K + pf::BK - 1) / pf::BK);
-    a.err = reinterpret_cast<uint32_t *>(workspace);
+    a.err = reinterpret_cast<uint32_t *>(reinterpret_cast<uint8_t *>(workspace) + kStatusWordOffset);
     a.row_tiles = (int)row_tiles;
     a.token_tiles = (int)token_tiles;
     {
@@ -848,6 +846,29 @@ cudaError_t launch_prefill_fp6(const uint16_t *x, int64_t N, int64_t M, int64_t 
                                void *workspace, int num_sms, cudaStream_t stream)
 {
     return prefill_impl(x, N, M, K, codes, scales, nullptr, n_weights, y, out_bf16, workspace, 1, num_sms, stream);
+}
+
+// Failure-path self-test: one thread waits, with the same bounded wait as the
+// pipelines above, on a barrier that nothing arrives at.  When the wait gives
+// up (tc::kWaitLimitNs of wall time) the kernel records kStatusSelftest in the
+// status word, as a compute kernel records its own code, and returns; nothing
+// faults and the context stays usable.
+__global__ void wait_timeout_selftest_kernel(uint32_t *status)
+{
+    __shared__ __align__(8) uint64_t bar;
+    if (threadIdx.x != 0)
+        return;
+    tc::mbar_init(&bar, 1);
+    tc::fence_mbar_init();
+    if (!tc::mbar_wait(&bar, 0))  // phase 0 never completes
+        atomicExch(status, kStatusSelftest);
+}
+
+cudaError_t launch_wait_timeout_selftest(void *workspace, cudaStream_t stream)
+{
+    uint32_t *status = reinterpret_cast<uint32_t *>(reinterpret_cast<uint8_t *>(workspace) + kStatusWordOffset);
+    wait_timeout_selftest_kernel<<<1, 32, 0, stream>>>(status);
+    return cudaGetLastError();
 }
 
 }  // namespace nvfp4

@@ -46,10 +46,17 @@
  *     calls of any shapes.  Do not write to it between skinny calls (a quantise or
  *     prefill call on the same buffer counts as writing), and zero it again
  *     after a call that failed.  The quantise and prefill calls need no
- *     initialisation and leave their workspace undefined.
+ *     initialisation and leave their workspace undefined, except that the
+ *     product calls keep a device status word at byte NVFP4_STATUS_WORD_OFFSET
+ *     (see nvfp4_device_status).
  *   - Errors: arguments are checked on the host before anything is enqueued;
  *     a bad argument returns a nonzero nvfp4_status and nothing runs.  A
  *     failed launch returns NVFP4_ERR_CUDA.  The library never aborts or prints.
+ *     Every wait inside a kernel is bounded: a pipeline that stops making
+ *     progress gives up after 2 s of wall time, records a code in the
+ *     workspace's status word and returns (the outputs are then undefined),
+ *     so the GPU never hangs and the context stays usable; the launching call
+ *     has already returned, so the code is read with nvfp4_device_status.
  *   - Determinism: the reduction order is fixed by the shapes alone, so repeated
  *     calls give bit-identical results, and row n of an N-token call equals the
  *     same token in any other call with the same weights, M and K on the same
@@ -83,7 +90,8 @@ typedef enum {
     NVFP4_ERR_INVALID_ARG = 1,       /* null pointer, negative size, misalignment, bad enum */
     NVFP4_ERR_UNSUPPORTED_SHAPE = 2, /* K % 16 != 0, N outside the call's range, size overflow */
     NVFP4_ERR_WORKSPACE = 3,         /* workspace smaller than nvfp4_workspace_bytes() */
-    NVFP4_ERR_CUDA = 4               /* a CUDA runtime call or kernel launch failed */
+    NVFP4_ERR_CUDA = 4,              /* a CUDA runtime call or kernel launch failed */
+    NVFP4_ERR_DEVICE_TIMEOUT = 5     /* a kernel's bounded wait gave up (nvfp4_device_status) */
 } nvfp4_status;
 
 /* Operation ids for nvfp4_workspace_bytes. */
@@ -298,6 +306,34 @@ int nvfp4_gemv_skinny_noalloc(const uint16_t *x, int64_t N,
                               const uint8_t *codes, const uint8_t *scales,
                               const float *tensor_scale, int64_t M, int64_t K,
                               void *y, int out_dtype, nvfp4_stream_t stream);
+
+/* Device-side failures.  The product calls keep a 32-bit status word at byte
+ * NVFP4_STATUS_WORD_OFFSET of their workspace (every product workspace is at
+ * least 256 bytes).  A tensor-core kernel (skinny with K % 256 == 0, prefill)
+ * whose bounded pipeline wait runs out (2 s) stores a nonzero code there and
+ * returns: 1..7 from the prefill kernel, 11..25 from the skinny kernel, 127
+ * from nvfp4_selftest_wait_timeout.  No kernel clears the word, so it reports
+ * any failure since it was last cleared; it starts clean when the workspace is
+ * zero-filled (required for the skinny calls; do it for a prefill workspace
+ * too before reading its status).  A quantise call overwrites the word. */
+#define NVFP4_STATUS_WORD_OFFSET 128
+
+/* Read the status word of `workspace` (device, at least
+ * NVFP4_STATUS_WORD_OFFSET + 4 bytes, 16-byte aligned) after the work enqueued
+ * on `stream` so far: synchronises `stream`, stores the word in *code (if
+ * code is not NULL) and returns NVFP4_OK when it is zero, else
+ * NVFP4_ERR_DEVICE_TIMEOUT.  With clear != 0 a nonzero word is reset to zero
+ * on `stream` afterwards.  NVFP4_ERR_INVALID_ARG for a null, misaligned or too
+ * small workspace; NVFP4_ERR_CUDA if the copy or the synchronisation fails. */
+int nvfp4_device_status(const void *workspace, size_t workspace_bytes, int clear, uint32_t *code,
+                        nvfp4_stream_t stream);
+
+/* Test of the failure path above: enqueues one thread that waits, with the
+ * kernels' own bounded wait, on a barrier that nothing completes, so after
+ * 2 s it records code 127 in the status word of `workspace` and exits.  It
+ * faults nothing and computes nothing; the arguments are checked as for
+ * nvfp4_device_status. */
+int nvfp4_selftest_wait_timeout(void *workspace, size_t workspace_bytes, nvfp4_stream_t stream);
 
 #ifdef __cplusplus
 }

@@ -157,7 +157,7 @@ def quantize_bf16(w_bits, lib=None):
 #
 # The pages re-encode NVFP4 checkpoints into each engine's own layout at load
 # time (bw24 README, safetensors loader; bw24 wiki Home) without printing the
-# source layout.  This build defines one external layout to import: the codes
+# source layout.  This library defines one external layout to import: the codes
 # as in the canonical layout ([M][K/2], even k in the low nibble) and the
 # E4M3 block scales in 128 x 4 blocks, the block arrangement block-scaled
 # tensor-core GEMMs read:

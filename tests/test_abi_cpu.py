@@ -33,8 +33,9 @@ def test_python_binding_has_the_c_names():
 
 def test_version_and_status_strings(lib):
     assert g.nvfp4_version() >= 100
-    for st in range(5):
+    for st in range(6):
         assert g.nvfp4_status_string(st).startswith("NVFP4_")
+    assert "TIMEOUT" in g.nvfp4_status_string(g.NVFP4_ERR_DEVICE_TIMEOUT)
     assert "unknown" in g.nvfp4_status_string(99)
 
 
@@ -174,3 +175,26 @@ def test_fp6_calls_reject_bad_arguments(lib):
                                      _P(FAKE), g.nvfp4_workspace_bytes(g.NVFP4_OP_FP6_GATEUP_SWIGLU, 4, 64, 128),
                                      None)
     assert st == binding.NVFP4_ERR_INVALID_ARG  # null up codes
+
+
+def test_status_calls_reject_bad_workspaces(lib):
+    """Argument checks of the device-status calls, all before any CUDA call."""
+    code = ctypes.c_uint32(7)
+    need = binding.NVFP4_STATUS_WORD_OFFSET + 4
+    rd = lambda ws, n: lib.nvfp4_device_status(_P(ws), n, 1, ctypes.byref(code), None)
+    assert rd(0, 256) == binding.NVFP4_ERR_INVALID_ARG
+    assert rd(FAKE + 4, 256) == binding.NVFP4_ERR_INVALID_ARG
+    assert rd(FAKE, need - 1) == binding.NVFP4_ERR_INVALID_ARG
+    assert code.value == 7  # untouched on a rejected call
+    st = lambda ws, n: lib.nvfp4_selftest_wait_timeout(_P(ws), n, None)
+    assert st(0, 256) == binding.NVFP4_ERR_INVALID_ARG
+    assert st(FAKE + 8, 256) == binding.NVFP4_ERR_INVALID_ARG
+    assert st(FAKE, need - 1) == binding.NVFP4_ERR_INVALID_ARG
+    # every product workspace holds the status word
+    for op, N in ((g.NVFP4_OP_GEMV_SKINNY, 1), (g.NVFP4_OP_GATEUP_SWIGLU, 4), (g.NVFP4_OP_GEMM_PREFILL, 600),
+                  (g.NVFP4_OP_GATEUP_SWIGLU, 600), (g.NVFP4_OP_FP6_GEMM, 4), (g.NVFP4_OP_FP6_GEMM, 600),
+                  (g.NVFP4_OP_FP6_GATEUP_SWIGLU, 1)):
+        for M, K in ((64, 128), (4096, 4096), (333, 4112)):
+            if op in (g.NVFP4_OP_FP6_GEMM, g.NVFP4_OP_FP6_GATEUP_SWIGLU) and K % 128:
+                continue
+            assert g.nvfp4_workspace_bytes(op, N, M, K) >= need, (op, N, M, K)

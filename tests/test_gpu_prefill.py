@@ -14,14 +14,19 @@ pytestmark = pytest.mark.gpu
 
 
 def workspace(op, N, M, K):
+    """A prefill workspace filled with garbage (the call needs no initialised
+    workspace) except for the device status word, zeroed so it can be read."""
     n = g.nvfp4_workspace_bytes(op, N, M, K)
-    ws = torch.full((max(n, 16),), 0xAB, dtype=torch.uint8, device=DEV)
+    ws = torch.full((max(n, 256),), 0xAB, dtype=torch.uint8, device=DEV)
+    ws[g.NVFP4_STATUS_WORD_OFFSET:g.NVFP4_STATUS_WORD_OFFSET + 4] = 0
     return ws
 
 
 def timeout_flag(ws):
-    """Word 0 of the prefill workspace: nonzero if a pipeline wait gave up."""
-    return int(ws[:4].view(torch.int32).item())
+    """The device status word: nonzero if a pipeline wait gave up."""
+    st, code = g.nvfp4_device_status(ws, clear=False)
+    assert (st == g.NVFP4_OK) == (code == 0)
+    return code
 
 
 @pytest.mark.parametrize("N,M,K", [(17, 48, 272), (40, 130, 512), (256, 128, 64), (257, 256, 1024),
