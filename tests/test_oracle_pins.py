@@ -609,8 +609,39 @@ def check_fp6_gemv_exact_small(lib):
             assert abs(Fraction(A[n, m]) - aexact) <= Fraction(1, 10 ** 12) * aexact
 
 
+def check_fp6_swiglu(lib):
+    """h = silu(g) * u for FP6 weights against exact rational g and u (codes
+    from the independent re-derivation), plus the g = 0 limit of SiLU."""
+    rng = np.random.default_rng(31)
+    K = 256
+    gw = (rng.standard_normal((3, K)) * 0.3).astype(np.float32)
+    uw = (rng.standard_normal((3, K)) * 0.3).astype(np.float32)
+    gc, gs = fp6_quantize_ref(gw)
+    uc, us = fp6_quantize_ref(uw)
+    x = bf16_round(rng.standard_normal((2, K)))
+    h, gr, ur, Ag, Au = oracle.fp6_swiglu(x, (gc, gs), (uc, us), lib=lib)
+
+    def wq(c, sc, m):
+        codes = unpack6_ref(c[m], K)
+        return [Fraction(e2m3_ref(codes[k])) * Fraction(2) ** (int(sc[m, k // 128]) - 127) for k in range(K)]
+
+    for m in range(3):
+        gq, uq = wq(gc, gs, m), wq(uc, us, m)
+        for n in range(2):
+            xs = [Fraction(bf16_value(b)) for b in x[n]]
+            ge = float(sum(a * b for a, b in zip(gq, xs)))
+            ue = float(sum(a * b for a, b in zip(uq, xs)))
+            he = ge / (1.0 + math.exp(-ge)) * ue
+            assert abs(gr[n, m] - ge) <= 1e-12 * Ag[n, m] + 1e-300
+            assert abs(ur[n, m] - ue) <= 1e-12 * Au[n, m] + 1e-300
+            assert abs(h[n, m] - he) <= 1e-12 * (abs(he) + Ag[n, m] * abs(ue) + Au[n, m] * abs(ge)) + 1e-300
+    # an all-zero gate (codes 0, smallest scale) makes every h zero
+    h0, *_ = oracle.fp6_swiglu(x, (np.zeros_like(gc), np.zeros_like(gs)), (uc, us), lib=lib)
+    assert not h0.any()
+
+
 ALL_CHECKS += [check_fp6_e2m3_table, check_fp6_e2m3_encode, check_fp6_hand_block,
-               check_fp6_quantize_random, check_fp6_gemv_exact_small]
+               check_fp6_quantize_random, check_fp6_gemv_exact_small, check_fp6_swiglu]
 
 
 # (test_oracle_pin above runs every entry of ALL_CHECKS, these included)
