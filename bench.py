@@ -16,8 +16,9 @@ codes + scales + x + y), the roofline of the dominant kernel, an end-to-end
 number with host<->device copies, the oracle timed on host cores, and the SM
 clocks sampled during the timed region.
 
---impl reference times the CPU oracle (the only reference implementation this
-build has) on a bounded sample of the same workload, in the same unit.
+--impl reference times the CPU oracle (no other reference implementation of
+this path exists) on a bounded sample of the same workload, in the same unit,
+on all host cores.
 Under torchrun every rank runs its own replica (no collective on the data
 path; the path does not shard), rank 0 prints.
 """
