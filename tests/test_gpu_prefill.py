@@ -84,7 +84,7 @@ def _sample(n, total, seed, edges):
     return np.unique(np.concatenate([rng.integers(0, total, n), edges]))
 
 
-@pytest.mark.parametrize("N", [512, 2048])
+@pytest.mark.parametrize("N", [512, 2048, 8192])
 def test_prefill_gateup_full_size_sampled(N):
     """Full-size prefill gate/up (5120 -> 17408 each, SwiGLU), sampled outputs."""
     M, K = inputs.LAYER_27B.shapes()["gate"]
