@@ -12,7 +12,8 @@ order).  This module compiles it with gcc on first use and wraps it with
 ctypes for numpy arrays.
 
 It also covers the ingest helpers (bf16-input quantiser, the blocked 128 x 4
-scale layout) and the FP6 E2M3 block-scaled variant of the weights.
+scale layout), the FP6 E2M3 block-scaled variant of the weights, and the W4A4
+product (activations quantised to NVFP4 as well).
 
 Pins (tests/test_oracle_pins.py) tie every function here to something other
 than itself: brute-force nearest-value searches, PyTorch's float8_e4m3fn
@@ -80,6 +81,8 @@ def _bind(lib):
     lib.nvfp4_oracle_fp6_quantize.argtypes = [P, i64, i64, P, P]
     lib.nvfp4_oracle_fp6_gemv.restype = None
     lib.nvfp4_oracle_fp6_gemv.argtypes = [P, i64, i64, P, i64, P, P, i64, P, i64, P, P]
+    lib.nvfp4_oracle_w4a4_gemm.restype = None
+    lib.nvfp4_oracle_w4a4_gemm.argtypes = [P, P, f32, i64, i64, P, i64, P, P, f32, i64, P, i64, P, P]
     return lib
 
 
@@ -333,3 +336,32 @@ def load_variant(path: str):
     that plant a mistake in a copy of the oracle source and check that the pins
     catch it)."""
     return _bind(ctypes.CDLL(path))
+
+
+# --------------------------------------------------------------------------
+# W4A4: activations quantised to NVFP4 as well
+# --------------------------------------------------------------------------
+
+def quantize_activations(x_bf16_bits, lib=None):
+    """bf16 activations [N, K] -> one NVFP4 tensor (codes, scales, ts) by the
+    weights' recipe: the matrix is quantised exactly as a bf16 weight matrix."""
+    return quantize_bf16(x_bf16_bits, lib)
+
+
+def w4a4_gemm(xq, wq, rows=None, tokens=None, lib=None):
+    """y_ref, A (fp64) [n_tokens, n_rows] of ts_x * ts_w * sum_k dec(x) dec(w)
+    for xq = (codes, scales, ts) of the activations [N, K] and wq = (codes,
+    scales, ts) of the weights [M, K]; |y - y_ref| <= 1e-5 A + 1e-7."""
+    xc, xs = _c(xq[0], np.uint8), _c(xq[1], np.uint8)
+    wc, ws = _c(wq[0], np.uint8), _c(wq[1], np.uint8)
+    N, K = xc.shape[0], 2 * xc.shape[1]
+    M = wc.shape[0]
+    assert xs.shape == (N, K // 16) and wc.shape == (M, K // 2) and ws.shape == (M, K // 16)
+    r, nr = _index(rows, M)
+    t, nt = _index(tokens, N)
+    y = np.zeros((nt, nr), np.float64)
+    A = np.zeros((nt, nr), np.float64)
+    (lib or _load()).nvfp4_oracle_w4a4_gemm(_ptr(xc), _ptr(xs), float(np.float32(xq[2])), N, K, _ptr(t), nt,
+                                            _ptr(wc), _ptr(ws), float(np.float32(wq[2])), M, _ptr(r), nr,
+                                            _ptr(y), _ptr(A))
+    return y, A

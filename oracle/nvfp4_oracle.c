@@ -435,3 +435,49 @@ void nvfp4_oracle_fp6_gemv(const uint16_t *x, int64_t N_total, int64_t K,
         }
     }
 }
+
+/* ------------------------------------------------------------------------- */
+/* W4A4: activations quantised to NVFP4 as well                               */
+/* ------------------------------------------------------------------------- */
+/*
+ * The opt-in prefill arm that quantises the activations to FP4 too (bw24
+ * README, Gemma section, the paragraph on prefill against llama.cpp: W4A4 with
+ * FP4 activations is faster but a different numeric class, which forks outputs
+ * on long prompts).  Readings, since the page names the class and nothing
+ * more:
+ *   - the activation matrix x[N][K] is one NVFP4 tensor, quantised by the same
+ *     recipe as the weights (its bf16 elements taken as their exact fp32
+ *     values): one tensor scale for the whole matrix, one E4M3 scale per 16
+ *     consecutive k of a token row, E2M1 codes, the same layout;
+ *   - the product is the plain definition with both operands decoded exactly:
+ *     y[n][m] = ts_x * ts_w * sum_k e2m1(cx) e4m3(sx) e2m1(cw) e4m3(sw).
+ * Every term is exact in fp64 (at most 12 significant bits); the sum runs in
+ * k order and the two fp32 tensor scales multiply it at the end. */
+void nvfp4_oracle_w4a4_gemm(const uint8_t *x_codes, const uint8_t *x_scales, float x_ts,
+                            int64_t N_total, int64_t K, const int64_t *tokens, int64_t n_tokens,
+                            const uint8_t *codes, const uint8_t *scales, float ts,
+                            int64_t M, const int64_t *rows, int64_t n_rows,
+                            double *y, double *A)
+{
+    if (tokens == NULL)
+        n_tokens = N_total;
+    if (rows == NULL)
+        n_rows = M;
+    const double scale = (double)x_ts * (double)ts;  /* exact: 24 + 24 bits */
+    for (int64_t i = 0; i < n_tokens; ++i) {
+        int64_t n = tokens ? tokens[i] : i;
+        for (int64_t j = 0; j < n_rows; ++j) {
+            int64_t m = rows ? rows[j] : j;
+            double sum = 0.0, asum = 0.0;
+            for (int64_t k = 0; k < K; ++k) {
+                double t = weight_unscaled(x_codes, x_scales, K, n, k) *
+                           weight_unscaled(codes, scales, K, m, k);
+                sum += t;
+                asum += fabs(t);
+            }
+            y[i * n_rows + j] = scale * sum;
+            if (A)
+                A[i * n_rows + j] = fabs(scale) * asum;
+        }
+    }
+}

@@ -55,6 +55,10 @@ MUTANTS = {
     "fp6_x_row_stride_wrong": ("const uint16_t *xrow = x + n * K;", "const uint16_t *xrow = x + n;"),
     "fp6_scale_bias_126": ("ldexp(1.0, (int)scales[m * (K / 128) + k / 128] - 127)",
                            "ldexp(1.0, (int)scales[m * (K / 128) + k / 128] - 126)"),
+    "w4a4_activation_scale_dropped": ("const double scale = (double)x_ts * (double)ts;",
+                                      "const double scale = (double)ts;"),
+    "w4a4_token_index_is_position": ("weight_unscaled(x_codes, x_scales, K, n, k)",
+                                     "weight_unscaled(x_codes, x_scales, K, i, k)"),
 }
 
 

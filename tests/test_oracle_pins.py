@@ -644,6 +644,74 @@ ALL_CHECKS += [check_fp6_e2m3_table, check_fp6_e2m3_encode, check_fp6_hand_block
                check_fp6_quantize_random, check_fp6_gemv_exact_small, check_fp6_swiglu]
 
 
+# ---------------------------------------------------------------------------
+# W4A4: activations quantised to NVFP4 as well
+# ---------------------------------------------------------------------------
+
+def check_w4a4_exact_small(lib):
+    """Activation bytes from the independent recipe; products from exact rationals."""
+    rng = np.random.default_rng(37)
+    N, M, K = 3, 4, 48
+    xb = bf16_round(rng.standard_normal((N, K)).astype(np.float32) * np.array([[1.0], [8.0], [0.25]], np.float32))
+    xf = (xb.astype(np.uint32) << np.uint32(16)).view(np.float32)
+    xq = oracle.quantize_activations(xb, lib=lib)
+    rxq = quantize_ref(xf)
+    assert xq[2] == rxq[2] and np.array_equal(xq[1], rxq[1]) and np.array_equal(xq[0], rxq[0])
+    w = (rng.standard_normal((M, K)) * 0.02).astype(np.float32)
+    wq = quantize_ref(w)
+    y, A = oracle.w4a4_gemm(rxq, wq, lib=lib)
+    xd, wd = dequant_ref(*rxq), dequant_ref(*wq)
+    for n in range(N):
+        for m in range(M):
+            terms = [xd[n][k] * wd[m][k] for k in range(K)]
+            exact = sum(terms, Fraction(0))
+            aexact = sum((abs(t) for t in terms), Fraction(0))
+            assert abs(Fraction(y[n, m]) - exact) <= Fraction(1, 10 ** 12) * aexact + Fraction(1, 10 ** 300)
+            assert abs(Fraction(A[n, m]) - aexact) <= Fraction(1, 10 ** 12) * aexact + Fraction(1, 10 ** 300)
+    # row / token subsets, in the order asked
+    ys, As = oracle.w4a4_gemm(rxq, wq, rows=[3, 1], tokens=[2, 0], lib=lib)
+    assert ys[0, 0] == y[2, 3] and ys[1, 1] == y[0, 1] and As[1, 0] == A[0, 3]
+
+
+def check_w4a4_equals_w4a16_on_exact_activations(lib):
+    """With an activation tensor scale of 1 the decoded activations
+    e2m1 * e4m3 have at most 6 significant bits, so they are exact bf16
+    values; the W4A4 product must then equal the W4A16 product of those bf16
+    activations bit for bit (same exact terms, same k order)."""
+    rng = np.random.default_rng(41)
+    N, M, K = 3, 5, 64
+    xc = rng.integers(0, 256, (N, K // 2), dtype=np.uint8)
+    xs = rng.integers(0x08, 0x7F, (N, K // 16), dtype=np.uint8)  # normal, finite E4M3 bytes
+    xd = np.array([[float(v) for v in row] for row in dequant_ref(xc, xs, np.float32(1.0))], np.float64)
+    xb = bf16_round(xd.astype(np.float32))
+    assert np.array_equal((xb.astype(np.uint32) << np.uint32(16)).view(np.float32).astype(np.float64), xd)
+    w = (rng.standard_normal((M, K)) * 0.02).astype(np.float32)
+    wq = quantize_ref(w)
+    y4, A4 = oracle.w4a4_gemm((xc, xs, np.float32(1.0)), wq, lib=lib)
+    y16, A16 = oracle.gemv(xb, *wq, lib=lib)
+    assert np.array_equal(y4, y16) and np.array_equal(A4, A16)
+
+
+def check_w4a4_operand_symmetry_and_zero(lib):
+    """The definition is symmetric in its two NVFP4 operands; zero activations
+    give a zero tensor scale and a zero product."""
+    rng = np.random.default_rng(43)
+    K = 32
+    a = quantize_ref((rng.standard_normal((3, K)) * 0.5).astype(np.float32))
+    b = quantize_ref((rng.standard_normal((5, K)) * 0.02).astype(np.float32))
+    yab, Aab = oracle.w4a4_gemm(a, b, lib=lib)
+    yba, Aba = oracle.w4a4_gemm(b, a, lib=lib)
+    assert np.array_equal(yab, yba.T) and np.array_equal(Aab, Aba.T)
+    z = oracle.quantize_activations(np.zeros((2, K), np.uint16), lib=lib)
+    assert z[2] == 0 and not z[0].any() and not z[1].any()
+    yz, Az = oracle.w4a4_gemm(z, b, lib=lib)
+    assert not yz.any() and not Az.any()
+
+
+ALL_CHECKS += [check_w4a4_exact_small, check_w4a4_equals_w4a16_on_exact_activations,
+               check_w4a4_operand_symmetry_and_zero]
+
+
 # (test_oracle_pin above runs every entry of ALL_CHECKS, these included)
 
 
