@@ -1172,13 +1172,12 @@ bool make_map(CUtensorMap *map, CUtensorMapDataType dt, const void *base, uint64
 template <int NW, int FMT = 0>
 cudaError_t set_smem_attr()
 {
-    static std::once_flag once;
-    static cudaError_t attr_err = cudaSuccess;
-    std::call_once(once, [] {
-        attr_err = cudaFuncSetAttribute(skinny_tc_kernel<NW, FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        (int)Cfg<NW, FMT>::kSmemBytes);
+    static std::once_flag once[kMaxDevices];
+    static cudaError_t attr_err[kMaxDevices];
+    return once_per_device(once, attr_err, [] {
+        return cudaFuncSetAttribute(skinny_tc_kernel<NW, FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)Cfg<NW, FMT>::kSmemBytes);
     });
-    return attr_err;
 }
 
 template <int NW, int FMT = 0>

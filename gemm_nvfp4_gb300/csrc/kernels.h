@@ -5,7 +5,27 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <mutex>
+
 namespace nvfp4 {
+
+// Runs `set` once for each device it is called on (the current device) and
+// returns that device's result.  Function attributes such as the dynamic
+// shared-memory limit belong to each device's context, so a process that
+// drives several GPUs must set them on every one.
+constexpr int kMaxDevices = 64;
+template <class F>
+cudaError_t once_per_device(std::once_flag (&flags)[kMaxDevices], cudaError_t (&results)[kMaxDevices], F &&set)
+{
+    int dev = 0;
+    const cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    if (dev < 0 || dev >= kMaxDevices)
+        return cudaErrorInvalidDevice;
+    std::call_once(flags[dev], [&] { results[dev] = set(); });
+    return results[dev];
+}
 
 // Byte offset of the device status word inside the workspace of every product
 // call (skinny, gate/up, prefill; NVFP4 and FP6).  A tensor-core kernel whose

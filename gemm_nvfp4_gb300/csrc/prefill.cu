@@ -697,11 +697,11 @@ template <int NW, bool ALIGNED, int FMT = 0, bool TMAC = false, int TN = BN>
 cudaError_t launch_t(const CUtensorMap &map, const WeightMaps &wm, const Args &a, cudaStream_t stream)
 {
     using C = Cfg<NW, TMAC, FMT, TN>;
-    static std::once_flag once;
-    static cudaError_t attr_err = cudaSuccess;
-    std::call_once(once, [] {
-        attr_err = cudaFuncSetAttribute(prefill_kernel<NW, ALIGNED, FMT, TMAC, TN>,
-                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmemBytes);
+    static std::once_flag once[kMaxDevices];
+    static cudaError_t attr_errs[kMaxDevices];
+    const cudaError_t attr_err = once_per_device(once, attr_errs, [] {
+        return cudaFuncSetAttribute(prefill_kernel<NW, ALIGNED, FMT, TMAC, TN>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmemBytes);
     });
     if (attr_err != cudaSuccess)
         return attr_err;
