@@ -37,7 +37,7 @@
  *     stream) and returns without synchronising.  Results are ready when the
  *     stream reaches that point.
  *   - Workspace: scratch device memory of at least nvfp4_workspace_bytes(...)
- *     bytes, 256-byte aligned, owned by the caller and not used by anything
+ *     bytes, 16-byte aligned (checked), owned by the caller and not used by anything
  *     else while the call's kernels run.  Calls that share a workspace must be
  *     ordered on one stream.  The products with N <= 16 (skinny path) keep
  *     split-K arrival counters in it: their workspace must be zero-filled
