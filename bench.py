@@ -345,10 +345,25 @@ def read_traffic(kernel_key):
     return None
 
 
-def prefill_tflops(dev, reps=5):
+def time_calls(fn, reps):
+    """Mean milliseconds of `reps` back-to-back calls on the current stream,
+    CUDA events, after one warm-up call."""
+    fn()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        fn()
+    e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / reps
+
+
+def prefill_tflops(dev, reps=10):
     """Prefill GEMM throughput on the 27B-class gate/up (SwiGLU) and down
     matrices at N = 512, 2048, 8192 (dense bf16-equivalent FLOPs, 2*N*M*K per
-    matrix), timed with CUDA events after one warm-up call each."""
+    matrix), timed with CUDA events after one warm-up call each; outputs and
+    workspaces are allocated before the timed calls."""
     import gemm_nvfp4_gb300 as g
     from gemm_nvfp4_gb300 import inputs
     shapes = inputs.LAYER_27B.shapes()
@@ -361,20 +376,18 @@ def prefill_tflops(dev, reps=5):
     for N in (512, 2048, 8192):
         xg = inputs.activations(N, Kg, seed=N, device=dev)
         xd = inputs.activations(N, Kd, seed=N + 1, device=dev)
+        h = torch.empty(N, Mg, dtype=torch.float32, device=dev)
+        y = torch.empty(N, Md, dtype=torch.float32, device=dev)
+        wsg = torch.zeros(g.nvfp4_workspace_bytes(g.NVFP4_OP_GATEUP_SWIGLU, N, Mg, Kg), dtype=torch.uint8,
+                          device=dev)
+        wsd = torch.zeros(g.nvfp4_workspace_bytes(g.NVFP4_OP_GEMM_PREFILL, N, Md, Kd), dtype=torch.uint8,
+                          device=dev)
         for name, fn, flops in (
-                ("gateup", lambda: g.nvfp4_gateup_swiglu(xg, Wg, Wu), 2 * 2.0 * N * Mg * Kg),
-                ("down", lambda: g.nvfp4_gemm_prefill(xd, Wd), 2.0 * N * Md * Kd)):
-            fn()
-            torch.cuda.synchronize()
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record()
-            for _ in range(reps):
-                fn()
-            e1.record()
-            torch.cuda.synchronize()
-            ms = e0.elapsed_time(e1) / reps
+                ("gateup", lambda: g.nvfp4_gateup_swiglu(xg, Wg, Wu, out=h, workspace=wsg), 2 * 2.0 * N * Mg * Kg),
+                ("down", lambda: g.nvfp4_gemm_prefill(xd, Wd, out=y, workspace=wsd), 2.0 * N * Md * Kd)):
+            ms = time_calls(fn, reps)
             out["shapes"][f"{name} N={N}"] = {"ms": ms, "tflops": flops / (ms * 1e-3) / 1e12}
-        del xg, xd
+        del xg, xd, h, y
     torch.cuda.empty_cache()
     return out
 
@@ -473,18 +486,14 @@ def fp6_measure(dev, layers=4, reps=10):
     N = 2048
     xg = inputs.activations(N, Kg, seed=5, device=dev)
     xd = inputs.activations(N, Kd, seed=6, device=dev)
-    for name, fn, flops in (("gateup", lambda: g.nvfp4_fp6_gateup_swiglu(xg, Ws[0][0], Ws[0][1]),
+    h = torch.empty(N, Mg, dtype=torch.float32, device=dev)
+    y = torch.empty(N, Md, dtype=torch.float32, device=dev)
+    wsg = torch.zeros(g.nvfp4_workspace_bytes(g.NVFP4_OP_FP6_GATEUP_SWIGLU, N, Mg, Kg), dtype=torch.uint8, device=dev)
+    wsd = torch.zeros(g.nvfp4_workspace_bytes(g.NVFP4_OP_FP6_GEMM, N, Md, Kd), dtype=torch.uint8, device=dev)
+    for name, fn, flops in (("gateup", lambda: g.nvfp4_fp6_gateup_swiglu(xg, Ws[0][0], Ws[0][1], out=h, workspace=wsg),
                              2 * 2.0 * N * Mg * Kg),
-                            ("down", lambda: g.nvfp4_fp6_gemm(xd, Ws[0][2]), 2.0 * N * Md * Kd)):
-        fn()
-        torch.cuda.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record()
-        for _ in range(5):
-            fn()
-        e1.record()
-        torch.cuda.synchronize()
-        ms = e0.elapsed_time(e1) / 5
+                            ("down", lambda: g.nvfp4_fp6_gemm(xd, Ws[0][2], out=y, workspace=wsd), 2.0 * N * Md * Kd)):
+        ms = time_calls(fn, 10)
         tf = flops / (ms * 1e-3) / 1e12
         out["prefill"][f"{name} N={N}"] = {"ms": ms, "tflops": tf, "frac": tf / peak_tf if peak_tf else None}
     del Ws
