@@ -386,7 +386,9 @@ def prefill_tflops(dev, reps=10):
                 ("gateup", lambda: g.nvfp4_gateup_swiglu(xg, Wg, Wu, out=h, workspace=wsg), 2 * 2.0 * N * Mg * Kg),
                 ("down", lambda: g.nvfp4_gemm_prefill(xd, Wd, out=y, workspace=wsd), 2.0 * N * Md * Kd)):
             ms = time_calls(fn, reps)
-            out["shapes"][f"{name} N={N}"] = {"ms": ms, "tflops": flops / (ms * 1e-3) / 1e12}
+            tf = flops / (ms * 1e-3) / 1e12
+            out["shapes"][f"{name} N={N}"] = {"ms": ms, "tflops": tf,
+                                               "frac": tf / out["peak_bf16"] if out["peak_bf16"] else None}
         del xg, xd, h, y
     torch.cuda.empty_cache()
     return out
