@@ -26,6 +26,20 @@ def test_exports_every_declared_function(lib):
         assert hasattr(lib, name), f"{name} declared in include/nvfp4.h but not exported"
 
 
+def test_exports_nothing_undeclared(lib):
+    """Every nvfp4_* function the library exports is declared in the header."""
+    import shutil
+    import subprocess
+    nm = shutil.which("nm")
+    if nm is None:
+        pytest.skip("no nm on this host")
+    out = subprocess.run([nm, "-D", "--defined-only", g.library_path()], capture_output=True, text=True,
+                         check=True).stdout
+    exported = {f[2] for f in (line.split() for line in out.splitlines())
+                if len(f) == 3 and f[1] == "T" and f[2].startswith("nvfp4_")}
+    assert exported == set(g.header_functions())
+
+
 def test_python_binding_has_the_c_names():
     for name in g.header_functions():
         assert callable(getattr(g, name)), name
