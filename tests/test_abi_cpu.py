@@ -204,11 +204,11 @@ def test_status_calls_reject_bad_workspaces(lib):
     assert st(0, 256) == binding.NVFP4_ERR_INVALID_ARG
     assert st(FAKE + 8, 256) == binding.NVFP4_ERR_INVALID_ARG
     assert st(FAKE, need - 1) == binding.NVFP4_ERR_INVALID_ARG
-    # every product workspace holds the status word
+    # every product workspace holds the status word (the header promises 256 bytes at least)
     for op, N in ((g.NVFP4_OP_GEMV_SKINNY, 1), (g.NVFP4_OP_GATEUP_SWIGLU, 4), (g.NVFP4_OP_GEMM_PREFILL, 600),
                   (g.NVFP4_OP_GATEUP_SWIGLU, 600), (g.NVFP4_OP_FP6_GEMM, 4), (g.NVFP4_OP_FP6_GEMM, 600),
                   (g.NVFP4_OP_FP6_GATEUP_SWIGLU, 1)):
         for M, K in ((64, 128), (4096, 4096), (333, 4112)):
             if op in (g.NVFP4_OP_FP6_GEMM, g.NVFP4_OP_FP6_GATEUP_SWIGLU) and K % 128:
                 continue
-            assert g.nvfp4_workspace_bytes(op, N, M, K) >= need, (op, N, M, K)
+            assert g.nvfp4_workspace_bytes(op, N, M, K) >= 256 >= need, (op, N, M, K)
