@@ -93,6 +93,10 @@ def load_library():
         lib.nvfp4_gemm_prefill.argtypes = [P, i64, P, P, P, i64, i64, P, i32, P, sz, P]
         lib.nvfp4_gemv_skinny_noalloc.restype = i32
         lib.nvfp4_gemv_skinny_noalloc.argtypes = [P, i64, P, P, P, i64, i64, P, i32, P]
+        lib.nvfp4_noalloc_status.restype = i32
+        lib.nvfp4_noalloc_status.argtypes = [i32, ctypes.POINTER(ctypes.c_uint32), P]
+        lib.nvfp4_noalloc_selftest_wait_timeout.restype = i32
+        lib.nvfp4_noalloc_selftest_wait_timeout.argtypes = [P]
         lib.nvfp4_device_status.restype = i32
         lib.nvfp4_device_status.argtypes = [P, sz, i32, ctypes.POINTER(ctypes.c_uint32), P]
         lib.nvfp4_selftest_wait_timeout.restype = i32
@@ -379,3 +383,20 @@ def nvfp4_gemv_skinny_noalloc(x: torch.Tensor, W: NVFP4Weight, out_dtype=torch.f
                                                   _out_code(y.dtype), _stream(stream))
     _check(st, "nvfp4_gemv_skinny_noalloc")
     return y
+
+
+def nvfp4_noalloc_status(clear: bool = True, stream=None) -> tuple[int, int]:
+    """(status, code) of the status word in the no-allocation array of the
+    current device; with clear=True a nonzero word zero-fills the array."""
+    code = ctypes.c_uint32(0)
+    st = load_library().nvfp4_noalloc_status(int(bool(clear)), ctypes.byref(code), _stream(stream))
+    if st not in (NVFP4_OK, NVFP4_ERR_DEVICE_TIMEOUT):
+        raise NVFP4Error(st, "nvfp4_noalloc_status")
+    return st, code.value
+
+
+def nvfp4_noalloc_selftest_wait_timeout(stream=None) -> None:
+    """Enqueue the bounded-wait self-test against the no-allocation array."""
+    _check(load_library().nvfp4_noalloc_selftest_wait_timeout(_stream(stream)),
+           "nvfp4_noalloc_selftest_wait_timeout")
+

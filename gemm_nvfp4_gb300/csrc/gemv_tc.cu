@@ -1130,6 +1130,11 @@ skinny_tc_kernel(const __grid_constant__ CUtensorMap m_codes0, const __grid_cons
     __syncwarp();
     tc::fence_before_sync();
     __syncthreads();
+    // Cluster-K: no CTA leaves while a peer may still read its shared memory
+    // or arrive on its barriers (even after a wait of either gave up).  Every
+    // wait before this point is bounded, so every thread gets here.
+    if (a.cs > 1)
+        tc::cluster_sync();
     if (warp == 0) {
         tc::fence_after_sync();
         tc::tmem_dealloc(tmem, kTmemCols);

@@ -107,3 +107,14 @@ cudaError_t launch_skinny_tc(const uint16_t *x, int N, int64_t M, int64_t K, con
 size_t skinny_workspace_bytes(int64_t M, int64_t K, int n_weights);
 
 }  // namespace nvfp4
+
+namespace nvfp4 {
+
+// Host-side argument checks of nvfp4_gemv_skinny (everything but the
+// workspace): returns an nvfp4_status; *nothing_to_do is set when the call is
+// valid but enqueues nothing (N == 0 or M == 0).
+int check_skinny_call(const uint16_t *x, int64_t N, const uint8_t *codes, const uint8_t *scales,
+                      const float *tensor_scale, int64_t M, int64_t K, const void *y, int out_dtype,
+                      bool *nothing_to_do);
+
+}  // namespace nvfp4

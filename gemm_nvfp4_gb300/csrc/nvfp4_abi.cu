@@ -105,6 +105,26 @@ int run_products(const uint16_t *x, int64_t N, int64_t M, int64_t K, const uint8
 
 }  // namespace
 
+namespace nvfp4 {
+
+int check_skinny_call(const uint16_t *x, int64_t N, const uint8_t *codes, const uint8_t *scales,
+                      const float *tensor_scale, int64_t M, int64_t K, const void *y, int out_dtype,
+                      bool *nothing_to_do)
+{
+    *nothing_to_do = false;
+    int rc = check_product(x, N, M, K, codes, scales, tensor_scale, y, out_dtype);
+    if (rc != NVFP4_OK)
+        return rc;
+    if (N < 1 || N > kMaxSkinnyN) {
+        *nothing_to_do = N == 0;
+        return N == 0 ? NVFP4_OK : NVFP4_ERR_UNSUPPORTED_SHAPE;
+    }
+    *nothing_to_do = M == 0;
+    return NVFP4_OK;
+}
+
+}  // namespace nvfp4
+
 extern "C" {
 
 const char *nvfp4_status_string(int status)
@@ -315,13 +335,10 @@ int nvfp4_gemv_skinny(const uint16_t *x, int64_t N, const uint8_t *codes, const 
                       const float *tensor_scale, int64_t M, int64_t K, void *y, int out_dtype, void *workspace,
                       size_t workspace_bytes, nvfp4_stream_t stream)
 {
-    int rc = check_product(x, N, M, K, codes, scales, tensor_scale, y, out_dtype);
-    if (rc != NVFP4_OK)
+    bool nothing = false;
+    int rc = nvfp4::check_skinny_call(x, N, codes, scales, tensor_scale, M, K, y, out_dtype, &nothing);
+    if (rc != NVFP4_OK || nothing)
         return rc;
-    if (N < 1 || N > kMaxSkinnyN)
-        return N == 0 ? NVFP4_OK : NVFP4_ERR_UNSUPPORTED_SHAPE;
-    if (M == 0)
-        return NVFP4_OK;
     rc = check_workspace(workspace, workspace_bytes, nvfp4_workspace_bytes(NVFP4_OP_GEMV_SKINNY, N, M, K));
     if (rc != NVFP4_OK)
         return rc;

@@ -295,17 +295,43 @@ int nvfp4_fp6_gateup_swiglu(const uint16_t *x, int64_t N,
  *   - Size limit: returns NVFP4_ERR_WORKSPACE, with nothing enqueued, when the
  *     problem needs more scratch than NVFP4_NOALLOC_SCRATCH_BYTES (that is,
  *     when nvfp4_workspace_bytes(NVFP4_OP_GEMV_SKINNY, N, M, K) exceeds it).
+ *   - Set-up is repeated when the current CUDA context changes (after
+ *     cudaDeviceReset, or from another context on the same device): the
+ *     address is cached together with the context's id.
  *   - Sharing: every call on a device uses the same array.  It starts
  *     zero-filled and every call leaves its split-K counters at zero, as the
  *     skinny workspace contract requires.  Calls whose kernels overlap on the GPU
  *     (different streams without ordering) race on the array; order them on
- *     one stream. */
+ *     one stream.
+ *   - Failures: the array holds the device status word and the split-K
+ *     counters like any skinny workspace.  After a call whose bounded wait gave
+ *     up (see nvfp4_device_status), the counters may be left set and later
+ *     no-allocation calls on that device can return wrong sums: read the word
+ *     with nvfp4_noalloc_status and clear it (which zero-fills the array)
+ *     before the next call.
+ * Arguments are checked exactly as by nvfp4_gemv_skinny, before the size
+ * limit and before any CUDA call. */
 #define NVFP4_NOALLOC_SCRATCH_BYTES ((size_t)8 << 20)
 
 int nvfp4_gemv_skinny_noalloc(const uint16_t *x, int64_t N,
                               const uint8_t *codes, const uint8_t *scales,
                               const float *tensor_scale, int64_t M, int64_t K,
                               void *y, int out_dtype, nvfp4_stream_t stream);
+
+/* Status of the no-allocation array on the current device, for callers that
+ * cannot pass its address to nvfp4_device_status: synchronises `stream`,
+ * stores the status word in *code (if not NULL) and returns NVFP4_OK when it
+ * is zero, else NVFP4_ERR_DEVICE_TIMEOUT.  With clear != 0 and a nonzero word
+ * the whole array is zero-filled on `stream` (cudaMemsetAsync), which resets
+ * the word and any split-K counter a failed call left set.  Allocates nothing;
+ * NVFP4_ERR_CUDA if a CUDA call fails.  The paper has no counterpart. */
+int nvfp4_noalloc_status(int clear, uint32_t *code, nvfp4_stream_t stream);
+
+/* The failure-path self-test of nvfp4_selftest_wait_timeout run against the
+ * no-allocation array of the current device: after 2 s it records code 127 in
+ * the array's status word, which nvfp4_noalloc_status then reports.  Faults
+ * nothing; allocates nothing.  The paper has no counterpart. */
+int nvfp4_noalloc_selftest_wait_timeout(nvfp4_stream_t stream);
 
 /* Device-side failures.  The product calls keep a 32-bit status word at byte
  * NVFP4_STATUS_WORD_OFFSET of their workspace (every product workspace is at

@@ -33,6 +33,10 @@ int main(void)
     int bad = 0;
     uint32_t code = 0;
     const uint16_t *x = NULL;
+    /* a 16-byte-aligned address that is never dereferenced: the calls below
+       return from their host-side checks */
+    static uint16_t fake_buf[16];
+    const uint16_t *fake16 = (const uint16_t *)(((uintptr_t)fake_buf + 15) & ~(uintptr_t)15);
     size_t ws;
 
     bad |= nvfp4_version() < 100;
@@ -50,9 +54,14 @@ int main(void)
                   "device status without a workspace");
     /* a problem whose scratch exceeds the fixed array is refused before any CUDA call */
     bad |= nvfp4_workspace_bytes(NVFP4_OP_GEMV_SKINNY, 1, 64, (int64_t)1 << 20) <= NVFP4_NOALLOC_SCRATCH_BYTES;
+    bad |= expect(nvfp4_gemv_skinny_noalloc(fake16, 1, (const uint8_t *)fake16, (const uint8_t *)fake16,
+                                            (const float *)fake16, 64, (int64_t)1 << 20, (void *)fake16,
+                                            NVFP4_OUT_F32, NULL),
+                  NVFP4_ERR_WORKSPACE, "no-allocation call beyond its scratch");
+    /* bad arguments are reported as by nvfp4_gemv_skinny, before the size limit */
     bad |= expect(nvfp4_gemv_skinny_noalloc(x, 1, NULL, NULL, NULL, 64, (int64_t)1 << 20, NULL, NVFP4_OUT_F32,
                                             NULL),
-                  NVFP4_ERR_WORKSPACE, "no-allocation call beyond its scratch");
+                  NVFP4_ERR_INVALID_ARG, "no-allocation call with null pointers");
     printf(bad ? "FAILED\n" : "ok\n");
     return bad;
 }

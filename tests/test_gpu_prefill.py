@@ -104,9 +104,10 @@ def test_prefill_gateup_full_size_sampled(N):
     assert_close(got, h_ref, swiglu_tol(h_ref, g_ref, u_ref, Ag, Au), f"gate/up prefill N={N}")
 
 
-@pytest.mark.parametrize("N", [512, 8192])
+@pytest.mark.parametrize("N", [512, 2048, 8192])
 def test_prefill_down_full_size_sampled(N):
-    """Full-size prefill down projection (17408 -> 5120), fresh bf16 inputs."""
+    """Full-size prefill down projection (17408 -> 5120), fresh bf16 inputs, at
+    every token count the benchmark times (N = 2048 runs the 192-token tile)."""
     M, K = inputs.LAYER_27B.shapes()["down"]
     w = inputs.weights(M, K, seed=400, device=DEV)
     x = inputs.activations(N, K, seed=401, device=DEV)
@@ -116,8 +117,8 @@ def test_prefill_down_full_size_sampled(N):
     torch.cuda.synchronize()
     assert timeout_flag(ws) == 0
     ref_w = oracle.quantize(w.cpu().numpy())
-    rows = _sample(16, M, N, [0, 127, 128, M - 1])
-    toks = _sample(5, N, N + 2, [0, 255, 256, N - 1])
+    rows = _sample(24, M, N, [0, 127, 128, M - 1])
+    toks = _sample(8, N, N + 2, [0, 191, 192, 255, 256, N - 1])
     y_ref, A = oracle.gemv(bf16_bits(x), *ref_w, rows=rows, tokens=toks)
     got = to_np(y)[np.ix_(toks, rows)]
     assert_close(got, y_ref, gemv_tol(y_ref, A, torch.bfloat16), f"down prefill N={N}")

@@ -728,3 +728,39 @@ def test_fp6_pack_and_dequantize_helpers():
         assert all(d[m, k] == e2m3_ref(cc[k]) * 2.0 ** (int(s[m, 0]) - 127) for k in range(128))
     with pytest.raises(ValueError):
         oracle.fp6_quantize(np.zeros((1, 64), np.float32))
+
+
+def test_dequantize_pinned_by_hand_block_and_closed_form():
+    """oracle.dequantize against the hand-worked block (its printed E2M1 values
+    times the decoded scale 448 and the tensor scale), against the E2M1 list and
+    PyTorch's E4M3 decode on a two-block row (each block its own scale byte,
+    both nibble orders), and against a one-hot product of the C oracle."""
+    ts = float(np.float32(np.float32(0.6) / np.float32(2688.0)))
+    codes_hex = "7 D 3 1 0 F 5 A 3 4 E 1 7 8 5 C".split()
+    values = [6, -3, 1.5, 0.5, 0, -6, 3, -1, 1.5, 2, -4, 0.5, 6, -0.0, 3, -2]
+    c = [int(h, 16) for h in codes_hex]
+    packed = np.array([[c[2 * j] | (c[2 * j + 1] << 4) for j in range(8)]], np.uint8)
+    d = oracle.dequantize(packed, np.array([[0x7E]], np.uint8), ts)
+    assert d.shape == (1, 16)
+    assert [float(v) for v in d[0]] == [v * 448.0 * ts for v in values]
+    assert math.copysign(1.0, d[0, 13]) == -1.0  # code 8 is -0
+    # two blocks with different scale bytes; every code in both nibble positions
+    e4 = e4m3_torch_table()
+    row = np.zeros((1, 16), np.uint8)
+    for j in range(16):
+        row[0, j] = (j & 15) | (((15 - j) & 15) << 4)
+    sc = np.array([[0x31, 0x5B]], np.uint8)
+    d2 = oracle.dequantize(row, sc, 1.0)
+    for k in range(32):
+        byte = int(row[0, k // 2])
+        code = byte & 15 if k % 2 == 0 else byte >> 4
+        assert d2[0, k] == e2m1_ref(code) * float(e4[sc[0, k // 16]])
+    # the C oracle's product with a one-hot activation reads the same weight
+    w = np.random.default_rng(5).standard_normal((3, 64)).astype(np.float32) * 0.02
+    qc, qs, qts = oracle.quantize(w)
+    dq = oracle.dequantize(qc, qs, qts)
+    for k in (0, 17, 63):
+        x = np.zeros((1, 64), np.uint16)
+        x[0, k] = 0x3F80  # bf16 1.0
+        y, _ = oracle.gemv(x, qc, qs, qts)
+        assert np.array_equal(y[0], dq[:, k])
