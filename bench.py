@@ -62,6 +62,8 @@ def parse():
     ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--no-ingest", action="store_true")
     ap.add_argument("--no-fp6", action="store_true")
+    ap.add_argument("--no-streams", action="store_true",
+                    help="skip the other decode workloads, the single-matrix stream and the chains")
     ap.add_argument("--fp6-only", action="store_true",
                     help="print the FP6 measurement (27B-class MLP stream and prefill) and exit")
     ap.add_argument("--ingest-only", action="store_true",
@@ -175,7 +177,7 @@ class ClockSampler:
 class LayerStream:
     """Rotating NVFP4 layers + per-layer activations and outputs on one GPU."""
 
-    def __init__(self, workload: str, device, n_layers=None):
+    def __init__(self, workload: str, device, n_layers=None, layers_from=None):
         import gemm_nvfp4_gb300 as g
         from gemm_nvfp4_gb300 import inputs
         self.g = g
@@ -186,20 +188,26 @@ class LayerStream:
         self.workload = workload
         shapes = self.shape.shapes()
         self.shapes = shapes
-        # base layer: quantise each matrix once on the GPU, then replicate
-        base = {}
-        for name, (M, K) in shapes.items():
-            w = inputs.weights(M, K, seed=inputs.matrix_seed(name), heavy_tail=heavy, device=device)
-            base[name] = g.nvfp4_quantize(w)
-            del w
-        torch.cuda.synchronize()
-        self.layers = []
-        for _ in range(self.n_layers):
-            layer = {}
-            for name, W in base.items():
-                layer[name] = g.NVFP4Weight(W.codes.clone(), W.scales.clone(), W.tensor_scale.clone())
-            self.layers.append(layer)
-        del base
+        self.device = device
+        if layers_from is not None:
+            # same weights as another stream of this layer shape (another N)
+            self.layers = layers_from.layers
+            self.n_layers = layers_from.n_layers
+        else:
+            # base layer: quantise each matrix once on the GPU, then replicate
+            base = {}
+            for name, (M, K) in shapes.items():
+                w = inputs.weights(M, K, seed=inputs.matrix_seed(name), heavy_tail=heavy, device=device)
+                base[name] = g.nvfp4_quantize(w)
+                del w
+            torch.cuda.synchronize()
+            self.layers = []
+            for _ in range(self.n_layers):
+                layer = {}
+                for name, W in base.items():
+                    layer[name] = g.NVFP4Weight(W.codes.clone(), W.scales.clone(), W.tensor_scale.clone())
+                self.layers.append(layer)
+            del base
         # activations per layer and matrix (bf16 N(0,1), the step's inputs) and
         # outputs, as views into one input and one output buffer so the
         # end-to-end run moves each with a single copy
@@ -284,6 +292,57 @@ class LayerStream:
             self.run_all(only)
         torch.cuda.synchronize()
         return graph
+
+    def stream_jobs(self):
+        """The step as one product list: every call of every layer on its own
+        activations and outputs (the same buffers as the per-call step)."""
+        g, jobs = self.g, []
+        for li in range(self.n_layers):
+            L, X, Y = self.layers[li], self.x[li], self.y[li]
+            jobs.append(g.SkinnyJob(L["qkv"], Y["qkv"], x=X["qkv"]))
+            jobs.append(g.SkinnyJob(L["o"], Y["o"], x=X["o"]))
+            jobs.append(g.SkinnyJob((L["gate"], L["up"]), Y["gate"], x=X["gate"]))
+            jobs.append(g.SkinnyJob(L["down"], Y["down"], x=X["down"]))
+        return jobs
+
+    def chain_jobs(self):
+        """The step as a dependent decode chain: per layer QKV reads the previous
+        layer's down output (layer 0: its own input), O reads a caller buffer
+        (attention's output, which this library does not compute), gate/up +
+        SwiGLU reads O's output and down reads the SwiGLU output; the outputs a
+        later job reads are bf16."""
+        g, jobs = self.g, []
+        N, dev = self.N, self.device
+        hidden, ffn = self.shapes["o"][0], self.shapes["gate"][0]
+        self.chain_out = []
+        prev = None
+        for li in range(self.n_layers):
+            L, X, Y = self.layers[li], self.x[li], self.y[li]
+            o_out = torch.empty(N, hidden, dtype=torch.bfloat16, device=dev)
+            h_out = torch.empty(N, ffn, dtype=torch.bfloat16, device=dev)
+            d_out = torch.empty(N, hidden, dtype=torch.bfloat16, device=dev)
+            self.chain_out += [o_out, h_out, d_out]
+            if prev is None:
+                jobs.append(g.SkinnyJob(L["qkv"], Y["qkv"], x=X["qkv"]))
+            else:
+                jobs.append(g.SkinnyJob(L["qkv"], Y["qkv"], input=prev))
+            jobs.append(g.SkinnyJob(L["o"], o_out, x=X["o"]))
+            jobs.append(g.SkinnyJob((L["gate"], L["up"]), h_out, input=len(jobs) - 1))
+            jobs.append(g.SkinnyJob(L["down"], d_out, input=len(jobs) - 1))
+            prev = len(jobs) - 1
+        return jobs
+
+    def chain_bytes(self):
+        """Algorithmic bytes of the chain step: the weights once, every job's
+        activations read and outputs written (bf16 where a later job reads them)."""
+        N = self.N
+        hidden, ffn, qkv = self.shapes["o"][0], self.shapes["gate"][0], self.shapes["qkv"][0]
+        per_layer = (sum(M * K // 2 + M * K // 16 for M, K in self.shapes.values())
+                     + N * hidden * 2 + N * qkv * 4          # QKV: x in, fp32 out
+                     + N * hidden * 2 + N * hidden * 2       # O
+                     + N * hidden * 2 + N * ffn * 2          # gate/up
+                     + N * ffn * 2 + N * hidden * 2)         # down
+        return self.n_layers * per_layer
 
     def host_io(self):
         """Pinned host copies of the step's inputs and outputs (for e2e)."""
@@ -627,6 +686,85 @@ def run_reference(args, world, rank):
     print(json.dumps(line), flush=True)
 
 
+def capture_graph(fn):
+    """Capture fn(stream) once as a CUDA graph (after one eager call)."""
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        fn(s)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        fn(s)
+    torch.cuda.synchronize()
+    return graph
+
+
+def time_plan(plan, steps, warmup):
+    import gemm_nvfp4_gb300 as g
+    graph = capture_graph(lambda s: g.nvfp4_stream_run(plan, stream=s))
+    ms = time_graph(graph, steps, warmup, 1)
+    st_, code = g.nvfp4_device_status(plan.buffer, clear=False)
+    assert st_ == g.NVFP4_OK, f"a stream wait gave up (code {code})"
+    return ms
+
+
+def stream_entry(nbytes, ms, N, peak, layers=None):
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    d = {"ms": ms, "gbs": gbs, "frac": gbs / peak, "bytes": nbytes}
+    if layers is not None:
+        d["tokens_per_s_per_stream"] = N / (ms * 1e-3)
+    return d
+
+
+def more_streams(dev, st0, args, peak):
+    """The other decode workloads (27B-class streams at N = 1/4/9/16, the
+    deep-verify ones with heavy-tailed weights and outlier tokens), the single
+    4096 x 4096 matrix over 32 rotating copies at N = 1, and the dependent
+    chains, each as one product list per step."""
+    import gemm_nvfp4_gb300 as g
+    from gemm_nvfp4_gb300 import inputs
+    streams, chains = {}, {}
+    steps, warm = max(args.steps, 10), max(args.warmup, 3)
+    # the default workload's chain
+    plan = g.nvfp4_stream_plan(st0.chain_jobs(), st0.N)
+    chains[st0.workload] = stream_entry(st0.chain_bytes(), time_plan(plan, steps, warm), st0.N, peak, True)
+    del plan
+    base = {}
+    for wl in ("dense27b-n1", "dense27b-n4", "dense27b-n9", "dense27b-n16"):
+        if wl == st0.workload:
+            continue
+        heavy = WORKLOADS[wl][3]
+        st = LayerStream(wl, dev, layers_from=base.get(heavy))
+        base.setdefault(heavy, st)
+        plan = g.nvfp4_stream_plan(st.stream_jobs(), st.N)
+        streams[wl] = stream_entry(st.step_bytes(), time_plan(plan, steps, warm), st.N, peak, True)
+        del plan
+        if wl in ("dense27b-n1", "dense27b-n4"):
+            plan = g.nvfp4_stream_plan(st.chain_jobs(), st.N)
+            chains[wl] = stream_entry(st.chain_bytes(), time_plan(plan, steps, warm), st.N, peak, True)
+            del plan
+        if st is not base.get(heavy):
+            del st
+    del base
+    torch.cuda.empty_cache()
+    # the single NVFP4 matrix (4096 x 4096, seed 0) over 32 rotating copies, N = 1
+    M = K = 4096
+    W = g.nvfp4_quantize(inputs.weights(M, K, seed=0, device=dev))
+    jobs = []
+    for c in range(32):
+        Wc = g.NVFP4Weight(W.codes.clone(), W.scales.clone(), W.tensor_scale.clone())
+        x = inputs.activations(1, K, seed=1 + c, device=dev)
+        jobs.append(g.SkinnyJob(Wc, torch.empty(1, M, dtype=torch.float32, device=dev), x=x))
+    plan = g.nvfp4_stream_plan(jobs, 1)
+    nbytes = 32 * (M * K // 2 + M * K // 16 + K * 2 + M * 4)
+    streams["single4096-n1"] = stream_entry(nbytes, time_plan(plan, steps, warm), 1, peak)
+    streams["single4096-n1"]["copies"] = 32
+    del plan, jobs, W
+    torch.cuda.empty_cache()
+    return streams, chains
+
+
 def main():
     args = parse()
     world, rank, local = dist_setup(args)
@@ -645,15 +783,27 @@ def main():
     if args.fp6_only:
         print(json.dumps(fp6_measure(dev)), flush=True)
         return
+    import gemm_nvfp4_gb300 as g
     st = LayerStream(args.workload, dev, args.layers)
-    graph = st.capture(only=args.only)
-    dom_graph = st.capture(only="gateup")
+    hbm_peak, _, peak_kind = read_peaks()
+    if args.only is None:
+        # the step: every call of every layer as one product list, one launch
+        plan = g.nvfp4_stream_plan(st.stream_jobs(), st.N)
+        graph = capture_graph(lambda s: g.nvfp4_stream_run(plan, stream=s))
+        launches_per_step = 1
+    else:
+        plan = None
+        graph = st.capture(only=args.only)
+        launches_per_step = st.launches_per_step(args.only)
+    calls_graph = st.capture(only=args.only) if args.only is None else None
 
     with ClockSampler(torch.cuda.current_device()) as clk:
         ms = time_graph(graph, args.steps, args.warmup, world)
-        dom_ms = time_graph(dom_graph, args.steps, args.warmup, world)
+        calls_ms = time_graph(calls_graph, args.steps, args.warmup, world) if calls_graph is not None else None
     clocks = clk.summary()
     ms = max_over_ranks(ms, world)
+    if plan is not None:
+        assert g.nvfp4_device_status(plan.buffer, clear=False)[0] == g.NVFP4_OK, "a stream wait gave up"
 
     # end to end: pinned host inputs -> device, graph, device -> pinned host outputs
     xs, ys = st.host_io()
@@ -683,11 +833,19 @@ def main():
     step_bytes = st.step_bytes(args.only)
     value = world * step_bytes / (ms * 1e-3) / 1e9
     e2e_value = world * step_bytes / (e2e_ms * 1e-3) / 1e9
-    hbm_peak, _, peak_kind = read_peaks()
-    dom_bytes = st.call_bytes("gateup")
-    dom_per_launch_ms = dom_ms / st.n_layers
-    achieved = dom_bytes / (dom_per_launch_ms * 1e-3) / 1e9
-    traffic = read_traffic(f"skinny_tc_kernel<2> {args.workload}")
+    # the dominant kernel is the whole step's single launch: its algorithmic
+    # bytes per launch over its CUDA-event time on the replay stream
+    achieved = step_bytes / (ms * 1e-3) / 1e9
+    traffic = read_traffic(f"stream_kernel {args.workload}")
+    calls = None
+    if calls_ms is not None:
+        cg = step_bytes / (calls_ms * 1e-3) / 1e9
+        calls = {"what": "the same step as separate calls (prep + main kernel per call, PDL-chained, "
+                         "one CUDA graph)", "ms": calls_ms, "gbs": cg, "frac": cg / hbm_peak,
+                 "launches_per_step": st.launches_per_step()}
+    streams = chains = None
+    if not args.no_streams and args.only is None and world == 1:
+        streams, chains = more_streams(dev, st, args, hbm_peak)
 
     prefill = prefill_tflops(dev) if not args.no_prefill else None
     ingest = ingest_gbs(dev) if not args.no_ingest else None
@@ -708,15 +866,18 @@ def main():
                        "l2": "inputs larger than L2 (rotating layers)", "graph": "one CUDA graph per step",
                        "tokens_per_s_per_stream": world * st.N / (ms * 1e-3),
                        "frac_of_8TBs": value / world / 8000.0},
-            "roofline": {"bound": "hbm", "kernel": "nvfp4_gateup_swiglu (fused gate/up + SwiGLU)",
+            "roofline": {"bound": "hbm", "kernel": "stream_kernel (the step's product list, one launch)",
                          "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
                          "frac": achieved / hbm_peak if hbm_peak else None, "traffic": traffic,
                          "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
                          else "fallback 6.8 TB/s",
-                         "timing": f"{st.n_layers} back-to-back calls captured alone, CUDA events"},
+                         "timing": "CUDA events around graph replays of the launch on the replay stream"},
+            "calls": calls,
+            "streams": streams,
+            "chain": chains,
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-            "gpu_launches": st.launches_per_step(args.only) * args.steps,
+            "gpu_launches": launches_per_step * args.steps,
             "clocks": clocks,
             "prefill": prefill,
             "ingest": ingest,

@@ -14,7 +14,8 @@ from .binding import (NVFP4_ERR_DEVICE_TIMEOUT, NVFP4_OK, NVFP4_STATUS_WORD_OFFS
                       header_functions, library_path, load_library, nvfp4_gateup_swiglu,
                       nvfp4_blocked_scale_bytes, nvfp4_gemm_prefill, nvfp4_gemv_skinny,
                       nvfp4_gemv_skinny_noalloc, nvfp4_import_blocked_scales, nvfp4_noalloc_selftest_wait_timeout,
-                      nvfp4_noalloc_status, nvfp4_quantize,
+                      nvfp4_noalloc_status, SkinnyJob, StreamPlan, nvfp4_stream_plan, nvfp4_stream_plan_bytes,
+                      nvfp4_stream_run, nvfp4_quantize,
                       nvfp4_quantize_bf16, nvfp4_selftest_wait_timeout, nvfp4_status_string, nvfp4_version,
                       nvfp4_workspace_bytes)
 
@@ -29,4 +30,5 @@ __all__ = [
     "NVFP4_OUT_F32", "NVFP4_OUT_BF16",
     "nvfp4_device_status", "nvfp4_selftest_wait_timeout", "NVFP4_OK", "NVFP4_ERR_DEVICE_TIMEOUT",
     "NVFP4_STATUS_WORD_OFFSET", "nvfp4_noalloc_status", "nvfp4_noalloc_selftest_wait_timeout",
+    "SkinnyJob", "StreamPlan", "nvfp4_stream_plan", "nvfp4_stream_plan_bytes", "nvfp4_stream_run",
 ]

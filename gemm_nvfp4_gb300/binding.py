@@ -40,6 +40,14 @@ _lock = threading.Lock()
 _lib = None
 
 
+class SkinnyJobC(ctypes.Structure):
+    """nvfp4_skinny_job of include/nvfp4.h."""
+    _fields_ = [("x", ctypes.c_void_p), ("x_ld", ctypes.c_int64), ("input", ctypes.c_int32),
+                ("n_weights", ctypes.c_int32), ("codes", ctypes.c_void_p * 2), ("scales", ctypes.c_void_p * 2),
+                ("tensor_scale", ctypes.c_void_p * 2), ("M", ctypes.c_int64), ("K", ctypes.c_int64),
+                ("y", ctypes.c_void_p), ("out_dtype", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+
+
 class NVFP4Error(RuntimeError):
     def __init__(self, status: int, where: str):
         self.status = status
@@ -93,6 +101,12 @@ def load_library():
         lib.nvfp4_gemm_prefill.argtypes = [P, i64, P, P, P, i64, i64, P, i32, P, sz, P]
         lib.nvfp4_gemv_skinny_noalloc.restype = i32
         lib.nvfp4_gemv_skinny_noalloc.argtypes = [P, i64, P, P, P, i64, i64, P, i32, P]
+        lib.nvfp4_stream_plan_bytes.restype = sz
+        lib.nvfp4_stream_plan_bytes.argtypes = [ctypes.POINTER(SkinnyJobC), i32, i64]
+        lib.nvfp4_stream_plan.restype = i32
+        lib.nvfp4_stream_plan.argtypes = [ctypes.POINTER(SkinnyJobC), i32, i64, P, sz, P]
+        lib.nvfp4_stream_run.restype = i32
+        lib.nvfp4_stream_run.argtypes = [P, sz, P]
         lib.nvfp4_noalloc_status.restype = i32
         lib.nvfp4_noalloc_status.argtypes = [i32, ctypes.POINTER(ctypes.c_uint32), P]
         lib.nvfp4_noalloc_selftest_wait_timeout.restype = i32
@@ -399,4 +413,82 @@ def nvfp4_noalloc_selftest_wait_timeout(stream=None) -> None:
     """Enqueue the bounded-wait self-test against the no-allocation array."""
     _check(load_library().nvfp4_noalloc_selftest_wait_timeout(_stream(stream)),
            "nvfp4_noalloc_selftest_wait_timeout")
+
+
+# ---------------------------------------------------------------------------
+# Product lists in one launch (nvfp4_stream_plan / nvfp4_stream_run)
+# ---------------------------------------------------------------------------
+
+@dataclass
+class SkinnyJob:
+    """One product of a list: y = x . W^T, or silu(x . Wg^T) * (x . Wu^T) when
+    W is a (gate, up) pair.  x is a bf16 [N, K] tensor (rows may be strided),
+    or None with `input` the index of an earlier job whose bf16 output is x."""
+    W: object                       # NVFP4Weight, or (gate, up) NVFP4Weights
+    y: torch.Tensor                 # [N, M] float32 or bfloat16
+    x: torch.Tensor | None = None
+    input: int = -1
+
+    def weights(self):
+        return list(self.W) if isinstance(self.W, (tuple, list)) else [self.W]
+
+
+def _job_structs(jobs):
+    arr = (SkinnyJobC * len(jobs))()
+    for i, j in enumerate(jobs):
+        ws = j.weights()
+        c = arr[i]
+        if j.x is not None:
+            if j.x.dtype != torch.bfloat16 or j.x.stride(1) != 1:
+                raise ValueError("job activations must be bf16 with unit stride along K")
+            c.x = j.x.data_ptr()
+            c.x_ld = j.x.stride(0)
+        c.input = int(j.input)
+        c.n_weights = len(ws)
+        for k, W in enumerate(ws):
+            c.codes[k] = W.codes.data_ptr()
+            c.scales[k] = W.scales.data_ptr()
+            c.tensor_scale[k] = W.tensor_scale.data_ptr()
+        c.M = ws[0].M
+        c.K = ws[0].K
+        c.y = j.y.data_ptr()
+        c.out_dtype = _out_code(j.y.dtype)
+    return arr
+
+
+class StreamPlan:
+    """A plan buffer (device) and the tensors its jobs point to (kept alive)."""
+
+    def __init__(self, buffer: torch.Tensor, jobs, N: int):
+        self.buffer = buffer
+        self.jobs = list(jobs)
+        self.N = N
+
+    def nbytes(self) -> int:
+        return self.buffer.numel()
+
+
+def nvfp4_stream_plan_bytes(jobs, N: int) -> int:
+    arr = _job_structs(jobs)
+    return load_library().nvfp4_stream_plan_bytes(arr, len(jobs), int(N))
+
+
+def nvfp4_stream_plan(jobs, N: int, device=None, stream=None) -> StreamPlan:
+    """Build the device plan of a job list (synchronises the stream)."""
+    arr = _job_structs(jobs)
+    lib = load_library()
+    need = lib.nvfp4_stream_plan_bytes(arr, len(jobs), int(N))
+    if need == 0:
+        raise NVFP4Error(NVFP4_ERR_INVALID_ARG, "nvfp4_stream_plan_bytes")
+    dev = device or jobs[0].y.device
+    buf = torch.empty(need, dtype=torch.uint8, device=dev)
+    st = lib.nvfp4_stream_plan(arr, len(jobs), int(N), _ptr(buf), need, _stream(stream))
+    _check(st, "nvfp4_stream_plan")
+    return StreamPlan(buf, jobs, int(N))
+
+
+def nvfp4_stream_run(plan: StreamPlan, stream=None) -> None:
+    """Run every job of a plan (one launch, asynchronous)."""
+    st = load_library().nvfp4_stream_run(_ptr(plan.buffer), plan.nbytes(), _stream(stream))
+    _check(st, "nvfp4_stream_run")
 

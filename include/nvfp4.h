@@ -228,6 +228,72 @@ int nvfp4_gemm_prefill(const uint16_t *x, int64_t N,
                        void *workspace, size_t workspace_bytes, nvfp4_stream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * Skinny product lists in one launch: the decode step of a stack of layers.
+ *
+ * A decode step multiplies every weight matrix of every layer by the same few
+ * tokens; at N = 1 one matrix streams in a few microseconds, so per-launch
+ * costs would dominate.  A list of products (jobs) runs as one persistent
+ * launch in which every SM streams the weights of all jobs back to back (the
+ * one-replay-per-token decode of bw24 README, CUDA-graph decode, and the
+ * persistent MLP chain of qwentin README, "How it works").  A job's
+ * activations are a caller buffer or the bf16 output of an earlier job of the
+ * list, so a dependent chain (O -> gate/up + SwiGLU -> down -> next layer)
+ * runs inside the launch: a job that reads an earlier output, and every job
+ * after it, waits until all jobs before it are final.
+ *
+ * Results: each job's output is y = x . dequant(W)^T (or silu(g) * u), within
+ * the accuracy bound of nvfp4_gemv_skinny; repeated runs of a plan give
+ * bit-identical outputs.  The split of K across SMs follows the whole list,
+ * so bits may differ from the same product made by nvfp4_gemv_skinny.
+ * Requirements: N = 1..16 tokens for every job; K % 256 == 0.
+ * ------------------------------------------------------------------------- */
+
+/* One product of a list. */
+typedef struct {
+    const uint16_t *x;          /* device bf16 [N][x_ld] activations (input == -1) */
+    int64_t x_ld;               /* elements between token rows of x; 0 means K (multiple of 8) */
+    int32_t input;              /* -1: x as given; j >= 0: x is the output of job j of the list
+                                   (j earlier than this job; that output must be bf16, with
+                                   M >= this K and M % 8 == 0; token n's x is its row n) */
+    int32_t n_weights;          /* 1: y = x . W^T;  2: y = silu(x . Wg^T) * (x . Wu^T) */
+    const uint8_t *codes[2];    /* device NVFP4 weights [M][K/2] ([0] gate, [1] up) */
+    const uint8_t *scales[2];   /* device E4M3 block scales [M][K/16] */
+    const float *tensor_scale[2]; /* device fp32 tensor scales */
+    int64_t M, K;
+    void *y;                    /* device output [N][M], fp32 or bf16 bits */
+    int32_t out_dtype;          /* NVFP4_OUT_F32 or NVFP4_OUT_BF16 */
+    int32_t reserved;           /* set to 0 */
+} nvfp4_skinny_job;
+
+/* Device bytes of the plan of `jobs` (0 if the list is invalid).  Host only;
+ * an upper bound that holds on any device. */
+size_t nvfp4_stream_plan_bytes(const nvfp4_skinny_job *jobs, int n_jobs, int64_t N);
+
+/* Build the plan of a job list for the current device in `plan` (device
+ * memory of nvfp4_stream_plan_bytes bytes, 256-byte aligned, owned by the
+ * caller): the jobs' tensor maps, the split of every job's work across the
+ * SMs, and the run state, zero-filled.  Copies from the host and
+ * synchronises `stream`, so build plans before any stream capture.  The
+ * plan holds the device pointers of the jobs: their buffers must stay where
+ * they are for as long as the plan is run.
+ * Errors: NVFP4_ERR_INVALID_ARG (null, misaligned, bad enum, an input that is
+ * not an earlier bf16 output wide enough), NVFP4_ERR_UNSUPPORTED_SHAPE (N
+ * outside 1..16, K % 256 != 0), NVFP4_ERR_WORKSPACE (plan_bytes too small),
+ * NVFP4_ERR_CUDA. */
+int nvfp4_stream_plan(const nvfp4_skinny_job *jobs, int n_jobs, int64_t N,
+                      void *plan, size_t plan_bytes, nvfp4_stream_t stream);
+
+/* Run every job of a plan: one kernel launch, asynchronous on `stream`,
+ * capturable in a CUDA graph.  Runs of one plan must be ordered on one
+ * stream; the plan is its own workspace and keeps the device status word at
+ * byte NVFP4_STATUS_WORD_OFFSET (read it with nvfp4_device_status(plan, ...)).
+ * After a run whose bounded wait gave up, build the plan again before the
+ * next run.  NVFP4_ERR_INVALID_ARG for a null or misaligned plan or
+ * plan_bytes below 256; a plan built on a device with another SM count is
+ * refused on the device (status word code 31). */
+int nvfp4_stream_run(void *plan, size_t plan_bytes, nvfp4_stream_t stream);
+
+/* ---------------------------------------------------------------------------
  * FP6 E2M3 block-scaled weights: the 6-bit weight tier the pages use for
  * quality (qwentin README, "Highlights" and "How it works": E2M3 weights with
  * 128-wide block scales on the block-scaled tensor-core MMA).  Same products,

@@ -212,3 +212,63 @@ def test_status_calls_reject_bad_workspaces(lib):
             if op in (g.NVFP4_OP_FP6_GEMM, g.NVFP4_OP_FP6_GATEUP_SWIGLU) and K % 128:
                 continue
             assert g.nvfp4_workspace_bytes(op, N, M, K) >= 256 >= need, (op, N, M, K)
+
+
+def _job(x=FAKE, inp=-1, nw=1, M=256, K=512, out=1, codes=FAKE, y=FAKE, x_ld=0):
+    j = binding.SkinnyJobC()
+    j.x = x
+    j.x_ld = x_ld
+    j.input = inp
+    j.n_weights = nw
+    for k in range(min(nw, 2)):
+        j.codes[k] = codes
+        j.scales[k] = FAKE
+        j.tensor_scale[k] = FAKE
+    j.M, j.K, j.y, j.out_dtype = M, K, y, out
+    return j
+
+
+def _arr(*jobs):
+    a = (binding.SkinnyJobC * len(jobs))()
+    for i, j in enumerate(jobs):
+        a[i] = j
+    return a
+
+
+def test_stream_plan_size_and_checks_on_the_host(lib):
+    """nvfp4_stream_plan_bytes is host arithmetic; bad lists are refused by it
+    and by nvfp4_stream_plan before any CUDA call."""
+    size = lambda a, N=4: lib.nvfp4_stream_plan_bytes(a, len(a), N)
+    ok = _arr(_job(), _job(inp=0, K=256), _job(nw=2, M=512, K=256, inp=1, out=1), _job(inp=2, M=128, K=512))
+    n_ok = size(ok)
+    assert n_ok >= 256 and n_ok % 256 == 0
+    assert size(ok, N=16) >= n_ok            # more tokens, more statistics items
+    assert size(ok, N=0) == 0 and size(ok, N=17) == 0
+    bad = [
+        _arr(_job(inp=0)),                            # job 0 cannot read an output
+        _arr(_job(out=0), _job(inp=0, K=256)),        # input is not bf16
+        _arr(_job(M=128), _job(inp=0, K=256)),        # input narrower than K
+        _arr(_job(M=260), _job(inp=0, K=256)),        # input row stride not a multiple of 8 elements
+        _arr(_job(K=272)),                            # K % 256 != 0
+        _arr(_job(nw=3)),
+        _arr(_job(out=2)),
+        _arr(_job(x=0)),                              # null activations
+        _arr(_job(x=FAKE + 8)),                       # misaligned activations
+        _arr(_job(codes=FAKE + 4)),                   # misaligned codes
+        _arr(_job(y=0)),
+        _arr(_job(x_ld=520)),                         # a valid row stride (>= K, multiple of 8)
+    ]
+    for a in bad[:-1]:
+        assert size(a) == 0
+    assert size(bad[-1]) > 0                      # 520 is a valid row stride
+    assert size(_arr(_job(x_ld=500))) == 0        # a row stride below K
+    plan = lambda a, p, n: lib.nvfp4_stream_plan(a, len(a), 4, _P(p), n, None)
+    assert plan(ok, FAKE, n_ok - 1) == binding.NVFP4_ERR_WORKSPACE
+    assert plan(ok, 0, n_ok) == binding.NVFP4_ERR_INVALID_ARG
+    assert plan(ok, FAKE + 16, n_ok) == binding.NVFP4_ERR_INVALID_ARG  # the plan must be 256-byte aligned
+    assert plan(bad[0], FAKE, n_ok) == binding.NVFP4_ERR_INVALID_ARG
+    assert lib.nvfp4_stream_plan(ok, len(ok), 17, _P(FAKE), n_ok, None) == binding.NVFP4_ERR_UNSUPPORTED_SHAPE
+    run = lambda p, n: lib.nvfp4_stream_run(_P(p), n, None)
+    assert run(0, n_ok) == binding.NVFP4_ERR_INVALID_ARG
+    assert run(FAKE + 16, n_ok) == binding.NVFP4_ERR_INVALID_ARG
+    assert run(FAKE, 255) == binding.NVFP4_ERR_INVALID_ARG
