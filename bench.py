@@ -72,6 +72,9 @@ def parse():
     ap.add_argument("--layers", type=int, default=None, help="override the number of layers in the stream")
     ap.add_argument("--only", choices=["qkv", "o", "gateup", "down"], default=None,
                     help="time only this call kind of every layer")
+    ap.add_argument("--profile-stream", action="store_true",
+                    help="three launches of the workload's product list over --layers layers (default 4) and exit "
+                         "(for ncu captures)")
     ap.add_argument("--prefill-profile", default=None, metavar="gateup:N|down:N",
                     help="run three prefill calls of one 27B-class shape and exit (for ncu captures)")
     return ap.parse_args()
@@ -776,6 +779,15 @@ def main():
     dev = torch.device("cuda", torch.cuda.current_device())
     if args.prefill_profile:
         prefill_profile(dev, args.prefill_profile)
+        return
+    if args.profile_stream:
+        import gemm_nvfp4_gb300 as g
+        st = LayerStream(args.workload, dev, args.layers or 4)
+        plan = g.nvfp4_stream_plan(st.stream_jobs(), st.N)
+        for _ in range(3):
+            g.nvfp4_stream_run(plan)
+        torch.cuda.synchronize()
+        assert g.nvfp4_device_status(plan.buffer, clear=False)[0] == g.NVFP4_OK
         return
     if args.ingest_only:
         print(json.dumps(ingest_gbs(dev)), flush=True)

@@ -63,12 +63,18 @@ using sk::dequant_chunk;
 constexpr int BM = 128;    // weight rows per tile (MMA M, TMEM lanes)
 constexpr int BKU = 256;   // k per unit
 constexpr int NTOK = 16;   // MMA N (tokens, padded)
-// Warp roles (28 warps): 0..3 MMA issuers, 4 and 5 weight producers, 6 the
-// activation producer, 7 the activation converter, 8..11 epilogue, 12..27
+// Warp roles (32 warps): 0..7 MMA issuers, 8 and 9 weight producers, 10 the
+// activation producer, 11 the activation converter, 12..15 epilogue, 16..31
 // dequantisers (four groups of four warps, one warp per TMEM lane quarter).
-constexpr int kMmaWarps = 4;
-constexpr int kEpiWarp0 = 8;
-constexpr int kFirstDqWarp = 12;
+// A thread issuing tcgen05.mma spends on the order of a hundred cycles per
+// instruction, and a unit needs 16 of them (M = 128, N = 16, K = 16 each), so
+// eight issuing threads share them, two per unit each.
+constexpr int kMmaWarps = 8;
+constexpr int kWProdWarp0 = 8;
+constexpr int kXProdWarp = 10;
+constexpr int kConvWarp = 11;
+constexpr int kEpiWarp0 = 12;
+constexpr int kFirstDqWarp = 16;
 constexpr int kDqWarps = 16;
 constexpr int kThreads = (kFirstDqWarp + kDqWarps) * 32;
 constexpr int kEpiThreads = 128;
@@ -84,9 +90,9 @@ constexpr int kXRingBytes = 32768;
 constexpr int kXMaxStages = 8;
 constexpr int kUnitSlots = 8;                   // unit-completion barriers (>= the activation and A rings, in units)
 NVFP4_DEVINL int xrows_of(int N) { return N <= 8 ? 8 : 16; }
-constexpr int kAStages = 6;                     // TMEM A ring (half units)
+constexpr int kAStages = 4;                     // TMEM A ring (half units)
 constexpr int kACols = 64;
-constexpr int kDCols = 64;                      // one accumulator buffer: 4 chains x 16 columns
+constexpr int kDCols = 128;                     // one accumulator buffer: 8 chains x 16 columns
 constexpr uint32_t kTmemCols = 512;
 constexpr int kJobSlots = 8;                    // per-job info ring (mode, factors)
 constexpr int kReaders = 8;                     // warps reading one weight stage (2 halves x 4 warps)
@@ -395,99 +401,64 @@ __device__ __noinline__ bool publish_job(uint8_t *plan, const PlanView &v, int N
 namespace nvfp4 {
 namespace st {
 
-__global__ void __launch_bounds__(kThreads, 1) stream_kernel(uint8_t *plan)
+
+// Everything the roles of stream_kernel share, set up once per CTA.  Each role
+// runs in its own non-inlined function, so the registers one role needs (the
+// epilogue holds 32 partial sums per thread) do not crowd another's loop.
+struct Ctx {
+    uint8_t *plan;
+    const PlanHeader *H;
+    const PlanHeader *hs;
+    uint8_t *c_ring, *x_ring;
+    JobInfo *jinfo;
+    uint64_t *c_full, *c_empty, *x_raw, *x_full, *u_done, *a_full, *d_full, *d_empty, *j_full, *j_empty;
+    int *last_s;
+    uint32_t *red_s;
+    const Seg *segs;
+    const JobDesc *jobs;
+    uint32_t tmem_a, tmem_d;
+    int n_seg, N, P, n_jobs, xrows, x_sub, x_unit, x_stages, warp, lane, b;
+    bool ok;
+};
+
+#define NVFP4_STREAM_UNPACK(c)                                                                              \
+    uint8_t *plan = (c).plan;                                                                               \
+    const PlanHeader *H = (c).H;                                                                            \
+    const PlanHeader &hd = *(c).hs;                                                                         \
+    uint8_t *c_ring = (c).c_ring, *x_ring = (c).x_ring;                                                     \
+    JobInfo *jinfo = (c).jinfo;                                                                             \
+    uint64_t *c_full = (c).c_full, *c_empty = (c).c_empty, *x_raw = (c).x_raw, *x_full = (c).x_full;      \
+    uint64_t *u_done = (c).u_done, *a_full = (c).a_full, *d_full = (c).d_full, *d_empty = (c).d_empty;   \
+    uint64_t *j_full = (c).j_full, *j_empty = (c).j_empty;                                                 \
+    int *last_s = (c).last_s;                                                                               \
+    uint32_t *red_s = (c).red_s;                                                                            \
+    const Seg *segs = (c).segs;                                                                             \
+    const JobDesc *jobs = (c).jobs;                                                                         \
+    const uint32_t tmem_a = (c).tmem_a, tmem_d = (c).tmem_d;                                              \
+    const int n_seg = (c).n_seg, N = (c).N, P = (c).P, n_jobs = (c).n_jobs;                               \
+    const int xrows = (c).xrows, x_sub = (c).x_sub, x_unit = (c).x_unit, x_stages = (c).x_stages;         \
+    const int warp = (c).warp, lane = (c).lane, b = (c).b;                                                  \
+    const bool ok = (c).ok;                                                                                 \
+    (void)plan; (void)H; (void)hd; (void)c_ring; (void)x_ring; (void)jinfo; (void)c_full; (void)c_empty;    \
+    (void)x_raw; (void)x_full; (void)u_done; (void)a_full; (void)d_full; (void)d_empty; (void)j_full;      \
+    (void)j_empty; (void)last_s; (void)red_s; (void)segs; (void)jobs; (void)tmem_a; (void)tmem_d;          \
+    (void)n_seg; (void)N; (void)P; (void)n_jobs; (void)xrows; (void)x_sub; (void)x_unit; (void)x_stages;   \
+    (void)warp; (void)lane; (void)b; (void)ok
+
+// Role: weight producers.
+__device__ __noinline__ void role_wprod(const Ctx &c)
 {
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t *c_ring = smem;                                        // [kCStages][codes 16 KB, scales 2 KB]
-    uint8_t *x_ring = c_ring + (size_t)kCStages * kStageBytes;     // [x_stages][x_unit]
-    JobInfo *jinfo = reinterpret_cast<JobInfo *>(x_ring + (size_t)kXRingBytes);
-    uint64_t *bars = reinterpret_cast<uint64_t *>(jinfo + kJobSlots);
-    uint64_t *c_full = bars;
-    uint64_t *c_empty = c_full + kCStages;
-    uint64_t *x_raw = c_empty + kCStages;
-    uint64_t *x_full = x_raw + kXMaxStages;
-    // u_done[u % 8]: every MMA of unit u has completed (one commit per issuer
-    // and unit); it frees the unit's activation slot and its two A items.
-    uint64_t *u_done = x_full + kXMaxStages;
-    uint64_t *a_full = u_done + kUnitSlots;
-    uint64_t *d_full = a_full + kAStages;
-    uint64_t *d_empty = d_full + 2;
-    uint64_t *j_full = d_empty + 2;
-    uint64_t *j_empty = j_full + kJobSlots;
-    uint32_t *misc = reinterpret_cast<uint32_t *>(bars + 96);
-    uint32_t *tmem_slot = misc;       // [0]
-    int *ok_s = reinterpret_cast<int *>(misc + 1);
-    int *last_s = reinterpret_cast<int *>(misc + 2);
-    uint32_t *red_s = misc + 8;       // [8] reductions of the epilogue warps
-    static_assert(2 * kCStages + 2 * kXMaxStages + kUnitSlots + kAStages + 4 + 2 * kJobSlots <= 96, "barrier count");
+    NVFP4_STREAM_UNPACK(c);
 
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int b = blockIdx.x;
-    const PlanHeader *H = reinterpret_cast<const PlanHeader *>(plan);
-
-    if (threadIdx.x == 0) {
-        tc::griddep_launch_dependents();
-        for (int s = 0; s < kCStages; ++s) {
-            tc::mbar_init(&c_full[s], 1);
-            tc::mbar_init(&c_empty[s], kReaders);
-        }
-        for (int s = 0; s < kXMaxStages; ++s) {
-            tc::mbar_init(&x_raw[s], 1);
-            tc::mbar_init(&x_full[s], 1);
-
-        }
-        for (int s = 0; s < kAStages; ++s) {
-            tc::mbar_init(&a_full[s], 4);
-
-        }
-        for (int s = 0; s < kUnitSlots; ++s)
-            tc::mbar_init(&u_done[s], kMmaWarps);
-        for (int s = 0; s < 2; ++s) {
-            tc::mbar_init(&d_full[s], kMmaWarps);
-            tc::mbar_init(&d_empty[s], kEpiThreads / 32);
-        }
-        for (int s = 0; s < kJobSlots; ++s) {
-            tc::mbar_init(&j_full[s], 1);
-            tc::mbar_init(&j_empty[s], 2);  // the epilogue and the converter
-        }
-        tc::fence_mbar_init();
-        // The plan's constant part was written before any run; a plan built for
-        // another grid size is refused.
-        *ok_s = (H->magic == kPlanMagic && H->P == (int)gridDim.x) ? 1 : 0;
-        if (!*ok_s && H->magic == kPlanMagic)
-            fail(plan, 31);
-    }
-    if (warp == 0)
-        tc::tmem_alloc(tmem_slot, kTmemCols);
-    tc::fence_before_sync();
-    __syncthreads();
-    tc::fence_after_sync();
-    const uint32_t tmem = *tmem_slot;
-    const uint32_t tmem_a = tmem;
-    const uint32_t tmem_d = tmem + kAStages * kACols;
-    const bool ok = *ok_s != 0;
-
-    const PlanHeader hd = *H;  // constant fields (epoch is read after the grid dependency)
-    const PlanView v = view(plan, hd);
-    const int N = hd.N, P = hd.P, n_jobs = hd.n_jobs;
-    const int xrows = xrows_of(N);
-    const int x_sub = xrows * 128;                 // bytes of one sub-box
-    const int x_unit = 4 * x_sub;
-    const int x_stages = kXRingBytes / x_unit;
-    const Seg *segs = v.segs + (ok ? v.seg_start[b] : 0);
-    const int n_seg = ok ? v.seg_start[b + 1] - v.seg_start[b] : 0;
-
-    if (warp == 4 || warp == 5) {
         // ---- weight producers: even / odd units of the CTA's sequence ----
         if (lane == 0) {
-            const int par = warp - 4;
+            const int par = warp - kWProdWarp0;
             int u = 0;
             bool stop = false;
             int prev = -1;
             for (int si = 0; si < n_seg && !stop; ++si) {
                 const Seg sg = segs[si];
-                const JobDesc *J = v.jobs + sg.job;
+                const JobDesc *J = jobs + sg.job;
                 const int nw = J->nw;
                 if (sg.job != prev) {
                     prev = sg.job;
@@ -514,7 +485,13 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(uint8_t *plan)
                 }
             }
         }
-    } else if (warp == 6) {
+}
+
+// Role: activation producer.
+__device__ __noinline__ void role_xprod(const Ctx &c)
+{
+    NVFP4_STREAM_UNPACK(c);
+
         // ---- activation producer: per job, wait for its inputs and publish its
         // operand format and scales; per unit, the N token rows of the unit's
         // four 64-k sub-boxes as bf16 through the job's tensor map (rows >= N of
@@ -524,6 +501,7 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(uint8_t *plan)
         tc::fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0 && ok) {
+            const PlanView v = view(plan, hd);
             tc::griddep_wait();
             const uint64_t e = *reinterpret_cast<volatile const uint64_t *>(&H->epoch);
             const uint32_t row_bytes = (uint32_t)N * 128;
@@ -531,7 +509,7 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(uint8_t *plan)
             bool stop = false;
             for (int si = 0; si < n_seg && !stop; ++si) {
                 const Seg sg = segs[si];
-                const JobDesc *J = v.jobs + sg.job;
+                const JobDesc *J = jobs + sg.job;
                 if (sg.job != prev) {
                     prev = sg.job;
                     ++lj;
@@ -573,7 +551,13 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(uint8_t *plan)
                 }
             }
         }
-    } else if (warp == 7) {
+}
+
+// Role: activation converter.
+__device__ __noinline__ void role_conv(const Ctx &c)
+{
+    NVFP4_STREAM_UNPACK(c);
+
         // ---- activation converter, for an earlier job's output in f16 mode:
         // bf16 -> f16 * 2^s_n in place (the 128-byte swizzle moves whole
         // 16-byte chunks, so each chunk converts where it lies), then the unit
@@ -623,18 +607,25 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(uint8_t *plan)
             if (lane == 0 && (si + 1 == n_seg || segs[si + 1].job != sg.job))
                 tc::mbar_arrive(&j_empty[lj % kJobSlots]);
         }
-    } else if (warp < kMmaWarps) {
+}
+
+// Role: MMA issuers.
+__device__ __noinline__ void role_mma(const Ctx &c)
+{
+    NVFP4_STREAM_UNPACK(c);
+
         // ---- MMA issuers: issuer w owns accumulator slot w.  One matrix: chain
-        // w takes the K steps kk = w (mod 4) of every half unit; a gate/up pair:
-        // slot w is matrix w / 2, chain w % 2, K steps kk = w (mod 2) of that
-        // matrix's half units ----
+        // w takes K step kk = w of every half unit (eight K steps); a gate/up
+        // pair: slot w is matrix w / 4, chain w % 4, K steps kk = w (mod 4) of
+        // that matrix's half units (the gate and up units of a k range run on
+        // the two halves of the issuers at the same time) ----
         if (lane == 0) {
             int u = 0, t = 0, lj = -1, prev = -1;
             uint32_t idesc = 0;
             bool stop = false;
             for (int si = 0; si < n_seg && !stop; ++si) {
                 const Seg sg = segs[si];
-                const int nw = v.jobs[sg.job].nw;
+                const int nw = jobs[sg.job].nw;
                 if (sg.job != prev) {
                     prev = sg.job;
                     ++lj;
@@ -660,8 +651,8 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(uint8_t *plan)
                         break;
                     }
                     const uint64_t bdesc0 = tc::smem_desc_sw128(x_ring + (size_t)s * x_unit);
-                    const bool mine = nw == 1 || (q % 2) == (warp >> 1);
-                    const int nk = nw == 1 ? 2 : 4, kk0 = nw == 1 ? warp : (warp & 1), kstep = nw == 1 ? 4 : 2;
+                    const bool mine = nw == 1 || (q % 2) == (warp >> 2);
+                    const int nk = nw == 1 ? 1 : 2, kk0 = nw == 1 ? warp : (warp & 3), kstep = 4;
                     for (int h = 0; h < 2; ++h, ++t) {
                         const int sa = t % kAStages;
                         if (!tc::mbar_wait(&a_full[sa], (uint32_t)(t / kAStages) & 1)) {
@@ -690,8 +681,15 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(uint8_t *plan)
                     tc::mma_commit(&d_full[buf]);
             }
         }
-    } else if (warp >= kEpiWarp0 && warp < kEpiWarp0 + 4) {
-        // ---- epilogue (warps 8..11, one per TMEM lane quarter) ----
+}
+
+// Role: epilogue.
+__device__ __noinline__ void role_epi(const Ctx &c)
+{
+    NVFP4_STREAM_UNPACK(c);
+
+        // ---- epilogue (one warp per TMEM lane quarter) ----
+        const PlanView v = view(plan, hd);
         const int et = threadIdx.x - kEpiWarp0 * 32;  // 0..127
         const int quarter = warp & 3;
         const int r = quarter * 32 + lane;
@@ -759,7 +757,7 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(uint8_t *plan)
         int lj = -1, prev = -1;
         for (int si = 0; si < n_seg; ++si) {
             const Seg sg = segs[si];
-            const JobDesc *J = v.jobs + sg.job;
+            const JobDesc *J = jobs + sg.job;
             const int nw = J->nw;
             if (sg.job != prev) {
                 prev = sg.job;
@@ -777,35 +775,37 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(uint8_t *plan)
                 break;
             }
             tc::fence_after_sync();
-            // accumulator slots 0..3 (16 columns each), added in a fixed order
+            // accumulator slots 0..7 (16 columns each), added in a fixed order:
+            // one matrix: slots 0..7; a gate/up pair: gate 0..3, up 4..7
             float sum[2][NTOK];
-            {
-                uint32_t a0[NTOK], a1[NTOK];
-                tc::tmem_ld_32x32b_x16(tmem_d + buf * kDCols + 0 * 16 + lane_off, a0);
-                tc::tmem_ld_32x32b_x16(tmem_d + buf * kDCols + 1 * 16 + lane_off, a1);
-                tc::tmem_ld_wait();
 #pragma unroll
-                for (int n = 0; n < NTOK; ++n)
-                    sum[0][n] = (0.0f + __uint_as_float(a0[n])) + __uint_as_float(a1[n]);
-                tc::tmem_ld_32x32b_x16(tmem_d + buf * kDCols + 2 * 16 + lane_off, a0);
-                tc::tmem_ld_32x32b_x16(tmem_d + buf * kDCols + 3 * 16 + lane_off, a1);
+            for (int n = 0; n < NTOK; ++n)
+                sum[0][n] = sum[1][n] = 0.0f;
+#pragma unroll 1
+            for (int sl = 0; sl < 8; ++sl) {
+                uint32_t a[NTOK];
+                tc::tmem_ld_32x32b_x16(tmem_d + buf * kDCols + sl * 16 + lane_off, a);
                 tc::tmem_ld_wait();
-                if (nw == 1) {
+                if (nw == 2 && sl >= 4) {
 #pragma unroll
-                    for (int n = 0; n < NTOK; ++n) {
-                        sum[0][n] = (sum[0][n] + __uint_as_float(a0[n])) + __uint_as_float(a1[n]);
-                        sum[1][n] = 0.0f;
-                    }
+                    for (int n = 0; n < NTOK; ++n)
+                        sum[1][n] += __uint_as_float(a[n]);
                 } else {
-                    // a matrix with no unit in the segment got no MMA: its slots hold stale values
-                    const bool g_ok = (sg.qe - sg.qb >= 2) || (sg.qb % 2 == 0);
-                    const bool u_ok = (sg.qe - sg.qb >= 2) || (sg.qb % 2 == 1);
 #pragma unroll
-                    for (int n = 0; n < NTOK; ++n) {
-                        sum[1][n] = u_ok ? (0.0f + __uint_as_float(a0[n])) + __uint_as_float(a1[n]) : 0.0f;
-                        if (!g_ok)
-                            sum[0][n] = 0.0f;
-                    }
+                    for (int n = 0; n < NTOK; ++n)
+                        sum[0][n] += __uint_as_float(a[n]);
+                }
+            }
+            if (nw == 2) {
+                // a matrix with no unit in the segment got no MMA: its slots hold stale values
+                const bool g_ok = (sg.qe - sg.qb >= 2) || (sg.qb % 2 == 0);
+                const bool u_ok = (sg.qe - sg.qb >= 2) || (sg.qb % 2 == 1);
+#pragma unroll
+                for (int n = 0; n < NTOK; ++n) {
+                    if (!g_ok)
+                        sum[0][n] = 0.0f;
+                    if (!u_ok)
+                        sum[1][n] = 0.0f;
                 }
             }
             tc::fence_before_sync();
@@ -914,7 +914,13 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(uint8_t *plan)
                     tc::mbar_arrive(&j_empty[lj % kJobSlots]);
             }
         }
-    } else if (warp >= kFirstDqWarp) {
+}
+
+// Role: dequantisers.
+__device__ __noinline__ void role_dq(const Ctx &c)
+{
+    NVFP4_STREAM_UNPACK(c);
+
         // ---- dequantisers: group g takes half units t = g (mod 4) ----
         const int g = (warp - kFirstDqWarp) >> 2;
         const int quarter = warp & 3;
@@ -968,17 +974,13 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(uint8_t *plan)
                     }
                     tc::fence_after_sync();
                     const uint32_t acol = tmem_a + (uint32_t)(sa * kACols) + lane_off;
-                    {
-                        uint32_t out[32];
-                        dequant_chunk(cw[0], sc8.x & 0xFFFF, mode, out);
-                        dequant_chunk(cw[1], sc8.x >> 16, mode, out + 16);
-                        tc::tmem_st_32x32b_x32(acol, out);
-                    }
-                    {
-                        uint32_t out[32];
-                        dequant_chunk(cw[2], sc8.y & 0xFFFF, mode, out);
-                        dequant_chunk(cw[3], sc8.y >> 16, mode, out + 16);
-                        tc::tmem_st_32x32b_x32(acol + 32, out);
+                    // one 16-byte chunk (32 k) at a time: 16 columns per store
+#pragma unroll
+                    for (int cc = 0; cc < 4; ++cc) {
+                        uint32_t out[16];
+                        const uint32_t sw = cc < 2 ? sc8.x : sc8.y;
+                        dequant_chunk(cw[cc], (cc & 1) ? sw >> 16 : sw & 0xFFFF, mode, out);
+                        tc::tmem_st_32x32b_x16(acol + 16 * cc, out);
                     }
                     tc::tmem_st_wait();
                     tc::fence_before_sync();
@@ -988,7 +990,145 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(uint8_t *plan)
                 }
             }
         }
+}
+
+__global__ void __launch_bounds__(kThreads, 1) stream_kernel(uint8_t *plan)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t *c_ring = smem;                                        // [kCStages][codes 16 KB, scales 2 KB]
+    uint8_t *x_ring = c_ring + (size_t)kCStages * kStageBytes;     // [x_stages][x_unit]
+    JobInfo *jinfo = reinterpret_cast<JobInfo *>(x_ring + (size_t)kXRingBytes);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(jinfo + kJobSlots);
+    uint64_t *c_full = bars;
+    uint64_t *c_empty = c_full + kCStages;
+    uint64_t *x_raw = c_empty + kCStages;
+    uint64_t *x_full = x_raw + kXMaxStages;
+    // u_done[u % 8]: every MMA of unit u has completed (one commit per issuer
+    // and unit); it frees the unit's activation slot and its two A items.
+    uint64_t *u_done = x_full + kXMaxStages;
+    uint64_t *a_full = u_done + kUnitSlots;
+    uint64_t *d_full = a_full + kAStages;
+    uint64_t *d_empty = d_full + 2;
+    uint64_t *j_full = d_empty + 2;
+    uint64_t *j_empty = j_full + kJobSlots;
+    uint32_t *misc = reinterpret_cast<uint32_t *>(bars + 96);
+    uint32_t *tmem_slot = misc;       // [0]
+    int *ok_s = reinterpret_cast<int *>(misc + 1);
+    int *last_s = reinterpret_cast<int *>(misc + 2);
+    uint32_t *red_s = misc + 8;       // [8] reductions of the epilogue warps
+    PlanHeader *hs = reinterpret_cast<PlanHeader *>(misc + 32);  // the plan header, copied once
+    static_assert(2 * kCStages + 2 * kXMaxStages + kUnitSlots + kAStages + 4 + 2 * kJobSlots <= 96, "barrier count");
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int b = blockIdx.x;
+    const PlanHeader *H = reinterpret_cast<const PlanHeader *>(plan);
+
+    if (threadIdx.x == 0) {
+        tc::griddep_launch_dependents();
+        for (int s = 0; s < kCStages; ++s) {
+            tc::mbar_init(&c_full[s], 1);
+            tc::mbar_init(&c_empty[s], kReaders);
+        }
+        for (int s = 0; s < kXMaxStages; ++s) {
+            tc::mbar_init(&x_raw[s], 1);
+            tc::mbar_init(&x_full[s], 1);
+
+        }
+        for (int s = 0; s < kAStages; ++s) {
+            tc::mbar_init(&a_full[s], 4);
+
+        }
+        for (int s = 0; s < kUnitSlots; ++s)
+            tc::mbar_init(&u_done[s], kMmaWarps);
+        for (int s = 0; s < 2; ++s) {
+            tc::mbar_init(&d_full[s], kMmaWarps);
+            tc::mbar_init(&d_empty[s], kEpiThreads / 32);
+        }
+        for (int s = 0; s < kJobSlots; ++s) {
+            tc::mbar_init(&j_full[s], 1);
+            tc::mbar_init(&j_empty[s], 2);  // the epilogue and the converter
+        }
+        tc::fence_mbar_init();
+        // The plan's constant part was written before any run; a plan built for
+        // another grid size is refused.
+        *ok_s = (H->magic == kPlanMagic && H->P == (int)gridDim.x) ? 1 : 0;
+        *hs = *H;  // constant fields (the epoch is read after the grid dependency)
+        if (!*ok_s && H->magic == kPlanMagic)
+            fail(plan, 31);
     }
+    if (warp == 0)
+        tc::tmem_alloc(tmem_slot, kTmemCols);
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
+    const uint32_t tmem_a = tmem;
+    const uint32_t tmem_d = tmem + kAStages * kACols;
+    const bool ok = *ok_s != 0;
+
+    const PlanHeader &hd = *hs;
+    const int N = hd.N, P = hd.P, n_jobs = hd.n_jobs;
+    const int xrows = xrows_of(N);
+    const int x_sub = xrows * 128;                 // bytes of one sub-box
+    const int x_unit = 4 * x_sub;
+    const int x_stages = kXRingBytes / x_unit;
+    const Seg *segs;
+    int n_seg;
+    {
+        const int32_t *seg_start = reinterpret_cast<const int32_t *>(plan + hd.off_seg_start);
+        segs = reinterpret_cast<const Seg *>(plan + hd.off_segs) + (ok ? seg_start[b] : 0);
+        n_seg = ok ? seg_start[b + 1] - seg_start[b] : 0;
+    }
+    const JobDesc *jobs = reinterpret_cast<const JobDesc *>(plan + hd.off_jobs);
+
+    Ctx c;
+    c.plan = plan;
+    c.H = H;
+    c.hs = hs;
+    c.c_ring = c_ring;
+    c.x_ring = x_ring;
+    c.jinfo = jinfo;
+    c.c_full = c_full;
+    c.c_empty = c_empty;
+    c.x_raw = x_raw;
+    c.x_full = x_full;
+    c.u_done = u_done;
+    c.a_full = a_full;
+    c.d_full = d_full;
+    c.d_empty = d_empty;
+    c.j_full = j_full;
+    c.j_empty = j_empty;
+    c.last_s = last_s;
+    c.red_s = red_s;
+    c.segs = segs;
+    c.jobs = jobs;
+    c.tmem_a = tmem_a;
+    c.tmem_d = tmem_d;
+    c.n_seg = n_seg;
+    c.N = N;
+    c.P = P;
+    c.n_jobs = n_jobs;
+    c.xrows = xrows;
+    c.x_sub = x_sub;
+    c.x_unit = x_unit;
+    c.x_stages = x_stages;
+    c.warp = warp;
+    c.lane = lane;
+    c.b = b;
+    c.ok = ok;
+    if (warp == kWProdWarp0 || warp == kWProdWarp0 + 1)
+        role_wprod(c);
+    else if (warp == kXProdWarp)
+        role_xprod(c);
+    else if (warp == kConvWarp)
+        role_conv(c);
+    else if (warp < kMmaWarps)
+        role_mma(c);
+    else if (warp >= kEpiWarp0 && warp < kEpiWarp0 + 4)
+        role_epi(c);
+    else
+        role_dq(c);
 
     // Lane 0 of the producer and MMA warps ran their loops alone: reconverge
     // each warp first, so the block-wide barrier really waits for every thread.
