@@ -100,6 +100,9 @@ constexpr int kMaxN = 16;
 constexpr int kPartialFloats = 2 * NTOK * BM;   // one split segment: [matrix][token][row]
 static_assert(kAStages * kACols + 2 * kDCols <= (int)kTmemCols, "TMEM budget");
 static_assert(kUnitSlots >= kXMaxStages && kUnitSlots >= kAStages / 2, "unit barriers cover both rings");
+static_assert((kUnitSlots & (kUnitSlots - 1)) == 0, "unit barrier index by mask");
+static_assert(kAStages == 4 && kCStages % 2 == 0,
+              "dequantiser group g owns A slot g and walks every other unit's weight stage");
 
 // ---------------------------------------------------------------------------
 // Plan layout (device memory, built by stream_plan; every offset from the
@@ -454,6 +457,8 @@ __device__ __noinline__ void role_wprod(const Ctx &c)
         if (lane == 0) {
             const int par = warp - kWProdWarp0;
             int u = 0;
+            int ws = par;
+            uint32_t wph = 0;
             bool stop = false;
             int prev = -1;
             for (int si = 0; si < n_seg && !stop; ++si) {
@@ -470,8 +475,13 @@ __device__ __noinline__ void role_wprod(const Ctx &c)
                 for (int q = sg.qb; q < sg.qe; ++q, ++u) {
                     if ((u & 1) != par)
                         continue;
-                    const int s = u % kCStages;
-                    const uint32_t ph = (uint32_t)(u / kCStages) & 1;
+                    const int s = ws;          // stage of unit u (u % kCStages), advanced two units at a time
+                    const uint32_t ph = wph;
+                    ws += 2;
+                    if (ws >= kCStages) {
+                        ws -= kCStages;
+                        wph ^= 1;
+                    }
                     if (!tc::mbar_wait(&c_empty[s], ph ^ 1)) {
                         fail(plan, 32);
                         stop = true;
@@ -505,7 +515,7 @@ __device__ __noinline__ void role_xprod(const Ctx &c)
             tc::griddep_wait();
             const uint64_t e = *reinterpret_cast<volatile const uint64_t *>(&H->epoch);
             const uint32_t row_bytes = (uint32_t)N * 128;
-            int u = 0, lj = -1, prev = -1;
+            int u = 0, lj = -1, prev = -1, xs = 0;
             bool stop = false;
             for (int si = 0; si < n_seg && !stop; ++si) {
                 const Seg sg = segs[si];
@@ -526,10 +536,12 @@ __device__ __noinline__ void role_xprod(const Ctx &c)
                 const bool conv = ji->convert != 0;
                 const uint8_t *img = plan + (J->img_off > 0 ? J->img_off : 0);
                 for (int q = sg.qb; q < sg.qe; ++q, ++u) {
-                    const int s = u % x_stages;
+                    const int s = xs;
+                    if (++xs == x_stages)
+                        xs = 0;
                     // the slot's previous unit (u - x_stages) has been consumed
                     const int pu = u - x_stages;
-                    if (pu >= 0 && !tc::mbar_wait(&u_done[pu % kUnitSlots], (uint32_t)(pu / kUnitSlots) & 1)) {
+                    if (pu >= 0 && !tc::mbar_wait(&u_done[pu & (kUnitSlots - 1)], (uint32_t)(pu / kUnitSlots) & 1)) {
                         fail(plan, 33);
                         stop = true;
                         break;
@@ -582,7 +594,7 @@ __device__ __noinline__ void role_conv(const Ctx &c)
             }
             const JobInfo *ji = jinfo + lj % kJobSlots;
             for (int q = sg.qb; q < sg.qe && conv; ++q, ++u) {
-                const int s = u % x_stages;
+                const int s = (int)((uint32_t)u % (uint32_t)x_stages);
                 if (!tc::mbar_wait(&x_raw[s], (rawph >> s) & 1)) {
                     fail(plan, 38);
                     stop = true;
@@ -613,74 +625,90 @@ __device__ __noinline__ void role_conv(const Ctx &c)
 __device__ __noinline__ void role_mma(const Ctx &c)
 {
     NVFP4_STREAM_UNPACK(c);
-
-        // ---- MMA issuers: issuer w owns accumulator slot w.  One matrix: chain
-        // w takes K step kk = w of every half unit (eight K steps); a gate/up
-        // pair: slot w is matrix w / 4, chain w % 4, K steps kk = w (mod 4) of
-        // that matrix's half units (the gate and up units of a k range run on
-        // the two halves of the issuers at the same time) ----
-        if (lane == 0) {
-            int u = 0, t = 0, lj = -1, prev = -1;
-            uint32_t idesc = 0;
-            bool stop = false;
-            for (int si = 0; si < n_seg && !stop; ++si) {
-                const Seg sg = segs[si];
-                const int nw = jobs[sg.job].nw;
-                if (sg.job != prev) {
-                    prev = sg.job;
-                    ++lj;
-                    if (!tc::mbar_wait(&j_full[lj % kJobSlots], ((uint32_t)lj / kJobSlots) & 1)) {
-                        fail(plan, 39);
-                        break;
-                    }
-                    idesc = tc::idesc_f16kind(BM, NTOK, (uint32_t)jinfo[lj % kJobSlots].mode);
-                }
-                const int buf = si & 1;
-                if (!tc::mbar_wait(&d_empty[buf], (((uint32_t)si >> 1) & 1) ^ 1)) {
-                    fail(plan, 40);
-                    break;
-                }
-                tc::fence_after_sync();
-                const uint32_t dcol = tmem_d + (uint32_t)(buf * kDCols + warp * 16);
-                bool fresh = true;
-                for (int q = sg.qb; q < sg.qe; ++q, ++u) {
-                    const int s = u % x_stages;
-                    if (!tc::mbar_wait(&x_full[s], (uint32_t)(u / x_stages) & 1)) {
-                        fail(plan, 41);
-                        stop = true;
-                        break;
-                    }
-                    const uint64_t bdesc0 = tc::smem_desc_sw128(x_ring + (size_t)s * x_unit);
-                    const bool mine = nw == 1 || (q % 2) == (warp >> 2);
-                    const int nk = nw == 1 ? 1 : 2, kk0 = nw == 1 ? warp : (warp & 3), kstep = 4;
-                    for (int h = 0; h < 2; ++h, ++t) {
-                        const int sa = t % kAStages;
-                        if (!tc::mbar_wait(&a_full[sa], (uint32_t)(t / kAStages) & 1)) {
-                            fail(plan, 42);
-                            stop = true;
-                            break;
-                        }
-                        tc::fence_after_sync();
-                        const uint32_t acol = tmem_a + (uint32_t)(sa * kACols);
-                        if (mine) {
-                            for (int i = 0; i < nk; ++i) {
-                                const int kk = kk0 + kstep * i;      // K step (16 k) within the half unit
-                                const int kl = h * 128 + kk * 16;    // k within the unit
-                                // B: sub-box kl / 64 of the unit, 32-byte step kl % 64 in it (16-byte units)
-                                const uint32_t boff = (uint32_t)((kl >> 6) * (x_sub / 16) + 2 * ((kl >> 4) & 3));
-                                tc::mma_f16_ts(dcol, acol + (uint32_t)(kk * 8), bdesc0 + boff, idesc, fresh ? 0u : 1u);
-                                fresh = false;
-                            }
-                        }
-                    }
-                    if (stop)
-                        break;
-                    tc::mma_commit(&u_done[u % kUnitSlots]);
-                }
-                if (!stop)
-                    tc::mma_commit(&d_full[buf]);
+    // ---- MMA issuers: issuer w owns accumulator slot w.  One matrix: chain
+    // w takes K step kk = w of every half unit (eight K steps); a gate/up
+    // pair: slot w is matrix w / 4, chain w % 4, K steps kk = w (mod 4) of
+    // that matrix's half units (the gate and up units of a k range run on
+    // the two halves of the issuers at the same time).  Ring positions are
+    // advanced incrementally: no divisions in the loop. ----
+    if (lane != 0)
+        return;
+    int lj = -1, prev = -1;
+    uint32_t idesc = 0;
+    int xs = 0, sa = 0;            // activation and A ring slots
+    uint32_t xph = 0, aph = 0;     // their phases
+    uint32_t ud = 0;               // unit counter (completion barrier u % kUnitSlots)
+    for (int si = 0; si < n_seg; ++si) {
+        const Seg sg = segs[si];
+        const int nw = jobs[sg.job].nw;
+        if (sg.job != prev) {
+            prev = sg.job;
+            ++lj;
+            if (!tc::mbar_wait(&j_full[lj % kJobSlots], ((uint32_t)lj / kJobSlots) & 1)) {
+                fail(plan, 39);
+                return;
+            }
+            idesc = tc::idesc_f16kind(BM, NTOK, (uint32_t)jinfo[lj % kJobSlots].mode);
+        }
+        const int buf = si & 1;
+        if (!tc::mbar_wait(&d_empty[buf], (((uint32_t)si >> 1) & 1) ^ 1)) {
+            fail(plan, 40);
+            return;
+        }
+        tc::fence_after_sync();
+        const uint32_t dcol = tmem_d + (uint32_t)(buf * kDCols + warp * 16);
+        // this issuer's K steps of a half unit, as A column and B descriptor offsets
+        const int nk = nw == 1 ? 1 : 2, kk0 = nw == 1 ? warp : (warp & 3);
+        uint32_t aoff[2], boff[2][2];
+        for (int i = 0; i < 2; ++i) {
+            const int kk = kk0 + 4 * i;
+            aoff[i] = (uint32_t)(kk * 8);
+            for (int h = 0; h < 2; ++h) {
+                const int kl = h * 128 + kk * 16;  // k within the unit
+                // B: sub-box kl / 64 of the unit, 32-byte step kl % 64 in it (16-byte units)
+                boff[h][i] = (uint32_t)((kl >> 6) * (x_sub / 16) + 2 * ((kl >> 4) & 3));
             }
         }
+        const uint64_t xdesc = tc::smem_desc_sw128(x_ring);
+        bool fresh = true;
+        for (int q = sg.qb; q < sg.qe; ++q) {
+            const bool mine = nw == 1 || (q & 1) == (warp >> 2);
+            if (mine) {
+                if (!tc::mbar_wait(&x_full[xs], xph)) {
+                    fail(plan, 41);
+                    return;
+                }
+                const uint64_t bdesc0 = xdesc + (uint64_t)((xs * x_unit) >> 4);
+                for (int h = 0; h < 2; ++h) {
+                    if (!tc::mbar_wait(&a_full[sa], aph)) {
+                        fail(plan, 42);
+                        return;
+                    }
+                    tc::fence_after_sync();
+                    const uint32_t acol = tmem_a + (uint32_t)(sa * kACols);
+                    for (int i = 0; i < nk; ++i) {
+                        tc::mma_f16_ts(dcol, acol + aoff[i], bdesc0 + boff[h][i], idesc, fresh ? 0u : 1u);
+                        fresh = false;
+                    }
+                    if (++sa == kAStages) {
+                        sa = 0;
+                        aph ^= 1;
+                    }
+                }
+            } else if (++sa, ++sa >= kAStages) {  // skip the unit's two half units
+                sa -= kAStages;
+                aph ^= 1;
+            }
+            // the unit's MMAs of this thread (if any) are done -> its share of u_done
+            tc::mma_commit(&u_done[ud & (kUnitSlots - 1)]);
+            ++ud;
+            if (++xs == x_stages) {
+                xs = 0;
+                xph ^= 1;
+            }
+        }
+        tc::mma_commit(&d_full[buf]);
+    }
 }
 
 // Role: epilogue.
@@ -920,76 +948,97 @@ __device__ __noinline__ void role_epi(const Ctx &c)
 __device__ __noinline__ void role_dq(const Ctx &c)
 {
     NVFP4_STREAM_UNPACK(c);
-
-        // ---- dequantisers: group g takes half units t = g (mod 4) ----
-        const int g = (warp - kFirstDqWarp) >> 2;
-        const int quarter = warp & 3;
-        const int r = quarter * 32 + lane;
-        const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-        const int swz = r & 7;
-        int u = 0, lj = -1, prev = -1, have = -1, mode = 0;
-        bool stop = false;
-        for (int si = 0; si < n_seg && !stop; ++si) {
-            const Seg sg = segs[si];
-            if (sg.job != prev) {
-                prev = sg.job;
+    // ---- dequantisers: half unit t = 2u + h goes to group t % 4, so group g
+    // takes half h = g % 2 of the units u = g / 2 (mod 2), always into A slot
+    // g; it walks its units two at a time with incremental ring positions ----
+    const int g = (warp - kFirstDqWarp) >> 2;
+    const int h = g & 1;
+    const int quarter = warp & 3;
+    const int r = quarter * 32 + lane;
+    const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+    const int swz = r & 7;
+    if (n_seg == 0)
+        return;
+    // cursor over the CTA's units: segment si, unit q of its tile, local job lj
+    int si = 0, lj = 0;
+    int job = segs[0].job, qe = segs[0].qe;
+    int q = segs[0].qb;
+    auto step = [&](int k) -> bool {  // advance k units; false past the last one
+        q += k;
+        while (q >= qe) {
+            const int over = q - qe;
+            if (++si >= n_seg)
+                return false;
+            const int nj = segs[si].job;
+            if (nj != job)
                 ++lj;
+            job = nj;
+            qe = segs[si].qe;
+            q = segs[si].qb + over;
+        }
+        return true;
+    };
+    if (!step(g >> 1))
+        return;
+    uint32_t u = (uint32_t)(g >> 1);
+    int sc = g >> 1;               // weight stage of unit u (u % kCStages) and its phase
+    uint32_t phc = 0;
+    int have = -1, mode = 0;
+    const uint32_t acol = tmem_a + (uint32_t)(g * kACols) + lane_off;
+    for (;;) {
+        if (have != lj) {
+            if (!tc::mbar_wait(&j_full[lj % kJobSlots], ((uint32_t)lj / kJobSlots) & 1)) {
+                fail(plan, 45);
+                return;
             }
-            for (int q = sg.qb; q < sg.qe && !stop; ++q, ++u) {
-                for (int h = 0; h < 2; ++h) {
-                    const int t = 2 * u + h;
-                    if ((t & 3) != g)
-                        continue;
-                    if (have != lj) {
-                        if (!tc::mbar_wait(&j_full[lj % kJobSlots], ((uint32_t)lj / kJobSlots) & 1)) {
-                            fail(plan, 45);
-                            stop = true;
-                            break;
-                        }
-                        mode = jinfo[lj % kJobSlots].mode;
-                        have = lj;
-                    }
-                    const int sc = u % kCStages;
-                    if (!tc::mbar_wait(&c_full[sc], (uint32_t)(u / kCStages) & 1)) {
-                        fail(plan, 46);
-                        stop = true;
-                        break;
-                    }
-                    const uint8_t *stage = c_ring + (size_t)sc * kStageBytes;
-                    const uint8_t *crow = stage + r * 128;
-                    uint4 cw[4];
+            mode = jinfo[lj % kJobSlots].mode;
+            have = lj;
+        }
+        if (!tc::mbar_wait(&c_full[sc], phc)) {
+            fail(plan, 46);
+            return;
+        }
+        const uint8_t *stage = c_ring + (size_t)sc * kStageBytes;
+        const uint8_t *crow = stage + r * 128;
+        uint4 cw[4];
 #pragma unroll
-                    for (int c = 0; c < 4; ++c)
-                        cw[c] = *reinterpret_cast<const uint4 *>(crow + (((h * 4 + c) ^ swz) << 4));
-                    const uint2 sc8 = *reinterpret_cast<const uint2 *>(stage + kCodeBox + r * 16 + h * 8);
-                    __syncwarp();
-                    if (lane == 0)
-                        tc::mbar_arrive(&c_empty[sc]);
-                    const int sa = t % kAStages;
-                    const int pu = (t - kAStages) >> 1;  // unit of the slot's previous item
-                    if (t >= kAStages && !tc::mbar_wait(&u_done[pu % kUnitSlots], (uint32_t)(pu / kUnitSlots) & 1)) {
-                        fail(plan, 47);
-                        stop = true;
-                        break;
-                    }
-                    tc::fence_after_sync();
-                    const uint32_t acol = tmem_a + (uint32_t)(sa * kACols) + lane_off;
-                    // one 16-byte chunk (32 k) at a time: 16 columns per store
-#pragma unroll
-                    for (int cc = 0; cc < 4; ++cc) {
-                        uint32_t out[16];
-                        const uint32_t sw = cc < 2 ? sc8.x : sc8.y;
-                        dequant_chunk(cw[cc], (cc & 1) ? sw >> 16 : sw & 0xFFFF, mode, out);
-                        tc::tmem_st_32x32b_x16(acol + 16 * cc, out);
-                    }
-                    tc::tmem_st_wait();
-                    tc::fence_before_sync();
-                    __syncwarp();
-                    if (lane == 0)
-                        tc::mbar_arrive(&a_full[sa]);
-                }
+        for (int cc = 0; cc < 4; ++cc)
+            cw[cc] = *reinterpret_cast<const uint4 *>(crow + (((h * 4 + cc) ^ swz) << 4));
+        const uint2 sc8 = *reinterpret_cast<const uint2 *>(stage + kCodeBox + r * 16 + h * 8);
+        __syncwarp();
+        if (lane == 0)
+            tc::mbar_arrive(&c_empty[sc]);
+        // A slot g was last filled for unit u - 2: its MMAs must have completed
+        if (u >= 2) {
+            const uint32_t pu = u - 2;
+            if (!tc::mbar_wait(&u_done[pu & (kUnitSlots - 1)], (pu / kUnitSlots) & 1)) {
+                fail(plan, 47);
+                return;
             }
         }
+        tc::fence_after_sync();
+        // one 16-byte chunk (32 k) at a time: 16 columns per store
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) {
+            uint32_t out[16];
+            const uint32_t sw = cc < 2 ? sc8.x : sc8.y;
+            dequant_chunk(cw[cc], (cc & 1) ? sw >> 16 : sw & 0xFFFF, mode, out);
+            tc::tmem_st_32x32b_x16(acol + 16 * cc, out);
+        }
+        tc::tmem_st_wait();
+        tc::fence_before_sync();
+        __syncwarp();
+        if (lane == 0)
+            tc::mbar_arrive(&a_full[g]);
+        u += 2;
+        sc += 2;
+        if (sc >= kCStages) {
+            sc -= kCStages;
+            phc ^= 1;
+        }
+        if (!step(2))
+            return;
+    }
 }
 
 __global__ void __launch_bounds__(kThreads, 1) stream_kernel(uint8_t *plan)
