@@ -114,7 +114,88 @@ struct Args {
     int num_kb;
     uint32_t *err;
     int row_tiles, token_tiles, group;  // raster: groups of `group` row tiles
+    // Split mode (one matrix, A in tensor memory, fewer tiles than SMs): the
+    // grid's CTAs take equal contiguous ranges of the (tile, 256-k group)
+    // units, so a CTA has at most two tile segments; a tile shared by several
+    // CTAs is finished by the last to arrive, adding every CTA's fp32 partial
+    // in CTA order.
+    int split;
+    int grid;             // CTAs: one per tile, or (split mode) one per SM
+    int kq;               // 256-k groups per tile (num_kb / 4)
+    int64_t units;        // tiles * kq
+    float *partial;       // [2 * gridDim][TN][BM] raw fp32 accumulators
+    uint32_t *counters;   // [tiles] arrivals (zeroed by the host before the launch)
 };
+
+// Tile index -> (row tile, token tile) in the raster order: groups of `group`
+// weight row tiles; inside a group row tiles vary fastest, then token tiles.
+NVFP4_DEVINL void tile_coords(const Args &a, int64_t tile, int64_t &row_tile, int64_t &token_tile)
+{
+    const int64_t per_group = (int64_t)a.group * a.token_tiles;
+    const int64_t gidx = tile / per_group;
+    const int64_t first = gidx * a.group;
+    const int64_t rows = (a.row_tiles - first) < a.group ? (a.row_tiles - first) : a.group;
+    const int64_t in = tile - gidx * per_group;
+    row_tile = first + in % rows;
+    token_tile = in / rows;
+}
+
+// The k blocks a CTA computes: one segment (a whole tile) without split mode,
+// else one or two segments of its unit range.  Scalars, not arrays: the
+// segment of a stage is picked with selects, so nothing goes to local memory.
+struct Segs {
+    int n;
+    int64_t tile_a, tile_b;
+    int kb0_a, kb0_b, nkb_a, nkb_b;  // first 64-k block and number of blocks of each segment
+    int64_t m0_a, m0_b;
+    int n0_a, n0_b;
+    bool whole_a, whole_b;
+};
+
+// CTA whose unit range holds unit u (ranges [b * units / G, (b + 1) * units / G)).
+NVFP4_DEVINL int64_t split_cta_of(int64_t u, int64_t units, int64_t G) { return ((u + 1) * G - 1) / units; }
+
+template <int TN, bool SPLIT>
+NVFP4_DEVINL Segs cta_segments(const Args &a, int64_t b, int64_t G)
+{
+    Segs sg{};
+    if (!SPLIT) {
+        sg.n = 1;
+        sg.tile_a = b;
+        sg.kb0_a = 0;
+        sg.nkb_a = a.num_kb;
+        sg.whole_a = true;
+    } else {
+        const int64_t lo = b * a.units / G, hi = (b + 1) * a.units / G;
+        sg.n = 0;
+        if (lo < hi) {
+            const int64_t t = lo / a.kq;
+            const int64_t e = (t + 1) * a.kq < hi ? (t + 1) * a.kq : hi;
+            sg.n = 1;
+            sg.tile_a = t;
+            sg.kb0_a = (int)(lo - t * a.kq) * 4;
+            sg.nkb_a = (int)(e - lo) * 4;
+            sg.whole_a = (lo == t * a.kq) && (e == (t + 1) * a.kq);
+            if (e < hi) {  // the range reaches into the next tile (at most one more: units / G <= kq)
+                sg.n = 2;
+                sg.tile_b = t + 1;
+                sg.kb0_b = 0;
+                sg.nkb_b = (int)(hi - e) * 4;
+                sg.whole_b = hi == (t + 2) * a.kq;
+            }
+        }
+    }
+    int64_t rt, tt;
+    tile_coords(a, sg.tile_a, rt, tt);
+    sg.m0_a = rt * BM;
+    sg.n0_a = (int)(tt * TN);
+    if (sg.n > 1) {
+        tile_coords(a, sg.tile_b, rt, tt);
+        sg.m0_b = rt * BM;
+        sg.n0_b = (int)(tt * TN);
+    }
+    return sg;
+}
 
 // Exact bf16 dequantisation of one 32-bit code word (k = 8q .. 8q+7) into
 // four bf16x2 words in natural k order, each value e2m1 * scale * 2^-8.
@@ -207,7 +288,7 @@ struct WeightMaps {
 
 // TN: tokens per tile (MMA N), 256 or 192; the host picks it per call so that
 // the grid fills the SMs' waves (the accumulation order does not depend on it).
-template <int NW, bool ALIGNED, int FMT = 0, bool TMAC = false, int TN = BN>
+template <int NW, bool ALIGNED, int FMT = 0, bool TMAC = false, int TN = BN, bool SPLIT = false>
 __global__ void __launch_bounds__(TMAC ? kThreadsTma : kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ WeightMaps wmaps, Args a)
 {
@@ -228,26 +309,23 @@ __global__ void __launch_bounds__(TMAC ? kThreadsTma : kThreads, 1)
     uint64_t *bars = reinterpret_cast<uint64_t *>(sb + (size_t)S * kBBytes + C::kRingBytes);
     uint64_t *full_a = bars, *full_b = bars + S, *empty = bars + 2 * S, *tmem_full = bars + 3 * S;
     uint64_t *cfull = bars + 3 * S + 1, *cempty = cfull + SC, *sfull = cempty + SC, *sempty = sfull + 2;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sempty + 2);
+    uint64_t *tmem_empty = sempty + 2;  // split mode: segment 0's accumulator has been read
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(tmem_empty + 1);
+    int *last_s = reinterpret_cast<int *>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    // Raster: the grid walks groups of `group` weight row tiles; inside a group
-    // row tiles vary fastest, then token tiles.  The host picks the group so
-    // that the operand re-read across the grid stays resident in L2.
-    int64_t row_tile, token_tile;
-    {
-        const int64_t bid = blockIdx.x;
-        const int64_t per_group = (int64_t)a.group * a.token_tiles;
-        const int64_t gidx = bid / per_group;
-        const int64_t first = gidx * a.group;
-        const int64_t rows = (a.row_tiles - first) < a.group ? (a.row_tiles - first) : a.group;
-        const int64_t in = bid - gidx * per_group;
-        row_tile = first + in % rows;
-        token_tile = in / rows;
-    }
-    const int64_t m0 = row_tile * BM;
-    const int n0 = (int)(token_tile * TN);
-    const int num_kb = a.num_kb;
+    // The CTA's k blocks: one whole tile (raster order: the host picks the
+    // raster so that the operand re-read across the grid stays resident in
+    // L2), or in split mode one or two segments of its unit range.  Stage i of
+    // the CTA runs k block kb_of(i) of segment seg_of(i); ring positions follow i.
+    static_assert(!SPLIT || (NW == 1 && TMAC && FMT == 0), "split mode: one NVFP4 matrix, A in tensor memory");
+    const Segs sgs = cta_segments<TN, SPLIT>(a, blockIdx.x, gridDim.x);
+    const int64_t m0 = sgs.m0_a;
+    const int num_kb = SPLIT ? sgs.nkb_a + (sgs.n > 1 ? sgs.nkb_b : 0) : a.num_kb;
+    auto in_b = [&](int i) -> bool { return SPLIT && sgs.n > 1 && i >= sgs.nkb_a; };
+    auto kb_of = [&](int i) -> int { return in_b(i) ? sgs.kb0_b + (i - sgs.nkb_a) : sgs.kb0_a + i; };
+    auto m0_of = [&](int i) -> int64_t { return in_b(i) ? sgs.m0_b : sgs.m0_a; };
+    auto n0_of = [&](int i) -> int { return in_b(i) ? sgs.n0_b : sgs.n0_a; };
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
@@ -256,6 +334,7 @@ __global__ void __launch_bounds__(TMAC ? kThreadsTma : kThreads, 1)
             tc::mbar_init(&empty[s], C::kIssue);
         }
         tc::mbar_init(tmem_full, C::kIssue);
+        tc::mbar_init(tmem_empty, kDqWarps);
         if (TMAC) {
             for (int c = 0; c < SC; ++c) {
                 tc::mbar_init(&cfull[c], 1);
@@ -287,7 +366,7 @@ __global__ void __launch_bounds__(TMAC ? kThreadsTma : kThreads, 1)
                     break;
                 }
                 tc::mbar_arrive_expect_tx(&full_b[s], kBBytes);
-                tc::tma_load_2d(sb + (size_t)s * kBBytes, &tmap_x, &full_b[s], kb * BK, n0);
+                tc::tma_load_2d(sb + (size_t)s * kBBytes, &tmap_x, &full_b[s], kb_of(kb) * BK, n0_of(kb));
             }
         }
     } else if (warp < kFirstDqWarp) {
@@ -300,6 +379,17 @@ __global__ void __launch_bounds__(TMAC ? kThreadsTma : kThreads, 1)
             // one issuer, one accumulator, A from tensor memory
             constexpr uint32_t idesc = tc::idesc_bf16(BM, TN);
             for (int kb = 0; kb < num_kb; ++kb) {
+                const bool seg_start = kb == 0 || (SPLIT && sgs.n > 1 && kb == sgs.nkb_a);
+                if (SPLIT && kb > 0 && seg_start) {
+                    // split mode: segment 0 is complete; its accumulator must be
+                    // read by the epilogue before segment 1 overwrites it
+                    tc::mma_commit(tmem_full);
+                    if (!tc::mbar_wait(tmem_empty, 0)) {
+                        fail(a, 8);
+                        break;
+                    }
+                    tc::fence_after_sync();
+                }
                 const int s = kb % S;
                 const uint32_t ph = (kb / S) & 1;
                 if (!tc::mbar_wait(&full_a[s], ph) || !tc::mbar_wait(&full_b[s], ph)) {
@@ -311,7 +401,7 @@ __global__ void __launch_bounds__(TMAC ? kThreadsTma : kThreads, 1)
                 const uint32_t acol = tmem_base + C::kAcol0 + s * (BK / 2);
 #pragma unroll
                 for (int k = 0; k < BK / 16; ++k)
-                    tc::mma_f16_ts(tmem_base, acol + 8 * k, bdesc + 2 * k, idesc, (kb > 0 || k > 0) ? 1u : 0u);
+                    tc::mma_f16_ts(tmem_base, acol + 8 * k, bdesc + 2 * k, idesc, (!seg_start || k > 0) ? 1u : 0u);
                 tc::mma_commit(&empty[s]);
             }
             tc::mma_commit(tmem_full);
@@ -368,7 +458,7 @@ __global__ void __launch_bounds__(TMAC ? kThreadsTma : kThreads, 1)
 #pragma unroll
                     for (int mi = 0; mi < NW; ++mi)
                         tc::tma_load_2d(ss_ring + ((size_t)ss * NW + mi) * kSBytes, &wmaps.scales[mi], &sfull[ss],
-                                        sg * 16, (int)m0);
+                                        (kb_of(kb) >> 2) * 16, (int)m0_of(kb));
                 }
                 const int c = kb % SC;
                 if (!tc::mbar_wait(&cempty[c], ((uint32_t)(kb / SC) & 1) ^ 1)) {
@@ -379,7 +469,7 @@ __global__ void __launch_bounds__(TMAC ? kThreadsTma : kThreads, 1)
 #pragma unroll
                 for (int mi = 0; mi < NW; ++mi)
                     tc::tma_load_2d(sc_ring + ((size_t)c * NW + mi) * kCBytes, &wmaps.codes[mi], &cfull[c],
-                                    kb * kCRow, (int)m0);
+                                    kb_of(kb) * kCRow, (int)m0_of(kb));
             }
         }
     } else {
@@ -417,6 +507,152 @@ __global__ void __launch_bounds__(TMAC ? kThreadsTma : kThreads, 1)
                     tc::mbar_arrive(&full_a[s]);
             }
         };
+        // Epilogue of segment seg: TMEM -> registers -> global.  A whole tile
+        // is stored directly; a split segment stores its raw fp32 accumulators
+        // ([token][row] in the CTA's slot) and the last CTA of the tile adds
+        // every contributor's slot in CTA order.
+        auto finish_split = [&](int seg) {
+            const int dq = threadIdx.x - kFirstDqWarp * 32;  // 0..255
+            tc::named_bar_sync(1, kDqWarps * 32);             // every partial store of this CTA is done
+            const int64_t G = gridDim.x;
+            const int64_t t = seg ? sgs.tile_b : sgs.tile_a;
+            const int64_t b_lo = split_cta_of(t * a.kq, a.units, G);
+            const int64_t b_hi = split_cta_of((t + 1) * a.kq - 1, a.units, G);
+            if (dq == 0) {
+                // release: this CTA's partial (ordered by the barrier); acquire: the others'
+                uint32_t old;
+                asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(old) : "l"(a.counters + t) : "memory");
+                *last_s = old == (uint32_t)(b_hi - b_lo);
+                if (*last_s)
+                    a.counters[t] = 0;
+            }
+            tc::named_bar_sync(1, kDqWarps * 32);
+            if (!*last_s)
+                return;
+            // thread: rows 4 rq .. 4 rq + 3 (one 16-byte load per contributor and
+            // token), token columns cg, cg + 8, ...; contributors added in CTA order
+            const int rq = dq & 31, cg = dq >> 5;
+            const int64_t mq = (seg ? sgs.m0_b : sgs.m0_a) + 4 * rq;
+            const int64_t sn0 = seg ? sgs.n0_b : sgs.n0_a;
+            const float tsv = FMT == 0 ? __ldg(a.ts[0]) * 256.0f : 1.0f;
+            const int nc = (int)(b_hi - b_lo) + 1;
+            const float *src[4];
+            for (int c = 0; c < 4; ++c) {
+                const int64_t bb = b_lo + (c < nc ? c : nc - 1);
+                src[c] = a.partial + (size_t)(2 * bb + (t - (bb * a.units / G) / a.kq)) * TN * BM + 4 * rq;
+            }
+#pragma unroll 2
+            for (int col = cg; col < TN; col += 8) {
+                const int64_t n = sn0 + col;
+                if (n >= a.N)
+                    break;
+                float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+                for (int c0 = 0; c0 < nc; c0 += 4) {
+                    float4 v[4];
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        const float *p = c0 == 0 ? src[c] : a.partial + (size_t)(2 * (b_lo + c0 + c) +
+                                            (t - ((b_lo + c0 + c) * a.units / G) / a.kq)) * TN * BM + 4 * rq;
+                        v[c] = (c0 + c < nc) ? __ldcg(reinterpret_cast<const float4 *>(p + (size_t)col * BM))
+                                             : make_float4(0.f, 0.f, 0.f, 0.f);
+                    }
+#pragma unroll
+                    for (int c = 0; c < 4; ++c)
+                        if (c0 + c < nc) {
+                            acc.x += v[c].x;
+                            acc.y += v[c].y;
+                            acc.z += v[c].z;
+                            acc.w += v[c].w;
+                        }
+                }
+                const float r4[4] = {acc.x, acc.y, acc.z, acc.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int64_t m = mq + e;
+                    if (m < a.M) {
+                        const float vv = r4[e] * tsv;
+                        const int64_t idx = n * a.M + m;
+                        if (a.out_bf16)
+                            reinterpret_cast<uint16_t *>(a.y)[idx] = f32_to_bf16(vv);
+                        else
+                            reinterpret_cast<float *>(a.y)[idx] = vv;
+                    }
+                }
+            }
+        };
+        auto epilogue = [&](int seg) {
+            bool have = tc::mbar_wait(tmem_full, (uint32_t)seg & 1);
+            const bool split_seg = SPLIT && !(seg ? sgs.whole_b : sgs.whole_a);
+            if (SPLIT)
+                have = tc::bar_and(1, kDqWarps * 32, have);  // uniform: named barriers follow
+            if (!have)
+                fail(a, 4);
+            tc::fence_after_sync();
+            const int64_t sm0 = seg ? sgs.m0_b : sgs.m0_a;
+            const int sn0 = seg ? sgs.n0_b : sgs.n0_a;
+            if (have) {
+                const int quarter = warp & 3;          // TMEM lanes this warp may access
+                const int chalf = (warp - kFirstDqWarp) >> 2;  // which half of the TN token columns
+                const int64_t mrow = sm0 + quarter * 32 + lane;
+                float ts[NW];
+#pragma unroll
+                for (int mi = 0; mi < NW; ++mi)
+                    ts[mi] = FMT == 0 ? __ldg(a.ts[mi]) * 256.0f : 1.0f;
+                float *slot = a.partial + (size_t)(2 * blockIdx.x + seg) * TN * BM + quarter * 32 + lane;
+                // TA: only column chunks holding at least one real token
+                // (warp-uniform; a runtime bound also keeps this loop rolled)
+#pragma unroll 1
+                for (int cc = 0; cc < TN / 64 && (!TA || sn0 + chalf * (TN / 2) + cc * 32 < a.N); ++cc) {
+                    const int col = chalf * (TN / 2) + cc * 32;
+                    const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + col;
+                    // two accumulators: gate and up, or (one matrix) K steps 0-1 and 2-3
+                    uint32_t r[2][32];
+                    tc::tmem_ld_32x32b_x32(taddr, r[0]);
+                    if (!TA)
+                        tc::tmem_ld_32x32b_x32(taddr + TN, r[1]);
+                    tc::tmem_ld_wait();
+                    if (SPLIT && split_seg) {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            slot[(size_t)(col + j) * BM] = __uint_as_float(r[0][j]);
+                    } else if (mrow < a.M) {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) {
+                            const int64_t n = (int64_t)sn0 + col + j;
+                            if (n < a.N) {
+                                float v;
+                                if (TA) {
+                                    v = __uint_as_float(r[0][j]) * ts[0];
+                                } else if (NW == 1) {
+                                    v = (__uint_as_float(r[0][j]) + __uint_as_float(r[1][j])) * ts[0];
+                                } else {
+                                    const float gg = __uint_as_float(r[0][j]) * ts[0];
+                                    const float uu = __uint_as_float(r[NW - 1][j]) * ts[NW - 1];
+                                    v = __fdiv_rn(gg, 1.0f + expf(-gg)) * uu;
+                                }
+                                const int64_t idx = n * a.M + mrow;
+                                if (a.out_bf16)
+                                    reinterpret_cast<uint16_t *>(a.y)[idx] = f32_to_bf16(v);
+                                else
+                                    reinterpret_cast<float *>(a.y)[idx] = v;
+                            }
+                        }
+                    }
+                }
+            }
+            if (SPLIT && seg + 1 < sgs.n) {
+                // segment 1 follows: hand the accumulator back to the MMA issuer
+                tc::fence_before_sync();
+                __syncwarp();
+                if (lane == 0)
+                    tc::mbar_arrive(tmem_empty);
+            }
+            if constexpr (SPLIT) {
+                if (split_seg && have)
+                    finish_split(seg);
+            }
+        };
+        bool epi0_done = false;
         if constexpr (TMAC && FMT == 1) {
             // FP6 codes from the TMA ring; the scale byte of a row (one per
             // 128 k = two stages) through a small register prefetch ring.
@@ -494,6 +730,10 @@ __global__ void __launch_bounds__(TMAC ? kThreadsTma : kThreads, 1)
             // Codes and scales from the TMA rings; a warp releases a ring slot
             // once its lanes have turned the slot's bytes into bf16 tiles.
             for (int kb = 0; kb < num_kb; ++kb) {
+                if (SPLIT && sgs.n > 1 && kb == sgs.nkb_a) {  // split mode: segment 0 is done
+                    epilogue(0);
+                    epi0_done = true;
+                }
                 const int c = kb % SC;
                 const int ss = (kb >> 2) & 1;
                 if (!tc::mbar_wait(&cfull[c], (uint32_t)(kb / SC) & 1) ||
@@ -610,56 +850,10 @@ __global__ void __launch_bounds__(TMAC ? kThreadsTma : kThreads, 1)
             }
         }
 
-        // ---------------- epilogue: TMEM -> registers -> global ----------------
-        const bool have = tc::mbar_wait(tmem_full, 0);
-        if (!have)
-            fail(a, 4);
-        tc::fence_after_sync();
-        if (have) {
-            const int quarter = warp & 3;          // TMEM lanes this warp may access
-            const int chalf = (warp - kFirstDqWarp) >> 2;  // which half of the TN token columns
-            const int64_t mrow = m0 + quarter * 32 + lane;
-            float ts[NW];
-#pragma unroll
-            for (int mi = 0; mi < NW; ++mi)
-                ts[mi] = FMT == 0 ? __ldg(a.ts[mi]) * 256.0f : 1.0f;
-            // TA: only column chunks holding at least one real token
-            // (warp-uniform; a runtime bound also keeps this loop rolled)
-#pragma unroll 1
-            for (int cc = 0; cc < TN / 64 && (!TA || n0 + chalf * (TN / 2) + cc * 32 < a.N); ++cc) {
-                const int col = chalf * (TN / 2) + cc * 32;
-                const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + col;
-                // two accumulators: gate and up, or (one matrix) K steps 0-1 and 2-3
-                uint32_t r[2][32];
-                tc::tmem_ld_32x32b_x32(taddr, r[0]);
-                if (!TA)
-                    tc::tmem_ld_32x32b_x32(taddr + TN, r[1]);
-                tc::tmem_ld_wait();
-                if (mrow < a.M) {
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        const int64_t n = (int64_t)n0 + col + j;
-                        if (n < a.N) {
-                            float v;
-                            if (TA) {
-                                v = __uint_as_float(r[0][j]) * ts[0];
-                            } else if (NW == 1) {
-                                v = (__uint_as_float(r[0][j]) + __uint_as_float(r[1][j])) * ts[0];
-                            } else {
-                                const float gg = __uint_as_float(r[0][j]) * ts[0];
-                                const float uu = __uint_as_float(r[NW - 1][j]) * ts[NW - 1];
-                                v = __fdiv_rn(gg, 1.0f + expf(-gg)) * uu;
-                            }
-                            const int64_t idx = n * a.M + mrow;
-                            if (a.out_bf16)
-                                reinterpret_cast<uint16_t *>(a.y)[idx] = f32_to_bf16(v);
-                            else
-                                reinterpret_cast<float *>(a.y)[idx] = v;
-                        }
-                    }
-                }
-            }
-        }
+        if (SPLIT && sgs.n > 1 && !epi0_done)
+            epilogue(0);
+        if (!SPLIT || sgs.n > 0)
+            epilogue(SPLIT ? sgs.n - 1 : 0);
     }
 
     // Lane 0 of warps 0 and 1 ran the producer / MMA loops alone: reconverge
@@ -693,20 +887,20 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
     return fn;
 }
 
-template <int NW, bool ALIGNED, int FMT = 0, bool TMAC = false, int TN = BN>
+template <int NW, bool ALIGNED, int FMT = 0, bool TMAC = false, int TN = BN, bool SPLIT = false>
 cudaError_t launch_t(const CUtensorMap &map, const WeightMaps &wm, const Args &a, cudaStream_t stream)
 {
     using C = Cfg<NW, TMAC, FMT, TN>;
     static std::once_flag once[kMaxDevices];
     static cudaError_t attr_errs[kMaxDevices];
     const cudaError_t attr_err = once_per_device(once, attr_errs, [] {
-        return cudaFuncSetAttribute(prefill_kernel<NW, ALIGNED, FMT, TMAC, TN>,
+        return cudaFuncSetAttribute(prefill_kernel<NW, ALIGNED, FMT, TMAC, TN, SPLIT>,
                                     cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmemBytes);
     });
     if (attr_err != cudaSuccess)
         return attr_err;
-    dim3 grid((unsigned)((int64_t)a.row_tiles * a.token_tiles));
-    prefill_kernel<NW, ALIGNED, FMT, TMAC, TN>
+    dim3 grid((unsigned)a.grid);
+    prefill_kernel<NW, ALIGNED, FMT, TMAC, TN, SPLIT>
         <<<grid, TMAC ? kThreadsTma : kThreads, C::kSmemBytes, stream>>>(map, wm, a);
     return cudaGetLastError();
 }
@@ -740,10 +934,31 @@ static bool encode_rows(PFN_cuTensorMapEncodeTiled_v12000 encode, CUtensorMap *m
 
 }  // namespace pf
 
+// Split mode (see Args): one NVFP4 matrix with K % 256 == 0 whose 256-token
+// tiles would fill less than three quarters of the SMs.  Its workspace holds
+// the tile counters and two partial slots per CTA; the size bound holds for
+// any device with up to kMaxSplitCtas SMs, so it depends on the shape alone.
+constexpr int kMaxSplitCtas = 256;
+constexpr size_t kSplitCounterBytes = 1024;  // one u32 per tile (< kMaxSplitCtas tiles)
+
+static bool split_possible(int64_t N, int64_t M, int64_t K, int n_weights)
+{
+    const int64_t tiles = ((M + pf::BM - 1) / pf::BM) * ((N + pf::BN - 1) / pf::BN);
+    return n_weights == 1 && K % 256 == 0 && tiles * 4 < (int64_t)kMaxSplitCtas * 3;
+}
+
+static bool use_split(int64_t N, int64_t M, int64_t K, int n_weights, int num_sms)
+{
+    const int64_t tiles = ((M + pf::BM - 1) / pf::BM) * ((N + pf::BN - 1) / pf::BN);
+    return split_possible(N, M, K, n_weights) && num_sms <= kMaxSplitCtas && tiles * 4 < (int64_t)num_sms * 3;
+}
+
 size_t prefill_workspace_bytes(int64_t N, int64_t M, int64_t K, int n_weights)
 {
-    (void)N; (void)M; (void)K; (void)n_weights;
-    return 256;  // the device status word at kStatusWordOffset, nothing else
+    // the device status word at kStatusWordOffset; split mode adds its counters and partials
+    if (!split_possible(N, M, K, n_weights))
+        return 256;
+    return 256 + kSplitCounterBytes + (size_t)2 * kMaxSplitCtas * pf::BN * pf::BM * sizeof(float);
 }
 
 static cudaError_t prefill_impl(const uint16_t *x, int64_t N, int64_t M, int64_t K, const uint8_t *const *codes,
@@ -755,7 +970,8 @@ static cudaError_t prefill_impl(const uint16_t *x, int64_t N, int64_t M, int64_t
         return cudaErrorNotSupported;
     const bool tma_weights = fmt == 1 || K % 256 == 0;
     const int64_t row_tiles = (M + pf::BM - 1) / pf::BM;
-    const int tn = tma_weights ? pf::pick_token_tile(N, row_tiles, num_sms) : pf::BN;
+    const bool split = fmt == 0 && use_split(N, M, K, n_weights, num_sms);
+    const int tn = split ? pf::BN : tma_weights ? pf::pick_token_tile(N, row_tiles, num_sms) : pf::BN;
     const int64_t token_tiles = (N + tn - 1) / tn;
     if (row_tiles * token_tiles > 0x7FFFFFFF)
         return cudaErrorInvalidValue;
@@ -785,12 +1001,30 @@ static cudaError_t prefill_impl(const uint16_t *x, int64_t N, int64_t M, int64_t
     a.err = reinterpret_cast<uint32_t *>(reinterpret_cast<uint8_t *>(workspace) + kStatusWordOffset);
     a.row_tiles = (int)row_tiles;
     a.token_tiles = (int)token_tiles;
+    a.split = split ? 1 : 0;
+    if (split) {
+        uint8_t *ws = reinterpret_cast<uint8_t *>(workspace);
+        a.kq = a.num_kb / 4;
+        a.units = row_tiles * token_tiles * a.kq;
+        a.counters = reinterpret_cast<uint32_t *>(ws + 256);
+        a.partial = reinterpret_cast<float *>(ws + 256 + kSplitCounterBytes);
+        // at most one CTA per unit: every CTA's range is non-empty, so a
+        // tile's contributors are the contiguous CTAs b_lo .. b_hi
+        a.grid = (int)std::min<int64_t>(num_sms, a.units);
+        const cudaError_t me = cudaMemsetAsync(a.counters, 0, (size_t)row_tiles * token_tiles * 4, stream);
+        if (me != cudaSuccess)
+            return me;
+    } else {
+        a.grid = (int)(row_tiles * token_tiles);
+    }
     {
         // Which operand stays in L2 for the whole grid: if the activations fit,
         // token tiles vary fastest (group of 1 row tile: x is read from HBM
         // once, each weight row tile once per wave); else if the weights fit,
         // row tiles vary fastest (one group of all rows); else groups whose
-        // weights fit.
+        // weights fit.  (Keeping the 50 MB of weights resident instead of the
+        // 71 MB of activations for the 27B down projection at N = 2048 was
+        // measured slower: 0.50 against 0.54 of the bf16 peak.)
         constexpr double kL2Budget = 110e6;  // of the 129 MB L2
         const double x_bytes = (double)N * (double)K * 2.0;
         const double w_tile = (double)pf::BM * (double)K * (fmt == 1 ? 0.7578125 : 0.5625) * n_weights;
@@ -822,6 +1056,8 @@ static cudaError_t prefill_impl(const uint16_t *x, int64_t N, int64_t M, int64_t
             if (!pf::encode_rows(encode, &wm.codes[i], codes[i], K / 2, M, pf::BK / 2) ||
                 !pf::encode_rows(encode, &wm.scales[i], scales[i], K / 16, M, 16))
                 return cudaErrorInvalidValue;
+        if (split)
+            return pf::launch_t<1, true, 0, true, 256, true>(map, wm, a, stream);
         if (tn == 192)
             return n_weights == 1 ? pf::launch_t<1, true, 0, true, 192>(map, wm, a, stream)
                                   : pf::launch_t<2, true, 0, true, 192>(map, wm, a, stream);

@@ -57,14 +57,17 @@
  *     workspace's status word and returns (the outputs are then undefined),
  *     so the GPU never hangs and the context stays usable; the launching call
  *     has already returned, so the code is read with nvfp4_device_status.
- *   - Determinism: the reduction order is fixed by the shapes alone, so repeated
- *     calls give bit-identical results, and row n of an N-token call equals the
- *     same token in any other call with the same weights, M and K on the same
- *     side of N = 16 (floating-point summation order is part of the contract:
- *     bw24 wiki Home, list of checks every kernel change must pass, and bw24
- *     README, where decode and verify launch the same kernel symbols and agree
- *     bit for bit).  Across N = 16 (skinny vs tensor-core prefill kernel) the
- *     rows agree within the accuracy bound below.  A skinny call in which
+ *   - Determinism: the reduction order is fixed by the shapes alone (and the
+ *     device's SM count), so repeated calls give bit-identical results.  For
+ *     N <= 16 (skinny kernel) row n of an N-token call equals the same token in
+ *     any other call with N <= 16 and the same weights, M and K (floating-point
+ *     summation order is part of the contract: bw24 wiki Home, list of checks
+ *     every kernel change must pass, and bw24 README, where decode and verify
+ *     launch the same kernel symbols and agree bit for bit).  For N > 16 (the
+ *     tensor-core prefill kernel) a shape with too few tiles to fill the SMs
+ *     splits K across thread blocks in a way that depends on N, so rows of
+ *     calls with different N > 16 (and across N = 16) agree within the
+ *     accuracy bound below, bit for bit only when neither call splits.  A skinny call in which
  *     some token's activations are not all exact in f16 after scaling by a
  *     power of two (a dynamic range wider than f16's) switches the whole call
  *     to bf16 operands; its rows also agree within the bound.

@@ -127,9 +127,10 @@ def test_prefill_down_full_size_sampled(N):
 @pytest.mark.parametrize("fmt", ["nvfp4", "fp6"])
 def test_token_rows_independent_of_tile_choice(fmt):
     """The launch picks 192- or 256-token tiles from N and the SM count
-    (N = 600 and N = 4096 over 32 row tiles take different tiles on a 152-SM
-    GPU); a token's row is the same bits either way."""
-    M, K = 4096, 1024
+    (N = 600 and N = 4096 over 64 row tiles take different tiles on a 152-SM
+    GPU; N = 300 fills two token tiles); a token's row is the same bits either
+    way.  These shapes keep enough tiles to fill the SMs, so no call splits K."""
+    M, K = 8192, 1024
     w = inputs.weights(M, K, seed=81, device=DEV)
     x = inputs.activations(4096, K, seed=82, device=DEV)
     if fmt == "nvfp4":
@@ -140,7 +141,28 @@ def test_token_rows_independent_of_tile_choice(fmt):
         run = lambda xx: g.nvfp4_fp6_gemm(xx, W)
     y_all = run(x)
     y_600 = run(x[:600].contiguous())
-    y_40 = run(x[100:140].contiguous())
+    y_300 = run(x[100:400].contiguous())
     torch.cuda.synchronize()
     assert torch.equal(y_600, y_all[:600])
-    assert torch.equal(y_40, y_all[100:140])
+    assert torch.equal(y_300, y_all[100:400])
+
+
+@pytest.mark.parametrize("N,M,K", [(40, 130, 512), (600, 384, 4096), (512, 5120, 4352)])
+def test_split_k_prefill_deterministic(N, M, K):
+    """Shapes with too few tiles for the SMs split K across CTAs (fp32
+    partials added by the last CTA of each tile, in CTA order): repeated calls
+    give the same bits, and the result matches the oracle."""
+    w = inputs.weights(M, K, seed=N + 5, device=DEV)
+    x = inputs.activations(N, K, seed=N + 6, device=DEV)
+    W = g.nvfp4_quantize(w)
+    ws = workspace(g.NVFP4_OP_GEMM_PREFILL, N, M, K)
+    y1 = g.nvfp4_gemm_prefill(x, W, workspace=ws)
+    y2 = g.nvfp4_gemm_prefill(x, W, workspace=ws)
+    torch.cuda.synchronize()
+    assert timeout_flag(ws) == 0
+    assert torch.equal(y1, y2)
+    ref_w = oracle.quantize(w.cpu().numpy())
+    rows = _sample(24, M, N + 7, [0, 127, 128, M - 1])
+    toks = _sample(6, N, N + 8, [0, N - 1])
+    y_ref, A = oracle.gemv(bf16_bits(x), *ref_w, rows=rows, tokens=toks)
+    assert_close(to_np(y1)[np.ix_(toks, rows)], y_ref, gemv_tol(y_ref, A), f"split prefill N={N}")
