@@ -85,7 +85,7 @@ cudaError_t launch_prefill_fp6(const uint16_t *x, int64_t N, int64_t M, int64_t 
 
 namespace nvfp4 {
 
-size_t prefill_workspace_bytes(int64_t N, int64_t M, int64_t K, int n_weights);
+size_t prefill_workspace_bytes(int64_t N, int64_t M, int64_t K, int n_weights, int fmt);
 
 cudaError_t launch_prefill(const uint16_t *x, int64_t N, int64_t M, int64_t K, const uint8_t *const *codes,
                            const uint8_t *const *scales, const float *const *ts, int n_weights, void *y,

@@ -151,15 +151,15 @@ size_t nvfp4_workspace_bytes(int op, int64_t N, int64_t M, int64_t K)
     switch (op) {
     case NVFP4_OP_QUANTIZE: return (size_t)kQuantPartials * 4;
     case NVFP4_OP_GEMV_SKINNY: return (N >= 1 && N <= kMaxSkinnyN) ? skinny_ws(M, K, 1) : 0;
-    case NVFP4_OP_GATEUP_SWIGLU: return N <= kMaxSkinnyN ? skinny_ws(M, K, 2) : prefill_workspace_bytes(N, M, K, 2);
-    case NVFP4_OP_GEMM_PREFILL: return N <= kMaxSkinnyN ? skinny_ws(M, K, 1) : prefill_workspace_bytes(N, M, K, 1);
+    case NVFP4_OP_GATEUP_SWIGLU: return N <= kMaxSkinnyN ? skinny_ws(M, K, 2) : prefill_workspace_bytes(N, M, K, 2, 0);
+    case NVFP4_OP_GEMM_PREFILL: return N <= kMaxSkinnyN ? skinny_ws(M, K, 1) : prefill_workspace_bytes(N, M, K, 1, 0);
     case NVFP4_OP_FP6_GEMM:
     case NVFP4_OP_FP6_GATEUP_SWIGLU: {
         if (K % 128 != 0)
             return 0;
         const int nw = op == NVFP4_OP_FP6_GEMM ? 1 : 2;
         if (N > kMaxSkinnyN)
-            return prefill_workspace_bytes(N, M, K, nw);
+            return prefill_workspace_bytes(N, M, K, nw, 1);
         return skinny_tc_supported(M, K) ? skinny_tc_workspace_bytes(M, K, nw) : gemv_mma_workspace_bytes(nw);
     }
     default: return 0;

@@ -76,6 +76,10 @@ constexpr int kSBytes = BM * 16;         // NVFP4 scales of four stages: 128 row
 // codes of one stage: 128 rows x 32 bytes (NVFP4) or 48 bytes (FP6)
 template <int FMT> constexpr int code_row_bytes() { return FMT == 0 ? BK / 2 : BK / 4 * 3; }
 constexpr int kABytes = BM * BK * 2;  // 16 KB per weight matrix per stage
+constexpr int kMaxContrib = 64;       // split mode: CTAs sharing one tile, at most
+constexpr int kFixCols = 64;                 // split mode fix-up by bulk copies: token columns per chunk
+constexpr int kFixChunk = kFixCols * BM * 4;  // 32 KB of a partial
+constexpr int kFixBufs = 4;                   // chunk buffers in the activation ring
 
 // TMAC: the weight codes and scales reach shared memory by TMA (a code ring
 // of kSc stages and a scale ring of two 4-stage groups) instead of per-thread
@@ -114,17 +118,22 @@ struct Args {
     int num_kb;
     uint32_t *err;
     int row_tiles, token_tiles, group;  // raster: groups of `group` row tiles
-    // Split mode (one matrix, A in tensor memory, fewer tiles than SMs): the
-    // grid's CTAs take equal contiguous ranges of the (tile, 256-k group)
-    // units, so a CTA has at most two tile segments; a tile shared by several
+    // Split mode (stream-K; one matrix, A in tensor memory): the tiles from
+    // sk_base / kq on are cut into (tile, 256-k group) units, and CTA b takes
+    // the b-th of sk_grid equal contiguous unit ranges: a partial tile at
+    // each end of the range, whole tiles between.  A tile shared by several
     // CTAs is finished by the last to arrive, adding every CTA's fp32 partial
-    // in CTA order.
+    // in CTA order.  The tiles before sk_base / kq belong to a whole-tile
+    // launch that precedes this one on the stream.
     int split;
-    int grid;             // CTAs: one per tile, or (split mode) one per SM
+    int grid;             // CTAs: one per tile, or (split mode) sk_grid
     int kq;               // 256-k groups per tile (num_kb / 4)
-    int64_t units;        // tiles * kq
-    float *partial;       // [2 * gridDim][TN][BM] raw fp32 accumulators
-    uint32_t *counters;   // [tiles] arrivals (zeroed by the host before the launch)
+    int after_whole;      // split mode: a whole-tile launch comes between the counter zeroing and this one
+    int64_t sk_base;      // first stream-K unit: (tiles of the whole-tile launch) * kq
+    int64_t units;        // stream-K units
+    int sk_grid;          // CTAs sharing them (<= units)
+    float *partial;       // [2 * gridDim][TN][BM] raw fp32 accumulators: a CTA's first and last segment
+    uint32_t *counters;   // [gridDim] arrivals, by a shared tile's first CTA (zeroed by the host)
 };
 
 // Tile index -> (row tile, token tile) in the raster order: groups of `group`
@@ -140,61 +149,86 @@ NVFP4_DEVINL void tile_coords(const Args &a, int64_t tile, int64_t &row_tile, in
     token_tile = in / rows;
 }
 
-// The k blocks a CTA computes: one segment (a whole tile) without split mode,
-// else one or two segments of its unit range.  Scalars, not arrays: the
-// segment of a stage is picked with selects, so nothing goes to local memory.
-struct Segs {
-    int n;
-    int64_t tile_a, tile_b;
-    int kb0_a, kb0_b, nkb_a, nkb_b;  // first 64-k block and number of blocks of each segment
-    int64_t m0_a, m0_b;
-    int n0_a, n0_b;
-    bool whole_a, whole_b;
+// A CTA's walk over its k blocks.  Without split mode: one whole tile.  In
+// split mode: its unit range [lo, hi), which crosses tiles (a partial tile at
+// each end, whole tiles between).  Every role walks the same sequence of
+// (segment, 64-k block) stages with its own cursor: an outer loop over
+// segments, whose inner loop over the segment's k blocks is the whole-tile
+// loop (the divisions of tile_coords run once per segment, not per stage).
+struct SegCursor {
+    int64_t tile;   // tile of the current segment
+    int64_t hi;     // end of the CTA's unit range (absolute units)
+    int kb;         // first 64-k block of the segment (within its tile)
+    int kb_end;     // end of the segment (64-k blocks)
+    int seg;        // segment number within the CTA
+    int64_t m0;     // first weight row of the tile
+    int n0;         // first token of the tile
+    bool whole;     // the segment covers the whole K range of its tile
 };
 
-// CTA whose unit range holds unit u (ranges [b * units / G, (b + 1) * units / G)).
+// Stream-K CTA whose unit range holds stream-K unit u (relative to sk_base;
+// ranges [b * units / G, (b + 1) * units / G), G = sk_grid <= units, so none
+// is empty).
 NVFP4_DEVINL int64_t split_cta_of(int64_t u, int64_t units, int64_t G) { return ((u + 1) * G - 1) / units; }
 
-template <int TN, bool SPLIT>
-NVFP4_DEVINL Segs cta_segments(const Args &a, int64_t b, int64_t G)
+// First tile of stream-K CTA b's range.
+NVFP4_DEVINL int64_t sk_first_tile(const Args &a, int64_t b)
 {
-    Segs sg{};
-    if (!SPLIT) {
-        sg.n = 1;
-        sg.tile_a = b;
-        sg.kb0_a = 0;
-        sg.nkb_a = a.num_kb;
-        sg.whole_a = true;
-    } else {
-        const int64_t lo = b * a.units / G, hi = (b + 1) * a.units / G;
-        sg.n = 0;
-        if (lo < hi) {
-            const int64_t t = lo / a.kq;
-            const int64_t e = (t + 1) * a.kq < hi ? (t + 1) * a.kq : hi;
-            sg.n = 1;
-            sg.tile_a = t;
-            sg.kb0_a = (int)(lo - t * a.kq) * 4;
-            sg.nkb_a = (int)(e - lo) * 4;
-            sg.whole_a = (lo == t * a.kq) && (e == (t + 1) * a.kq);
-            if (e < hi) {  // the range reaches into the next tile (at most one more: units / G <= kq)
-                sg.n = 2;
-                sg.tile_b = t + 1;
-                sg.kb0_b = 0;
-                sg.nkb_b = (int)(hi - e) * 4;
-                sg.whole_b = hi == (t + 2) * a.kq;
-            }
-        }
-    }
+    return (a.sk_base + b * a.units / a.sk_grid) / a.kq;
+}
+
+template <int TN>
+NVFP4_DEVINL void seg_coords(const Args &a, SegCursor &c)
+{
     int64_t rt, tt;
-    tile_coords(a, sg.tile_a, rt, tt);
-    sg.m0_a = rt * BM;
-    sg.n0_a = (int)(tt * TN);
-    if (sg.n > 1) {
-        tile_coords(a, sg.tile_b, rt, tt);
-        sg.m0_b = rt * BM;
-        sg.n0_b = (int)(tt * TN);
+    tile_coords(a, c.tile, rt, tt);
+    c.m0 = rt * BM;
+    c.n0 = (int)(tt * TN);
+}
+
+template <int TN>
+NVFP4_DEVINL void seg_enter(const Args &a, SegCursor &c, int64_t lo)
+{
+    c.tile = lo / a.kq;
+    const int64_t base = c.tile * a.kq;
+    const int64_t e = base + a.kq < c.hi ? base + a.kq : c.hi;
+    c.kb = (int)(lo - base) * 4;
+    c.kb_end = (int)(e - base) * 4;
+    c.whole = lo == base && e == base + a.kq;
+    seg_coords<TN>(a, c);
+}
+
+template <int TN, bool SPLIT>
+NVFP4_DEVINL SegCursor cta_cursor(const Args &a, int64_t b, int &num_kb)
+{
+    SegCursor c{};
+    if (!SPLIT) {
+        c.tile = b;
+        c.kb_end = a.num_kb;
+        c.whole = true;
+        num_kb = a.num_kb;
+        seg_coords<TN>(a, c);
+    } else {
+        const int64_t lo = a.sk_base + b * a.units / a.sk_grid;
+        c.hi = a.sk_base + (b + 1) * a.units / a.sk_grid;
+        num_kb = (int)(c.hi - lo) * 4;
+        seg_enter<TN>(a, c, lo);
     }
-    return sg;
+    return c;
+}
+
+// More segments follow the cursor's one.
+NVFP4_DEVINL bool seg_more(const Args &a, const SegCursor &c) { return (c.tile + 1) * a.kq < c.hi; }
+
+// Move to the start of the next segment (false if there is none).
+template <int TN>
+NVFP4_DEVINL bool seg_skip(const Args &a, SegCursor &c)
+{
+    if (!seg_more(a, c))
+        return false;
+    ++c.seg;
+    seg_enter<TN>(a, c, (c.tile + 1) * a.kq);
+    return true;
 }
 
 // Exact bf16 dequantisation of one 32-bit code word (k = 8q .. 8q+7) into
@@ -312,20 +346,27 @@ __global__ void __launch_bounds__(TMAC ? kThreadsTma : kThreads, 1)
     uint64_t *tmem_empty = sempty + 2;  // split mode: segment 0's accumulator has been read
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(tmem_empty + 1);
     int *last_s = reinterpret_cast<int *>(tmem_slot + 1);
+    // split mode: the chunk buffers of a fix-up by bulk copies (full,
+    // empty), and the partial slots of a shared tile's contributors (the
+    // second half of the 1024-byte barrier area)
+    uint64_t *fx_full = bars + 48, *fx_empty = bars + 48 + kFixBufs;
+    const float **contrib = reinterpret_cast<const float **>(bars + 64);
+    static_assert(3 * S + 1 + 2 * SC + 4 + 1 + 1 <= 48, "barriers, TMEM slot and flag below the fix-up barriers");
+    static_assert(48 + 2 * kFixBufs <= 64, "fix-up barriers below the contributor table");
+    static_assert(!SPLIT || (size_t)S * kBBytes >= (size_t)kFixBufs * kFixChunk, "fix-up chunks fit the activation ring");
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // A stream-K launch that follows this one on the stream may take the SMs
+    // as they free up (it computes other tiles).
+    tc::griddep_launch_dependents();
     // The CTA's k blocks: one whole tile (raster order: the host picks the
     // raster so that the operand re-read across the grid stays resident in
-    // L2), or in split mode one or two segments of its unit range.  Stage i of
-    // the CTA runs k block kb_of(i) of segment seg_of(i); ring positions follow i.
+    // L2), or in split mode the segments of its unit range.  Stage i of the
+    // CTA runs the cursor's k block; ring positions follow i.
     static_assert(!SPLIT || (NW == 1 && TMAC && FMT == 0), "split mode: one NVFP4 matrix, A in tensor memory");
-    const Segs sgs = cta_segments<TN, SPLIT>(a, blockIdx.x, gridDim.x);
-    const int64_t m0 = sgs.m0_a;
-    const int num_kb = SPLIT ? sgs.nkb_a + (sgs.n > 1 ? sgs.nkb_b : 0) : a.num_kb;
-    auto in_b = [&](int i) -> bool { return SPLIT && sgs.n > 1 && i >= sgs.nkb_a; };
-    auto kb_of = [&](int i) -> int { return in_b(i) ? sgs.kb0_b + (i - sgs.nkb_a) : sgs.kb0_a + i; };
-    auto m0_of = [&](int i) -> int64_t { return in_b(i) ? sgs.m0_b : sgs.m0_a; };
-    auto n0_of = [&](int i) -> int { return in_b(i) ? sgs.n0_b : sgs.n0_a; };
+    int num_kb;
+    const SegCursor c0 = cta_cursor<TN, SPLIT>(a, blockIdx.x, num_kb);
+    const int64_t m0 = c0.m0;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
@@ -335,6 +376,12 @@ __global__ void __launch_bounds__(TMAC ? kThreadsTma : kThreads, 1)
         }
         tc::mbar_init(tmem_full, C::kIssue);
         tc::mbar_init(tmem_empty, kDqWarps);
+        if (SPLIT) {
+            for (int b = 0; b < kFixBufs; ++b) {
+                tc::mbar_init(&fx_full[b], 1);
+                tc::mbar_init(&fx_empty[b], kDqWarps);
+            }
+        }
         if (TMAC) {
             for (int c = 0; c < SC; ++c) {
                 tc::mbar_init(&cfull[c], 1);
@@ -358,16 +405,24 @@ __global__ void __launch_bounds__(TMAC ? kThreadsTma : kThreads, 1)
     if (warp == 0) {
         // ---------------- TMA producer (x tiles) ----------------
         if (lane == 0) {
-            for (int kb = 0; kb < num_kb; ++kb) {
-                const int s = kb % S;
-                const uint32_t ph = (kb / S) & 1;
-                if (!tc::mbar_wait(&empty[s], ph ^ 1)) {
-                    fail(a, 1);
-                    break;
+            SegCursor cur = c0;
+            int kb = 0;  // the CTA's stage: ring position
+            bool ok = true;
+            do {
+                // the segment's k blocks kt (within its tile)
+                const int k1 = SPLIT ? cur.kb_end : num_kb;
+                for (int kt = SPLIT ? cur.kb : 0; kt < k1; ++kt, ++kb) {
+                    const int s = kb % S;
+                    const uint32_t ph = (kb / S) & 1;
+                    if (!tc::mbar_wait(&empty[s], ph ^ 1)) {
+                        fail(a, 1);
+                        ok = false;
+                        break;
+                    }
+                    tc::mbar_arrive_expect_tx(&full_b[s], kBBytes);
+                    tc::tma_load_2d(sb + (size_t)s * kBBytes, &tmap_x, &full_b[s], kt * BK, cur.n0);
                 }
-                tc::mbar_arrive_expect_tx(&full_b[s], kBBytes);
-                tc::tma_load_2d(sb + (size_t)s * kBBytes, &tmap_x, &full_b[s], kb_of(kb) * BK, n0_of(kb));
-            }
+            } while (SPLIT && ok && seg_skip<TN>(a, cur));
         }
     } else if (warp < kFirstDqWarp) {
         // ---------------- MMA issuers (warps 1, 2) ----------------
@@ -378,31 +433,37 @@ __global__ void __launch_bounds__(TMAC ? kThreadsTma : kThreads, 1)
         if (TA && lane == 0 && warp == 1) {
             // one issuer, one accumulator, A from tensor memory
             constexpr uint32_t idesc = tc::idesc_bf16(BM, TN);
-            for (int kb = 0; kb < num_kb; ++kb) {
-                const bool seg_start = kb == 0 || (SPLIT && sgs.n > 1 && kb == sgs.nkb_a);
-                if (SPLIT && kb > 0 && seg_start) {
-                    // split mode: segment 0 is complete; its accumulator must be
-                    // read by the epilogue before segment 1 overwrites it
-                    tc::mma_commit(tmem_full);
-                    if (!tc::mbar_wait(tmem_empty, 0)) {
-                        fail(a, 8);
+            SegCursor cur = c0;
+            int kb = 0;  // the CTA's stage: ring position
+            bool ok = true;
+            for (;;) {
+                const int k0 = SPLIT ? cur.kb : 0, k1 = SPLIT ? cur.kb_end : num_kb;
+                for (int kt = k0; kt < k1; ++kt, ++kb) {
+                    const int s = kb % S;
+                    const uint32_t ph = (kb / S) & 1;
+                    if (!tc::mbar_wait(&full_a[s], ph) || !tc::mbar_wait(&full_b[s], ph)) {
+                        fail(a, 2);
+                        ok = false;
                         break;
                     }
                     tc::fence_after_sync();
+                    const uint64_t bdesc = tc::smem_desc_sw128(sb + (size_t)s * kBBytes);
+                    const uint32_t acol = tmem_base + C::kAcol0 + s * (BK / 2);
+#pragma unroll
+                    for (int k = 0; k < BK / 16; ++k)
+                        tc::mma_f16_ts(tmem_base, acol + 8 * k, bdesc + 2 * k, idesc, (kt > k0 || k > 0) ? 1u : 0u);
+                    tc::mma_commit(&empty[s]);
                 }
-                const int s = kb % S;
-                const uint32_t ph = (kb / S) & 1;
-                if (!tc::mbar_wait(&full_a[s], ph) || !tc::mbar_wait(&full_b[s], ph)) {
-                    fail(a, 2);
+                if (!SPLIT || !ok || !seg_skip<TN>(a, cur))
+                    break;
+                // split mode: the segment is complete; its accumulator must be
+                // read by the epilogue before the next segment overwrites it
+                tc::mma_commit(tmem_full);
+                if (!tc::mbar_wait(tmem_empty, (uint32_t)(cur.seg - 1) & 1)) {
+                    fail(a, 8);
                     break;
                 }
                 tc::fence_after_sync();
-                const uint64_t bdesc = tc::smem_desc_sw128(sb + (size_t)s * kBBytes);
-                const uint32_t acol = tmem_base + C::kAcol0 + s * (BK / 2);
-#pragma unroll
-                for (int k = 0; k < BK / 16; ++k)
-                    tc::mma_f16_ts(tmem_base, acol + 8 * k, bdesc + 2 * k, idesc, (!seg_start || k > 0) ? 1u : 0u);
-                tc::mma_commit(&empty[s]);
             }
             tc::mma_commit(tmem_full);
         } else if (!TA && lane == 0) {
@@ -447,30 +508,39 @@ __global__ void __launch_bounds__(TMAC ? kThreadsTma : kThreads, 1)
                 if (FMT == 0)
                     tc::prefetch_tensormap(&wmaps.scales[mi]);
             }
-            for (int kb = 0; kb < num_kb; ++kb) {
-                if (FMT == 0 && (kb & 3) == 0) {
-                    const int sg = kb >> 2, ss = sg & 1;
-                    if (!tc::mbar_wait(&sempty[ss], ((uint32_t)(sg >> 1) & 1) ^ 1)) {
-                        fail(a, 6);
+            SegCursor cur = c0;
+            int kb = 0;  // the CTA's stage: ring position (segments are whole 4-stage groups)
+            bool ok = true;
+            do {
+                const int m0c = (int)cur.m0;
+                const int k1 = SPLIT ? cur.kb_end : num_kb;
+                for (int kt = SPLIT ? cur.kb : 0; kt < k1; ++kt, ++kb) {
+                    if (FMT == 0 && (kb & 3) == 0) {
+                        const int sg = kb >> 2, ss = sg & 1;
+                        if (!tc::mbar_wait(&sempty[ss], ((uint32_t)(sg >> 1) & 1) ^ 1)) {
+                            fail(a, 6);
+                            ok = false;
+                            break;
+                        }
+                        tc::mbar_arrive_expect_tx(&sfull[ss], NW * kSBytes);
+#pragma unroll
+                        for (int mi = 0; mi < NW; ++mi)
+                            tc::tma_load_2d(ss_ring + ((size_t)ss * NW + mi) * kSBytes, &wmaps.scales[mi],
+                                            &sfull[ss], (kt >> 2) * 16, m0c);
+                    }
+                    const int c = kb % SC;
+                    if (!tc::mbar_wait(&cempty[c], ((uint32_t)(kb / SC) & 1) ^ 1)) {
+                        fail(a, 7);
+                        ok = false;
                         break;
                     }
-                    tc::mbar_arrive_expect_tx(&sfull[ss], NW * kSBytes);
+                    tc::mbar_arrive_expect_tx(&cfull[c], NW * kCBytes);
 #pragma unroll
                     for (int mi = 0; mi < NW; ++mi)
-                        tc::tma_load_2d(ss_ring + ((size_t)ss * NW + mi) * kSBytes, &wmaps.scales[mi], &sfull[ss],
-                                        (kb_of(kb) >> 2) * 16, (int)m0_of(kb));
+                        tc::tma_load_2d(sc_ring + ((size_t)c * NW + mi) * kCBytes, &wmaps.codes[mi], &cfull[c],
+                                        kt * kCRow, m0c);
                 }
-                const int c = kb % SC;
-                if (!tc::mbar_wait(&cempty[c], ((uint32_t)(kb / SC) & 1) ^ 1)) {
-                    fail(a, 7);
-                    break;
-                }
-                tc::mbar_arrive_expect_tx(&cfull[c], NW * kCBytes);
-#pragma unroll
-                for (int mi = 0; mi < NW; ++mi)
-                    tc::tma_load_2d(sc_ring + ((size_t)c * NW + mi) * kCBytes, &wmaps.codes[mi], &cfull[c],
-                                    kb_of(kb) * kCRow, (int)m0_of(kb));
-            }
+            } while (SPLIT && ok && seg_skip<TN>(a, cur));
         }
     } else {
         // ---------------- dequantise producers ----------------
@@ -511,85 +581,197 @@ __global__ void __launch_bounds__(TMAC ? kThreadsTma : kThreads, 1)
         // is stored directly; a split segment stores its raw fp32 accumulators
         // ([token][row] in the CTA's slot) and the last CTA of the tile adds
         // every contributor's slot in CTA order.
-        auto finish_split = [&](int seg) {
-            const int dq = threadIdx.x - kFirstDqWarp * 32;  // 0..255
-            tc::named_bar_sync(1, kDqWarps * 32);             // every partial store of this CTA is done
-            const int64_t G = gridDim.x;
-            const int64_t t = seg ? sgs.tile_b : sgs.tile_a;
-            const int64_t b_lo = split_cta_of(t * a.kq, a.units, G);
-            const int64_t b_hi = split_cta_of((t + 1) * a.kq - 1, a.units, G);
-            if (dq == 0) {
-                // release: this CTA's partial (ordered by the barrier); acquire: the others'
-                uint32_t old;
-                asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(old) : "l"(a.counters + t) : "memory");
-                *last_s = old == (uint32_t)(b_hi - b_lo);
-                if (*last_s)
-                    a.counters[t] = 0;
-            }
-            tc::named_bar_sync(1, kDqWarps * 32);
-            if (!*last_s)
-                return;
-            // thread: rows 4 rq .. 4 rq + 3 (one 16-byte load per contributor and
-            // token), token columns cg, cg + 8, ...; contributors added in CTA order
-            const int rq = dq & 31, cg = dq >> 5;
-            const int64_t mq = (seg ? sgs.m0_b : sgs.m0_a) + 4 * rq;
-            const int64_t sn0 = seg ? sgs.n0_b : sgs.n0_a;
-            const float tsv = FMT == 0 ? __ldg(a.ts[0]) * 256.0f : 1.0f;
-            const int nc = (int)(b_hi - b_lo) + 1;
-            const float *src[4];
-            for (int c = 0; c < 4; ++c) {
-                const int64_t bb = b_lo + (c < nc ? c : nc - 1);
-                src[c] = a.partial + (size_t)(2 * bb + (t - (bb * a.units / G) / a.kq)) * TN * BM + 4 * rq;
-            }
-#pragma unroll 2
-            for (int col = cg; col < TN; col += 8) {
-                const int64_t n = sn0 + col;
-                if (n >= a.N)
-                    break;
-                float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-                for (int c0 = 0; c0 < nc; c0 += 4) {
-                    float4 v[4];
+        // Store four rows (mq .. mq + 3) of token n of a shared tile's sum.
+        auto store4 = [&](int64_t n, int64_t mq, float4 v) {
+            const int64_t idx = n * a.M + mq;
+            if ((a.M & 3) == 0 && mq + 3 < a.M) {  // 16- / 8-byte aligned, all in range
+                if (a.out_bf16)
+                    *reinterpret_cast<uint2 *>(reinterpret_cast<uint16_t *>(a.y) + idx) =
+                        make_uint2(f32_to_bf16(v.x) | ((uint32_t)f32_to_bf16(v.y) << 16),
+                                   f32_to_bf16(v.z) | ((uint32_t)f32_to_bf16(v.w) << 16));
+                else
+                    *reinterpret_cast<float4 *>(reinterpret_cast<float *>(a.y) + idx) = v;
+            } else {
+                const float r4[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        const float *p = c0 == 0 ? src[c] : a.partial + (size_t)(2 * (b_lo + c0 + c) +
-                                            (t - ((b_lo + c0 + c) * a.units / G) / a.kq)) * TN * BM + 4 * rq;
-                        v[c] = (c0 + c < nc) ? __ldcg(reinterpret_cast<const float4 *>(p + (size_t)col * BM))
-                                             : make_float4(0.f, 0.f, 0.f, 0.f);
-                    }
-#pragma unroll
-                    for (int c = 0; c < 4; ++c)
-                        if (c0 + c < nc) {
-                            acc.x += v[c].x;
-                            acc.y += v[c].y;
-                            acc.z += v[c].z;
-                            acc.w += v[c].w;
-                        }
-                }
-                const float r4[4] = {acc.x, acc.y, acc.z, acc.w};
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int64_t m = mq + e;
-                    if (m < a.M) {
-                        const float vv = r4[e] * tsv;
-                        const int64_t idx = n * a.M + m;
+                for (int e = 0; e < 4; ++e)
+                    if (mq + e < a.M) {
                         if (a.out_bf16)
-                            reinterpret_cast<uint16_t *>(a.y)[idx] = f32_to_bf16(vv);
+                            reinterpret_cast<uint16_t *>(a.y)[idx + e] = f32_to_bf16(r4[e]);
                         else
-                            reinterpret_cast<float *>(a.y)[idx] = vv;
+                            reinterpret_cast<float *>(a.y)[idx + e] = r4[e];
+                    }
+            }
+        };
+        // Sum of a shared tile's partials through shared memory: chunk i is
+        // the q-th 64 token columns (q = i / nc) of contributor i % nc, in
+        // buffer i % kFixBufs of the activation ring; one thread issues the
+        // bulk copies, every thread adds rows 4 rq .. 4 rq + 3 of columns
+        // cg + 8 j of each chunk in contributor order.
+        auto fixup_bulk = [&](const SegCursor &sg, int nc) {
+            const int dq = threadIdx.x - kFirstDqWarp * 32;  // 0..255
+            const int rq = dq & 31, cg = dq >> 5;
+            const int ncols = (int)(a.N - sg.n0 < TN ? a.N - sg.n0 : TN);
+            const int chunks = ((ncols + kFixCols - 1) / kFixCols) * nc;
+            const float tsv = __ldg(a.ts[0]) * 256.0f;
+            auto issue = [&](int i) {
+                const int b = i % kFixBufs;
+                if (!tc::mbar_wait(&fx_empty[b], ((uint32_t)(i / kFixBufs) & 1) ^ 1)) {
+                    fail(a, 10);
+                    return;
+                }
+                tc::mbar_arrive_expect_tx(&fx_full[b], kFixChunk);
+                tc::bulk_load(sb + (size_t)b * kFixChunk, contrib[i % nc] + (size_t)(i / nc) * (kFixChunk / 4),
+                              kFixChunk, &fx_full[b]);
+            };
+            if (dq == 0)
+                for (int i = 0; i < kFixBufs && i < chunks; ++i)
+                    issue(i);
+            float4 acc[kFixCols / 8];
+            for (int i = 0; i < chunks; ++i) {
+                const int b = i % kFixBufs, c = i % nc, q = i / nc;
+                if (c == 0) {
+#pragma unroll
+                    for (int j = 0; j < kFixCols / 8; ++j)
+                        acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+                if (!tc::mbar_wait(&fx_full[b], (uint32_t)(i / kFixBufs) & 1)) {
+                    fail(a, 11);
+                    return;
+                }
+                const float4 *src = reinterpret_cast<const float4 *>(sb + (size_t)b * kFixChunk);
+#pragma unroll
+                for (int j = 0; j < kFixCols / 8; ++j) {
+                    const float4 v = src[(cg + 8 * j) * (BM / 4) + rq];  // column cg + 8 j, rows 4 rq ..
+                    acc[j].x += v.x;
+                    acc[j].y += v.y;
+                    acc[j].z += v.z;
+                    acc[j].w += v.w;
+                }
+                __syncwarp();
+                if (lane == 0)
+                    tc::mbar_arrive(&fx_empty[b]);
+                if (dq == 0 && i + kFixBufs < chunks)
+                    issue(i + kFixBufs);
+                if (c == nc - 1) {
+#pragma unroll
+                    for (int j = 0; j < kFixCols / 8; ++j) {
+                        const int col = q * kFixCols + cg + 8 * j;
+                        if (col < ncols)
+                            store4(sg.n0 + col, sg.m0 + 4 * rq,
+                                   make_float4(acc[j].x * tsv, acc[j].y * tsv, acc[j].z * tsv, acc[j].w * tsv));
                     }
                 }
             }
         };
-        auto epilogue = [&](int seg) {
-            bool have = tc::mbar_wait(tmem_full, (uint32_t)seg & 1);
-            const bool split_seg = SPLIT && !(seg ? sgs.whole_b : sgs.whole_a);
+        auto finish_split = [&](const SegCursor &sg) {
+            const int dq = threadIdx.x - kFirstDqWarp * 32;  // 0..255
+            tc::named_bar_sync(1, kDqWarps * 32);             // every partial store of this CTA is done
+            const int64_t G = a.sk_grid;
+            const int64_t t = sg.tile;  // a stream-K tile (sk_base is a tile boundary)
+            const int64_t b_lo = split_cta_of(t * a.kq - a.sk_base, a.units, G);
+            const int64_t b_hi = split_cta_of((t + 1) * a.kq - 1 - a.sk_base, a.units, G);
+            const int nc = (int)(b_hi - b_lo) + 1;  // contributors (<= kMaxContrib, by the host's plan)
+            if (nc > kMaxContrib) {  // cannot happen with the host's plan: refuse rather than overrun the table
+                if (dq == 0)
+                    fail(a, 9);
+                return;
+            }
+            if (dq == 0) {
+                // The counters are zeroed by the launch before this one on
+                // the stream, which it may overlap (programmatic dependent
+                // launch): wait for that launch before the first use (a no-op
+                // once it has completed).  After a whole-tile launch the
+                // zeroing came before that launch, and waiting would stall
+                // the fix-up until the last whole tile is done.
+                if (!a.after_whole)
+                    tc::griddep_wait();
+                // release: this CTA's partial (ordered by the barrier); acquire:
+                // the others'.  A CTA is the first contributor of at most one
+                // shared tile (its last segment), so the counter is b_lo's.
+                uint32_t old;
+                asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;"
+                             : "=r"(old)
+                             : "l"(a.counters + b_lo)
+                             : "memory");
+                *last_s = old == (uint32_t)(nc - 1);
+                if (*last_s)
+                    a.counters[b_lo] = 0;
+            }
+            // contributor c's partial of tile t: its first segment's slot if t
+            // is its first tile, else its last segment's (one 64-bit division
+            // each, so computed once)
+            if (dq < nc)
+                contrib[dq] = a.partial +
+                              (size_t)(2 * (b_lo + dq) + (t != sk_first_tile(a, b_lo + dq) ? 1 : 0)) * TN * BM;
+            tc::named_bar_sync(1, kDqWarps * 32);
+            if (!*last_s)
+                return;
+            if (!seg_more(a, sg)) {
+                // the CTA's last segment: its activation ring is idle, so
+                // the partials come in by bulk copies, 32 KB chunks in four
+                // buffers
+                fixup_bulk(sg, nc);
+                return;
+            }
+            // thread: rows 4 rq .. 4 rq + 3 and token columns cg + 8 i; four
+            // columns per pass and four contributors per load batch, so that
+            // sixteen 16-byte loads are in flight; contributors are added in
+            // CTA order
+            const int rq = dq & 31, cg = dq >> 5;
+            const int64_t mq = sg.m0 + 4 * rq;
+            const int ncols = (int)(a.N - sg.n0 < TN ? a.N - sg.n0 : TN);
+            const float tsv = FMT == 0 ? __ldg(a.ts[0]) * 256.0f : 1.0f;
+#pragma unroll 1
+            for (int col0 = cg; col0 < ncols; col0 += 32) {
+                float4 acc[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 1
+                for (int c0 = 0; c0 < nc; c0 += 4) {
+                    float4 v[4][4];
+#pragma unroll
+                    for (int c = 0; c < 4; ++c)
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            const int col = col0 + 8 * j;
+                            v[c][j] = (c0 + c < nc && col < ncols)
+                                          ? __ldcg(reinterpret_cast<const float4 *>(contrib[c0 + c] +
+                                                                                    (size_t)col * BM + 4 * rq))
+                                          : make_float4(0.f, 0.f, 0.f, 0.f);
+                        }
+#pragma unroll
+                    for (int c = 0; c < 4; ++c)
+#pragma unroll
+                        for (int j = 0; j < 4; ++j)
+                            if (c0 + c < nc) {
+                                acc[j].x += v[c][j].x;
+                                acc[j].y += v[c][j].y;
+                                acc[j].z += v[c][j].z;
+                                acc[j].w += v[c][j].w;
+                            }
+                }
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const int col = col0 + 8 * j;
+                    if (col >= ncols)
+                        break;
+                    store4(sg.n0 + col, mq,
+                           make_float4(acc[j].x * tsv, acc[j].y * tsv, acc[j].z * tsv, acc[j].w * tsv));
+                }
+            }
+        };
+        auto epilogue = [&](const SegCursor &sg) {
+            bool have = tc::mbar_wait(tmem_full, (uint32_t)sg.seg & 1);
+            const bool split_seg = SPLIT && !sg.whole;
             if (SPLIT)
                 have = tc::bar_and(1, kDqWarps * 32, have);  // uniform: named barriers follow
             if (!have)
                 fail(a, 4);
             tc::fence_after_sync();
-            const int64_t sm0 = seg ? sgs.m0_b : sgs.m0_a;
-            const int sn0 = seg ? sgs.n0_b : sgs.n0_a;
+            const int64_t sm0 = sg.m0;
+            const int sn0 = sg.n0;
             if (have) {
                 const int quarter = warp & 3;          // TMEM lanes this warp may access
                 const int chalf = (warp - kFirstDqWarp) >> 2;  // which half of the TN token columns
@@ -598,7 +780,12 @@ __global__ void __launch_bounds__(TMAC ? kThreadsTma : kThreads, 1)
 #pragma unroll
                 for (int mi = 0; mi < NW; ++mi)
                     ts[mi] = FMT == 0 ? __ldg(a.ts[mi]) * 256.0f : 1.0f;
-                float *slot = a.partial + (size_t)(2 * blockIdx.x + seg) * TN * BM + quarter * 32 + lane;
+                // a partial segment is the first (slot 0) or last (slot 1) of the
+                // CTA's stream-K range
+                float *slot = a.partial +
+                              (size_t)(2 * blockIdx.x + (SPLIT && sg.tile != sk_first_tile(a, blockIdx.x) ? 1 : 0)) *
+                                  TN * BM +
+                              quarter * 32 + lane;
                 // TA: only column chunks holding at least one real token
                 // (warp-uniform; a runtime bound also keeps this loop rolled)
 #pragma unroll 1
@@ -640,8 +827,8 @@ __global__ void __launch_bounds__(TMAC ? kThreadsTma : kThreads, 1)
                     }
                 }
             }
-            if (SPLIT && seg + 1 < sgs.n) {
-                // segment 1 follows: hand the accumulator back to the MMA issuer
+            if (SPLIT && seg_more(a, sg)) {
+                // another segment follows: hand the accumulator back to the MMA issuer
                 tc::fence_before_sync();
                 __syncwarp();
                 if (lane == 0)
@@ -649,10 +836,10 @@ __global__ void __launch_bounds__(TMAC ? kThreadsTma : kThreads, 1)
             }
             if constexpr (SPLIT) {
                 if (split_seg && have)
-                    finish_split(seg);
+                    finish_split(sg);
             }
         };
-        bool epi0_done = false;
+        SegCursor dcur = c0;  // the dequantisers' stage cursor
         if constexpr (TMAC && FMT == 1) {
             // FP6 codes from the TMA ring; the scale byte of a row (one per
             // 128 k = two stages) through a small register prefetch ring.
@@ -729,63 +916,69 @@ __global__ void __launch_bounds__(TMAC ? kThreadsTma : kThreads, 1)
         if constexpr (TMAC && FMT == 0) {
             // Codes and scales from the TMA rings; a warp releases a ring slot
             // once its lanes have turned the slot's bytes into bf16 tiles.
-            for (int kb = 0; kb < num_kb; ++kb) {
-                if (SPLIT && sgs.n > 1 && kb == sgs.nkb_a) {  // split mode: segment 0 is done
-                    epilogue(0);
-                    epi0_done = true;
-                }
-                const int c = kb % SC;
-                const int ss = (kb >> 2) & 1;
-                if (!tc::mbar_wait(&cfull[c], (uint32_t)(kb / SC) & 1) ||
-                    ((kb & 3) == 0 && !tc::mbar_wait(&sfull[ss], (uint32_t)(kb >> 3) & 1))) {
-                    fail(a, 5);
-                    ok = false;
-                    break;
-                }
-                DqItem cur[NW];
+            // Stage kb is a ring position; in split mode the segments follow
+            // one another, each ending with its epilogue.
+            int kb = 0;
+            for (;;) {
+                const int kend = kb + (SPLIT ? dcur.kb_end - dcur.kb : num_kb);
+                for (; kb < kend; ++kb) {
+                    const int c = kb % SC;
+                    const int ss = (kb >> 2) & 1;
+                    if (!tc::mbar_wait(&cfull[c], (uint32_t)(kb / SC) & 1) ||
+                        ((kb & 3) == 0 && !tc::mbar_wait(&sfull[ss], (uint32_t)(kb >> 3) & 1))) {
+                        fail(a, 5);
+                        ok = false;
+                        break;
+                    }
+                    DqItem cur[NW];
 #pragma unroll
-                for (int mi = 0; mi < NW; ++mi) {
-                    cur[mi].code = *reinterpret_cast<const uint4 *>(sc_ring + ((size_t)c * NW + mi) * kCBytes +
-                                                                    row * kCRow + half * 16);
-                    cur[mi].scl = *reinterpret_cast<const uint16_t *>(ss_ring + ((size_t)ss * NW + mi) * kSBytes +
-                                                                      row * 16 + (kb & 3) * 4 + half * 2);
-                }
-                const int s = kb % S;
-                if (!tc::mbar_wait(&empty[s], ((uint32_t)(kb / S) & 1) ^ 1)) {
-                    fail(a, 3);
-                    ok = false;
-                    break;
-                }
-                if (TA)
-                    tc::fence_after_sync();  // the MMAs that read this A stage are complete
+                    for (int mi = 0; mi < NW; ++mi) {
+                        cur[mi].code = *reinterpret_cast<const uint4 *>(sc_ring + ((size_t)c * NW + mi) * kCBytes +
+                                                                        row * kCRow + half * 16);
+                        cur[mi].scl = *reinterpret_cast<const uint16_t *>(ss_ring + ((size_t)ss * NW + mi) * kSBytes +
+                                                                          row * 16 + (kb & 3) * 4 + half * 2);
+                    }
+                    const int s = kb % S;
+                    if (!tc::mbar_wait(&empty[s], ((uint32_t)(kb / S) & 1) ^ 1)) {
+                        fail(a, 3);
+                        ok = false;
+                        break;
+                    }
+                    if (TA)
+                        tc::fence_after_sync();  // the MMAs that read this A stage are complete
 #pragma unroll
-                for (int mi = 0; mi < NW; ++mi) {
-                    const uint32_t mlo = scale_mult_bf16(cur[mi].scl);
-                    const uint32_t mhi = scale_mult_bf16(cur[mi].scl >> 8);
-                    const uint32_t words[4] = {cur[mi].code.x, cur[mi].code.y, cur[mi].code.z, cur[mi].code.w};
-                    if constexpr (TA) {
-                        uint4 v[4];
+                    for (int mi = 0; mi < NW; ++mi) {
+                        const uint32_t mlo = scale_mult_bf16(cur[mi].scl);
+                        const uint32_t mhi = scale_mult_bf16(cur[mi].scl >> 8);
+                        const uint32_t words[4] = {cur[mi].code.x, cur[mi].code.y, cur[mi].code.z, cur[mi].code.w};
+                        if constexpr (TA) {
+                            uint4 v[4];
 #pragma unroll
-                        for (int q = 0; q < 4; ++q)
-                            v[q] = dequant_word_natural(words[q], q < 2 ? mlo : mhi);
-                        put_a_tmem(s, v);
-                    } else {
-                        uint8_t *arow = sa + ((size_t)s * NW + mi) * kABytes + row * 128;
+                            for (int q = 0; q < 4; ++q)
+                                v[q] = dequant_word_natural(words[q], q < 2 ? mlo : mhi);
+                            put_a_tmem(s, v);
+                        } else {
+                            uint8_t *arow = sa + ((size_t)s * NW + mi) * kABytes + row * 128;
 #pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            const uint4 v = dequant_word_natural(words[q], q < 2 ? mlo : mhi);
-                            const int chunk = half * 4 + q;
-                            *reinterpret_cast<uint4 *>(arow + ((chunk ^ (row & 7)) << 4)) = v;
+                            for (int q = 0; q < 4; ++q) {
+                                const uint4 v = dequant_word_natural(words[q], q < 2 ? mlo : mhi);
+                                const int chunk = half * 4 + q;
+                                *reinterpret_cast<uint4 *>(arow + ((chunk ^ (row & 7)) << 4)) = v;
+                            }
                         }
                     }
+                    publish_a(s);
+                    __syncwarp();
+                    if (lane == 0) {
+                        tc::mbar_arrive(&cempty[c]);
+                        if ((kb & 3) == 3)
+                            tc::mbar_arrive(&sempty[ss]);
+                    }
                 }
-                publish_a(s);
-                __syncwarp();
-                if (lane == 0) {
-                    tc::mbar_arrive(&cempty[c]);
-                    if ((kb & 3) == 3)
-                        tc::mbar_arrive(&sempty[ss]);
-                }
+                if (!SPLIT || !ok || !seg_more(a, dcur))
+                    break;
+                epilogue(dcur);
+                seg_skip<TN>(a, dcur);
             }
         }
         auto load = [&](int mi, int kb) -> Item {
@@ -850,10 +1043,13 @@ __global__ void __launch_bounds__(TMAC ? kThreadsTma : kThreads, 1)
             }
         }
 
-        if (SPLIT && sgs.n > 1 && !epi0_done)
-            epilogue(0);
-        if (!SPLIT || sgs.n > 0)
-            epilogue(SPLIT ? sgs.n - 1 : 0);
+        // The last segment's epilogue.  After a failed wait the loop ends
+        // early: the epilogues of the segments it did not reach still run
+        // (their waits give up too), so that every dequantiser warp meets the
+        // epilogues' named barriers the same number of times.
+        do {
+            epilogue(dcur);
+        } while (SPLIT && seg_skip<TN>(a, dcur));
     }
 
     // Lane 0 of warps 0 and 1 ran the producer / MMA loops alone: reconverge
@@ -866,6 +1062,21 @@ __global__ void __launch_bounds__(TMAC ? kThreadsTma : kThreads, 1)
         tc::fence_after_sync();
         tc::tmem_dealloc(tmem_base, C::kTmemCols);
     }
+    // A stream-K launch overlaps the launch before it on the stream (the
+    // counter zeroing, or the whole tiles: it reads nothing they write but
+    // the counters) and completes only after it, so that work ordered after
+    // this call sees every tile.
+    if (SPLIT && threadIdx.x == 0)
+        tc::griddep_wait();
+}
+
+// Zero the split-mode arrival counters; a stream-K launch that follows may
+// start at once (it waits for this one before its first counter access).
+__global__ void split_counters_zero_kernel(uint32_t *counters, int n)
+{
+    tc::griddep_launch_dependents();
+    for (int i = threadIdx.x; i < n; i += blockDim.x)
+        counters[i] = 0;
 }
 
 // ---------------------------------------------------------------------------
@@ -900,6 +1111,21 @@ cudaError_t launch_t(const CUtensorMap &map, const WeightMaps &wm, const Args &a
     if (attr_err != cudaSuccess)
         return attr_err;
     dim3 grid((unsigned)a.grid);
+    if (SPLIT) {
+        // programmatic dependent launch: the CTAs start on SMs the launch
+        // before it has finished with
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = grid;
+        cfg.blockDim = dim3(TMAC ? kThreadsTma : kThreads);
+        cfg.dynamicSmemBytes = C::kSmemBytes;
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        return cudaLaunchKernelEx(&cfg, prefill_kernel<NW, ALIGNED, FMT, TMAC, TN, SPLIT>, map, wm, a);
+    }
     prefill_kernel<NW, ALIGNED, FMT, TMAC, TN, SPLIT>
         <<<grid, TMAC ? kThreadsTma : kThreads, C::kSmemBytes, stream>>>(map, wm, a);
     return cudaGetLastError();
@@ -934,31 +1160,114 @@ static bool encode_rows(PFN_cuTensorMapEncodeTiled_v12000 encode, CUtensorMap *m
 
 }  // namespace pf
 
-// Split mode (see Args): one NVFP4 matrix with K % 256 == 0 whose 256-token
-// tiles would fill less than three quarters of the SMs.  Its workspace holds
-// the tile counters and two partial slots per CTA; the size bound holds for
-// any device with up to kMaxSplitCtas SMs, so it depends on the shape alone.
+// Split mode (see Args): one NVFP4 matrix with K % 256 == 0.  Its workspace
+// holds a counter and two partial slots per CTA; the grid has at most
+// min(kMaxSplitCtas, units) CTAs, so the size depends on the shape alone.
 constexpr int kMaxSplitCtas = 256;
-constexpr size_t kSplitCounterBytes = 1024;  // one u32 per tile (< kMaxSplitCtas tiles)
+constexpr size_t kSplitCounterBytes = 1024;  // one u32 per CTA
 
-static bool split_possible(int64_t N, int64_t M, int64_t K, int n_weights)
+static bool split_possible(int64_t K, int n_weights, int fmt) { return fmt == 0 && n_weights == 1 && K % 256 == 0; }
+
+static int64_t split_units(int64_t N, int64_t M, int64_t K)
 {
-    const int64_t tiles = ((M + pf::BM - 1) / pf::BM) * ((N + pf::BN - 1) / pf::BN);
-    return n_weights == 1 && K % 256 == 0 && tiles * 4 < (int64_t)kMaxSplitCtas * 3;
+    return ((M + pf::BM - 1) / pf::BM) * ((N + pf::BN - 1) / pf::BN) * (K / 256);
 }
 
-static bool use_split(int64_t N, int64_t M, int64_t K, int n_weights, int num_sms)
+// How a split call shares its work (see Args).
+struct SplitPlan {
+    int64_t dp_waves;  // waves of whole tiles in a launch of their own, before the stream-K launch
+    int64_t units;     // stream-K units after them
+    int64_t sk_grid;   // CTAs sharing the stream-K units
+};
+
+// Of the 129 MB L2, what a launch's operands may take and still be read from
+// HBM about once.
+constexpr double kL2Budget = 110e6;
+
+// The split for a single NVFP4 matrix, and whether it beats whole tiles
+// alone.  Two forms:
+//   - operands resident in L2 (x and the weights fit): every unit is shared
+//     out, each CTA an equal contiguous range (up to two partial tiles);
+//     CTAs at different k of a tile cost nothing extra when nothing is
+//     evicted;
+//   - otherwise the full waves run as whole tiles (a launch of their own)
+//     and the R = tiles mod SMs tiles left split into f equal k slices, one
+//     CTA each: slice j of every tile starts at the same k, so the CTAs
+//     sharing a token tile still read the same activations at the same
+//     time, as in a wave.
+// Time in 64-k stages of a 256-token tile: a tile of TN tokens takes
+// num_kb * (0.25 + TN / 256) / 1.25 stages plus kFixed (prologue, pipeline
+// fill, epilogue); whole tiles run in waves of num_sms CTAs.  A split CTA
+// pays kFixed for each of up to three segments, and the last CTA of a shared
+// tile to arrive adds every contributor's 128 KB partial: kPerContrib stages
+// each.  A tile has at most kMaxContrib contributors.
+static bool split_plan(int64_t N, int64_t M, int64_t K, int n_weights, int fmt, int num_sms, SplitPlan *sp)
 {
-    const int64_t tiles = ((M + pf::BM - 1) / pf::BM) * ((N + pf::BN - 1) / pf::BN);
-    return split_possible(N, M, K, n_weights) && num_sms <= kMaxSplitCtas && tiles * 4 < (int64_t)num_sms * 3;
+    if (!split_possible(K, n_weights, fmt) || num_sms > kMaxSplitCtas)
+        return false;
+    constexpr double kFixed = 10.0, kPerContrib = 2.0;
+    const int64_t row_tiles = (M + pf::BM - 1) / pf::BM;
+    const int64_t kq = K / 256;
+    const double num_kb = (double)(K / pf::BK);
+    auto whole = [&](int tn) {
+        const int64_t ctas = row_tiles * ((N + tn - 1) / tn);
+        const int64_t waves = (ctas + num_sms - 1) / num_sms;
+        return (double)waves * (num_kb * (0.25 + tn / 256.0) / 1.25 + kFixed);
+    };
+    const double best_whole = whole(192) < whole(256) ? whole(192) : whole(256);
+    const int64_t tiles = row_tiles * ((N + pf::BN - 1) / pf::BN);
+    const double operand_bytes = (double)N * (double)K * 2.0 + (double)M * (double)K * 0.5625;
+    double t_split;
+    if (operand_bytes <= kL2Budget) {
+        sp->dp_waves = 0;
+        sp->units = tiles * kq;
+        int64_t G = sp->units < num_sms ? sp->units : num_sms;
+        // ranges of at least units / G units: a tile meets at most
+        // ceil(kq / (units / G)) + 1 of them
+        auto contributors = [&](int64_t g) {
+            const int64_t u = sp->units / g;
+            return (kq + u - 1) / u + 1;
+        };
+        while (G > 1 && contributors(G) > pf::kMaxContrib)
+            --G;
+        sp->sk_grid = G;
+        t_split = (double)sp->units * 4.0 / G + 3.0 * kFixed + kPerContrib * (double)contributors(G);
+    } else {
+        const int64_t rem = tiles % num_sms;
+        if (rem == 0)
+            return false;
+        int64_t fmax = num_sms / rem;
+        fmax = fmax < kq ? fmax : kq;
+        fmax = fmax < pf::kMaxContrib ? fmax : pf::kMaxContrib;
+        int64_t f = 1;
+        double best = num_kb;
+        for (int64_t ff = 2; ff <= fmax; ++ff) {
+            const double tf = num_kb / (double)ff + kPerContrib * (double)ff;
+            if (tf < best) {
+                best = tf;
+                f = ff;
+            }
+        }
+        if (f < 2)
+            return false;
+        sp->dp_waves = tiles / num_sms;
+        sp->units = rem * kq;
+        sp->sk_grid = rem * f;
+        t_split = (double)sp->dp_waves * (num_kb + kFixed) + best + 3.0 * kFixed;
+    }
+    if (sp->units / sp->sk_grid > (int64_t(1) << 24))
+        return false;  // a CTA's stage count must fit an int
+    return t_split < best_whole;
 }
 
-size_t prefill_workspace_bytes(int64_t N, int64_t M, int64_t K, int n_weights)
+size_t prefill_workspace_bytes(int64_t N, int64_t M, int64_t K, int n_weights, int fmt)
 {
     // the device status word at kStatusWordOffset; split mode adds its counters and partials
-    if (!split_possible(N, M, K, n_weights))
+    if (!split_possible(K, n_weights, fmt))
         return 256;
-    return 256 + kSplitCounterBytes + (size_t)2 * kMaxSplitCtas * pf::BN * pf::BM * sizeof(float);
+    const int64_t units = split_units(N, M, K);
+    const int64_t ctas = units < kMaxSplitCtas ? units : kMaxSplitCtas;
+    return 256 + kSplitCounterBytes + (size_t)2 * ctas * pf::BN * pf::BM * sizeof(float);
 }
 
 static cudaError_t prefill_impl(const uint16_t *x, int64_t N, int64_t M, int64_t K, const uint8_t *const *codes,
@@ -970,7 +1279,8 @@ static cudaError_t prefill_impl(const uint16_t *x, int64_t N, int64_t M, int64_t
         return cudaErrorNotSupported;
     const bool tma_weights = fmt == 1 || K % 256 == 0;
     const int64_t row_tiles = (M + pf::BM - 1) / pf::BM;
-    const bool split = fmt == 0 && use_split(N, M, K, n_weights, num_sms);
+    SplitPlan sp{};
+    const bool split = split_plan(N, M, K, n_weights, fmt, num_sms, &sp);
     const int tn = split ? pf::BN : tma_weights ? pf::pick_token_tile(N, row_tiles, num_sms) : pf::BN;
     const int64_t token_tiles = (N + tn - 1) / tn;
     if (row_tiles * token_tiles > 0x7FFFFFFF)
@@ -1005,15 +1315,19 @@ static cudaError_t prefill_impl(const uint16_t *x, int64_t N, int64_t M, int64_t
     if (split) {
         uint8_t *ws = reinterpret_cast<uint8_t *>(workspace);
         a.kq = a.num_kb / 4;
-        a.units = row_tiles * token_tiles * a.kq;
+        a.after_whole = sp.dp_waves > 0;
+        a.sk_base = sp.dp_waves * num_sms * a.kq;
+        a.units = sp.units;
         a.counters = reinterpret_cast<uint32_t *>(ws + 256);
         a.partial = reinterpret_cast<float *>(ws + 256 + kSplitCounterBytes);
-        // at most one CTA per unit: every CTA's range is non-empty, so a
+        // at most one stream-K CTA per unit: every range is non-empty, so a
         // tile's contributors are the contiguous CTAs b_lo .. b_hi
-        a.grid = (int)std::min<int64_t>(num_sms, a.units);
-        const cudaError_t me = cudaMemsetAsync(a.counters, 0, (size_t)row_tiles * token_tiles * 4, stream);
-        if (me != cudaSuccess)
-            return me;
+        a.sk_grid = (int)sp.sk_grid;
+        a.grid = a.sk_grid;
+        pf::split_counters_zero_kernel<<<1, 256, 0, stream>>>(a.counters, a.grid);
+        const cudaError_t ze = cudaGetLastError();
+        if (ze != cudaSuccess)
+            return ze;
     } else {
         a.grid = (int)(row_tiles * token_tiles);
     }
@@ -1025,7 +1339,6 @@ static cudaError_t prefill_impl(const uint16_t *x, int64_t N, int64_t M, int64_t
         // weights fit.  (Keeping the 50 MB of weights resident instead of the
         // 71 MB of activations for the 27B down projection at N = 2048 was
         // measured slower: 0.50 against 0.54 of the bf16 peak.)
-        constexpr double kL2Budget = 110e6;  // of the 129 MB L2
         const double x_bytes = (double)N * (double)K * 2.0;
         const double w_tile = (double)pf::BM * (double)K * (fmt == 1 ? 0.7578125 : 0.5625) * n_weights;
         int g;
@@ -1056,8 +1369,19 @@ static cudaError_t prefill_impl(const uint16_t *x, int64_t N, int64_t M, int64_t
             if (!pf::encode_rows(encode, &wm.codes[i], codes[i], K / 2, M, pf::BK / 2) ||
                 !pf::encode_rows(encode, &wm.scales[i], scales[i], K / 16, M, 16))
                 return cudaErrorInvalidValue;
-        if (split)
+        if (split) {
+            if (sp.dp_waves > 0) {
+                // the full waves: whole tiles 0 .. dp_waves * SMs - 1
+                pf::Args w = a;
+                w.split = 0;
+                w.after_whole = 0;
+                w.grid = (int)(sp.dp_waves * num_sms);
+                const cudaError_t e = pf::launch_t<1, true, 0, true, 256>(map, wm, w, stream);
+                if (e != cudaSuccess)
+                    return e;
+            }
             return pf::launch_t<1, true, 0, true, 256, true>(map, wm, a, stream);
+        }
         if (tn == 192)
             return n_weights == 1 ? pf::launch_t<1, true, 0, true, 192>(map, wm, a, stream)
                                   : pf::launch_t<2, true, 0, true, 192>(map, wm, a, stream);

@@ -95,12 +95,7 @@ NVFP4_DEVINL uint32_t atom_add_acq_rel(uint32_t *p, uint32_t v)
 
 NVFP4_DEVINL float silu_mul(float g, float u) { return __fdiv_rn(g, 1.0f + expf(-g)) * u; }
 
-NVFP4_DEVINL void bulk_load(void *dst, const void *src, uint32_t bytes, uint64_t *bar)
-{
-    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-                 ::"r"(tc::smem_addr(dst)), "l"(src), "r"(bytes), "r"(tc::smem_addr(bar))
-                 : "memory");
-}
+using tc::bulk_load;
 
 // Host: encode a 2-D TMA tensor map (inner dimension first); false if the
 // driver entry point is missing or the encoder rejects the arguments.

@@ -272,6 +272,15 @@ NVFP4_DEVINL uint64_t smem_desc_kmajor_sw128(const void *base) { return smem_des
 NVFP4_DEVINL void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 NVFP4_DEVINL void griddep_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
+// Untiled bulk copy global -> shared memory of `bytes` (a multiple of 16;
+// both addresses 16-byte aligned), completing on `bar` as transaction bytes.
+NVFP4_DEVINL void bulk_load(void *dst, const void *src, uint32_t bytes, uint64_t *bar)
+{
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                 ::"r"(smem_addr(dst)), "l"(src), "r"(bytes), "r"(smem_addr(bar))
+                 : "memory");
+}
+
 NVFP4_DEVINL void named_bar_sync(uint32_t id, uint32_t nthreads)
 {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");

@@ -64,11 +64,11 @@
  *     summation order is part of the contract: bw24 wiki Home, list of checks
  *     every kernel change must pass, and bw24 README, where decode and verify
  *     launch the same kernel symbols and agree bit for bit).  For N > 16 (the
- *     tensor-core prefill kernel) a shape with too few tiles to fill the SMs
- *     splits K across thread blocks in a way that depends on N, so rows of
- *     calls with different N > 16 (and across N = 16) agree within the
- *     accuracy bound below, bit for bit only when neither call splits.  A skinny call in which
- *     some token's activations are not all exact in f16 after scaling by a
+ *     tensor-core prefill kernel) a single matrix whose tiles would leave the
+ *     last wave of SMs poorly filled splits K across thread blocks (stream-K)
+ *     in a way that depends on N, so rows of calls with different N > 16 (and
+ *     across N = 16) agree within the accuracy bound below, bit for bit only
+ *     when neither call splits.  A skinny call in which some token's activations are not all exact in f16 after scaling by a
  *     power of two (a dynamic range wider than f16's) switches the whole call
  *     to bf16 operands; its rows also agree within the bound.
  *   - Accuracy: every product code * scale * x is exact (bf16 operands, fp32

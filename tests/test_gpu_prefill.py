@@ -129,13 +129,15 @@ def test_token_rows_independent_of_tile_choice(fmt):
     """The launch picks 192- or 256-token tiles from N and the SM count
     (N = 600 and N = 4096 over 64 row tiles take different tiles on a 152-SM
     GPU; N = 300 fills two token tiles); a token's row is the same bits either
-    way.  These shapes keep enough tiles to fill the SMs, so no call splits K."""
+    way.  The operations here never split K (an NVFP4 gate/up pair, one FP6
+    matrix), so the contract is bit identity."""
     M, K = 8192, 1024
     w = inputs.weights(M, K, seed=81, device=DEV)
     x = inputs.activations(4096, K, seed=82, device=DEV)
     if fmt == "nvfp4":
-        W = g.nvfp4_quantize(w)
-        run = lambda xx: g.nvfp4_gemm_prefill(xx, W)
+        Wg = g.nvfp4_quantize(w)
+        Wu = g.nvfp4_quantize(inputs.weights(M, K, seed=83, device=DEV))
+        run = lambda xx: g.nvfp4_gateup_swiglu(xx, Wg, Wu)
     else:
         W = g.nvfp4_fp6_quantize(w)
         run = lambda xx: g.nvfp4_fp6_gemm(xx, W)
@@ -147,11 +149,17 @@ def test_token_rows_independent_of_tile_choice(fmt):
     assert torch.equal(y_300, y_all[100:400])
 
 
-@pytest.mark.parametrize("N,M,K", [(40, 130, 512), (600, 384, 4096), (512, 5120, 4352)])
+@pytest.mark.parametrize("N,M,K", [(40, 130, 512), (600, 384, 4096), (700, 1300, 3072), (2100, 640, 8192),
+                                   (4096, 4096, 512), (4096, 1280, 16384)])
 def test_split_k_prefill_deterministic(N, M, K):
-    """Shapes with too few tiles for the SMs split K across CTAs (fp32
-    partials added by the last CTA of each tile, in CTA order): repeated calls
-    give the same bits, and the result matches the oracle."""
+    """Single matrices whose tiles fill the SMs' last wave poorly split K
+    across CTAs: with operands that fit in L2, contiguous unit ranges (a part
+    of one tile, parts of two, or whole tiles between two parts); with larger
+    operands (the last shape: 134 MB of activations), whole-tile waves and
+    then equal k slices of the tiles left.  fp32 partials are added by the
+    last CTA of each shared tile, in CTA order.  Repeated calls give the same
+    bits, and the result matches the oracle.  Ragged row and token tiles
+    included."""
     w = inputs.weights(M, K, seed=N + 5, device=DEV)
     x = inputs.activations(N, K, seed=N + 6, device=DEV)
     W = g.nvfp4_quantize(w)

@@ -48,8 +48,11 @@ def test_status_clean_after_every_kind_of_product():
         g.nvfp4_gateup_swiglu(x, W, Wu, workspace=ws)
         g.nvfp4_fp6_gemm(x, F, workspace=ws)
     assert g.nvfp4_device_status(ws) == (g.NVFP4_OK, 0)
-    pws = torch.zeros(g.nvfp4_workspace_bytes(g.NVFP4_OP_GATEUP_SWIGLU, 600, M, K), dtype=torch.uint8,
-                      device=DEV)
+    # one workspace for every prefill call below: the largest they need (a
+    # single NVFP4 matrix may split K, which needs partial slots)
+    pws = torch.zeros(max(g.nvfp4_workspace_bytes(op, N, M, K) for N in (40, 600)
+                          for op in (g.NVFP4_OP_GEMM_PREFILL, g.NVFP4_OP_GATEUP_SWIGLU, g.NVFP4_OP_FP6_GEMM)),
+                      dtype=torch.uint8, device=DEV)
     for N in (40, 600):
         x = inputs.activations(N, K, seed=N, device=DEV)
         g.nvfp4_gemm_prefill(x, W, workspace=pws)
@@ -84,7 +87,8 @@ def test_wait_timeout_is_reported_and_the_context_stays_usable():
     _check_rows(y4, x, ref_w, "skinny N=4 after a reported timeout")
     _check_rows(y1, x[:1], ref_w, "skinny N=1 after a reported timeout")
 
-    # prefill-sized workspace (256 bytes) and the prefill kernel afterwards
+    # a prefill workspace (status word, and split-mode counters and partial
+    # slots) and the prefill kernel afterwards
     pws = torch.zeros(g.nvfp4_workspace_bytes(g.NVFP4_OP_GEMM_PREFILL, 300, M, K), dtype=torch.uint8,
                       device=DEV)
     g.nvfp4_selftest_wait_timeout(pws)
