@@ -378,11 +378,11 @@ def read_peaks():
     return 6800.0, 1900.0, "fallback"
 
 
-KERNEL_SOURCES = ("gemv_tc.cu", "tcgen05.cuh", "common.cuh")
+KERNEL_SOURCES = ("stream.cu", "skinny.cuh", "tcgen05.cuh", "common.cuh")
 
 
 def kernel_source_hash():
-    """Hash of the skinny kernel's sources (the ncu traffic summary records it)."""
+    """Hash of the stream kernel's sources (the ncu traffic summary records it)."""
     import hashlib
     h = hashlib.sha256()
     for name in KERNEL_SOURCES:
