@@ -466,6 +466,8 @@ __device__ __noinline__ void role_wprod(const CtxRef &cr)
         // ---- weight producers: even / odd units of the CTA's sequence ----
         if (lane == 0) {
             const int par = warp - kWProdWarp0;
+            const uint32_t c_empty_a = tc::smem_addr(c_empty), c_full_a = tc::smem_addr(c_full);
+            const uint32_t ring_a = tc::smem_addr(c_ring);
             int u = 0;
             int ws = par;
             uint32_t wph = 0;
@@ -492,16 +494,17 @@ __device__ __noinline__ void role_wprod(const CtxRef &cr)
                         ws -= kCStages;
                         wph ^= 1;
                     }
-                    if (!tc::mbar_wait(&c_empty[s], ph ^ 1)) {
+                    if (!tc::mbar_wait_a(c_empty_a + 8u * (uint32_t)s, ph ^ 1)) {
                         fail(plan, 32);
                         stop = true;
                         break;
                     }
-                    uint8_t *stg = c_ring + (size_t)s * kStageBytes;
-                    tc::mbar_arrive_expect_tx(&c_full[s], kStageBytes);
+                    const uint32_t stg = ring_a + (uint32_t)s * (uint32_t)kStageBytes;
+                    const uint32_t full = c_full_a + 8u * (uint32_t)s;
+                    tc::mbar_arrive_expect_tx_a(full, kStageBytes);
                     const int m = q % nw, j = q / nw;
-                    tc::tma_load_2d(stg, &J->codes[m], &c_full[s], j * (BKU / 2), sg.tile * BM);
-                    tc::tma_load_2d(stg + kCodeBox, &J->scales[m], &c_full[s], j * (BKU / 16), sg.tile * BM);
+                    tc::tma_load_2d_a(stg, &J->codes[m], full, j * (BKU / 2), sg.tile * BM);
+                    tc::tma_load_2d_a(stg + kCodeBox, &J->scales[m], full, j * (BKU / 16), sg.tile * BM);
                 }
             }
         }
@@ -525,6 +528,8 @@ __device__ __noinline__ void role_xprod(const CtxRef &cr)
             tc::griddep_wait();
             const uint64_t e = *reinterpret_cast<volatile const uint64_t *>(&H->epoch);
             const uint32_t row_bytes = (uint32_t)N * 128;
+            const uint32_t u_done_a = tc::smem_addr(u_done), xring_a = tc::smem_addr(x_ring);
+            const uint32_t x_raw_a = tc::smem_addr(x_raw), x_full_a = tc::smem_addr(x_full);
             int u = 0, lj = -1, prev = -1, xs = 0;
             bool stop = false;
             for (int si = 0; si < n_seg && !stop; ++si) {
@@ -551,24 +556,25 @@ __device__ __noinline__ void role_xprod(const CtxRef &cr)
                         xs = 0;
                     // the slot's previous unit (u - x_stages) has been consumed
                     const int pu = u - x_stages;
-                    if (pu >= 0 && !tc::mbar_wait(&u_done[pu & (kUnitSlots - 1)], (uint32_t)(pu / kUnitSlots) & 1)) {
+                    if (pu >= 0 &&
+                        !tc::mbar_wait_a(u_done_a + 8u * (uint32_t)(pu & (kUnitSlots - 1)), (uint32_t)(pu / kUnitSlots) & 1)) {
                         fail(plan, 33);
                         stop = true;
                         break;
                     }
-                    uint8_t *dst = x_ring + (size_t)s * x_unit;
-                    uint64_t *bar = conv ? &x_raw[s] : &x_full[s];
+                    const uint32_t dst = xring_a + (uint32_t)(s * x_unit);
+                    const uint32_t bar = (conv ? x_raw_a : x_full_a) + 8u * (uint32_t)s;
                     const int j = q / nw;
                     if (from_img) {
                         // the image has the slot's layout: one copy per unit
                         // (rows >= N are never read)
-                        tc::mbar_arrive_expect_tx(bar, (uint32_t)x_unit);
-                        sk::bulk_load(dst, img + (size_t)j * x_unit, (uint32_t)x_unit, bar);
+                        tc::mbar_arrive_expect_tx_a(bar, (uint32_t)x_unit);
+                        tc::bulk_load_a(dst, img + (size_t)j * x_unit, (uint32_t)x_unit, bar);
                     } else {
-                        tc::mbar_arrive_expect_tx(bar, 4 * row_bytes);
+                        tc::mbar_arrive_expect_tx_a(bar, 4 * row_bytes);
 #pragma unroll
                         for (int sb = 0; sb < 4; ++sb)
-                            tc::tma_load_2d(dst + sb * x_sub, &J->x, bar, j * BKU + sb * 64, 0);
+                            tc::tma_load_2d_a(dst + (uint32_t)(sb * x_sub), &J->x, bar, j * BKU + sb * 64, 0);
                     }
                 }
             }
@@ -643,6 +649,10 @@ __device__ __noinline__ void role_mma(const CtxRef &cr)
     // advanced incrementally: no divisions in the loop. ----
     if (lane != 0)
         return;
+    // barriers by 32-bit shared address (one register each, no conversion per use)
+    const uint32_t x_full_a = tc::smem_addr(x_full), a_full_a = tc::smem_addr(a_full);
+    const uint32_t u_done_a = tc::smem_addr(u_done), d_full_a = tc::smem_addr(d_full);
+    const uint32_t d_empty_a = tc::smem_addr(d_empty), j_full_a = tc::smem_addr(j_full);
     int lj = -1, prev = -1;
     uint32_t idesc = 0;
     int xs = 0, sa = 0;            // activation and A ring slots
@@ -654,14 +664,14 @@ __device__ __noinline__ void role_mma(const CtxRef &cr)
         if (sg.job != prev) {
             prev = sg.job;
             ++lj;
-            if (!tc::mbar_wait(&j_full[lj % kJobSlots], ((uint32_t)lj / kJobSlots) & 1)) {
+            if (!tc::mbar_wait_a(j_full_a + 8u * (uint32_t)(lj % kJobSlots), ((uint32_t)lj / kJobSlots) & 1)) {
                 fail(plan, 39);
                 return;
             }
             idesc = tc::idesc_f16kind(BM, NTOK, (uint32_t)jinfo[lj % kJobSlots].mode);
         }
         const int buf = si & 1;
-        if (!tc::mbar_wait(&d_empty[buf], (((uint32_t)si >> 1) & 1) ^ 1)) {
+        if (!tc::mbar_wait_a(d_empty_a + 8u * (uint32_t)buf, (((uint32_t)si >> 1) & 1) ^ 1)) {
             fail(plan, 40);
             return;
         }
@@ -684,13 +694,13 @@ __device__ __noinline__ void role_mma(const CtxRef &cr)
         for (int q = sg.qb; q < sg.qe; ++q) {
             const bool mine = nw == 1 || (q & 1) == (warp >> 2);
             if (mine) {
-                if (!tc::mbar_wait(&x_full[xs], xph)) {
+                if (!tc::mbar_wait_a(x_full_a + 8u * (uint32_t)xs, xph)) {
                     fail(plan, 41);
                     return;
                 }
                 const uint64_t bdesc0 = xdesc + (uint64_t)((xs * x_unit) >> 4);
                 for (int h = 0; h < 2; ++h) {
-                    if (!tc::mbar_wait(&a_full[sa], aph)) {
+                    if (!tc::mbar_wait_a(a_full_a + 8u * (uint32_t)sa, aph)) {
                         fail(plan, 42);
                         return;
                     }
@@ -710,14 +720,14 @@ __device__ __noinline__ void role_mma(const CtxRef &cr)
                 aph ^= 1;
             }
             // the unit's MMAs of this thread (if any) are done -> its share of u_done
-            tc::mma_commit(&u_done[ud & (kUnitSlots - 1)]);
+            tc::mma_commit_a(u_done_a + 8u * (ud & (kUnitSlots - 1)));
             ++ud;
             if (++xs == x_stages) {
                 xs = 0;
                 xph ^= 1;
             }
         }
-        tc::mma_commit(&d_full[buf]);
+        tc::mma_commit_a(d_full_a + 8u * (uint32_t)buf);
     }
 }
 
@@ -792,6 +802,8 @@ __device__ __noinline__ void role_epi(const CtxRef &cr)
                     v.stats_out[((size_t)((e + 1) & 1) * n_jobs + jj) * NTOK + et] = TokStat{0, 0};
         }
         // 3. the CTA's segments
+        const uint32_t j_full_a = tc::smem_addr(j_full), d_full_a = tc::smem_addr(d_full);
+        const uint32_t d_empty_a = tc::smem_addr(d_empty);
         int lj = -1, prev = -1;
         for (int si = 0; si < n_seg; ++si) {
             const Seg sg = segs[si];
@@ -801,14 +813,15 @@ __device__ __noinline__ void role_epi(const CtxRef &cr)
                 prev = sg.job;
                 ++lj;
                 if (!tc::bar_and(1, kEpiThreads,
-                                 tc::mbar_wait(&j_full[lj % kJobSlots], ((uint32_t)lj / kJobSlots) & 1))) {
+                                 tc::mbar_wait_a(j_full_a + 8u * (uint32_t)(lj % kJobSlots),
+                                                 ((uint32_t)lj / kJobSlots) & 1))) {
                     fail(plan, 43);
                     break;
                 }
             }
             const JobInfo *ji = jinfo + lj % kJobSlots;
             const int buf = si & 1;
-            if (!tc::bar_and(1, kEpiThreads, tc::mbar_wait(&d_full[buf], ((uint32_t)si >> 1) & 1))) {
+            if (!tc::bar_and(1, kEpiThreads, tc::mbar_wait_a(d_full_a + 8u * (uint32_t)buf, ((uint32_t)si >> 1) & 1))) {
                 fail(plan, 44);
                 break;
             }
@@ -849,7 +862,7 @@ __device__ __noinline__ void role_epi(const CtxRef &cr)
             tc::fence_before_sync();
             __syncwarp();
             if (lane == 0)
-                tc::mbar_arrive(&d_empty[buf]);
+                tc::mbar_arrive_a(d_empty_a + 8u * (uint32_t)buf);
 
             bool final_tile = false;
             TokStat *ost = v.stats_out + ((size_t)(e & 1) * n_jobs + sg.job) * NTOK;
@@ -960,7 +973,9 @@ __device__ __noinline__ void role_dq(const CtxRef &cr)
     NVFP4_STREAM_UNPACK(cr);
     // ---- dequantisers: half unit t = 2u + h goes to group t % 4, so group g
     // takes half h = g % 2 of the units u = g / 2 (mod 2), always into A slot
-    // g; it walks its units two at a time with incremental ring positions ----
+    // g; it walks its units two at a time with incremental ring positions.
+    // Shared memory is reached through 32-bit shared addresses (ld.shared,
+    // one register per address), which keeps the loop within its registers. ----
     const int g = (warp - kFirstDqWarp) >> 2;
     const int h = g & 1;
     const int quarter = warp & 3;
@@ -969,6 +984,12 @@ __device__ __noinline__ void role_dq(const CtxRef &cr)
     const int swz = r & 7;
     if (n_seg == 0)
         return;
+    const uint32_t c_full_a = tc::smem_addr(c_full), c_empty_a = tc::smem_addr(c_empty);
+    const uint32_t u_done_a = tc::smem_addr(u_done), a_full_a = tc::smem_addr(a_full) + 8u * (uint32_t)g;
+    const uint32_t j_full_a = tc::smem_addr(j_full), jinfo_a = tc::smem_addr(jinfo);
+    // this thread's row of the weight ring's code box, and of its scale box
+    const uint32_t ring_row = tc::smem_addr(c_ring) + (uint32_t)(r * 128);
+    const uint32_t ring_scl = tc::smem_addr(c_ring) + (uint32_t)(kCodeBox + r * 16 + h * 8);
     // cursor over the CTA's units: segment si, unit q of its tile, local job lj
     int si = 0, lj = 0;
     int job = segs[0].job, qe = segs[0].qe;
@@ -997,49 +1018,56 @@ __device__ __noinline__ void role_dq(const CtxRef &cr)
     const uint32_t acol = tmem_a + (uint32_t)(g * kACols) + lane_off;
     for (;;) {
         if (have != lj) {
-            if (!tc::mbar_wait(&j_full[lj % kJobSlots], ((uint32_t)lj / kJobSlots) & 1)) {
+            const uint32_t js = (uint32_t)(lj % kJobSlots);
+            if (!tc::mbar_wait_a(j_full_a + 8u * js, ((uint32_t)lj / kJobSlots) & 1)) {
                 fail(plan, 45);
                 return;
             }
-            mode = jinfo[lj % kJobSlots].mode;
+            mode = (int)tc::lds32(jinfo_a + js * (uint32_t)sizeof(JobInfo) + (uint32_t)offsetof(JobInfo, mode));
             have = lj;
         }
-        if (!tc::mbar_wait(&c_full[sc], phc)) {
+        if (!tc::mbar_wait_a(c_full_a + 8u * (uint32_t)sc, phc)) {
             fail(plan, 46);
             return;
         }
-        const uint8_t *stage = c_ring + (size_t)sc * kStageBytes;
-        const uint8_t *crow = stage + r * 128;
+        const uint32_t stage_off = (uint32_t)sc * (uint32_t)kStageBytes;
         uint4 cw[4];
 #pragma unroll
         for (int cc = 0; cc < 4; ++cc)
-            cw[cc] = *reinterpret_cast<const uint4 *>(crow + (((h * 4 + cc) ^ swz) << 4));
-        const uint2 sc8 = *reinterpret_cast<const uint2 *>(stage + kCodeBox + r * 16 + h * 8);
+            cw[cc] = tc::lds128(ring_row + stage_off + (uint32_t)(((h * 4 + cc) ^ swz) << 4));
+        const uint2 sc8 = tc::lds64(ring_scl + stage_off);
         __syncwarp();
         if (lane == 0)
-            tc::mbar_arrive(&c_empty[sc]);
+            tc::mbar_arrive_a(c_empty_a + 8u * (uint32_t)sc);
         // A slot g was last filled for unit u - 2: its MMAs must have completed
         if (u >= 2) {
             const uint32_t pu = u - 2;
-            if (!tc::mbar_wait(&u_done[pu & (kUnitSlots - 1)], (pu / kUnitSlots) & 1)) {
+            if (!tc::mbar_wait_a(u_done_a + 8u * (pu & (kUnitSlots - 1)), (pu / kUnitSlots) & 1)) {
                 fail(plan, 47);
                 return;
             }
         }
         tc::fence_after_sync();
-        // one 16-byte chunk (32 k) at a time: 16 columns per store
+        // one 16-byte chunk (32 k) at a time: 16 columns per store; the
+        // operand format is fixed per job, so each format has its own loop
+        auto put = [&](auto fmt) {
 #pragma unroll
-        for (int cc = 0; cc < 4; ++cc) {
-            uint32_t out[16];
-            const uint32_t sw = cc < 2 ? sc8.x : sc8.y;
-            dequant_chunk(cw[cc], (cc & 1) ? sw >> 16 : sw & 0xFFFF, mode, out);
-            tc::tmem_st_32x32b_x16(acol + 16 * cc, out);
-        }
+            for (int cc = 0; cc < 4; ++cc) {
+                uint32_t out[16];
+                const uint32_t sw = cc < 2 ? sc8.x : sc8.y;
+                dequant_chunk(cw[cc], (cc & 1) ? sw >> 16 : sw & 0xFFFF, decltype(fmt)::value, out);
+                tc::tmem_st_32x32b_x16(acol + 16 * cc, out);
+            }
+        };
+        if (mode == 0)
+            put(std::integral_constant<int, 0>{});
+        else
+            put(std::integral_constant<int, 1>{});
         tc::tmem_st_wait();
         tc::fence_before_sync();
         __syncwarp();
         if (lane == 0)
-            tc::mbar_arrive(&a_full[g]);
+            tc::mbar_arrive_a(a_full_a);
         u += 2;
         sc += 2;
         if (sc >= kCStages) {

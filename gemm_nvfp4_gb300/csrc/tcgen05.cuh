@@ -91,6 +91,84 @@ NVFP4_DEVINL bool mbar_wait(uint64_t *bar, uint32_t parity)
     }
 }
 
+// The same operations on 32-bit shared-memory addresses (smem_addr), for
+// loops that keep many barriers at hand: a shared address takes one register
+// where a generic pointer takes two and a conversion at every use.
+NVFP4_DEVINL void mbar_arrive_a(uint32_t bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+NVFP4_DEVINL bool mbar_try_wait_a(uint32_t bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+NVFP4_DEVINL bool mbar_try_wait_sleep_a(uint32_t bar, uint32_t parity, uint32_t hint_ns)
+{
+    uint32_t ok;
+    asm volatile(
+        "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3; selp.u32 %0, 1, 0, p; }"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+
+// mbar_wait on a shared address; the timed loop is out of line (it runs only
+// when the first test fails).
+__device__ __noinline__ bool mbar_wait_slow_a(uint32_t bar, uint32_t parity);
+
+NVFP4_DEVINL bool mbar_wait_a(uint32_t bar, uint32_t parity)
+{
+    if (mbar_try_wait_a(bar, parity))
+        return true;
+    return mbar_wait_slow_a(bar, parity);
+}
+
+__device__ __noinline__ inline bool mbar_wait_slow_a(uint32_t bar, uint32_t parity)
+{
+    const uint64_t t0 = globaltimer();
+    for (;;) {
+        if (mbar_try_wait_sleep_a(bar, parity, 20000u))
+            return true;
+        if (globaltimer() - t0 > kWaitLimitNs)
+            return false;
+    }
+}
+
+NVFP4_DEVINL void mbar_arrive_expect_tx_a(uint32_t bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+
+NVFP4_DEVINL uint4 lds128(uint32_t addr)
+{
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+    return v;
+}
+
+NVFP4_DEVINL uint2 lds64(uint32_t addr)
+{
+    uint2 v;
+    asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
+    return v;
+}
+
+NVFP4_DEVINL uint32_t lds32(uint32_t addr)
+{
+    uint32_t v;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
+    return v;
+}
+
 // Generic-proxy shared-memory writes -> visible to the async proxy (TMA, MMA).
 NVFP4_DEVINL void fence_proxy_async_smem()
 {
@@ -106,6 +184,15 @@ NVFP4_DEVINL void tma_load_2d(void *dst, const CUtensorMap *map, uint64_t *bar, 
     asm volatile(
         "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];"
         ::"r"(smem_addr(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_addr(bar)), "r"(c0), "r"(c1)
+        : "memory");
+}
+
+// tma_load_2d with 32-bit shared addresses for the destination and the barrier.
+NVFP4_DEVINL void tma_load_2d_a(uint32_t dst, const CUtensorMap *map, uint32_t bar, int c0, int c1)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];"
+        ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1)
         : "memory");
 }
 
@@ -177,6 +264,12 @@ NVFP4_DEVINL void mma_commit(uint64_t *bar)
 {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
                      smem_addr(bar))
+                 : "memory");
+}
+
+NVFP4_DEVINL void mma_commit_a(uint32_t bar)
+{
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
                  : "memory");
 }
 
@@ -278,6 +371,13 @@ NVFP4_DEVINL void bulk_load(void *dst, const void *src, uint32_t bytes, uint64_t
 {
     asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
                  ::"r"(smem_addr(dst)), "l"(src), "r"(bytes), "r"(smem_addr(bar))
+                 : "memory");
+}
+
+NVFP4_DEVINL void bulk_load_a(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar)
+{
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                 ::"r"(dst), "l"(src), "r"(bytes), "r"(bar)
                  : "memory");
 }
 
