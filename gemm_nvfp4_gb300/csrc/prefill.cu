@@ -843,6 +843,7 @@ __global__ void __launch_bounds__(TMAC ? kThreadsTma : kThreads, 1)
         if constexpr (TMAC && FMT == 1) {
             // FP6 codes from the TMA ring; the scale byte of a row (one per
             // 128 k = two stages) through a small register prefetch ring.
+            const uint32_t fp6_ring_a = tc::smem_addr(sc_ring) + (uint32_t)(row * kCRow + half * 24);
             const int64_t nblk = a.K / 128;
             auto scale_at = [&](int mi, int64_t blk) -> uint32_t {
                 return (m < a.M && blk < nblk) ? (uint32_t)__ldg(a.scales[mi] + m * nblk + blk) : 127u;
@@ -877,9 +878,8 @@ __global__ void __launch_bounds__(TMAC ? kThreadsTma : kThreads, 1)
 #pragma unroll
                 for (int mi = 0; mi < NW; ++mi)
 #pragma unroll
-                    for (int i = 0; i < 3; ++i)
-                        cw[mi][i] = *reinterpret_cast<const uint2 *>(sc_ring + ((size_t)c * NW + mi) * kCBytes +
-                                                                     row * kCRow + half * 24 + 8 * i);
+                    for (int i = 0; i < 3; ++i)  // ld.shared from 32-bit shared addresses
+                        cw[mi][i] = tc::lds64(fp6_ring_a + (uint32_t)((c * NW + mi) * kCBytes + 8 * i));
                 const int s = kb % S;
                 if (!tc::mbar_wait(&empty[s], ((uint32_t)(kb / S) & 1) ^ 1)) {
                     fail(a, 3);
@@ -918,6 +918,8 @@ __global__ void __launch_bounds__(TMAC ? kThreadsTma : kThreads, 1)
             // once its lanes have turned the slot's bytes into bf16 tiles.
             // Stage kb is a ring position; in split mode the segments follow
             // one another, each ending with its epilogue.
+            const uint32_t sc_ring_a = tc::smem_addr(sc_ring) + (uint32_t)(row * kCRow + half * 16);
+            const uint32_t ss_ring_a = tc::smem_addr(ss_ring) + (uint32_t)(row * 16 + half * 2);
             int kb = 0;
             for (;;) {
                 const int kend = kb + (SPLIT ? dcur.kb_end - dcur.kb : num_kb);
@@ -930,13 +932,13 @@ __global__ void __launch_bounds__(TMAC ? kThreadsTma : kThreads, 1)
                         ok = false;
                         break;
                     }
+                    // ld.shared from 32-bit shared addresses (a generic load
+                    // waits on the long scoreboard)
                     DqItem cur[NW];
 #pragma unroll
                     for (int mi = 0; mi < NW; ++mi) {
-                        cur[mi].code = *reinterpret_cast<const uint4 *>(sc_ring + ((size_t)c * NW + mi) * kCBytes +
-                                                                        row * kCRow + half * 16);
-                        cur[mi].scl = *reinterpret_cast<const uint16_t *>(ss_ring + ((size_t)ss * NW + mi) * kSBytes +
-                                                                          row * 16 + (kb & 3) * 4 + half * 2);
+                        cur[mi].code = tc::lds128(sc_ring_a + (uint32_t)((c * NW + mi) * kCBytes));
+                        cur[mi].scl = tc::lds16(ss_ring_a + (uint32_t)((ss * NW + mi) * kSBytes + (kb & 3) * 4));
                     }
                     const int s = kb % S;
                     if (!tc::mbar_wait(&empty[s], ((uint32_t)(kb / S) & 1) ^ 1)) {

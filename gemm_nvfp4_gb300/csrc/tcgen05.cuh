@@ -162,6 +162,13 @@ NVFP4_DEVINL uint2 lds64(uint32_t addr)
     return v;
 }
 
+NVFP4_DEVINL uint32_t lds16(uint32_t addr)
+{
+    uint16_t v;
+    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(addr));
+    return v;
+}
+
 NVFP4_DEVINL uint32_t lds32(uint32_t addr)
 {
     uint32_t v;
