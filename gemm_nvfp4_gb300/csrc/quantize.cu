@@ -42,13 +42,23 @@ template <> struct Src<float> {
     {
         return max(max(v.x & 0x7FFFFFFFu, v.y & 0x7FFFFFFFu), max(v.z & 0x7FFFFFFFu, v.w & 0x7FFFFFFFu));
     }
-    // Eight consecutive values starting at element 8 * hb.
-    static __device__ __forceinline__ void load8(const float *w, int64_t hb, float v[8])
+    // Eight consecutive values starting at element 8 * hb: loaded raw (so
+    // several half blocks can be in flight), then widened to fp32.
+    static constexpr int kUnroll = 2;  // half blocks in flight per thread
+    struct Raw {
+        uint4 a, b;
+    };
+    static __device__ __forceinline__ Raw load_raw(const float *w, int64_t hb)
     {
-        const float4 *p = reinterpret_cast<const float4 *>(w + hb * 8);
-        float4 a = __ldcs(p), b = __ldcs(p + 1);
-        v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
-        v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+        const uint4 *p = reinterpret_cast<const uint4 *>(w + hb * 8);
+        return Raw{__ldcs(p), __ldcs(p + 1)};
+    }
+    static __device__ __forceinline__ void widen(const Raw &r, float v[8])
+    {
+        v[0] = __uint_as_float(r.a.x); v[1] = __uint_as_float(r.a.y);
+        v[2] = __uint_as_float(r.a.z); v[3] = __uint_as_float(r.a.w);
+        v[4] = __uint_as_float(r.b.x); v[5] = __uint_as_float(r.b.y);
+        v[6] = __uint_as_float(r.b.z); v[7] = __uint_as_float(r.b.w);
     }
 };
 
@@ -63,10 +73,17 @@ template <> struct Src<uint16_t> {
     {
         return max(max(half_bits(v.x), half_bits(v.y)), max(half_bits(v.z), half_bits(v.w)));
     }
-    static __device__ __forceinline__ void load8(const uint16_t *w, int64_t hb, float v[8])
+    static constexpr int kUnroll = 4;  // half blocks in flight per thread (16 bytes each)
+    struct Raw {
+        uint4 a;
+    };
+    static __device__ __forceinline__ Raw load_raw(const uint16_t *w, int64_t hb)
     {
-        const uint4 a = __ldcs(reinterpret_cast<const uint4 *>(w + hb * 8));
-        const uint32_t words[4] = {a.x, a.y, a.z, a.w};
+        return Raw{__ldcs(reinterpret_cast<const uint4 *>(w + hb * 8))};
+    }
+    static __device__ __forceinline__ void widen(const Raw &r, float v[8])
+    {
+        const uint32_t words[4] = {r.a.x, r.a.y, r.a.z, r.a.w};
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
             v[2 * j] = __uint_as_float(words[j] << 16);
@@ -124,43 +141,56 @@ quantize_blocks_kernel(const T *__restrict__ w, int64_t n_half_blocks,
 
     // Two threads per 16-element block; each holds 8 consecutive weights.  The
     // loop runs warp-uniformly so the pair shuffle always has all 32 lanes.
+    // Each thread loads U half blocks (one grid stride apart) before it
+    // quantises any, so U loads per thread are in flight.
+    constexpr int U = Src<T>::kUnroll;
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
     const int lane = threadIdx.x & 31;
     for (int64_t base = (int64_t)blockIdx.x * blockDim.x + (threadIdx.x - lane); base < n_half_blocks;
-         base += stride) {
-        const int64_t hb = base + lane;
-        const bool active = hb < n_half_blocks;  // n_half_blocks is even: pairs are active together
-        float v[8];
-        float amax = 0.0f;
-        if (active) {
-            Src<T>::load8(w, hb, v);
+         base += stride * U) {
+        typename Src<T>::Raw raw[U];
 #pragma unroll
-            for (int j = 0; j < 8; ++j)
-                amax = fmaxf(amax, fabsf(v[j]));
+        for (int u = 0; u < U; ++u) {
+            const int64_t hb = base + u * stride + lane;
+            if (hb < n_half_blocks)
+                raw[u] = Src<T>::load_raw(w, hb);
         }
-        amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
-        if (!active)
-            continue;
-
-        uint32_t sb = 0;
-        if (ts > 0.0f) {
-            float q = __fdiv_rn(__fdiv_rn(amax, 6.0f), ts);
-            sb = f32_to_e4m3_satfinite(q);
-        }
-        const float d = __fmul_rn(e4m3_to_f32(sb), ts);
-
-        uint32_t packed = 0;
-        if (d != 0.0f) {
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                float lo = __fdiv_rn(v[2 * j], d);
-                float hi = __fdiv_rn(v[2 * j + 1], d);
-                packed |= f32x2_to_e2m1x2(lo, hi) << (8 * j);
+        for (int u = 0; u < U; ++u) {
+            const int64_t hb = base + u * stride + lane;
+            const bool active = hb < n_half_blocks;  // n_half_blocks is even: pairs are active together
+            float v[8];
+            float amax = 0.0f;
+            if (active) {
+                Src<T>::widen(raw[u], v);
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    amax = fmaxf(amax, fabsf(v[j]));
             }
+            amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
+            if (!active)
+                continue;
+
+            uint32_t sb = 0;
+            if (ts > 0.0f) {
+                float q = __fdiv_rn(__fdiv_rn(amax, 6.0f), ts);
+                sb = f32_to_e4m3_satfinite(q);
+            }
+            const float d = __fmul_rn(e4m3_to_f32(sb), ts);
+
+            uint32_t packed = 0;
+            if (d != 0.0f) {
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    float lo = __fdiv_rn(v[2 * j], d);
+                    float hi = __fdiv_rn(v[2 * j + 1], d);
+                    packed |= f32x2_to_e2m1x2(lo, hi) << (8 * j);
+                }
+            }
+            reinterpret_cast<uint32_t *>(codes)[hb] = packed;
+            if ((hb & 1) == 0)
+                scales[hb >> 1] = (uint8_t)sb;
         }
-        reinterpret_cast<uint32_t *>(codes)[hb] = packed;
-        if ((hb & 1) == 0)
-            scales[hb >> 1] = (uint8_t)sb;
     }
 }
 
@@ -177,7 +207,9 @@ static cudaError_t quantize_any(const T *w, int64_t M, int64_t K, uint8_t *codes
                                                                   partial);
     const int64_t n_half = n / 8;
     int64_t blocks_b = (n_half + kQuantThreads - 1) / kQuantThreads;
-    int grid_b = (int)std::min<int64_t>(std::max<int64_t>(blocks_b, 1), (int64_t)num_sms * 8);
+    // four CTAs of 256 threads fit an SM at this kernel's register count:
+    // one resident round, each thread looping over its half blocks
+    int grid_b = (int)std::min<int64_t>(std::max<int64_t>(blocks_b, 1), (int64_t)num_sms * 4);
     quantize_blocks_kernel<T><<<grid_b, kQuantThreads, 0, stream>>>(w, n_half, partial, grid_a, codes, scales,
                                                                      tensor_scale);
     return cudaGetLastError();
