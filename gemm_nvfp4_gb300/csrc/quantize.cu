@@ -354,9 +354,11 @@ cudaError_t launch_fp6_quantize_bf16(const uint16_t *w, int64_t M, int64_t K, ui
 //
 // One CTA per (128-row block, chunk of kImportBlocks scale-column blocks): the
 // chunk is contiguous in the blocked buffer (read with 16-byte loads into
-// shared memory), and its 128 output row segments are written with 4-byte
-// stores where rows start on 4-byte boundaries.  HBM-bound: every byte read
-// and written once.
+// shared memory), and its 128 output row segments are written with 16-byte
+// stores when rows start on 16-byte boundaries (S % 16 == 0; the output
+// buffer itself is 16-byte aligned by the call's contract), else with 4-byte
+// stores where rows start on 4-byte boundaries, else byte by byte.
+// HBM-bound: every byte read and written once.
 constexpr int kImportThreads = 256;
 constexpr int kImportBlocks = 16;  // 4-column blocks per CTA: 64 columns, 8 KB
 
@@ -373,7 +375,25 @@ import_blocked_scales_kernel(const uint8_t *__restrict__ blocked, int64_t M, int
         reinterpret_cast<uint4 *>(tile)[i] = __ldcs(src + i);
     __syncthreads();
 
-    // Thread t writes row t / 2, scale columns [32 * (t % 2), +32) of the chunk.
+    if ((S & 15) == 0) {
+        // Rows start on 16-byte boundaries: piece p = (row r, 16 scale
+        // columns q of the chunk) is four words, one from each of four
+        // consecutive blocks, written with one 16-byte store; a warp's 32
+        // pieces cover 8 rows x 64 contiguous bytes.
+        for (int p = threadIdx.x; p < 128 * (kImportBlocks / 4); p += kImportThreads) {
+            const int r = p / (kImportBlocks / 4), q = p % (kImportBlocks / 4);
+            const int64_t m = mb * 128 + r;
+            const int64_t c = kb0 * 4 + 16 * q;
+            if (m >= M || c >= S || 4 * q >= nblk)
+                continue;
+            const int w = (r & 31) * 4 + (r >> 5);  // word of row r inside a block
+            const uint4 v = make_uint4(tile[(4 * q + 0) * 128 + w], tile[(4 * q + 1) * 128 + w],
+                                       tile[(4 * q + 2) * 128 + w], tile[(4 * q + 3) * 128 + w]);
+            *reinterpret_cast<uint4 *>(scales + m * S + c) = v;
+        }
+        return;
+    }
+    // Other S: thread t writes row t / 2, scale columns [32 * (t % 2), +32) of the chunk.
     const int r = threadIdx.x >> 1;
     const int64_t m = mb * 128 + r;
     if (m >= M)

@@ -58,7 +58,7 @@ def test_quantize_bf16_zero_and_empty():
 
 
 @pytest.mark.parametrize("M,K", [(1, 16), (130, 80), (128, 64), (257, 1040), (300, 4000 // 16 * 16),
-                                 (17408, 5120), (4096, 12288)])
+                                 (17408, 5120), (4096, 12288), (200, 768)])
 def test_import_blocked_scales_matches_oracle(M, K):
     rng = np.random.default_rng(M + 3 * K)
     # random bytes everywhere, padding included: the import must ignore padding
