@@ -692,11 +692,39 @@ __device__ __noinline__ void role_mma(const CtxRef &cr)
                 boff[h][i] = (uint32_t)((kl >> 6) * (x_sub / 16) + 2 * ((kl >> 4) & 3));
             }
         }
+        // one matrix: this issuer's two K steps of its half unit (constant offsets)
+        uint32_t aoff1[2], boff1[2];
+        for (int i = 0; i < 2; ++i) {
+            const int kk = 2 * (warp & 3) + i;
+            const int kl = (warp >> 2) * 128 + kk * 16;
+            aoff1[i] = (uint32_t)(kk * 8);
+            boff1[i] = (uint32_t)((kl >> 6) * (x_sub / 16) + 2 * ((kl >> 4) & 3));
+        }
         const uint64_t xdesc = tc::smem_desc_sw128(x_ring);
         bool fresh = true;
         for (int q = sg.qb; q < sg.qe; ++q) {
             const bool mine = nw == 1 || (q & 1) == (warp >> 2);
-            if (mine) {
+            if (nw == 1) {
+                // one matrix: this issuer's half unit only (slot sa + half; sa advances by two)
+                if (!tc::mbar_wait_a(x_full_a + 8u * (uint32_t)xs, xph) ||
+                    !tc::mbar_wait_a(a_full_a + 8u * (uint32_t)(sa + (warp >> 2)), aph)) {
+                    fail(plan, 41);
+                    return;
+                }
+                tc::fence_after_sync();
+                const uint64_t bdesc0 = xdesc + (uint64_t)((xs * x_unit) >> 4);
+                const uint32_t acol = tmem_a + (uint32_t)((sa + (warp >> 2)) * kACols);
+#pragma unroll
+                for (int i = 0; i < 2; ++i) {
+                    tc::mma_f16_ts(dcol, acol + aoff1[i], bdesc0 + boff1[i], idesc, fresh ? 0u : 1u);
+                    fresh = false;
+                }
+                sa += 2;
+                if (sa == kAStages) {
+                    sa = 0;
+                    aph ^= 1;
+                }
+            } else if (mine) {
                 if (!tc::mbar_wait_a(x_full_a + 8u * (uint32_t)xs, xph)) {
                     fail(plan, 41);
                     return;
@@ -718,11 +746,9 @@ __device__ __noinline__ void role_mma(const CtxRef &cr)
                     tc::fence_after_sync();
                     const uint32_t acol = tmem_a + (uint32_t)(sa * kACols);
                     if (nw == 1) {
+#pragma unroll
                         for (int i = 0; i < 2; ++i) {
-                            const int kk = 2 * (warp & 3) + i;
-                            const int kl = h * 128 + kk * 16;
-                            const uint32_t bo = (uint32_t)((kl >> 6) * (x_sub / 16) + 2 * ((kl >> 4) & 3));
-                            tc::mma_f16_ts(dcol, acol + (uint32_t)(kk * 8), bdesc0 + bo, idesc, fresh ? 0u : 1u);
+                            tc::mma_f16_ts(dcol, acol + aoff1[i], bdesc0 + boff1[i], idesc, fresh ? 0u : 1u);
                             fresh = false;
                         }
                     } else {
