@@ -77,9 +77,8 @@ constexpr int kSBytes = BM * 16;         // NVFP4 scales of four stages: 128 row
 template <int FMT> constexpr int code_row_bytes() { return FMT == 0 ? BK / 2 : BK / 4 * 3; }
 constexpr int kABytes = BM * BK * 2;  // 16 KB per weight matrix per stage
 constexpr int kMaxContrib = 64;       // split mode: CTAs sharing one tile, at most
-constexpr int kFixCols = 64;                 // split mode fix-up by bulk copies: token columns per chunk
-constexpr int kFixChunk = kFixCols * BM * 4;  // 32 KB of a partial
-constexpr int kFixBufs = 4;                   // chunk buffers in the activation ring
+constexpr int kRedCols = 16;          // split-mode reduction: token columns per work item
+constexpr int kRedThreads = 256;      // its threads: rows 4 rq .. 4 rq + 3 of two columns each
 
 // TMAC: the weight codes and scales reach shared memory by TMA (a code ring
 // of kSc stages and a scale ring of two 4-stage groups) instead of per-thread
@@ -121,19 +120,19 @@ struct Args {
     // Split mode (stream-K; one matrix, A in tensor memory): the tiles from
     // sk_base / kq on are cut into (tile, 256-k group) units, and CTA b takes
     // the b-th of sk_grid equal contiguous unit ranges: a partial tile at
-    // each end of the range, whole tiles between.  A tile shared by several
-    // CTAs is finished by the last to arrive, adding every CTA's fp32 partial
-    // in CTA order.  The tiles before sk_base / kq belong to a whole-tile
-    // launch that precedes this one on the stream.
+    // each end of the range, whole tiles between.  A CTA stores the fp32
+    // accumulators of a tile it shares as a partial; the reduction launch
+    // that follows adds every shared tile's partials in CTA order.  The tiles
+    // before sk_base / kq belong to a whole-tile launch that precedes this one
+    // on the stream.
     int split;
     int grid;             // CTAs: one per tile, or (split mode) sk_grid
     int kq;               // 256-k groups per tile (num_kb / 4)
-    int after_whole;      // split mode: a whole-tile launch comes between the counter zeroing and this one
+    int after_whole;      // split mode: a whole-tile launch precedes this one
     int64_t sk_base;      // first stream-K unit: (tiles of the whole-tile launch) * kq
     int64_t units;        // stream-K units
     int sk_grid;          // CTAs sharing them (<= units)
     float *partial;       // [2 * gridDim][TN][BM] raw fp32 accumulators: a CTA's first and last segment
-    uint32_t *counters;   // [gridDim] arrivals, by a shared tile's first CTA (zeroed by the host)
 };
 
 // Tile index -> (row tile, token tile) in the raster order: groups of `group`
@@ -345,19 +344,13 @@ __global__ void __launch_bounds__(TMAC ? kThreadsTma : kThreads, 1)
     uint64_t *cfull = bars + 3 * S + 1, *cempty = cfull + SC, *sfull = cempty + SC, *sempty = sfull + 2;
     uint64_t *tmem_empty = sempty + 2;  // split mode: segment 0's accumulator has been read
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(tmem_empty + 1);
-    int *last_s = reinterpret_cast<int *>(tmem_slot + 1);
-    // split mode: the chunk buffers of a fix-up by bulk copies (full,
-    // empty), and the partial slots of a shared tile's contributors (the
-    // second half of the 1024-byte barrier area)
-    uint64_t *fx_full = bars + 48, *fx_empty = bars + 48 + kFixBufs;
-    const float **contrib = reinterpret_cast<const float **>(bars + 64);
-    static_assert(3 * S + 1 + 2 * SC + 4 + 1 + 1 <= 48, "barriers, TMEM slot and flag below the fix-up barriers");
-    static_assert(48 + 2 * kFixBufs <= 64, "fix-up barriers below the contributor table");
-    static_assert(!SPLIT || (size_t)S * kBBytes >= (size_t)kFixBufs * kFixChunk, "fix-up chunks fit the activation ring");
+    static_assert(3 * S + 1 + 2 * SC + 4 + 1 <= 128, "barriers and TMEM slot in the 1024-byte barrier area");
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    // A stream-K launch that follows this one on the stream may take the SMs
-    // as they free up (it computes other tiles).
+    // The launch that follows this one on the stream may take the SMs as they
+    // free up: after whole tiles the stream-K launch (it computes other
+    // tiles), after the stream-K launch its reduction (which waits for this
+    // launch's completion before reading anything).
     tc::griddep_launch_dependents();
     // The CTA's k blocks: one whole tile (raster order: the host picks the
     // raster so that the operand re-read across the grid stays resident in
@@ -376,12 +369,6 @@ __global__ void __launch_bounds__(TMAC ? kThreadsTma : kThreads, 1)
         }
         tc::mbar_init(tmem_full, C::kIssue);
         tc::mbar_init(tmem_empty, kDqWarps);
-        if (SPLIT) {
-            for (int b = 0; b < kFixBufs; ++b) {
-                tc::mbar_init(&fx_full[b], 1);
-                tc::mbar_init(&fx_empty[b], kDqWarps);
-            }
-        }
         if (TMAC) {
             for (int c = 0; c < SC; ++c) {
                 tc::mbar_init(&cfull[c], 1);
@@ -579,194 +566,10 @@ __global__ void __launch_bounds__(TMAC ? kThreadsTma : kThreads, 1)
         };
         // Epilogue of segment seg: TMEM -> registers -> global.  A whole tile
         // is stored directly; a split segment stores its raw fp32 accumulators
-        // ([token][row] in the CTA's slot) and the last CTA of the tile adds
-        // every contributor's slot in CTA order.
-        // Store four rows (mq .. mq + 3) of token n of a shared tile's sum.
-        auto store4 = [&](int64_t n, int64_t mq, float4 v) {
-            const int64_t idx = n * a.M + mq;
-            if ((a.M & 3) == 0 && mq + 3 < a.M) {  // 16- / 8-byte aligned, all in range
-                if (a.out_bf16)
-                    *reinterpret_cast<uint2 *>(reinterpret_cast<uint16_t *>(a.y) + idx) =
-                        make_uint2(f32_to_bf16(v.x) | ((uint32_t)f32_to_bf16(v.y) << 16),
-                                   f32_to_bf16(v.z) | ((uint32_t)f32_to_bf16(v.w) << 16));
-                else
-                    *reinterpret_cast<float4 *>(reinterpret_cast<float *>(a.y) + idx) = v;
-            } else {
-                const float r4[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-                for (int e = 0; e < 4; ++e)
-                    if (mq + e < a.M) {
-                        if (a.out_bf16)
-                            reinterpret_cast<uint16_t *>(a.y)[idx + e] = f32_to_bf16(r4[e]);
-                        else
-                            reinterpret_cast<float *>(a.y)[idx + e] = r4[e];
-                    }
-            }
-        };
-        // Sum of a shared tile's partials through shared memory: chunk i is
-        // the q-th 64 token columns (q = i / nc) of contributor i % nc, in
-        // buffer i % kFixBufs of the activation ring; one thread issues the
-        // bulk copies, every thread adds rows 4 rq .. 4 rq + 3 of columns
-        // cg + 8 j of each chunk in contributor order.
-        auto fixup_bulk = [&](const SegCursor &sg, int nc) {
-            const int dq = threadIdx.x - kFirstDqWarp * 32;  // 0..255
-            const int rq = dq & 31, cg = dq >> 5;
-            const int ncols = (int)(a.N - sg.n0 < TN ? a.N - sg.n0 : TN);
-            const int chunks = ((ncols + kFixCols - 1) / kFixCols) * nc;
-            const float tsv = __ldg(a.ts[0]) * 256.0f;
-            auto issue = [&](int i) {
-                const int b = i % kFixBufs;
-                if (!tc::mbar_wait(&fx_empty[b], ((uint32_t)(i / kFixBufs) & 1) ^ 1)) {
-                    fail(a, 10);
-                    return;
-                }
-                tc::mbar_arrive_expect_tx(&fx_full[b], kFixChunk);
-                tc::bulk_load(sb + (size_t)b * kFixChunk, contrib[i % nc] + (size_t)(i / nc) * (kFixChunk / 4),
-                              kFixChunk, &fx_full[b]);
-            };
-            if (dq == 0)
-                for (int i = 0; i < kFixBufs && i < chunks; ++i)
-                    issue(i);
-            float4 acc[kFixCols / 8];
-            for (int i = 0; i < chunks; ++i) {
-                const int b = i % kFixBufs, c = i % nc, q = i / nc;
-                if (c == 0) {
-#pragma unroll
-                    for (int j = 0; j < kFixCols / 8; ++j)
-                        acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
-                }
-                if (!tc::mbar_wait(&fx_full[b], (uint32_t)(i / kFixBufs) & 1)) {
-                    fail(a, 11);
-                    return;
-                }
-                const float4 *src = reinterpret_cast<const float4 *>(sb + (size_t)b * kFixChunk);
-#pragma unroll
-                for (int j = 0; j < kFixCols / 8; ++j) {
-                    const float4 v = src[(cg + 8 * j) * (BM / 4) + rq];  // column cg + 8 j, rows 4 rq ..
-                    acc[j].x += v.x;
-                    acc[j].y += v.y;
-                    acc[j].z += v.z;
-                    acc[j].w += v.w;
-                }
-                __syncwarp();
-                if (lane == 0)
-                    tc::mbar_arrive(&fx_empty[b]);
-                if (dq == 0 && i + kFixBufs < chunks)
-                    issue(i + kFixBufs);
-                if (c == nc - 1) {
-#pragma unroll
-                    for (int j = 0; j < kFixCols / 8; ++j) {
-                        const int col = q * kFixCols + cg + 8 * j;
-                        if (col < ncols)
-                            store4(sg.n0 + col, sg.m0 + 4 * rq,
-                                   make_float4(acc[j].x * tsv, acc[j].y * tsv, acc[j].z * tsv, acc[j].w * tsv));
-                    }
-                }
-            }
-        };
-        auto finish_split = [&](const SegCursor &sg) {
-            const int dq = threadIdx.x - kFirstDqWarp * 32;  // 0..255
-            tc::named_bar_sync(1, kDqWarps * 32);             // every partial store of this CTA is done
-            const int64_t G = a.sk_grid;
-            const int64_t t = sg.tile;  // a stream-K tile (sk_base is a tile boundary)
-            const int64_t b_lo = split_cta_of(t * a.kq - a.sk_base, a.units, G);
-            const int64_t b_hi = split_cta_of((t + 1) * a.kq - 1 - a.sk_base, a.units, G);
-            const int nc = (int)(b_hi - b_lo) + 1;  // contributors (<= kMaxContrib, by the host's plan)
-            if (nc > kMaxContrib) {  // cannot happen with the host's plan: refuse rather than overrun the table
-                if (dq == 0)
-                    fail(a, 9);
-                return;
-            }
-            if (dq == 0) {
-                // The counters are zeroed by the launch before this one on
-                // the stream, which it may overlap (programmatic dependent
-                // launch): wait for that launch before the first use (a no-op
-                // once it has completed).  After a whole-tile launch the
-                // zeroing came before that launch, and waiting would stall
-                // the fix-up until the last whole tile is done.
-                if (!a.after_whole)
-                    tc::griddep_wait();
-                // release: this CTA's partial (ordered by the barrier); acquire:
-                // the others'.  A CTA is the first contributor of at most one
-                // shared tile (its last segment), so the counter is b_lo's.
-                uint32_t old;
-                asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;"
-                             : "=r"(old)
-                             : "l"(a.counters + b_lo)
-                             : "memory");
-                *last_s = old == (uint32_t)(nc - 1);
-                if (*last_s)
-                    a.counters[b_lo] = 0;
-            }
-            // contributor c's partial of tile t: its first segment's slot if t
-            // is its first tile, else its last segment's (one 64-bit division
-            // each, so computed once)
-            if (dq < nc)
-                contrib[dq] = a.partial +
-                              (size_t)(2 * (b_lo + dq) + (t != sk_first_tile(a, b_lo + dq) ? 1 : 0)) * TN * BM;
-            tc::named_bar_sync(1, kDqWarps * 32);
-            if (!*last_s)
-                return;
-            if (!seg_more(a, sg)) {
-                // the CTA's last segment: its activation ring is idle, so
-                // the partials come in by bulk copies, 32 KB chunks in four
-                // buffers
-                fixup_bulk(sg, nc);
-                return;
-            }
-            // thread: rows 4 rq .. 4 rq + 3 and token columns cg + 8 i; four
-            // columns per pass and four contributors per load batch, so that
-            // sixteen 16-byte loads are in flight; contributors are added in
-            // CTA order
-            const int rq = dq & 31, cg = dq >> 5;
-            const int64_t mq = sg.m0 + 4 * rq;
-            const int ncols = (int)(a.N - sg.n0 < TN ? a.N - sg.n0 : TN);
-            const float tsv = FMT == 0 ? __ldg(a.ts[0]) * 256.0f : 1.0f;
-#pragma unroll 1
-            for (int col0 = cg; col0 < ncols; col0 += 32) {
-                float4 acc[4];
-#pragma unroll
-                for (int j = 0; j < 4; ++j)
-                    acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 1
-                for (int c0 = 0; c0 < nc; c0 += 4) {
-                    float4 v[4][4];
-#pragma unroll
-                    for (int c = 0; c < 4; ++c)
-#pragma unroll
-                        for (int j = 0; j < 4; ++j) {
-                            const int col = col0 + 8 * j;
-                            v[c][j] = (c0 + c < nc && col < ncols)
-                                          ? __ldcg(reinterpret_cast<const float4 *>(contrib[c0 + c] +
-                                                                                    (size_t)col * BM + 4 * rq))
-                                          : make_float4(0.f, 0.f, 0.f, 0.f);
-                        }
-#pragma unroll
-                    for (int c = 0; c < 4; ++c)
-#pragma unroll
-                        for (int j = 0; j < 4; ++j)
-                            if (c0 + c < nc) {
-                                acc[j].x += v[c][j].x;
-                                acc[j].y += v[c][j].y;
-                                acc[j].z += v[c][j].z;
-                                acc[j].w += v[c][j].w;
-                            }
-                }
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const int col = col0 + 8 * j;
-                    if (col >= ncols)
-                        break;
-                    store4(sg.n0 + col, mq,
-                           make_float4(acc[j].x * tsv, acc[j].y * tsv, acc[j].z * tsv, acc[j].w * tsv));
-                }
-            }
-        };
+        // ([token][row] in the CTA's slot) for the reduction launch.
         auto epilogue = [&](const SegCursor &sg) {
-            bool have = tc::mbar_wait(tmem_full, (uint32_t)sg.seg & 1);
+            const bool have = tc::mbar_wait(tmem_full, (uint32_t)sg.seg & 1);
             const bool split_seg = SPLIT && !sg.whole;
-            if (SPLIT)
-                have = tc::bar_and(1, kDqWarps * 32, have);  // uniform: named barriers follow
             if (!have)
                 fail(a, 4);
             tc::fence_after_sync();
@@ -833,10 +636,6 @@ __global__ void __launch_bounds__(TMAC ? kThreadsTma : kThreads, 1)
                 __syncwarp();
                 if (lane == 0)
                     tc::mbar_arrive(tmem_empty);
-            }
-            if constexpr (SPLIT) {
-                if (split_seg && have)
-                    finish_split(sg);
             }
         };
         SegCursor dcur = c0;  // the dequantisers' stage cursor
@@ -1064,21 +863,110 @@ __global__ void __launch_bounds__(TMAC ? kThreadsTma : kThreads, 1)
         tc::fence_after_sync();
         tc::tmem_dealloc(tmem_base, C::kTmemCols);
     }
-    // A stream-K launch overlaps the launch before it on the stream (the
-    // counter zeroing, or the whole tiles: it reads nothing they write but
-    // the counters) and completes only after it, so that work ordered after
+    // A stream-K launch after whole tiles overlaps them (it reads nothing
+    // they write) and completes only after them, so that work ordered after
     // this call sees every tile.
     if (SPLIT && threadIdx.x == 0)
         tc::griddep_wait();
 }
 
-// Zero the split-mode arrival counters; a stream-K launch that follows may
-// start at once (it waits for this one before its first counter access).
-__global__ void split_counters_zero_kernel(uint32_t *counters, int n)
+// Rows mq .. mq + 3 of token n of the output, from fp32 values.
+NVFP4_DEVINL void store_rows4(const Args &a, int64_t n, int64_t mq, float4 v)
 {
-    tc::griddep_launch_dependents();
-    for (int i = threadIdx.x; i < n; i += blockDim.x)
-        counters[i] = 0;
+    const int64_t idx = n * a.M + mq;
+    if ((a.M & 3) == 0 && mq + 3 < a.M) {  // 16- / 8-byte aligned, all in range
+        if (a.out_bf16)
+            *reinterpret_cast<uint2 *>(reinterpret_cast<uint16_t *>(a.y) + idx) =
+                make_uint2(f32_to_bf16(v.x) | ((uint32_t)f32_to_bf16(v.y) << 16),
+                           f32_to_bf16(v.z) | ((uint32_t)f32_to_bf16(v.w) << 16));
+        else
+            *reinterpret_cast<float4 *>(reinterpret_cast<float *>(a.y) + idx) = v;
+    } else {
+        const float r4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+            if (mq + e < a.M) {
+                if (a.out_bf16)
+                    reinterpret_cast<uint16_t *>(a.y)[idx + e] = f32_to_bf16(r4[e]);
+                else
+                    reinterpret_cast<float *>(a.y)[idx + e] = r4[e];
+            }
+    }
+}
+
+// Split mode, second launch (programmatic dependent launch after the
+// stream-K one): every tile that several CTAs shared is the sum of their
+// fp32 partials, added in CTA order (fixed by the shape, so deterministic),
+// times the tensor scale.  The work spreads over every SM: item (tile,
+// kRedCols token columns); thread (rq, cs) adds rows 4 rq .. 4 rq + 3 of
+// columns cs and cs + 8, four contributors per batch, so eight 16-byte loads
+// are in flight per thread.  A tile that one CTA covered whole was stored by
+// that CTA.
+__global__ void __launch_bounds__(kRedThreads, 4) split_reduce_kernel(Args a)
+{
+    tc::griddep_wait();  // the stream-K launch has completed: its partials are visible
+    constexpr int kItemsPerTile = BN / kRedCols;
+    const int64_t t0 = a.sk_base / a.kq;
+    const int64_t items = a.units / a.kq * kItemsPerTile;
+    const int rq = threadIdx.x & 31, cs = threadIdx.x >> 5;
+    const float tsv = __ldg(a.ts[0]) * 256.0f;
+    for (int64_t it = blockIdx.x; it < items; it += gridDim.x) {
+        const int64_t t = t0 + it / kItemsPerTile;
+        const int q = (int)(it % kItemsPerTile);
+        const int64_t b_lo = split_cta_of(t * a.kq - a.sk_base, a.units, a.sk_grid);
+        const int64_t b_hi = split_cta_of((t + 1) * a.kq - 1 - a.sk_base, a.units, a.sk_grid);
+        if (b_hi == b_lo)
+            continue;
+        int64_t rt, tt;
+        tile_coords(a, t, rt, tt);
+        const int64_t mq = rt * BM + 4 * rq;
+        const int64_t n0 = tt * BN;
+        const int ncols = (int)(a.N - n0 < BN ? a.N - n0 : BN);
+        const int col0 = q * kRedCols + cs;
+        if (col0 >= ncols)
+            continue;
+        const int nc = (int)(b_hi - b_lo) + 1;
+        float4 acc[2];
+#pragma unroll
+        for (int j = 0; j < 2; ++j)
+            acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int c0 = 0; c0 < nc; c0 += 4) {
+            float4 v[4][2];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                // contributor b's partial of tile t: its first segment's slot
+                // if t is its first tile, else its last segment's
+                const int64_t b = b_lo + c0 + c;
+                const float *p = nullptr;
+                if (c0 + c < nc)
+                    p = a.partial + (size_t)(2 * b + (t != sk_first_tile(a, b) ? 1 : 0)) * BN * BM;
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    const int col = col0 + 8 * j;
+                    v[c][j] = (p != nullptr && col < ncols)
+                                  ? __ldcg(reinterpret_cast<const float4 *>(p + (size_t)col * BM + 4 * rq))
+                                  : make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+            }
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+#pragma unroll
+                for (int j = 0; j < 2; ++j)
+                    if (c0 + c < nc) {
+                        acc[j].x += v[c][j].x;
+                        acc[j].y += v[c][j].y;
+                        acc[j].z += v[c][j].z;
+                        acc[j].w += v[c][j].w;
+                    }
+        }
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            const int col = col0 + 8 * j;
+            if (col < ncols)
+                store_rows4(a, n0 + col, mq,
+                            make_float4(acc[j].x * tsv, acc[j].y * tsv, acc[j].z * tsv, acc[j].w * tsv));
+        }
+    }
 }
 
 // ---------------------------------------------------------------------------
@@ -1113,9 +1001,9 @@ cudaError_t launch_t(const CUtensorMap &map, const WeightMaps &wm, const Args &a
     if (attr_err != cudaSuccess)
         return attr_err;
     dim3 grid((unsigned)a.grid);
-    if (SPLIT) {
-        // programmatic dependent launch: the CTAs start on SMs the launch
-        // before it has finished with
+    if (SPLIT && a.after_whole) {
+        // programmatic dependent launch: the CTAs start on SMs the whole-tile
+        // launch before it has finished with
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = grid;
         cfg.blockDim = dim3(TMAC ? kThreadsTma : kThreads);
@@ -1131,6 +1019,27 @@ cudaError_t launch_t(const CUtensorMap &map, const WeightMaps &wm, const Args &a
     prefill_kernel<NW, ALIGNED, FMT, TMAC, TN, SPLIT>
         <<<grid, TMAC ? kThreadsTma : kThreads, C::kSmemBytes, stream>>>(map, wm, a);
     return cudaGetLastError();
+}
+
+// The split-mode reduction, programmatically dependent on the stream-K
+// launch: its CTAs take SMs as the stream-K CTAs leave them and wait for that
+// launch's completion before reading a partial.  About eight resident CTAs
+// per SM keep enough loads in flight.
+inline cudaError_t launch_split_reduce(const Args &a, int num_sms, cudaStream_t stream)
+{
+    const int64_t items = a.units / a.kq * (BN / kRedCols);
+    const int64_t cap = (int64_t)num_sms * 8;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(items < cap ? items : cap));
+    cfg.blockDim = dim3(kRedThreads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, split_reduce_kernel, a);
 }
 
 // Token tile for a TMA-fed launch: 192 instead of 256 when that fills the
@@ -1163,10 +1072,9 @@ static bool encode_rows(PFN_cuTensorMapEncodeTiled_v12000 encode, CUtensorMap *m
 }  // namespace pf
 
 // Split mode (see Args): one NVFP4 matrix with K % 256 == 0.  Its workspace
-// holds a counter and two partial slots per CTA; the grid has at most
+// holds two partial slots per CTA; the grid has at most
 // min(kMaxSplitCtas, units) CTAs, so the size depends on the shape alone.
 constexpr int kMaxSplitCtas = 256;
-constexpr size_t kSplitCounterBytes = 1024;  // one u32 per CTA
 
 static bool split_possible(int64_t K, int n_weights, int fmt) { return fmt == 0 && n_weights == 1 && K % 256 == 0; }
 
@@ -1200,14 +1108,16 @@ constexpr double kL2Budget = 110e6;
 // Time in 64-k stages of a 256-token tile: a tile of TN tokens takes
 // num_kb * (0.25 + TN / 256) / 1.25 stages plus kFixed (prologue, pipeline
 // fill, epilogue); whole tiles run in waves of num_sms CTAs.  A split CTA
-// pays kFixed for each of up to three segments, and the last CTA of a shared
-// tile to arrive adds every contributor's 128 KB partial: kPerContrib stages
-// each.  A tile has at most kMaxContrib contributors.
+// pays kFixed for each of up to three segments, and the reduction launch
+// reads every 128 KB partial once, spread over the SMs: kRedFixed stages
+// plus 0.05 * 152 / SMs stages per partial.  A tile has at most
+// kMaxContrib contributors.
 static bool split_plan(int64_t N, int64_t M, int64_t K, int n_weights, int fmt, int num_sms, SplitPlan *sp)
 {
     if (!split_possible(K, n_weights, fmt) || num_sms > kMaxSplitCtas)
         return false;
-    constexpr double kFixed = 10.0, kPerContrib = 2.0;
+    constexpr double kFixed = 10.0, kRedFixed = 6.0;
+    const double red_per_partial = 0.05 * 152.0 / (double)num_sms;
     const int64_t row_tiles = (M + pf::BM - 1) / pf::BM;
     const int64_t kq = K / 256;
     const double num_kb = (double)(K / pf::BK);
@@ -1233,7 +1143,8 @@ static bool split_plan(int64_t N, int64_t M, int64_t K, int n_weights, int fmt, 
         while (G > 1 && contributors(G) > pf::kMaxContrib)
             --G;
         sp->sk_grid = G;
-        t_split = (double)sp->units * 4.0 / G + 3.0 * kFixed + kPerContrib * (double)contributors(G);
+        // partials: every range meets at most two shared tiles
+        t_split = (double)sp->units * 4.0 / G + 3.0 * kFixed + kRedFixed + red_per_partial * 2.0 * (double)G;
     } else {
         const int64_t rem = tiles % num_sms;
         if (rem == 0)
@@ -1244,7 +1155,7 @@ static bool split_plan(int64_t N, int64_t M, int64_t K, int n_weights, int fmt, 
         int64_t f = 1;
         double best = num_kb;
         for (int64_t ff = 2; ff <= fmax; ++ff) {
-            const double tf = num_kb / (double)ff + kPerContrib * (double)ff;
+            const double tf = num_kb / (double)ff + red_per_partial * (double)(rem * ff);
             if (tf < best) {
                 best = tf;
                 f = ff;
@@ -1255,7 +1166,7 @@ static bool split_plan(int64_t N, int64_t M, int64_t K, int n_weights, int fmt, 
         sp->dp_waves = tiles / num_sms;
         sp->units = rem * kq;
         sp->sk_grid = rem * f;
-        t_split = (double)sp->dp_waves * (num_kb + kFixed) + best + 3.0 * kFixed;
+        t_split = (double)sp->dp_waves * (num_kb + kFixed) + best + 3.0 * kFixed + kRedFixed;
     }
     if (sp->units / sp->sk_grid > (int64_t(1) << 24))
         return false;  // a CTA's stage count must fit an int
@@ -1264,12 +1175,12 @@ static bool split_plan(int64_t N, int64_t M, int64_t K, int n_weights, int fmt, 
 
 size_t prefill_workspace_bytes(int64_t N, int64_t M, int64_t K, int n_weights, int fmt)
 {
-    // the device status word at kStatusWordOffset; split mode adds its counters and partials
+    // the device status word at kStatusWordOffset; split mode adds its partials
     if (!split_possible(K, n_weights, fmt))
         return 256;
     const int64_t units = split_units(N, M, K);
     const int64_t ctas = units < kMaxSplitCtas ? units : kMaxSplitCtas;
-    return 256 + kSplitCounterBytes + (size_t)2 * ctas * pf::BN * pf::BM * sizeof(float);
+    return 256 + (size_t)2 * ctas * pf::BN * pf::BM * sizeof(float);
 }
 
 static cudaError_t prefill_impl(const uint16_t *x, int64_t N, int64_t M, int64_t K, const uint8_t *const *codes,
@@ -1320,16 +1231,11 @@ static cudaError_t prefill_impl(const uint16_t *x, int64_t N, int64_t M, int64_t
         a.after_whole = sp.dp_waves > 0;
         a.sk_base = sp.dp_waves * num_sms * a.kq;
         a.units = sp.units;
-        a.counters = reinterpret_cast<uint32_t *>(ws + 256);
-        a.partial = reinterpret_cast<float *>(ws + 256 + kSplitCounterBytes);
+        a.partial = reinterpret_cast<float *>(ws + 256);
         // at most one stream-K CTA per unit: every range is non-empty, so a
         // tile's contributors are the contiguous CTAs b_lo .. b_hi
         a.sk_grid = (int)sp.sk_grid;
         a.grid = a.sk_grid;
-        pf::split_counters_zero_kernel<<<1, 256, 0, stream>>>(a.counters, a.grid);
-        const cudaError_t ze = cudaGetLastError();
-        if (ze != cudaSuccess)
-            return ze;
     } else {
         a.grid = (int)(row_tiles * token_tiles);
     }
@@ -1382,7 +1288,10 @@ static cudaError_t prefill_impl(const uint16_t *x, int64_t N, int64_t M, int64_t
                 if (e != cudaSuccess)
                     return e;
             }
-            return pf::launch_t<1, true, 0, true, 256, true>(map, wm, a, stream);
+            const cudaError_t e = pf::launch_t<1, true, 0, true, 256, true>(map, wm, a, stream);
+            if (e != cudaSuccess)
+                return e;
+            return pf::launch_split_reduce(a, num_sms, stream);
         }
         if (tn == 192)
             return n_weights == 1 ? pf::launch_t<1, true, 0, true, 192>(map, wm, a, stream)

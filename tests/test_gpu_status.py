@@ -87,8 +87,8 @@ def test_wait_timeout_is_reported_and_the_context_stays_usable():
     _check_rows(y4, x, ref_w, "skinny N=4 after a reported timeout")
     _check_rows(y1, x[:1], ref_w, "skinny N=1 after a reported timeout")
 
-    # a prefill workspace (status word, and split-mode counters and partial
-    # slots) and the prefill kernel afterwards
+    # a prefill workspace (status word, and split-mode partial slots) and the
+    # prefill kernel afterwards
     pws = torch.zeros(g.nvfp4_workspace_bytes(g.NVFP4_OP_GEMM_PREFILL, 300, M, K), dtype=torch.uint8,
                       device=DEV)
     g.nvfp4_selftest_wait_timeout(pws)
