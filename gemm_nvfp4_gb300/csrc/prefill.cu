@@ -347,11 +347,6 @@ __global__ void __launch_bounds__(TMAC ? kThreadsTma : kThreads, 1)
     static_assert(3 * S + 1 + 2 * SC + 4 + 1 <= 128, "barriers and TMEM slot in the 1024-byte barrier area");
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    // The launch that follows this one on the stream may take the SMs as they
-    // free up: after whole tiles the stream-K launch (it computes other
-    // tiles), after the stream-K launch its reduction (which waits for this
-    // launch's completion before reading anything).
-    tc::griddep_launch_dependents();
     // The CTA's k blocks: one whole tile (raster order: the host picks the
     // raster so that the operand re-read across the grid stays resident in
     // L2), or in split mode the segments of its unit range.  Stage i of the
@@ -388,6 +383,19 @@ __global__ void __launch_bounds__(TMAC ? kThreadsTma : kThreads, 1)
     __syncthreads();
     tc::fence_after_sync();
     const uint32_t tmem_base = *tmem_slot;
+    // A stream-K launch is a programmatic dependent launch, so the set-up
+    // above overlaps the end of the kernel before it on the stream.  As the
+    // call's first launch it reads and writes nothing global before that
+    // kernel has completed; after whole tiles it reads nothing they write and
+    // waits for them before it exits.  (Whole-tile launches are ordinary
+    // ones: a wait in each of their CTAs cost 1-2 % over several waves.)
+    // Only then may the launch after this one start: after whole tiles the
+    // stream-K launch (it computes other tiles), after the stream-K launch
+    // its reduction (which waits for this launch's completion before reading
+    // anything).
+    if (SPLIT && !a.after_whole)
+        tc::griddep_wait();
+    tc::griddep_launch_dependents();
 
     if (warp == 0) {
         // ---------------- TMA producer (x tiles) ----------------
@@ -904,6 +912,9 @@ NVFP4_DEVINL void store_rows4(const Args &a, int64_t n, int64_t mq, float4 v)
 // that CTA.
 __global__ void __launch_bounds__(kRedThreads, 4) split_reduce_kernel(Args a)
 {
+    // The next call's first launch may take the SMs as they free up: it waits
+    // for this one's completion before any global access.
+    tc::griddep_launch_dependents();
     tc::griddep_wait();  // the stream-K launch has completed: its partials are visible
     constexpr int kItemsPerTile = BN / kRedCols;
     const int64_t t0 = a.sk_base / a.kq;
@@ -1001,9 +1012,9 @@ cudaError_t launch_t(const CUtensorMap &map, const WeightMaps &wm, const Args &a
     if (attr_err != cudaSuccess)
         return attr_err;
     dim3 grid((unsigned)a.grid);
-    if (SPLIT && a.after_whole) {
-        // programmatic dependent launch: the CTAs start on SMs the whole-tile
-        // launch before it has finished with
+    if (SPLIT) {
+        // programmatic dependent launch: the CTAs start on SMs as the kernel
+        // before them frees them (see the kernel for what waits for it)
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = grid;
         cfg.blockDim = dim3(TMAC ? kThreadsTma : kThreads);

@@ -107,7 +107,9 @@ def test_prefill_gateup_full_size_sampled(N):
 @pytest.mark.parametrize("N", [512, 2048, 8192])
 def test_prefill_down_full_size_sampled(N):
     """Full-size prefill down projection (17408 -> 5120), fresh bf16 inputs, at
-    every token count the benchmark times (N = 2048 runs the 192-token tile)."""
+    every token count the benchmark times: N = 512 splits every tile's K
+    across the SMs; N = 2048 and 8192 run whole-tile waves, then k slices of
+    the tiles left (split mode's two forms), each followed by its reduction."""
     M, K = inputs.LAYER_27B.shapes()["down"]
     w = inputs.weights(M, K, seed=400, device=DEV)
     x = inputs.activations(N, K, seed=401, device=DEV)
@@ -156,8 +158,8 @@ def test_split_k_prefill_deterministic(N, M, K):
     across CTAs: with operands that fit in L2, contiguous unit ranges (a part
     of one tile, parts of two, or whole tiles between two parts); with larger
     operands (the last shape: 134 MB of activations), whole-tile waves and
-    then equal k slices of the tiles left.  fp32 partials are added by the
-    last CTA of each shared tile, in CTA order.  Repeated calls give the same
+    then equal k slices of the tiles left.  fp32 partials are added by a
+    reduction launch, in CTA order.  Repeated calls give the same
     bits, and the result matches the oracle.  Ragged row and token tiles
     included."""
     w = inputs.weights(M, K, seed=N + 5, device=DEV)
@@ -174,3 +176,63 @@ def test_split_k_prefill_deterministic(N, M, K):
     toks = _sample(6, N, N + 8, [0, N - 1])
     y_ref, A = oracle.gemv(bf16_bits(x), *ref_w, rows=rows, tokens=toks)
     assert_close(to_np(y1)[np.ix_(toks, rows)], y_ref, gemv_tol(y_ref, A), f"split prefill N={N}")
+
+
+def test_dependent_prefill_chain_eager_and_graph():
+    """Three prefill calls back to back on one stream, each reading the output
+    of the one before: gate/up + SwiGLU with bf16 h, a down projection that
+    splits K (stream-K launch, then its reduction launch), and a product over
+    the down output (K % 256 != 0: the plain-load kernel).  Every prefill
+    launch is a programmatic dependent launch that waits for the kernel
+    before it before any global access, so each stage must agree with the
+    oracle run on the input that stage actually received, complete.  The
+    chain captured in a CUDA graph and replayed gives the eager bits."""
+    N, K0, M1, M2, M3 = 600, 512, 4096, 384, 256
+    wg = inputs.weights(M1, K0, seed=41, device=DEV)
+    wu = inputs.weights(M1, K0, seed=42, device=DEV)
+    wd = inputs.weights(M2, M1, seed=43, device=DEV)
+    w3 = inputs.weights(M3, M2, seed=44, device=DEV)
+    Wg, Wu, Wd, W3 = (g.nvfp4_quantize(w) for w in (wg, wu, wd, w3))
+    x = inputs.activations(N, K0, seed=45, device=DEV)
+    h = torch.empty(N, M1, dtype=torch.bfloat16, device=DEV)
+    y = torch.empty(N, M2, dtype=torch.bfloat16, device=DEV)
+    z = torch.empty(N, M3, dtype=torch.float32, device=DEV)
+    ws1 = workspace(g.NVFP4_OP_GATEUP_SWIGLU, N, M1, K0)
+    ws2 = workspace(g.NVFP4_OP_GEMM_PREFILL, N, M2, M1)
+    ws3 = workspace(g.NVFP4_OP_GEMM_PREFILL, N, M3, M2)
+
+    def chain(stream=None):
+        g.nvfp4_gateup_swiglu(x, Wg, Wu, out=h, workspace=ws1, stream=stream)
+        g.nvfp4_gemm_prefill(h, Wd, out=y, workspace=ws2, stream=stream)
+        g.nvfp4_gemm_prefill(y, W3, out=z, workspace=ws3, stream=stream)
+
+    chain()
+    torch.cuda.synchronize()
+    for ws in (ws1, ws2, ws3):
+        assert timeout_flag(ws) == 0
+    ref = [t.clone() for t in (h, y, z)]
+    toks = _sample(8, N, 46, [0, 255, 256, N - 1])
+    r1, r2, r3 = (_sample(24, M, 47 + i, [0, 127, 128, M - 1]) for i, M in enumerate((M1, M2, M3)))
+    h_ref, g_ref, u_ref, Ag, Au = oracle.swiglu(bf16_bits(x), oracle.quantize(wg.cpu().numpy()),
+                                                oracle.quantize(wu.cpu().numpy()), rows=r1, tokens=toks)
+    assert_close(to_np(h)[np.ix_(toks, r1)], h_ref,
+                 swiglu_tol(h_ref, g_ref, u_ref, Ag, Au, torch.bfloat16), "chain stage 1 (gate/up)")
+    y_ref, A = oracle.gemv(bf16_bits(h), *oracle.quantize(wd.cpu().numpy()), rows=r2, tokens=toks)
+    assert_close(to_np(y)[np.ix_(toks, r2)], y_ref, gemv_tol(y_ref, A, torch.bfloat16), "chain stage 2 (down)")
+    z_ref, A = oracle.gemv(bf16_bits(y), *oracle.quantize(w3.cpu().numpy()), rows=r3, tokens=toks)
+    assert_close(to_np(z)[np.ix_(toks, r3)], z_ref, gemv_tol(z_ref, A), "chain stage 3")
+
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        chain(stream=s)
+    for _ in range(3):
+        for t in (h, y, z):
+            t.zero_()
+        graph.replay()
+        torch.cuda.synchronize()
+        for t, t0 in zip((h, y, z), ref):
+            assert torch.equal(t, t0)
+    for ws in (ws1, ws2, ws3):
+        assert timeout_flag(ws) == 0
