@@ -906,10 +906,14 @@ NVFP4_DEVINL void store_rows4(const Args &a, int64_t n, int64_t mq, float4 v)
 // stream-K one): every tile that several CTAs shared is the sum of their
 // fp32 partials, added in CTA order (fixed by the shape, so deterministic),
 // times the tensor scale.  The work spreads over every SM: item (tile,
-// kRedCols token columns); thread (rq, cs) adds rows 4 rq .. 4 rq + 3 of
+// kRedCols token columns).  Each warp works out the item's contributors in
+// its lanes (lane c: contributor c's partial slot, c < 64 in two rounds; the
+// 64-bit divisions run once per lane, not once per thread and contributor)
+// and takes them by shuffle; thread (rq, cs) adds rows 4 rq .. 4 rq + 3 of
 // columns cs and cs + 8, four contributors per batch, so eight 16-byte loads
 // are in flight per thread.  A tile that one CTA covered whole was stored by
-// that CTA.
+// that CTA.  A slot or tile outside the plan's ranges (impossible with the
+// host's plan) records status 10 and skips the item.
 __global__ void __launch_bounds__(kRedThreads, 4) split_reduce_kernel(Args a)
 {
     // The next call's first launch may take the SMs as they free up: it waits
@@ -919,24 +923,43 @@ __global__ void __launch_bounds__(kRedThreads, 4) split_reduce_kernel(Args a)
     constexpr int kItemsPerTile = BN / kRedCols;
     const int64_t t0 = a.sk_base / a.kq;
     const int64_t items = a.units / a.kq * kItemsPerTile;
-    const int rq = threadIdx.x & 31, cs = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31, rq = lane, cs = threadIdx.x >> 5;
     const float tsv = __ldg(a.ts[0]) * 256.0f;
+    const uint32_t n_slots = 2u * (uint32_t)a.sk_grid;
     for (int64_t it = blockIdx.x; it < items; it += gridDim.x) {
         const int64_t t = t0 + it / kItemsPerTile;
         const int q = (int)(it % kItemsPerTile);
         const int64_t b_lo = split_cta_of(t * a.kq - a.sk_base, a.units, a.sk_grid);
         const int64_t b_hi = split_cta_of((t + 1) * a.kq - 1 - a.sk_base, a.units, a.sk_grid);
-        if (b_hi == b_lo)
+        const int nc = (int)(b_hi - b_lo) + 1;  // warp-uniform
+        if (nc < 2)
+            continue;  // a whole tile, stored by its CTA
+        // lane c (and c + 32): contributor c's partial slot, 2 b + (t is not
+        // b's first tile: its last segment's slot)
+        uint32_t slot_lo = 0, slot_hi = 0;
+        if (lane < nc)
+            slot_lo = (uint32_t)(2 * (b_lo + lane) + (t != sk_first_tile(a, b_lo + lane) ? 1 : 0));
+        if (lane + 32 < nc)
+            slot_hi = (uint32_t)(2 * (b_lo + lane + 32) + (t != sk_first_tile(a, b_lo + lane + 32) ? 1 : 0));
+        int64_t rt = 0, tt = 0;
+        if (lane == 0)
+            tile_coords(a, t, rt, tt);
+        rt = __shfl_sync(0xFFFFFFFFu, rt, 0);
+        tt = __shfl_sync(0xFFFFFFFFu, tt, 0);
+        const bool bad_slot = (lane < nc && slot_lo >= n_slots) || (lane + 32 < nc && slot_hi >= n_slots);
+        const bool bad = nc > kMaxContrib || rt < 0 || rt >= a.row_tiles || tt < 0 || tt >= a.token_tiles ||
+                         __any_sync(0xFFFFFFFFu, bad_slot);
+        if (bad) {
+            if (lane == 0)
+                fail(a, 10);
             continue;
-        int64_t rt, tt;
-        tile_coords(a, t, rt, tt);
+        }
         const int64_t mq = rt * BM + 4 * rq;
         const int64_t n0 = tt * BN;
         const int ncols = (int)(a.N - n0 < BN ? a.N - n0 : BN);
         const int col0 = q * kRedCols + cs;
         if (col0 >= ncols)
             continue;
-        const int nc = (int)(b_hi - b_lo) + 1;
         float4 acc[2];
 #pragma unroll
         for (int j = 0; j < 2; ++j)
@@ -945,17 +968,15 @@ __global__ void __launch_bounds__(kRedThreads, 4) split_reduce_kernel(Args a)
             float4 v[4][2];
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
-                // contributor b's partial of tile t: its first segment's slot
-                // if t is its first tile, else its last segment's
-                const int64_t b = b_lo + c0 + c;
-                const float *p = nullptr;
-                if (c0 + c < nc)
-                    p = a.partial + (size_t)(2 * b + (t != sk_first_tile(a, b) ? 1 : 0)) * BN * BM;
+                const int cc = c0 + c;
+                const uint32_t lo = __shfl_sync(0xFFFFFFFFu, slot_lo, cc & 31);
+                const uint32_t hi = __shfl_sync(0xFFFFFFFFu, slot_hi, cc & 31);
+                const float *p = a.partial + (size_t)(cc < 32 ? lo : hi) * BN * BM + 4 * rq;
 #pragma unroll
                 for (int j = 0; j < 2; ++j) {
                     const int col = col0 + 8 * j;
-                    v[c][j] = (p != nullptr && col < ncols)
-                                  ? __ldcg(reinterpret_cast<const float4 *>(p + (size_t)col * BM + 4 * rq))
+                    v[c][j] = (cc < nc && col < ncols)
+                                  ? __ldcg(reinterpret_cast<const float4 *>(p + (size_t)col * BM))
                                   : make_float4(0.f, 0.f, 0.f, 0.f);
                 }
             }
@@ -1034,8 +1055,9 @@ cudaError_t launch_t(const CUtensorMap &map, const WeightMaps &wm, const Args &a
 
 // The split-mode reduction, programmatically dependent on the stream-K
 // launch: its CTAs take SMs as the stream-K CTAs leave them and wait for that
-// launch's completion before reading a partial.  About eight resident CTAs
-// per SM keep enough loads in flight.
+// launch's completion before reading a partial.  Four CTAs fit on an SM;
+// the grid stops at eight CTAs per SM and takes any further items in its
+// grid-stride loop.
 inline cudaError_t launch_split_reduce(const Args &a, int num_sms, cudaStream_t stream)
 {
     const int64_t items = a.units / a.kq * (BN / kRedCols);

@@ -406,7 +406,7 @@ int nvfp4_noalloc_selftest_wait_timeout(nvfp4_stream_t stream);
  * NVFP4_STATUS_WORD_OFFSET of their workspace (every product workspace is at
  * least 256 bytes).  A tensor-core kernel (skinny with K % 256 == 0, prefill)
  * whose bounded pipeline wait runs out (2 s) stores a nonzero code there and
- * returns: 1..8 from the prefill kernel, 11..25 from the skinny kernel, 127
+ * returns: 1..10 from the prefill kernels, 11..25 from the skinny kernel, 127
  * from nvfp4_selftest_wait_timeout.  No kernel clears the word, so it reports
  * any failure since it was last cleared; it starts clean when the workspace is
  * zero-filled (required for the skinny calls; do it for a prefill workspace
