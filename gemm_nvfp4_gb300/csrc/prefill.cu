@@ -906,60 +906,60 @@ NVFP4_DEVINL void store_rows4(const Args &a, int64_t n, int64_t mq, float4 v)
 // stream-K one): every tile that several CTAs shared is the sum of their
 // fp32 partials, added in CTA order (fixed by the shape, so deterministic),
 // times the tensor scale.  The work spreads over every SM: item (tile,
-// kRedCols token columns).  Each warp works out the item's contributors in
-// its lanes (lane c: contributor c's partial slot, c < 64 in two rounds; the
-// 64-bit divisions run once per lane, not once per thread and contributor)
-// and takes them by shuffle; thread (rq, cs) adds rows 4 rq .. 4 rq + 3 of
+// kRedCols token columns); thread (rq, cs) adds rows 4 rq .. 4 rq + 3 of
 // columns cs and cs + 8, four contributors per batch, so eight 16-byte loads
 // are in flight per thread.  A tile that one CTA covered whole was stored by
-// that CTA.  A slot or tile outside the plan's ranges (impossible with the
-// host's plan) records status 10 and skips the item.
+// that CTA.
+// Contributors of tile t: CTAs b_lo .. b_hi.  Every one after b_lo starts its
+// range inside t, so t is its first tile and its partial is in slot 2 b;
+// b_lo's is in slot 2 b_lo, or 2 b_lo + 1 (its last segment) if its range
+// starts before t.  NARROW: the index arithmetic in 32 bits, which the host
+// picks when every intermediate fits (a fraction of the cost of 64-bit
+// divisions).  A contributor or tile outside the plan's ranges (impossible
+// with the host's plan) records status 10 and skips the item.
+template <bool NARROW>
 __global__ void __launch_bounds__(kRedThreads, 4) split_reduce_kernel(Args a)
 {
+    using I = typename std::conditional<NARROW, uint32_t, int64_t>::type;
     // The next call's first launch may take the SMs as they free up: it waits
     // for this one's completion before any global access.
     tc::griddep_launch_dependents();
     tc::griddep_wait();  // the stream-K launch has completed: its partials are visible
     constexpr int kItemsPerTile = BN / kRedCols;
-    const int64_t t0 = a.sk_base / a.kq;
+    const I units = (I)a.units, G = (I)a.sk_grid, kq = (I)a.kq, sk_base = (I)a.sk_base;
+    const I group = (I)a.group, token_tiles = (I)a.token_tiles, row_tiles = (I)a.row_tiles;
+    const I t0 = sk_base / kq;
     const int64_t items = a.units / a.kq * kItemsPerTile;
-    const int lane = threadIdx.x & 31, rq = lane, cs = threadIdx.x >> 5;
+    const int rq = threadIdx.x & 31, cs = threadIdx.x >> 5;
     const float tsv = __ldg(a.ts[0]) * 256.0f;
-    const uint32_t n_slots = 2u * (uint32_t)a.sk_grid;
     for (int64_t it = blockIdx.x; it < items; it += gridDim.x) {
-        const int64_t t = t0 + it / kItemsPerTile;
+        const I t = t0 + (I)(it / kItemsPerTile);
         const int q = (int)(it % kItemsPerTile);
-        const int64_t b_lo = split_cta_of(t * a.kq - a.sk_base, a.units, a.sk_grid);
-        const int64_t b_hi = split_cta_of((t + 1) * a.kq - 1 - a.sk_base, a.units, a.sk_grid);
-        const int nc = (int)(b_hi - b_lo) + 1;  // warp-uniform
+        const I b_lo = ((t * kq - sk_base + 1) * G - 1) / units;         // CTA of the tile's first unit
+        const I b_hi = (((t + 1) * kq - sk_base) * G - 1) / units;       // and of its last
+        const int nc = (int)(b_hi - b_lo) + 1;
         if (nc < 2)
-            continue;  // a whole tile, stored by its CTA
-        // lane c (and c + 32): contributor c's partial slot, 2 b + (t is not
-        // b's first tile: its last segment's slot)
-        uint32_t slot_lo = 0, slot_hi = 0;
-        if (lane < nc)
-            slot_lo = (uint32_t)(2 * (b_lo + lane) + (t != sk_first_tile(a, b_lo + lane) ? 1 : 0));
-        if (lane + 32 < nc)
-            slot_hi = (uint32_t)(2 * (b_lo + lane + 32) + (t != sk_first_tile(a, b_lo + lane + 32) ? 1 : 0));
-        int64_t rt = 0, tt = 0;
-        if (lane == 0)
-            tile_coords(a, t, rt, tt);
-        rt = __shfl_sync(0xFFFFFFFFu, rt, 0);
-        tt = __shfl_sync(0xFFFFFFFFu, tt, 0);
-        const bool bad_slot = (lane < nc && slot_lo >= n_slots) || (lane + 32 < nc && slot_hi >= n_slots);
-        const bool bad = nc > kMaxContrib || rt < 0 || rt >= a.row_tiles || tt < 0 || tt >= a.token_tiles ||
-                         __any_sync(0xFFFFFFFFu, bad_slot);
-        if (bad) {
-            if (lane == 0)
+            continue;
+        const uint32_t f0 = (sk_base + b_lo * units / G) / kq != t ? 1u : 0u;
+        // raster: groups of `group` row tiles, row tiles fastest inside a group
+        const I per_group = group * token_tiles;
+        const I gidx = t / per_group;
+        const I first = gidx * group;
+        const I rows = row_tiles - first < group ? row_tiles - first : group;
+        const I in = t - gidx * per_group;
+        const I rt = first + in % rows, tt = in / rows;
+        if (nc > kMaxContrib || b_hi >= G || rt >= row_tiles || tt >= token_tiles) {
+            if (threadIdx.x == 0)
                 fail(a, 10);
             continue;
         }
-        const int64_t mq = rt * BM + 4 * rq;
-        const int64_t n0 = tt * BN;
+        const int64_t mq = (int64_t)rt * BM + 4 * rq;
+        const int64_t n0 = (int64_t)tt * BN;
         const int ncols = (int)(a.N - n0 < BN ? a.N - n0 : BN);
         const int col0 = q * kRedCols + cs;
         if (col0 >= ncols)
             continue;
+        const float *base = a.partial + (size_t)(2 * (size_t)b_lo) * BN * BM + 4 * rq;
         float4 acc[2];
 #pragma unroll
         for (int j = 0; j < 2; ++j)
@@ -969,9 +969,7 @@ __global__ void __launch_bounds__(kRedThreads, 4) split_reduce_kernel(Args a)
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
                 const int cc = c0 + c;
-                const uint32_t lo = __shfl_sync(0xFFFFFFFFu, slot_lo, cc & 31);
-                const uint32_t hi = __shfl_sync(0xFFFFFFFFu, slot_hi, cc & 31);
-                const float *p = a.partial + (size_t)(cc < 32 ? lo : hi) * BN * BM + 4 * rq;
+                const float *p = base + (size_t)(2 * cc + (cc == 0 ? f0 : 0u)) * BN * BM;
 #pragma unroll
                 for (int j = 0; j < 2; ++j) {
                     const int col = col0 + 8 * j;
@@ -1072,7 +1070,14 @@ inline cudaError_t launch_split_reduce(const Args &a, int num_sms, cudaStream_t 
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, split_reduce_kernel, a);
+    // 32-bit index arithmetic when every intermediate fits: (u + 1) * G for
+    // a unit u, b * units for a CTA b < G, and the unit numbers themselves
+    const uint64_t lim = uint64_t(1) << 32;
+    const bool narrow = (uint64_t)(a.units + 1) * (uint64_t)a.sk_grid < lim &&
+                        (uint64_t)(a.sk_base + a.units) < lim;
+    if (narrow)
+        return cudaLaunchKernelEx(&cfg, split_reduce_kernel<true>, a);
+    return cudaLaunchKernelEx(&cfg, split_reduce_kernel<false>, a);
 }
 
 // Token tile for a TMA-fed launch: 192 instead of 256 when that fills the
