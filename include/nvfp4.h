@@ -350,7 +350,7 @@ int nvfp4_fp6_gateup_swiglu(const uint16_t *x, int64_t N,
                             void *workspace, size_t workspace_bytes, nvfp4_stream_t stream);
 
 /* Skinny product without a caller workspace, for callers that cannot allocate
- * device memory.  The paper has no counterpart for this call: it is an
+ * device memory.  The source pages have no counterpart for this call: it is an
  * addition of this library.  A plain C or Fortran host program with no
  * device allocator of its own, or a latency-critical loop that must not call
  * cudaMalloc (it synchronises the whole device), can use it.
@@ -393,21 +393,23 @@ int nvfp4_gemv_skinny_noalloc(const uint16_t *x, int64_t N,
  * is zero, else NVFP4_ERR_DEVICE_TIMEOUT.  With clear != 0 and a nonzero word
  * the whole array is zero-filled on `stream` (cudaMemsetAsync), which resets
  * the word and any split-K counter a failed call left set.  Allocates nothing;
- * NVFP4_ERR_CUDA if a CUDA call fails.  The paper has no counterpart. */
+ * NVFP4_ERR_CUDA if a CUDA call fails.  The source pages have no counterpart. */
 int nvfp4_noalloc_status(int clear, uint32_t *code, nvfp4_stream_t stream);
 
 /* The failure-path self-test of nvfp4_selftest_wait_timeout run against the
  * no-allocation array of the current device: after 2 s it records code 127 in
  * the array's status word, which nvfp4_noalloc_status then reports.  Faults
- * nothing; allocates nothing.  The paper has no counterpart. */
+ * nothing; allocates nothing.  The source pages have no counterpart. */
 int nvfp4_noalloc_selftest_wait_timeout(nvfp4_stream_t stream);
 
 /* Device-side failures.  The product calls keep a 32-bit status word at byte
  * NVFP4_STATUS_WORD_OFFSET of their workspace (every product workspace is at
  * least 256 bytes).  A tensor-core kernel (skinny with K % 256 == 0, prefill)
  * whose bounded pipeline wait runs out (2 s) stores a nonzero code there and
- * returns: 1..10 from the prefill kernels, 11..25 from the skinny kernel, 127
- * from nvfp4_selftest_wait_timeout.  No kernel clears the word, so it reports
+ * returns: 1..8 from the prefill kernel, 10 from its split-mode reduction
+ * (a contributor or tile outside the plan, which the host's plan rules out),
+ * 11..25 from the skinny kernel, 127 from nvfp4_selftest_wait_timeout.  No
+ * kernel clears the word, so it reports
  * any failure since it was last cleared; it starts clean when the workspace is
  * zero-filled (required for the skinny calls; do it for a prefill workspace
  * too before reading its status).  A quantise call overwrites the word. */
