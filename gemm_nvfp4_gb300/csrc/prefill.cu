@@ -165,11 +165,6 @@ struct SegCursor {
     bool whole;     // the segment covers the whole K range of its tile
 };
 
-// Stream-K CTA whose unit range holds stream-K unit u (relative to sk_base;
-// ranges [b * units / G, (b + 1) * units / G), G = sk_grid <= units, so none
-// is empty).
-NVFP4_DEVINL int64_t split_cta_of(int64_t u, int64_t units, int64_t G) { return ((u + 1) * G - 1) / units; }
-
 // First tile of stream-K CTA b's range.
 NVFP4_DEVINL int64_t sk_first_tile(const Args &a, int64_t b)
 {
@@ -935,6 +930,9 @@ __global__ void __launch_bounds__(kRedThreads, 4) split_reduce_kernel(Args a)
     for (int64_t it = blockIdx.x; it < items; it += gridDim.x) {
         const I t = t0 + (I)(it / kItemsPerTile);
         const int q = (int)(it % kItemsPerTile);
+        // CTA b's range is [b units / G, (b + 1) units / G) (relative to
+        // sk_base; G <= units, so none is empty): unit u lies in the range of
+        // CTA ((u + 1) G - 1) / units
         const I b_lo = ((t * kq - sk_base + 1) * G - 1) / units;         // CTA of the tile's first unit
         const I b_hi = (((t + 1) * kq - sk_base) * G - 1) / units;       // and of its last
         const int nc = (int)(b_hi - b_lo) + 1;
